@@ -1,0 +1,185 @@
+/*
+ * rope_chain.h -- C ABI of librope_chain.so: the speculative draft's context
+ * K/V chain (MuseSparkDSparkModel.precompute_and_store_context_kv) on one
+ * GB300 GPU (sm_103a).
+ *
+ * The chain, per context row t of width D = 8192 and draft layer l < L:
+ *   1. hidden RMSNorm of x[t], rounded to bf16                 rc_context_norms
+ *   2. layer l's input RMSNorm of that, stacked into [L, T, D]  rc_context_norms
+ *   3. K/V projection [L, T, D] x [L, D, 2*H*64]                rc_kv_project
+ *   4. weightless K-norm of every 64-wide key head, GPT-J RoPE,
+ *      and the slot-mapped insert of K and V into paged caches  rc_kv_store
+ *
+ * Sources, cited by web page title and symbol:
+ *   [ctx] "vllm.models.muse_spark.nvidia.specialized_decode.cutedsl.draft.context"
+ *   [rt]  "vllm.models.muse_spark.nvidia.specialized_decode.runtime.draft"
+ *   [bnd] "vllm.models.muse_spark.nvidia.specialized_decode.cutedsl.common.draft_boundary"
+ *
+ * Conventions for every call:
+ *   - Tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never frees or retains them.  Pointer ARRAYS (slots, caches) are HOST
+ *     arrays of device pointers, read during the call only.
+ *   - bf16 values travel as uint16_t bit patterns.
+ *   - Work is enqueued on `stream`; calls do not synchronise and do not
+ *     allocate device memory, so they can be issued inside CUDA graph
+ *     capture.  Outputs are valid once the stream reaches that point.
+ *   - Arguments are checked on the host before anything is launched; a
+ *     rejected call returns RC_ERR_INVALID_ARG or RC_ERR_UNSUPPORTED, leaves
+ *     every buffer untouched, and rc_last_error() says why.
+ *   - Floating point: FP32 arithmetic with the rounding points of [ctx]
+ *     (each product, sum and fma rounded to nearest even; nothing fused
+ *     beyond the fma the pages write); 1/sqrt is the correctly rounded
+ *     IEEE sqrt then divide (the pages use a hardware approximation).
+ *     Subnormals are kept.
+ */
+#ifndef ROPE_CHAIN_H
+#define ROPE_CHAIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RC_OK = 0,
+    RC_ERR_INVALID_ARG = 1,   /* malformed argument: null, misaligned, out of range */
+    RC_ERR_UNSUPPORTED = 2,   /* well-formed but outside what the kernels cover */
+    RC_ERR_CUDA = 3           /* a CUDA runtime call or launch failed */
+} rc_status;
+
+/* Weight layouts accepted by rc_kv_project. */
+typedef enum {
+    RC_W_KN = 0,   /* W[L, D, N]: N contiguous (the projection as x @ W) */
+    RC_W_NK = 1    /* W[L, N, D]: D contiguous (nn.Linear layout; [rt]
+                      ContextKV._project multiplies by its transpose) */
+} rc_weight_layout;
+
+/* Message of the last failed call on this host thread ("" if none). */
+const char *rc_last_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t rc_version(void);
+
+/*
+ * rc_context_norms -- steps 1 and 2.  [ctx] ContextNorms / _ContextNormsKernel,
+ * [rt] ContextKV._project (the stack), [bnd] boundary_fragments (norm order).
+ *
+ *   z[t]      = bf16( hidden_norm(x[t]) )
+ *   out[l, t] = bf16( pre_norm_l(z[t]) )         for l < L
+ * with norm(v)_c = (v_c * r) * gamma_c (or v_c * r when the weight is NULL),
+ * r = 1 / sqrt(fma(sum_c v_c^2, 1/D, eps)), the sum in a fixed documented
+ * order (thread t of 256 holds columns 2048k + 8t + i; in-thread (k, i)
+ * order; xor butterfly over each warp; the 8 warp sums left to right).
+ *
+ *   x         bf16 [T, D] row-major, contiguous, 16-byte aligned
+ *   T         rows, 0 <= T < 2^31 (T == 0: nothing is launched)
+ *   D         must be 8192 (the single-tile row norm); else RC_ERR_UNSUPPORTED
+ *   hidden_w  bf16 [D] hidden-norm weight, 16-byte aligned, or NULL (weightless)
+ *   pre_w     bf16 [L, D] layer input-norm weights, 16-byte aligned, or NULL
+ *   L         layers, 1 <= L <= 64
+ *   eps       shared by both norms
+ *   out       bf16 [L, T, D] contiguous, 16-byte aligned; must not overlap x
+ */
+rc_status rc_context_norms(const uint16_t *x, int64_t T, int32_t D,
+                           const uint16_t *hidden_w, const uint16_t *pre_w,
+                           int32_t L, float eps, uint16_t *out,
+                           cudaStream_t stream);
+
+/*
+ * rc_kv_project -- step 3.  [rt] ContextKV._project
+ * (torch.bmm(per_layer, stacked_kv_weight.transpose(1, 2))).
+ *
+ *   out[l, t, n] = bf16( sum_k normed[l, t, k] * W_l[k, n] )
+ * BF16 inputs, FP32 accumulation on the tensor cores (tcgen05), one
+ * rounding to bf16 at the end.  The summation order is the kernel's, so
+ * results agree with an exact sum to within bf16 rounding plus FP32
+ * accumulation error, not bit for bit.
+ *
+ *   normed     bf16 [L, T, D] contiguous, 16-byte aligned
+ *   W          bf16 weights in `w_layout`, contiguous, 16-byte aligned
+ *   w_layout   RC_W_KN or RC_W_NK
+ *   out        bf16 [L, T, N] contiguous, 16-byte aligned
+ *   L          1 <= L <= 4096;  T: 0 <= T <= 8388480 (T == 0: no launch)
+ *   D          multiple of 64, >= 64;  N: multiple of 128, >= 128
+ *   workspace  optional device scratch for split-K (16-byte aligned) and its
+ *              size in bytes; NULL/0 runs without split-K.  For few output
+ *              tiles the K dimension is split across CTAs and the FP32
+ *              partial sums are added in split order by a second kernel
+ *              (deterministic for a given workspace size).  The bytes that
+ *              give the full split are rc_kv_project_workspace_size().
+ */
+rc_status rc_kv_project(const uint16_t *normed, const uint16_t *W,
+                        int32_t w_layout, uint16_t *out, int32_t L, int64_t T,
+                        int32_t D, int32_t N, void *workspace,
+                        size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes rc_kv_project uses at most for these sizes on the current
+   device (0 when it would not split).  Host-only apart from one device
+   attribute query; returns 0 for invalid sizes. */
+size_t rc_kv_project_workspace_size(int32_t L, int64_t T, int32_t D, int32_t N);
+
+/*
+ * rc_kv_store -- step 4.  [ctx] ContextKvStore / _ContextKvStoreKernel,
+ * _sum_squares_64, _rope; [rt] ContextKV.store.
+ *
+ * For every layer l < L whose slots[l] is not NULL and every row t < rows,
+ * with s = slots[l][t]:
+ *   s < 0                                      row skipped (nothing read or written)
+ *   s >= num_blocks*block_size, or (cos_sin != NULL) positions[t] outside
+ *   [0, max_position)                          row skipped and counted in *err
+ *   otherwise, for each head h < H:
+ *     key   = bf16(k_h * r), r = 1/sqrt(fma(sum k_h^2, 1/64, eps)),
+ *             the sum folded as lane j holding the pair (2j, 2j+1): even and
+ *             odd squares each by an xor butterfly, then even + odd;
+ *     key   = GPT-J RoPE of each pair (2j, 2j+1) with c = cos_sin[pos, j],
+ *             s = cos_sin[pos, 32 + j]: (fma(x, c, -(y*s)), fma(y, c, x*s)),
+ *             rounded to bf16 (skipped when cos_sin is NULL);
+ *     caches[l][s / block_size, h, s % block_size, 0:64]   = key
+ *     caches[l][s / block_size, h, s % block_size, 64:128] = v[l, t, h, :]
+ *   No other cache element is written.
+ *
+ *   k, v          bf16 views [L, >=rows, H, 64]: element (l, t, h, e) at
+ *                 base + l*layer_stride + t*row_stride + h*64 + e; 4-byte
+ *                 aligned, strides even and >= 0.  For a projection output
+ *                 kv [L, T, 2*H*64]: k = kv, v = kv + 64*H, row stride
+ *                 128*H, layer stride T*128*H.
+ *   positions     int64 [rows] (read only with cos_sin), 8-byte aligned
+ *   slots         host array of L device pointers to int64 [rows]; NULL
+ *                 entries skip their layer
+ *   cos_sin       bf16 [max_position, 64] (cos in 0..31, sin in 32..63) or NULL
+ *   caches        host array of L device pointers to contiguous bf16
+ *                 [num_blocks, H, block_size, 128], 4-byte aligned
+ *   num_blocks, block_size   >= 1, num_blocks*block_size < 2^31
+ *   H             KV heads: 1, 2, 4, 8, 16 or 32
+ *   L             1 <= L <= 4096; layers go to the GPU 8 per launch
+ *   rows          rows to insert, 0 <= rows < 2^31 (0: nothing launched)
+ *   err           device int32 counter, incremented once per skipped
+ *                 (row, layer) as above; may be NULL
+ * Two non-negative slots of one layer that are equal write the same cache
+ * entry in an unspecified order (a precondition violation).
+ */
+rc_status rc_kv_store(const uint16_t *k, const uint16_t *v,
+                      int64_t k_layer_stride, int64_t k_row_stride,
+                      int64_t v_layer_stride, int64_t v_row_stride,
+                      const int64_t *positions, const int64_t *const *slots,
+                      const uint16_t *cos_sin, int64_t max_position,
+                      uint16_t *const *caches, int32_t num_blocks,
+                      int32_t block_size, int32_t H, int32_t L, float eps,
+                      int64_t rows, int32_t *err, cudaStream_t stream);
+
+/* Sticky fault bits raised on the device by the projection kernel when one
+   of its bounded waits gives up (bit 0: load pipeline, bit 1: tensor-core
+   pipeline, bit 2: accumulator, bit 3: drain).  A kernel that sees a raised
+   bit skips its work, so after a fault every projection is wrong until the
+   bits are cleared.  Reads (and with clear != 0 resets) the bits of the
+   current device; synchronises the device.  No page counterpart. */
+rc_status rc_read_device_faults(uint32_t *flags, int32_t clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROPE_CHAIN_H */

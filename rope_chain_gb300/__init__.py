@@ -1,0 +1,212 @@
+"""rope_chain_gb300: the speculative draft's context K/V chain on GB300.
+
+A thin ctypes binding of librope_chain.so (include/rope_chain.h).  It only
+marshals torch CUDA tensors into pointers, sizes and the current stream;
+every step of the chain runs in the library's CUDA kernels.  There is no CPU
+path: if the library is missing, every call raises.
+
+    normed = context_norms(x, hidden_w, pre_w, L, eps)          # [L, T, 8192]
+    kv     = kv_project(normed, W)                              # [L, T, 128*H]
+    kv_store_from_projection(kv, H, positions, slots, cos_sin, caches, eps)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "librope_chain.so")
+
+RC_OK, RC_ERR_INVALID_ARG, RC_ERR_UNSUPPORTED, RC_ERR_CUDA = 0, 1, 2, 3
+RC_W_KN, RC_W_NK = 0, 1
+HEAD_DIM = 64
+MAX_LAYERS_PER_LAUNCH = 8
+
+
+class RopeChainError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"status {status}: {message}")
+        self.status = status
+
+
+_lib = None
+_c = ctypes
+_vp = ctypes.c_void_p
+
+SIGNATURES = {
+    "rc_last_error": ([], _c.c_char_p),
+    "rc_version": ([], _c.c_int32),
+    "rc_context_norms": ([_vp, _c.c_int64, _c.c_int32, _vp, _vp, _c.c_int32, _c.c_float, _vp, _vp],
+                         _c.c_int),
+    "rc_kv_project": ([_vp, _vp, _c.c_int32, _vp, _c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32,
+                       _vp, _c.c_size_t, _vp], _c.c_int),
+    "rc_kv_project_workspace_size": ([_c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32], _c.c_size_t),
+    "rc_kv_store": ([_vp, _vp, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _vp,
+                     _c.POINTER(_vp), _vp, _c.c_int64, _c.POINTER(_vp), _c.c_int32, _c.c_int32,
+                     _c.c_int32, _c.c_int32, _c.c_float, _c.c_int64, _vp, _vp], _c.c_int),
+    "rc_read_device_faults": ([_c.POINTER(_c.c_uint32), _c.c_int32], _c.c_int),
+}
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != RC_OK:
+        raise RopeChainError(status, lib().rc_last_error().decode())
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _bf16(t: torch.Tensor, name: str) -> None:
+    if t.dtype != torch.bfloat16 or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA bfloat16 tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# ------------------------------------------------------------------- calls
+
+def context_norms(x: torch.Tensor, hidden_w: Optional[torch.Tensor],
+                  pre_w: Optional[torch.Tensor], L: int, eps: float,
+                  out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """bf16 [L, T, 8192] = stack_l(pre_norm_l(bf16(hidden_norm(x))))."""
+    _bf16(x, "x")
+    T, D = x.shape
+    if out is None:
+        out = torch.empty((L, T, D), dtype=torch.bfloat16, device=x.device)
+    _bf16(out, "out")
+    for w, n in ((hidden_w, "hidden_w"), (pre_w, "pre_w")):
+        if w is not None:
+            _bf16(w, n)
+    _check(lib().rc_context_norms(x.data_ptr(), T, D, _ptr(hidden_w), _ptr(pre_w), L, eps,
+                                  out.data_ptr(), _stream(stream)))
+    return out
+
+
+def workspace_size(L: int, T: int, D: int, N: int) -> int:
+    """Bytes of split-K scratch rc_kv_project uses for these sizes (0: none)."""
+    return int(lib().rc_kv_project_workspace_size(L, T, D, N))
+
+
+def kv_project(normed: torch.Tensor, W: torch.Tensor, out: Optional[torch.Tensor] = None,
+               w_layout: int = RC_W_KN, workspace: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+    """bf16 [L, T, N] = normed [L, T, D] x W, W [L, D, N] (RC_W_KN) or
+    [L, N, D] (RC_W_NK).  ``workspace`` (any dtype, contiguous) enables
+    split-K for small T; see workspace_size()."""
+    _bf16(normed, "normed")
+    _bf16(W, "W")
+    L, T, D = normed.shape
+    N = W.shape[2] if w_layout == RC_W_KN else W.shape[1]
+    if out is None:
+        out = torch.empty((L, T, N), dtype=torch.bfloat16, device=normed.device)
+    _bf16(out, "out")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        if not (workspace.is_cuda and workspace.is_contiguous()):
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check(lib().rc_kv_project(normed.data_ptr(), W.data_ptr(), w_layout, out.data_ptr(), L, T, D,
+                               N, ws_ptr, ws_bytes, _stream(stream)))
+    return out
+
+
+def kv_store(k: torch.Tensor, v: torch.Tensor, positions: Optional[torch.Tensor],
+             slots: Sequence[Optional[torch.Tensor]], cos_sin: Optional[torch.Tensor],
+             caches: Sequence[torch.Tensor], eps: float, rows: Optional[int] = None,
+             err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """K-norm, GPT-J RoPE (with ``cos_sin``) and paged insert.  ``k`` and
+    ``v`` are bf16 [L, T, H, 64] views (unit stride over the last two dims);
+    ``caches[l]`` bf16 [num_blocks, H, block_size, 128] contiguous;
+    ``slots[l]`` int64 [rows] or None; ``err`` an int32 [1] counter."""
+    L, T, H, hd = k.shape
+    if hd != HEAD_DIM or tuple(v.shape) != (L, T, H, hd):
+        raise ValueError("k and v must be [L, T, H, 64] views of one shape")
+    for t, n in ((k, "k"), (v, "v")):
+        if t.dtype != torch.bfloat16 or t.stride(3) != 1 or t.stride(2) != HEAD_DIM:
+            raise ValueError(f"{n} must be bf16 with strides (*, *, 64, 1)")
+    if len(slots) != L or len(caches) != L:
+        raise ValueError("slots and caches need one entry per layer")
+    nb, h_, bs, w_ = caches[0].shape
+    if h_ != H or w_ != 2 * HEAD_DIM:
+        raise ValueError("caches must be [num_blocks, H, block_size, 128]")
+    for c in caches:
+        _bf16(c, "cache")
+        if tuple(c.shape) != (nb, h_, bs, w_):
+            raise ValueError("all caches must have one shape")
+    for s in slots:
+        if s is not None and (s.dtype != torch.int64 or not s.is_contiguous() or not s.is_cuda):
+            raise ValueError("slots must be contiguous CUDA int64 tensors")
+    if rows is None:
+        first = next((s for s in slots if s is not None), None)
+        rows = 0 if first is None else first.shape[0]
+    for s in slots:
+        if s is not None and s.shape[0] < rows:
+            raise ValueError("every slot mapping needs at least `rows` entries")
+    if cos_sin is not None:
+        _bf16(cos_sin, "cos_sin")
+        if positions is None or positions.dtype != torch.int64 or not positions.is_contiguous():
+            raise ValueError("RoPE needs contiguous int64 positions")
+    slot_arr = (_vp * L)(*[_ptr(s) for s in slots])
+    cache_arr = (_vp * L)(*[c.data_ptr() for c in caches])
+    _check(lib().rc_kv_store(k.data_ptr(), v.data_ptr(), k.stride(0), k.stride(1), v.stride(0),
+                             v.stride(1), _ptr(positions), slot_arr, _ptr(cos_sin),
+                             0 if cos_sin is None else cos_sin.shape[0], cache_arr, nb, bs, H, L,
+                             eps, rows, _ptr(err), _stream(stream)))
+
+
+def split_kv(kv: torch.Tensor, H: int):
+    """K and V views of a projection output kv [L, T, 2*H*64]: K is the first
+    64H columns of each row, V the next 64H."""
+    L, T, N = kv.shape
+    v5 = kv.view(L, T, 2, H, HEAD_DIM)
+    return v5[:, :, 0], v5[:, :, 1]
+
+
+def kv_store_from_projection(kv: torch.Tensor, H: int, positions, slots, cos_sin, caches,
+                             eps: float, rows: Optional[int] = None, err=None, stream=None):
+    k, v = split_kv(kv, H)
+    kv_store(k, v, positions, slots, cos_sin, caches, eps, rows=rows, err=err, stream=stream)
+
+
+def context_kv_chain(x, hidden_w, pre_w, W, positions, slots, cos_sin, caches, eps, H,
+                     normed=None, kv=None, workspace=None, err=None, stream=None):
+    """The whole chain: norms, projection, store.  Intermediates may be
+    passed in to avoid allocation.  Returns (normed, kv)."""
+    L = len(caches)
+    normed = context_norms(x, hidden_w, pre_w, L, eps, out=normed, stream=stream)
+    kv = kv_project(normed, W, out=kv, workspace=workspace, stream=stream)
+    kv_store_from_projection(kv, H, positions, slots, cos_sin, caches, eps, err=err, stream=stream)
+    return normed, kv
+
+
+def read_device_faults(clear: bool = True) -> int:
+    """Sticky fault bits of the projection kernel's bounded waits (0: none)."""
+    f = ctypes.c_uint32(0)
+    _check(lib().rc_read_device_faults(ctypes.byref(f), 1 if clear else 0))
+    return int(f.value)

@@ -1,0 +1,138 @@
+// K1: the context norms (hidden RMSNorm -> bf16 -> each layer's input
+// RMSNorm, stacked to [L, T, 8192]).
+//
+// Page "vllm.models.muse_spark.nvidia.specialized_decode.cutedsl.draft.context",
+// _ContextNormsKernel: 256 threads per row, thread t holding the 16-byte
+// fragments at columns 8t + 2048k (k < 4), the hidden norm's output rounded
+// to bf16 before the layer norm reads it.  The pages launch one CTA per
+// (row, layer) and recompute the hidden norm L times; here one CTA handles a
+// row for all L layers: x is read once, both row sums are taken once (the
+// layer gains scale the norm's output, so the layer norm's inverse RMS is
+// the same for every layer), and only the per-layer scale and store repeat.
+//
+// Order of the sums (fixed, and the oracle's reading R1): each thread adds
+// its 32 squares in (k, i) order, each warp folds its 32 partials with an xor
+// butterfly, and the 8 warp sums are added left to right by every thread.
+#include "rc_internal.cuh"
+
+namespace rc {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kFrags = 4;             // 16-byte fragments per thread
+constexpr int kFragStride = 256;      // uint4 units between a thread's fragments
+
+__device__ __forceinline__ void unpack8(const uint4 &q, float *f) {
+    f[0] = bf16_lo(q.x); f[1] = bf16_hi(q.x);
+    f[2] = bf16_lo(q.y); f[3] = bf16_hi(q.y);
+    f[4] = bf16_lo(q.z); f[5] = bf16_hi(q.z);
+    f[6] = bf16_lo(q.w); f[7] = bf16_hi(q.w);
+}
+
+// Sum of squares of the row this CTA holds, in the documented order.
+__device__ __forceinline__ float row_sumsq(const float (&v)[32], float *sums, int warp, int lane) {
+    float p = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        p = __fadd_rn(p, __fmul_rn(v[i], v[i]));
+    p = warp_butterfly_sum(p);
+    if (lane == 0)
+        sums[warp] = p;
+    __syncthreads();
+    float s = sums[0];
+#pragma unroll
+    for (int w = 1; w < kThreads / 32; ++w)
+        s = __fadd_rn(s, sums[w]);
+    return s;
+}
+
+template <bool kHiddenW, bool kPreW>
+__global__ void __launch_bounds__(kThreads)
+k1_context_norms(const uint16_t *__restrict__ x, int64_t T,
+                 const uint16_t *__restrict__ hidden_w, const uint16_t *__restrict__ pre_w,
+                 int32_t L, float eps, uint16_t *__restrict__ out)
+{
+    __shared__ float sums[2][kThreads / 32];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t row = blockIdx.x;
+
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x) + row * (kHidden / 8);
+    uint4 q[kFrags];
+#pragma unroll
+    for (int k = 0; k < kFrags; ++k)
+        q[k] = __ldcs(xr + k * kFragStride + tid);          // read once: stream
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < kFrags; ++k)
+        unpack8(q[k], v + 8 * k);
+
+    // a1: hidden norm, rounded to bf16
+    const float r = inv_rms(row_sumsq(v, sums[0], warp, lane), 0x1p-13f, eps);
+    if (kHiddenW) {
+        const uint4 *g = reinterpret_cast<const uint4 *>(hidden_w);
+#pragma unroll
+        for (int k = 0; k < kFrags; ++k) {
+            float gf[8];
+            unpack8(__ldg(g + k * kFragStride + tid), gf);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                v[8 * k + i] = round_bf16(__fmul_rn(__fmul_rn(v[8 * k + i], r), gf[i]));
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            v[i] = round_bf16(__fmul_rn(v[i], r));
+    }
+
+    // a2: the layers' input norms share one inverse RMS
+    const float r2 = inv_rms(row_sumsq(v, sums[1], warp, lane), 0x1p-13f, eps);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        v[i] = __fmul_rn(v[i], r2);
+
+    for (int32_t l = 0; l < L; ++l) {
+        uint4 *o = reinterpret_cast<uint4 *>(out) + ((int64_t)l * T + row) * (kHidden / 8);
+        const uint4 *g = reinterpret_cast<const uint4 *>(pre_w) + (int64_t)l * (kHidden / 8);
+#pragma unroll
+        for (int k = 0; k < kFrags; ++k) {
+            float y[8];
+            if (kPreW) {
+                float gf[8];
+                unpack8(__ldg(g + k * kFragStride + tid), gf);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    y[i] = __fmul_rn(v[8 * k + i], gf[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    y[i] = v[8 * k + i];
+            }
+            uint4 w;
+            w.x = pack_bf16x2(y[0], y[1]);
+            w.y = pack_bf16x2(y[2], y[3]);
+            w.z = pack_bf16x2(y[4], y[5]);
+            w.w = pack_bf16x2(y[6], y[7]);
+            o[k * kFragStride + tid] = w;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_context_norms(const uint16_t *x, int64_t T, const uint16_t *hidden_w,
+                                 const uint16_t *pre_w, int32_t L, float eps,
+                                 uint16_t *out, cudaStream_t stream)
+{
+    const dim3 grid((unsigned)T), block(kThreads);
+    if (hidden_w && pre_w)
+        k1_context_norms<true, true><<<grid, block, 0, stream>>>(x, T, hidden_w, pre_w, L, eps, out);
+    else if (hidden_w)
+        k1_context_norms<true, false><<<grid, block, 0, stream>>>(x, T, hidden_w, pre_w, L, eps, out);
+    else if (pre_w)
+        k1_context_norms<false, true><<<grid, block, 0, stream>>>(x, T, hidden_w, pre_w, L, eps, out);
+    else
+        k1_context_norms<false, false><<<grid, block, 0, stream>>>(x, T, hidden_w, pre_w, L, eps, out);
+    return cudaGetLastError();
+}
+
+}  // namespace rc

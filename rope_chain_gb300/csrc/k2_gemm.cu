@@ -1,0 +1,515 @@
+// K2: the K/V projection out[l] = normed[l] x W[l] on the 5th-generation
+// tensor cores (tcgen05.mma kind::f16, BF16 in, FP32 accumulate in TMEM).
+//
+// Page "vllm.models.muse_spark.nvidia.specialized_decode.runtime.draft",
+// ContextKV._project: torch.bmm(per_layer [L, T, D], W^T) -> [L, T, 2*H*64].
+// The pages leave this GEMM to cuBLAS; this is a hand-written sm_103a
+// kernel instead.
+//
+// Design (one CTA per 128 x BN output tile of one layer and one K split):
+//   warp 0     one lane issues TMA tile loads (A: 128 rows x 64 K, B: 64 K x
+//              BN) into a STAGES-deep ring of 128-byte-swizzled smem stages;
+//   warp 1     allocates BN TMEM columns; one lane issues 4 MMAs of
+//              128 x BN x 16 per stage and commits each stage back to the
+//              loader, then commits the accumulator to the epilogue;
+//   warps 2-5  read the accumulator out of TMEM (warp w owns lanes
+//              32*(w%4) ...), round to bf16 (or keep FP32 partials for
+//              split-K) and store rows straight to global memory.
+// Every wait on an mbarrier is bounded by wall time; on timeout the kernel
+// raises a sticky fault bit, skips its remaining work, drains its own copies
+// and frees its TMEM.
+#include "rc_internal.cuh"
+
+#include <cuda.h>      // CUtensorMap and the tensor-map encoder's types
+#include <algorithm>
+#include <mutex>
+
+namespace rc {
+
+__device__ unsigned int g_project_faults;
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;                    // one 128-byte swizzle row of bf16
+constexpr int kThreads = 192;
+constexpr uint32_t kABytes = BM * BK * 2; // 16 KiB per stage
+constexpr unsigned long long kWaitNs = 1000000000ull;   // 1 s per wait
+
+enum : unsigned { kFaultLoad = 1u, kFaultMma = 2u, kFaultAccum = 4u, kFaultDrain = 8u };
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool faulted() {
+    return *reinterpret_cast<volatile unsigned int *>(&g_project_faults) != 0u;
+}
+
+__device__ __forceinline__ void raise_fault(unsigned bit) { atomicOr(&g_project_faults, bit); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0u;
+}
+
+// Wait for the phase with `parity` to complete; false after kWaitNs or when
+// another CTA has already raised a fault.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try(bar, parity))
+        return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try(bar, parity))
+            return true;
+        if ((it & 255u) == 0u && (faulted() || globaltimer() - t0 > kWaitNs))
+            return false;
+    }
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 family layout:
+// start >> 4 in bits 0-13, leading byte offset >> 4 in 16-29, stride byte
+// offset >> 4 in 32-45, version 1 at bit 46, swizzle mode 2 in bits 61-63).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: FP32 accumulator, BF16 A and B,
+// A K-major, B K-major or MN-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n, bool b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Same as mbar_wait but ignores other CTAs' faults: used to drain this
+// CTA's own copies and MMAs before it frees its smem and TMEM.
+__device__ __forceinline__ bool mbar_wait_own(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try(bar, parity))
+            return true;
+        if ((it & 255u) == 255u && globaltimer() - t0 > kWaitNs)
+            return false;
+    }
+}
+
+struct GemmArgs {
+    int32_t T, N, L;
+    int32_t kb_total, kb_per_split, splits;
+    uint16_t *out;       // bf16 [L, T, N] when splits == 1
+    float *partial;      // FP32 [splits, L, T, N] when splits > 1
+};
+
+template <int BN>
+struct Cfg {
+    static constexpr int kStages = BN == 256 ? 4 : 6;
+    static constexpr uint32_t kBBytes = BN * BK * 2;
+    static constexpr uint32_t kStageTx = kABytes + kBBytes;
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * (kABytes + kBBytes) + 256;
+};
+
+__device__ __forceinline__ uint32_t pack_acc(uint32_t a, uint32_t b) {
+    return pack_bf16x2(__uint_as_float(a), __uint_as_float(b));
+}
+
+template <int BN, bool kBmn>
+__global__ void __launch_bounds__(kThreads, 1)
+k2_project(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+           const GemmArgs g)
+{
+    using C = Cfg<BN>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sA = smem_u32(smem);
+    const uint32_t sB = sA + S * kABytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * (kABytes + C::kBBytes));
+    const uint32_t bar0 = smem_u32(bars);
+    const uint32_t accum = bar0 + 8u * (2 * S);
+    // words[0]: TMEM base address; words[1]: stages the MMA thread consumed
+    volatile uint32_t *words = reinterpret_cast<volatile uint32_t *>(bars + 2 * S + 1);
+
+    const int warp = __shfl_sync(0xFFFFFFFFu, (int)(threadIdx.x >> 5), 0);
+    const int lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * BN;
+    const int m0 = blockIdx.y * BM;
+    const int l = blockIdx.z / g.splits;
+    const int split = blockIdx.z - l * g.splits;
+    const int kb0 = split * g.kb_per_split;
+    const int nkb = min(g.kb_per_split, g.kb_total - kb0);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar0 + 8u * s, 1);          // full[s]: the loader's expect_tx
+            mbar_init(bar0 + 8u * (S + s), 1);    // empty[s]: the MMA thread's commit
+        }
+        mbar_init(accum, 1);
+        words[1] = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32((const void *)words)), "r"(BN) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = words[0];
+    const bool skip = faulted();
+
+    int issued = 0;
+    if (warp == 0) {
+        if (lane == 0 && !skip) {
+            for (int i = 0; i < nkb; ++i) {
+                const int s = i % S;
+                const uint32_t ph = (uint32_t)(i / S) & 1u;
+                if (!mbar_wait(bar0 + 8u * (S + s), ph ^ 1u)) {
+                    raise_fault(kFaultLoad);
+                    break;
+                }
+                const uint32_t full = bar0 + 8u * s;
+                mbar_expect_tx(full, C::kStageTx);
+                const int kc = (kb0 + i) * BK;
+                tma_load_3d(sA + s * kABytes, &tmA, kc, m0, l, full);
+                if (kBmn) {
+#pragma unroll
+                    for (int c = 0; c < BN / 64; ++c)
+                        tma_load_3d(sB + s * C::kBBytes + c * 8192u, &tmB, n0 + 64 * c, kc, l, full);
+                } else {
+                    tma_load_3d(sB + s * C::kBBytes, &tmB, kc, n0, l, full);
+                }
+                issued = i + 1;
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int consumed = 0;
+            if (!skip) {
+                constexpr uint32_t idesc = make_idesc(BM, BN, kBmn);
+                for (int i = 0; i < nkb; ++i) {
+                    const int s = i % S;
+                    const uint32_t ph = (uint32_t)(i / S) & 1u;
+                    if (!mbar_wait(bar0 + 8u * s, ph)) {
+                        raise_fault(kFaultMma);
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a = sA + s * kABytes, b = sB + s * C::kBBytes;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        // A: K-major, 8-row groups 1024 B apart; +32 B per 16 K.
+                        const uint64_t ad = smem_desc_sw128(a + 32u * kk, 16u, 1024u);
+                        // B: MN-major: 64-wide N chunks 8 KiB apart, 8-row K
+                        // groups 1024 B apart, +2 KiB per 16 K; K-major like A.
+                        const uint64_t bd = kBmn ? smem_desc_sw128(b + 2048u * kk, 8192u, 1024u)
+                                                 : smem_desc_sw128(b + 32u * kk, 16u, 1024u);
+                        mma_bf16(tmem, ad, bd, idesc, (i | kk) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar0 + 8u * (S + s));   // frees the stage when these MMAs finish
+                    consumed = i + 1;
+                }
+            }
+            words[1] = (uint32_t)consumed;
+            mma_commit(accum);                        // all MMAs issued above are done
+        }
+        __syncwarp();
+    } else {
+        const int q = warp & 3;                       // TMEM lane quadrant of this warp
+        bool ok = !skip && mbar_wait(accum, 0u);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok && !skip && lane == 0)
+            raise_fault(kFaultAccum);
+        if (ok) {
+            tc_fence_after();
+            const int row = m0 + 32 * q + lane;
+            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tbase + 32u * c, r);
+                if (row < g.T) {
+                    if (g.splits == 1) {
+                        uint4 *o = reinterpret_cast<uint4 *>(
+                            g.out + ((int64_t)l * g.T + row) * g.N + n0 + 32 * c);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            o[j] = make_uint4(pack_acc(r[8 * j], r[8 * j + 1]),
+                                              pack_acc(r[8 * j + 2], r[8 * j + 3]),
+                                              pack_acc(r[8 * j + 4], r[8 * j + 5]),
+                                              pack_acc(r[8 * j + 6], r[8 * j + 7]));
+                    } else {
+                        float4 *o = reinterpret_cast<float4 *>(
+                            g.partial + (((int64_t)split * g.L + l) * g.T + row) * g.N + n0 + 32 * c);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            o[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                               __uint_as_float(r[4 * j + 2]),
+                                               __uint_as_float(r[4 * j + 3]));
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0 && lane == 0) {
+        // Loads issued but never consumed exist only after a fault: wait for
+        // them to land before the CTA's shared memory goes away.
+        for (int i = (int)words[1]; i < issued; ++i)
+            if (!mbar_wait_own(bar0 + 8u * (i % S), (uint32_t)(i / S) & 1u)) {
+                raise_fault(kFaultDrain);
+                break;
+            }
+    }
+    if (warp == 1) {
+        if (lane == 0 && !mbar_wait_own(accum, 0u))
+            raise_fault(kFaultDrain);
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BN)
+                     : "memory");
+    }
+}
+
+// out = bf16(sum over splits of the FP32 partials), added in split order.
+__global__ void __launch_bounds__(256)
+k2_splitk_reduce(const float *__restrict__ partial, uint16_t *__restrict__ out, int64_t count,
+                 int splits)
+{
+    const int64_t n8 = count / 8;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const float4 *p = reinterpret_cast<const float4 *>(partial) + 2 * i;
+        float4 a = __ldcs(p), b = __ldcs(p + 1);
+        for (int s = 1; s < splits; ++s) {
+            const float4 *q = p + (int64_t)s * (count / 4);
+            const float4 c = __ldcs(q), d = __ldcs(q + 1);
+            a.x = __fadd_rn(a.x, c.x); a.y = __fadd_rn(a.y, c.y);
+            a.z = __fadd_rn(a.z, c.z); a.w = __fadd_rn(a.w, c.w);
+            b.x = __fadd_rn(b.x, d.x); b.y = __fadd_rn(b.y, d.y);
+            b.z = __fadd_rn(b.z, d.z); b.w = __fadd_rn(b.w, d.w);
+        }
+        reinterpret_cast<uint4 *>(out)[i] =
+            make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                       pack_bf16x2(b.z, b.w));
+    }
+}
+
+// ------------------------------------------------------------------ host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// A rank-3 bf16 tensor map, innermost dimension first, 128-byte swizzle.
+bool make_map(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+              uint32_t box0, uint32_t box1) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};   // bytes, dims 1 and 2
+    const cuuint32_t box[3] = {box0, box1, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, bool kBmn>
+cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &g,
+                        int n_tiles, int m_tiles, cudaStream_t stream) {
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(k2_project<BN, kBmn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)Cfg<BN>::kSmem);
+        if (e != cudaSuccess)
+            return e;
+        if (dev < 64)
+            configured[dev] = true;
+    }
+    const dim3 grid((unsigned)n_tiles, (unsigned)m_tiles, (unsigned)(g.L * g.splits));
+    k2_project<BN, kBmn><<<grid, kThreads, Cfg<BN>::kSmem, stream>>>(ma, mb, g);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+ProjectPlan plan_kv_project(int32_t L, int64_t T, int32_t D, int32_t N, int num_sms,
+                            size_t workspace_bytes)
+{
+    ProjectPlan p{};
+    p.bn = (N % 256 == 0) ? 256 : 128;
+    const int kb_total = D / BK;
+    const int64_t tiles = (int64_t)L * ((T + BM - 1) / BM) * (N / p.bn);
+    int splits = 1;
+    if (tiles < num_sms) {
+        splits = (int)(num_sms / tiles);
+        splits = std::min(splits, std::max(1, kb_total / 4));   // >= 4 K blocks per split
+    }
+    const size_t per_split = (size_t)L * (size_t)T * (size_t)N * sizeof(float);
+    while (splits > 1 && (size_t)splits * per_split > workspace_bytes)
+        --splits;
+    p.kb_per_split = (kb_total + splits - 1) / splits;
+    p.splits = (kb_total + p.kb_per_split - 1) / p.kb_per_split;   // no empty split
+    p.workspace = p.splits > 1 ? (size_t)p.splits * per_split : 0;
+    return p;
+}
+
+cudaError_t launch_kv_project(const uint16_t *normed, const uint16_t *W, bool w_nk, uint16_t *out,
+                              int32_t L, int64_t T, int32_t D, int32_t N, const ProjectPlan &plan,
+                              float *ws, cudaStream_t stream, const char **why)
+{
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, normed, (uint64_t)D, (uint64_t)T, (uint64_t)L, BK, BM)) {
+        *why = "tensor map of the normed rows could not be encoded";
+        return cudaErrorInvalidValue;
+    }
+    const bool ok_b = w_nk ? make_map(&mb, W, (uint64_t)D, (uint64_t)N, (uint64_t)L, BK, plan.bn)
+                           : make_map(&mb, W, (uint64_t)N, (uint64_t)D, (uint64_t)L, 64, BK);
+    if (!ok_b) {
+        *why = "tensor map of the weights could not be encoded";
+        return cudaErrorInvalidValue;
+    }
+    GemmArgs g;
+    g.T = (int32_t)T;
+    g.N = N;
+    g.L = L;
+    g.kb_total = D / BK;
+    g.kb_per_split = plan.kb_per_split;
+    g.splits = plan.splits;
+    g.out = out;
+    g.partial = ws;
+    const int n_tiles = N / plan.bn;
+    const int m_tiles = (int)((T + BM - 1) / BM);
+    cudaError_t e;
+    if (plan.bn == 256)
+        e = w_nk ? launch_tile<256, false>(ma, mb, g, n_tiles, m_tiles, stream)
+                 : launch_tile<256, true>(ma, mb, g, n_tiles, m_tiles, stream);
+    else
+        e = w_nk ? launch_tile<128, false>(ma, mb, g, n_tiles, m_tiles, stream)
+                 : launch_tile<128, true>(ma, mb, g, n_tiles, m_tiles, stream);
+    if (e != cudaSuccess || plan.splits == 1)
+        return e;
+    const int64_t count = (int64_t)L * T * N;
+    const int64_t blocks = std::min<int64_t>((count / 8 + 255) / 256, 152 * 16);
+    k2_splitk_reduce<<<(unsigned)blocks, 256, 0, stream>>>(ws, out, count, plan.splits);
+    return cudaGetLastError();
+}
+
+cudaError_t read_project_faults(uint32_t *flags, bool clear)
+{
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return e;
+    unsigned int v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_project_faults, sizeof v);
+    if (e != cudaSuccess)
+        return e;
+    *flags = v;
+    if (clear) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_project_faults, &zero, sizeof zero);
+    }
+    return e;
+}
+
+}  // namespace rc

@@ -1,0 +1,129 @@
+// K3: K-norm, GPT-J RoPE and the paged insert of K and V.
+//
+// Page "vllm.models.muse_spark.nvidia.specialized_decode.cutedsl.draft.context",
+// _ContextKvStoreKernel / _sum_squares_64 / _rope: one warp per (row, layer),
+// lane j holding the GPT-J pair (2j, 2j+1) of every head, the head's sum of
+// squares folded as even squares and odd squares separately by an xor
+// butterfly, then even + odd; the normed key rounded to bf16; the rotation
+// (fma(x, c, -(y*s)), fma(y, c, x*s)); K and V written as 4-byte words, so
+// each warp store covers 128 contiguous bytes of one head.
+//
+// Differences from the pages' kernel: 8 warps (rows) per CTA instead of one;
+// the slot is read first and a skipped row reads nothing else; a slot past
+// the cache or a position past the table skips the row and counts it in the
+// caller's error word instead of writing out of bounds.
+#include "rc_internal.cuh"
+
+namespace rc {
+namespace {
+
+constexpr int kWarps = 8;
+
+__device__ __forceinline__ void count_skip(int32_t *err, int lane) {
+    if (err != nullptr && lane == 0)
+        atomicAdd(err, 1);
+}
+
+template <int H, bool kRope>
+__global__ void __launch_bounds__(kWarps * 32)
+k3_kv_store(const __grid_constant__ StoreLaunch p)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * kWarps + warp;
+    const int layer = blockIdx.y;
+    if (row >= p.rows)
+        return;
+    const int64_t *slots = p.slots[layer];
+    if (slots == nullptr)
+        return;
+    const int64_t slot = __ldg(slots + row);
+    if (slot < 0)
+        return;
+    if (slot >= p.capacity) {
+        count_skip(p.err, lane);
+        return;
+    }
+    int64_t pos = 0;
+    if (kRope) {
+        pos = __ldg(p.positions + row);
+        if (pos < 0 || pos >= p.max_position) {
+            count_skip(p.err, lane);
+            return;
+        }
+    }
+
+    const uint32_t *kr = reinterpret_cast<const uint32_t *>(
+        p.k + (int64_t)layer * p.k_layer_stride + row * p.k_row_stride) + lane;
+    const uint32_t *vr = reinterpret_cast<const uint32_t *>(
+        p.v + (int64_t)layer * p.v_layer_stride + row * p.v_row_stride) + lane;
+    uint32_t kw[H], vw[H];
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+        kw[h] = __ldcs(kr + h * (kHeadDim / 2));
+        vw[h] = __ldcs(vr + h * (kHeadDim / 2));
+    }
+    float c = 1.0f, s = 0.0f;
+    if (kRope) {
+        const unsigned short *cs = reinterpret_cast<const unsigned short *>(p.cos_sin) + pos * kHeadDim;
+        c = __uint_as_float((uint32_t)__ldg(cs + lane) << 16);
+        s = __uint_as_float((uint32_t)__ldg(cs + kHeadDim / 2 + lane) << 16);
+    }
+
+    uint32_t ko[H];
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+        const float k0 = bf16_lo(kw[h]), k1 = bf16_hi(kw[h]);
+        const float even = warp_butterfly_sum(__fmul_rn(k0, k0));
+        const float odd = warp_butterfly_sum(__fmul_rn(k1, k1));
+        const float r = inv_rms(__fadd_rn(even, odd), 0x1p-6f, p.eps);
+        float n0 = round_bf16(__fmul_rn(k0, r));
+        float n1 = round_bf16(__fmul_rn(k1, r));
+        if (kRope) {
+            const float x = __fmaf_rn(n0, c, -__fmul_rn(n1, s));
+            const float y = __fmaf_rn(n1, c, __fmul_rn(n0, s));
+            n0 = x;
+            n1 = y;
+        }
+        ko[h] = pack_bf16x2(n0, n1);
+    }
+
+    // Slots of a cache fit 32 bits (checked on the host).
+    const uint32_t bs = (uint32_t)p.block_size;
+    const uint32_t blk = (uint32_t)slot / bs;
+    const uint32_t page = (uint32_t)slot - blk * bs;
+    uint32_t *dst = reinterpret_cast<uint32_t *>(p.caches[layer]) +
+                    (((int64_t)blk * H) * bs + page) * kHeadDim + lane;
+    const int64_t head_stride = (int64_t)bs * kHeadDim;      // in 4-byte words
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+        dst[h * head_stride] = ko[h];
+        dst[h * head_stride + kHeadDim / 2] = vw[h];          // V follows K
+    }
+}
+
+template <int H>
+cudaError_t launch_h(const StoreLaunch &p, int32_t layers, cudaStream_t stream) {
+    const dim3 grid((unsigned)((p.rows + kWarps - 1) / kWarps), (unsigned)layers);
+    if (p.cos_sin)
+        k3_kv_store<H, true><<<grid, kWarps * 32, 0, stream>>>(p);
+    else
+        k3_kv_store<H, false><<<grid, kWarps * 32, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_kv_store(const StoreLaunch &p, int32_t H, int32_t layers, cudaStream_t stream)
+{
+    switch (H) {
+    case 1: return launch_h<1>(p, layers, stream);
+    case 2: return launch_h<2>(p, layers, stream);
+    case 4: return launch_h<4>(p, layers, stream);
+    case 8: return launch_h<8>(p, layers, stream);
+    case 16: return launch_h<16>(p, layers, stream);
+    case 32: return launch_h<32>(p, layers, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace rc

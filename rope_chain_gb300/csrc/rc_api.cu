@@ -1,0 +1,234 @@
+// The C ABI of librope_chain.so (declared in include/rope_chain.h): argument
+// checks on the host, then launches on the caller's stream.  Nothing here
+// allocates device memory or synchronises, except rc_read_device_faults.
+#include "rope_chain.h"
+#include "rc_internal.cuh"
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+rc_status fail(rc_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+rc_status ok() {
+    g_err[0] = '\0';
+    return RC_OK;
+}
+
+rc_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(RC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+int num_sms_current() {
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 0;
+    if (dev < 64 && cache[dev])
+        return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    if (dev < 64)
+        cache[dev] = n;
+    return n;
+}
+
+constexpr int64_t kMaxProjectRows = 65535LL * 128;
+
+rc_status check_project_sizes(int32_t L, int64_t T, int32_t D, int32_t N) {
+    if (L < 1 || L > 4096)
+        return fail(RC_ERR_INVALID_ARG, "rc_kv_project: L=%d outside [1, 4096]", L);
+    if (T < 0 || T > kMaxProjectRows)
+        return fail(RC_ERR_INVALID_ARG, "rc_kv_project: T=%lld outside [0, %lld]", (long long)T,
+                    (long long)kMaxProjectRows);
+    if (D < 64 || D % 64 != 0)
+        return fail(RC_ERR_UNSUPPORTED, "rc_kv_project: D=%d is not a positive multiple of 64", D);
+    if (N < 128 || N % 128 != 0)
+        return fail(RC_ERR_UNSUPPORTED, "rc_kv_project: N=%d is not a positive multiple of 128", N);
+    return RC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *rc_last_error(void) { return g_err; }
+
+int32_t rc_version(void) { return 100; }
+
+rc_status rc_context_norms(const uint16_t *x, int64_t T, int32_t D, const uint16_t *hidden_w,
+                           const uint16_t *pre_w, int32_t L, float eps, uint16_t *out,
+                           cudaStream_t stream)
+{
+    if (D != rc::kHidden)
+        return fail(RC_ERR_UNSUPPORTED, "rc_context_norms: D=%d, the row norm takes D=8192", D);
+    if (T < 0 || T > 0x7FFFFFFFLL)
+        return fail(RC_ERR_INVALID_ARG, "rc_context_norms: T=%lld outside [0, 2^31)", (long long)T);
+    if (L < 1 || L > 64)
+        return fail(RC_ERR_INVALID_ARG, "rc_context_norms: L=%d outside [1, 64]", L);
+    if (!x || !out)
+        return fail(RC_ERR_INVALID_ARG, "rc_context_norms: x and out must not be NULL");
+    if (!aligned(x, 16) || !aligned(out, 16) || (hidden_w && !aligned(hidden_w, 16)) ||
+        (pre_w && !aligned(pre_w, 16)))
+        return fail(RC_ERR_INVALID_ARG, "rc_context_norms: x, out and weights must be 16-byte aligned");
+    const size_t xbytes = (size_t)T * D * 2, obytes = (size_t)L * T * D * 2;
+    if (T > 0 && overlap(x, xbytes, out, obytes))
+        return fail(RC_ERR_INVALID_ARG, "rc_context_norms: out overlaps x");
+    if (T == 0)
+        return ok();
+    const cudaError_t e = rc::launch_context_norms(x, T, hidden_w, pre_w, L, eps, out, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "rc_context_norms launch");
+    return ok();
+}
+
+size_t rc_kv_project_workspace_size(int32_t L, int64_t T, int32_t D, int32_t N)
+{
+    if (check_project_sizes(L, T, D, N) != RC_OK || T == 0)
+        return 0;
+    const int sms = num_sms_current();
+    if (sms <= 0)
+        return 0;
+    return rc::plan_kv_project(L, T, D, N, sms, SIZE_MAX).workspace;
+}
+
+rc_status rc_kv_project(const uint16_t *normed, const uint16_t *W, int32_t w_layout, uint16_t *out,
+                        int32_t L, int64_t T, int32_t D, int32_t N, void *workspace,
+                        size_t workspace_bytes, cudaStream_t stream)
+{
+    const rc_status s = check_project_sizes(L, T, D, N);
+    if (s != RC_OK)
+        return s;
+    if (w_layout != RC_W_KN && w_layout != RC_W_NK)
+        return fail(RC_ERR_INVALID_ARG, "rc_kv_project: unknown weight layout %d", w_layout);
+    if (!normed || !W || !out)
+        return fail(RC_ERR_INVALID_ARG, "rc_kv_project: normed, W and out must not be NULL");
+    if (!aligned(normed, 16) || !aligned(W, 16) || !aligned(out, 16) ||
+        (workspace && !aligned(workspace, 16)))
+        return fail(RC_ERR_INVALID_ARG, "rc_kv_project: operands must be 16-byte aligned");
+    if (T == 0)
+        return ok();
+    const size_t obytes = (size_t)L * T * N * 2;
+    if (overlap(out, obytes, normed, (size_t)L * T * D * 2) ||
+        overlap(out, obytes, W, (size_t)L * D * N * 2))
+        return fail(RC_ERR_INVALID_ARG, "rc_kv_project: out overlaps an input");
+    const int sms = num_sms_current();
+    if (sms <= 0)
+        return fail(RC_ERR_CUDA, "rc_kv_project: no current CUDA device");
+    const rc::ProjectPlan plan =
+        rc::plan_kv_project(L, T, D, N, sms, workspace ? workspace_bytes : 0);
+    if (plan.splits > 1 && overlap(workspace, plan.workspace, out, obytes))
+        return fail(RC_ERR_INVALID_ARG, "rc_kv_project: workspace overlaps out");
+    const char *why = "launch";
+    const cudaError_t e = rc::launch_kv_project(normed, W, w_layout == RC_W_NK, out, L, T, D, N,
+                                                plan, static_cast<float *>(workspace), stream, &why);
+    if (e != cudaSuccess)
+        return cuda_fail(e, why);
+    return ok();
+}
+
+rc_status rc_kv_store(const uint16_t *k, const uint16_t *v, int64_t k_layer_stride,
+                      int64_t k_row_stride, int64_t v_layer_stride, int64_t v_row_stride,
+                      const int64_t *positions, const int64_t *const *slots,
+                      const uint16_t *cos_sin, int64_t max_position, uint16_t *const *caches,
+                      int32_t num_blocks, int32_t block_size, int32_t H, int32_t L, float eps,
+                      int64_t rows, int32_t *err, cudaStream_t stream)
+{
+    if (H != 1 && H != 2 && H != 4 && H != 8 && H != 16 && H != 32)
+        return fail(RC_ERR_UNSUPPORTED, "rc_kv_store: H=%d is not a power of two <= 32", H);
+    if (L < 1 || L > 4096)
+        return fail(RC_ERR_INVALID_ARG, "rc_kv_store: L=%d outside [1, 4096]", L);
+    if (rows < 0 || rows > 0x7FFFFFFFLL)
+        return fail(RC_ERR_INVALID_ARG, "rc_kv_store: rows=%lld outside [0, 2^31)", (long long)rows);
+    if (num_blocks < 1 || block_size < 1 || (int64_t)num_blocks * block_size >= (1LL << 31))
+        return fail(RC_ERR_INVALID_ARG,
+                    "rc_kv_store: need num_blocks, block_size >= 1 and num_blocks*block_size < 2^31");
+    if (!k || !v || !slots || !caches)
+        return fail(RC_ERR_INVALID_ARG, "rc_kv_store: k, v, slots and caches must not be NULL");
+    if (!aligned(k, 4) || !aligned(v, 4))
+        return fail(RC_ERR_INVALID_ARG, "rc_kv_store: k and v must be 4-byte aligned");
+    if (k_layer_stride < 0 || k_row_stride < 0 || v_layer_stride < 0 || v_row_stride < 0 ||
+        (k_layer_stride | k_row_stride | v_layer_stride | v_row_stride) & 1)
+        return fail(RC_ERR_INVALID_ARG, "rc_kv_store: strides must be even and non-negative");
+    if (cos_sin) {
+        if (!positions || !aligned(positions, 8))
+            return fail(RC_ERR_INVALID_ARG, "rc_kv_store: RoPE needs 8-byte aligned positions");
+        if (max_position < 1)
+            return fail(RC_ERR_INVALID_ARG, "rc_kv_store: max_position must be >= 1 with a table");
+        if (!aligned(cos_sin, 2))
+            return fail(RC_ERR_INVALID_ARG, "rc_kv_store: cos_sin must be 2-byte aligned");
+    }
+    for (int32_t l = 0; l < L; ++l) {
+        if (!slots[l])
+            continue;
+        if (!aligned(slots[l], 8))
+            return fail(RC_ERR_INVALID_ARG, "rc_kv_store: slots[%d] must be 8-byte aligned", l);
+        if (!caches[l] || !aligned(caches[l], 4))
+            return fail(RC_ERR_INVALID_ARG, "rc_kv_store: caches[%d] must be a 4-byte aligned pointer", l);
+    }
+    if (rows == 0)
+        return ok();
+
+    // Layers go to the GPU in chunks of at most 8 (the pointer tables are
+    // kernel parameters); a chunk whose layers all lack slots is skipped.
+    for (int32_t first = 0; first < L; first += rc::kMaxLayersPerLaunch) {
+        const int32_t n = std::min(rc::kMaxLayersPerLaunch, L - first);
+        rc::StoreLaunch p{};
+        bool any = false;
+        for (int32_t i = 0; i < n; ++i) {
+            p.slots[i] = slots[first + i];
+            p.caches[i] = caches[first + i];
+            any = any || p.slots[i] != nullptr;
+        }
+        if (!any)
+            continue;
+        p.k = k + first * k_layer_stride;
+        p.v = v + first * v_layer_stride;
+        p.k_layer_stride = k_layer_stride;
+        p.k_row_stride = k_row_stride;
+        p.v_layer_stride = v_layer_stride;
+        p.v_row_stride = v_row_stride;
+        p.positions = positions;
+        p.cos_sin = cos_sin;
+        p.max_position = max_position;
+        p.capacity = (int64_t)num_blocks * block_size;
+        p.block_size = block_size;
+        p.rows = (int32_t)rows;
+        p.eps = eps;
+        p.err = err;
+        const cudaError_t e = rc::launch_kv_store(p, H, n, stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "rc_kv_store launch");
+    }
+    return ok();
+}
+
+rc_status rc_read_device_faults(uint32_t *flags, int32_t clear)
+{
+    if (!flags)
+        return fail(RC_ERR_INVALID_ARG, "rc_read_device_faults: flags must not be NULL");
+    const cudaError_t e = rc::read_project_faults(flags, clear != 0);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "rc_read_device_faults");
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,93 @@
+// Internal declarations shared by the CUDA translation units of
+// librope_chain.so.  Nothing here is part of the public C ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace rc {
+
+constexpr int kHidden = 8192;        // row width of the context norms
+constexpr int kHeadDim = 64;         // key/value head width
+constexpr int kMaxLayersPerLaunch = 8;
+
+// ---------------------------------------------------------------- bf16
+
+// Exact widening of the low / high bf16 of a packed pair.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Round to nearest even to bf16 and back to float.
+__device__ __forceinline__ float round_bf16(float v) {
+    return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+// Pack two floats, each rounded to nearest even, lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&p);
+}
+
+// Inverse RMS of a row or head: 1 / sqrt(fma(sumsq, inv_width, eps)), each
+// step correctly rounded (IEEE sqrt and divide).
+__device__ __forceinline__ float inv_rms(float sumsq, float inv_width, float eps) {
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fmaf_rn(sumsq, inv_width, eps)));
+}
+
+// xor-butterfly sum over the 32 lanes of a warp (offsets 16, 8, 4, 2, 1).
+__device__ __forceinline__ float warp_butterfly_sum(float v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+        v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// ------------------------------------------------------------- launches
+
+// Norms: grid of T CTAs x 256 threads; returns the launch error.
+cudaError_t launch_context_norms(const uint16_t *x, int64_t T, const uint16_t *hidden_w,
+                                 const uint16_t *pre_w, int32_t L, float eps,
+                                 uint16_t *out, cudaStream_t stream);
+
+struct StoreLaunch {
+    const uint16_t *k;               // layer 0 of this chunk
+    const uint16_t *v;
+    int64_t k_layer_stride, k_row_stride, v_layer_stride, v_row_stride;   // elements
+    const int64_t *positions;
+    const uint16_t *cos_sin;
+    int64_t max_position;
+    const int64_t *slots[kMaxLayersPerLaunch];
+    uint16_t *caches[kMaxLayersPerLaunch];
+    int64_t capacity;                // num_blocks * block_size
+    int32_t block_size;
+    int32_t rows;
+    float eps;
+    int32_t *err;
+};
+
+// Store: one chunk of <= 8 layers; H in {1,2,4,8,16,32}.
+cudaError_t launch_kv_store(const StoreLaunch &p, int32_t H, int32_t layers,
+                            cudaStream_t stream);
+
+struct ProjectPlan {
+    int bn;                // 128 or 256
+    int splits;            // >= 1
+    int kb_per_split;      // 64-wide K blocks per split
+    size_t workspace;      // bytes of FP32 partials when splits > 1
+};
+
+// Choose tile width and split count for the device's SM count.
+ProjectPlan plan_kv_project(int32_t L, int64_t T, int32_t D, int32_t N, int num_sms,
+                            size_t workspace_bytes);
+
+// Projection; `ws` holds the FP32 partials when plan.splits > 1.
+cudaError_t launch_kv_project(const uint16_t *normed, const uint16_t *W, bool w_nk,
+                              uint16_t *out, int32_t L, int64_t T, int32_t D, int32_t N,
+                              const ProjectPlan &plan, float *ws, cudaStream_t stream,
+                              const char **why);
+
+// Sticky device fault bits of the projection kernel (current device).
+cudaError_t read_project_faults(uint32_t *flags, bool clear);
+
+}  // namespace rc
