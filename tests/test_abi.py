@@ -1,0 +1,119 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the
+header declares, and rejects malformed calls on the host before any CUDA
+call (so these run on a machine with no GPU at all)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import rope_chain_gb300 as rc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rope_chain.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from rope_chain_gb300 import _build
+    _build.build()
+    return rc.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rc_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_symbols_are_exported(lib):
+    names = declared_functions()
+    assert {"rc_context_norms", "rc_kv_project", "rc_kv_store", "rc_last_error"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(rc.SIGNATURES)
+
+
+def test_version(lib):
+    assert lib.rc_version() == 100
+
+
+def A(v):
+    """A fake, suitably aligned device address: never dereferenced, because
+    every call below is rejected (or is empty) before anything is launched."""
+    return ctypes.c_void_p(v)
+
+
+def last(lib):
+    return lib.rc_last_error().decode()
+
+
+def test_norms_rejections(lib):
+    x, o = 0x10000, 0x200000
+    assert lib.rc_context_norms(A(x), 4, 4096, None, None, 1, 1e-6, A(o), None) == rc.RC_ERR_UNSUPPORTED
+    assert "8192" in last(lib)
+    assert lib.rc_context_norms(None, 4, 8192, None, None, 1, 1e-6, A(o), None) == rc.RC_ERR_INVALID_ARG
+    assert lib.rc_context_norms(A(x + 2), 4, 8192, None, None, 1, 1e-6, A(o), None) == rc.RC_ERR_INVALID_ARG
+    assert "aligned" in last(lib)
+    assert lib.rc_context_norms(A(x), 4, 8192, A(0x8), None, 1, 1e-6, A(o), None) == rc.RC_ERR_INVALID_ARG
+    assert lib.rc_context_norms(A(x), 4, 8192, None, None, 0, 1e-6, A(o), None) == rc.RC_ERR_INVALID_ARG
+    assert lib.rc_context_norms(A(x), -1, 8192, None, None, 1, 1e-6, A(o), None) == rc.RC_ERR_INVALID_ARG
+    # out overlapping x
+    assert lib.rc_context_norms(A(x), 4, 8192, None, None, 1, 1e-6, A(x + 16), None) == rc.RC_ERR_INVALID_ARG
+    assert "overlaps" in last(lib)
+    # T == 0 launches nothing and succeeds
+    assert lib.rc_context_norms(A(x), 0, 8192, None, None, 2, 1e-6, A(o), None) == rc.RC_OK
+    assert last(lib) == ""
+
+
+def test_project_rejections(lib):
+    a, w, o = 0x100000, 0x4000000, 0x8000000
+    call = lambda *kw: lib.rc_kv_project(*kw)
+    assert call(A(a), A(w), 0, A(o), 1, 8, 8192, 100, None, 0, None) == rc.RC_ERR_UNSUPPORTED
+    assert call(A(a), A(w), 0, A(o), 1, 8, 8100, 1024, None, 0, None) == rc.RC_ERR_UNSUPPORTED
+    assert call(A(a), A(w), 2, A(o), 1, 8, 8192, 1024, None, 0, None) == rc.RC_ERR_INVALID_ARG
+    assert call(A(a), A(w), 0, A(o), 0, 8, 8192, 1024, None, 0, None) == rc.RC_ERR_INVALID_ARG
+    assert call(A(a), A(w), 0, A(o), 1, 65535 * 128 + 1, 8192, 1024, None, 0, None) == rc.RC_ERR_INVALID_ARG
+    assert call(A(a + 8), A(w), 0, A(o), 1, 8, 8192, 1024, None, 0, None) == rc.RC_ERR_INVALID_ARG
+    assert call(None, A(w), 0, A(o), 1, 8, 8192, 1024, None, 0, None) == rc.RC_ERR_INVALID_ARG
+    assert call(A(a), A(w), 0, A(o), 1, 0, 8192, 1024, None, 0, None) == rc.RC_OK
+    assert lib.rc_kv_project_workspace_size(1, 8, 8192, 100) == 0
+
+
+def _store(lib, **over):
+    arg = dict(k=A(0x1000), v=A(0x1080), kls=1024, krs=128, vls=1024, vrs=128, positions=A(0x4000),
+               slots=[A(0x8000)], cos=None, maxpos=0, caches=[A(0x100000)], nb=4, bs=16, H=8,
+               L=1, eps=1e-6, rows=4, err=None)
+    arg.update(over)
+    L = arg["L"]
+    slots = (ctypes.c_void_p * max(L, 1))(*arg["slots"][:L])
+    caches = (ctypes.c_void_p * max(L, 1))(*arg["caches"][:L])
+    return lib.rc_kv_store(arg["k"], arg["v"], arg["kls"], arg["krs"], arg["vls"], arg["vrs"],
+                           arg["positions"], slots, arg["cos"], arg["maxpos"], caches, arg["nb"],
+                           arg["bs"], arg["H"], L, arg["eps"], arg["rows"], arg["err"], None)
+
+
+def test_store_rejections(lib):
+    assert _store(lib, H=3) == rc.RC_ERR_UNSUPPORTED
+    assert _store(lib, H=64) == rc.RC_ERR_UNSUPPORTED
+    assert _store(lib, k=A(0x1002)) == rc.RC_ERR_INVALID_ARG
+    assert _store(lib, krs=127) == rc.RC_ERR_INVALID_ARG
+    assert _store(lib, vls=-2) == rc.RC_ERR_INVALID_ARG
+    assert _store(lib, nb=1 << 20, bs=1 << 11) == rc.RC_ERR_INVALID_ARG   # 2^31 slots
+    assert _store(lib, nb=0) == rc.RC_ERR_INVALID_ARG
+    assert _store(lib, rows=-1) == rc.RC_ERR_INVALID_ARG
+    assert _store(lib, cos=A(0x9000), maxpos=0) == rc.RC_ERR_INVALID_ARG
+    assert _store(lib, cos=A(0x9000), maxpos=16, positions=None) == rc.RC_ERR_INVALID_ARG
+    assert _store(lib, slots=[A(0x8004)]) == rc.RC_ERR_INVALID_ARG
+    assert _store(lib, caches=[None]) == rc.RC_ERR_INVALID_ARG
+    assert "caches[0]" in last(lib)
+    # a layer without slots needs no cache; rows == 0 launches nothing
+    assert _store(lib, slots=[None], caches=[None], rows=0) == rc.RC_OK
+    assert _store(lib, rows=0) == rc.RC_OK
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(rc, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(rc, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        rc.lib()
