@@ -1,0 +1,359 @@
+"""Benchmark of the context K/V chain (norms -> projection -> store).
+
+One step = one pass of the whole chain over one batch of context rows of a
+workload (default: workload 2, T=512 rows, L=3 layers, H=8 KV heads, RoPE),
+inputs resident in HBM.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I]
+  python bench.py --impl reference ...   # the CPU oracle as the reference arm
+
+Under torchrun (N > 1) every rank runs its own replica of the workload on
+its own GPU (the rows of different batches are independent: weak scaling,
+no collective on the data path); the timed region is bracketed by a barrier
+and a device synchronisation, and the slowest rank's time counts.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "context rows/s through norm+proj+store; norm/store HBM GB/s vs GB300 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20          # > 129 MB L2: written between timed steps
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic_counts(w, splits: int):
+    """Per-step algorithmic bytes / flops of each kernel ('Rooflines')."""
+    T, D, L, H, N = w.T, w.D, w.L, w.H, w.N
+    k1 = 2 * T * D * (1 + L) + 2 * D * ((1 if w.hidden_weighted else 0) + (L if w.pre_weighted else 0))
+    k2_flops = 2 * L * T * D * N
+    k2_bytes = 2 * (L * T * D + L * D * N + L * T * N)
+    return dict(k1_bytes=k1, k2_flops=k2_flops, k2_bytes=k2_bytes, splits=splits)
+
+
+def store_bytes(w, slots, rope: bool) -> int:
+    """K3: per (row, layer) 8 B of slot; a row whose slot is in range reads
+    K and V (256 H B), writes 256 H B to the cache, and with RoPE reads its
+    position (8 B) and 128 B of table."""
+    total = 0
+    cap = w.num_blocks * w.block_size
+    for s in slots:
+        live = int(((s >= 0) & (s < cap)).sum())
+        total += 8 * len(s) + live * (512 * w.H + (8 + 128 if rope else 0))
+    return total
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_chain_rows(case, w, R: int, threads: int = 0) -> float:
+    """The oracle's whole chain on the first R rows of a workload; seconds."""
+    import numpy as np
+    import oracle
+    x = np.ascontiguousarray(case["x"][:R])
+    slots = [np.ascontiguousarray(s[:R]) for s in case["slots"]]
+    caches = [np.zeros(case["cache_shape"], dtype=np.uint16) for _ in range(w.L)]
+    t0 = time.perf_counter()
+    normed = oracle.context_norms(x, case["hidden_w"], case["pre_w"], w.L, w.eps, threads=threads)
+    kv64, _ = oracle.kv_project(normed, case["W"], with_abs=False, threads=threads)
+    kv = oracle.bf16_rn_f64_array(kv64)
+    oracle.kv_store_from_projection(kv, w.H, case["positions"][:R], slots, case["cos_sin"], caches,
+                                    w.eps, R, threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_sample_rows(w) -> int:
+    return min(w.T, 256)
+
+
+def base_record(args, w, world):
+    return {"metric": METRIC, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, shapes of the workload)",
+            "config": {"workload": f"workload {w.index}: {w.describe()} ({w.label})",
+                       "T": w.T, "D": w.D, "L": w.L, "H": w.H, "N": w.N, "rope": w.rope,
+                       "eps": w.eps, "num_blocks": w.num_blocks, "block_size": w.block_size,
+                       "parallelism": f"replicas x{world} (rows independent, no collective)"}}
+
+
+def run_reference(args, w):
+    """The reference arm: the CPU oracle on the host cores (rank 0 only)."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import workloads
+    oracle.build()
+    case = workloads.make_inputs(w)
+    R = cpu_sample_rows(w)
+    cores = oracle.max_threads()
+    for _ in range(args.warmup):
+        oracle_chain_rows(case, w, R)
+    times = [oracle_chain_rows(case, w, R) for _ in range(args.steps)]
+    total = sum(times)
+    value = R * args.steps / total
+    rec = base_record(args, w, world)
+    rec.update({"impl": "reference", "value": value, "ms_per_step": 1e3 * total / args.steps,
+                "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                                 "sample": f"first {R} rows of the workload per step, whole chain"},
+                "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}})
+    rec["dtype"] = "f32 (f64 projection)"
+    print(json.dumps(rec))
+
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+    import rope_chain_gb300 as rc
+    import workloads
+    from rope_chain_gb300 import _build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0 or not os.path.exists(rc.LIB_PATH):
+        _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    rc.lib()
+
+    case = workloads.make_inputs(w)
+    bf = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    x, hw, pw, W, cs = bf(case["x"]), bf(case["hidden_w"]), bf(case["pre_w"]), bf(case["W"]), bf(case["cos_sin"])
+    positions = torch.from_numpy(case["positions"]).to(dev)
+    slots = [torch.from_numpy(s).to(dev) for s in case["slots"]]
+    caches = [torch.zeros(case["cache_shape"], dtype=torch.bfloat16, device=dev) for _ in range(w.L)]
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    normed = torch.empty((w.L, w.T, w.D), dtype=torch.bfloat16, device=dev)
+    kv = torch.empty((w.L, w.T, w.N), dtype=torch.bfloat16, device=dev)
+    ws_bytes = rc.workspace_size(w.L, w.T, w.D, w.N)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    launches_per_step = 1 + (2 if ws_bytes else 1) + (w.L + 7) // 8
+
+    def chain(ev=None):
+        if ev:
+            ev[0].record()
+        rc.context_norms(x, hw, pw, w.L, w.eps, out=normed)
+        if ev:
+            ev[1].record()
+        rc.kv_project(normed, W, out=kv, workspace=ws)
+        if ev:
+            ev[2].record()
+        rc.kv_store_from_projection(kv, w.H, positions, slots, cs, caches, w.eps, err=err)
+        if ev:
+            ev[3].record()
+
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        chain()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)            # L2 flushed before every timed step (not timed)
+        chain(evs[i])
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    k_ms = [[e[j].elapsed_time(e[j + 1]) for e in evs] for j in range(3)]
+    total_ms = max_over_ranks(sum(step_ms), world)
+    faults = rc.read_device_faults(clear=True)
+    if faults:
+        raise RuntimeError(f"projection kernel raised fault bits {faults:#x}")
+
+    # ---- end to end: pinned host inputs copied in, the status word read back
+    x_h = torch.from_numpy(case["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    pos_h = torch.from_numpy(case["positions"]).pin_memory()
+    slots_h = [torch.from_numpy(s).pin_memory() for s in case["slots"]]
+    err_h = torch.zeros(1, dtype=torch.int32).pin_memory()
+    h2d = x_h.numel() * 2 + pos_h.numel() * 8 + sum(s.numel() * 8 for s in slots_h)
+
+    def e2e_step(ev0, ev1):
+        ev0.record()
+        x.copy_(x_h, non_blocking=True)
+        positions.copy_(pos_h, non_blocking=True)
+        for d, h in zip(slots, slots_h):
+            d.copy_(h, non_blocking=True)
+        chain()
+        err_h.copy_(err, non_blocking=True)
+        ev1.record()
+
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        e2e_step(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    torch.cuda.synchronize()
+    e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e2e_step(*e2e_evs[i])
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_evs), world)
+
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    counts = algorithmic_counts(w, 2 if ws_bytes else 1)
+    k3_bytes = store_bytes(w, case["slots"], w.rope)
+    k1_us = 1e3 * statistics.mean(k_ms[0])
+    k2_us = 1e3 * statistics.mean(k_ms[1])
+    k3_us = 1e3 * statistics.mean(k_ms[2])
+    hbm = peaks["hbm_gbs"]
+    tc = peaks["bf16_tflops"]
+    kern = {
+        "norms": {"us": k1_us, "GB/s": counts["k1_bytes"] / k1_us / 1e3,
+                  "frac": counts["k1_bytes"] / k1_us / 1e3 / hbm, "bound": "hbm"},
+        "project": {"us": k2_us, "TFLOP/s": counts["k2_flops"] / k2_us / 1e6,
+                    "frac": counts["k2_flops"] / k2_us / 1e6 / tc, "bound": "tensor",
+                    "split_k_workspace_bytes": ws_bytes},
+        "store": {"us": k3_us, "GB/s": k3_bytes / k3_us / 1e3, "frac": k3_bytes / k3_us / 1e3 / hbm,
+                  "bound": "hbm"},
+    }
+    dominant = max(kern, key=lambda k: kern[k]["us"])
+    d = kern[dominant]
+    if d["bound"] == "tensor":
+        roof = {"kernel": dominant, "bound": "tensor", "achieved": d["TFLOP/s"], "peak": tc,
+                "unit": "TFLOP/s", "frac": d["frac"], "traffic": None,
+                "peak_source": f"bf16_tflops (burst) of {peak_src}"}
+    else:
+        roof = {"kernel": dominant, "bound": "hbm", "achieved": d["GB/s"], "peak": hbm,
+                "unit": "GB/s", "frac": d["frac"], "traffic": None,
+                "peak_source": f"hbm_gbs of {peak_src}"}
+    import oracle
+    oracle.build()
+    R = cpu_sample_rows(w)
+    cpu_s = oracle_chain_rows(case, w, R)
+    rec = base_record(args, w, world)
+    rec["config"]["l2"] = "flushed (512 MiB write) before every timed step"
+    rec.update({
+        "value": world * w.T * args.steps / (total_ms / 1e3),
+        "ms_per_step": total_ms / args.steps,
+        "roofline": roof,
+        "kernels": kern,
+        "cpu_baseline": {"value": R / cpu_s, "unit": "rows/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": f"first {R} rows of the workload, whole chain, once"},
+        "e2e": {"value": world * w.T * args.steps / (e2e_ms / 1e3), "unit": "rows/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    })
+    print(json.dumps(rec))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    import workloads
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()
