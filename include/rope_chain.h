@@ -170,6 +170,33 @@ rc_status rc_kv_store(const uint16_t *k, const uint16_t *v,
                       int32_t block_size, int32_t H, int32_t L, float eps,
                       int64_t rows, int32_t *err, cudaStream_t stream);
 
+/*
+ * rc_kv_project_no_alloc -- rc_kv_project for callers that cannot allocate.
+ * The pages have no counterpart: it is an addition of this library.
+ *
+ * Some callers cannot call cudaMalloc or provide a workspace (code running
+ * inside an allocator or memory-pool callback, plug-ins whose host framework
+ * owns every device allocation, serving paths that must not touch the
+ * allocator once running).  This call takes the same operands as
+ * rc_kv_project minus the workspace and allocates nothing: its split-K
+ * scratch is a 24 MiB array inside the library, held on every GPU that loads
+ * the library until the process exits.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Sizes whose split-K plan needs more than 24 MiB are refused with
+ *     RC_ERR_UNSUPPORTED (on a 152-SM GB300 no size needs more than 20 MB).
+ *   - All calls share the array and it keeps the last call's contents; two
+ *     calls whose work overlaps on the GPU (e.g. on different streams) race
+ *     on it, so order them on one stream.  Nothing in it needs clearing:
+ *     each call writes every partial it reads.
+ * Results equal rc_kv_project's with a full-size workspace.
+ */
+rc_status rc_kv_project_no_alloc(const uint16_t *normed, const uint16_t *W,
+                                 int32_t w_layout, uint16_t *out, int32_t L,
+                                 int64_t T, int32_t D, int32_t N,
+                                 cudaStream_t stream);
+
 /* Sticky fault bits raised on the device by the projection kernel when one
    of its bounded waits gives up (bit 0: load pipeline, bit 1: tensor-core
    pipeline, bit 2: accumulator, bit 3: drain).  A kernel that sees a raised

@@ -48,6 +48,8 @@ SIGNATURES = {
                      _c.POINTER(_vp), _vp, _c.c_int64, _c.POINTER(_vp), _c.c_int32, _c.c_int32,
                      _c.c_int32, _c.c_int32, _c.c_float, _c.c_int64, _vp, _vp], _c.c_int),
     "rc_read_device_faults": ([_c.POINTER(_c.c_uint32), _c.c_int32], _c.c_int),
+    "rc_kv_project_no_alloc": ([_vp, _vp, _c.c_int32, _vp, _c.c_int32, _c.c_int64, _c.c_int32,
+                                _c.c_int32, _vp], _c.c_int),
 }
 
 
@@ -133,6 +135,22 @@ def kv_project(normed: torch.Tensor, W: torch.Tensor, out: Optional[torch.Tensor
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     _check(lib().rc_kv_project(normed.data_ptr(), W.data_ptr(), w_layout, out.data_ptr(), L, T, D,
                                N, ws_ptr, ws_bytes, _stream(stream)))
+    return out
+
+
+def kv_project_no_alloc(normed: torch.Tensor, W: torch.Tensor, out: torch.Tensor,
+                        w_layout: int = RC_W_KN, stream=None) -> torch.Tensor:
+    """kv_project for callers that cannot allocate device memory: the split-K
+    scratch lives inside the library (24 MiB per GPU), ``out`` must be given,
+    and calls that overlap on the GPU must not be issued (they share the
+    scratch)."""
+    _bf16(normed, "normed")
+    _bf16(W, "W")
+    _bf16(out, "out")
+    L, T, D = normed.shape
+    N = W.shape[2] if w_layout == RC_W_KN else W.shape[1]
+    _check(lib().rc_kv_project_no_alloc(normed.data_ptr(), W.data_ptr(), w_layout,
+                                        out.data_ptr(), L, T, D, N, _stream(stream)))
     return out
 
 

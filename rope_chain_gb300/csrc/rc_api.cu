@@ -68,6 +68,10 @@ rc_status check_project_sizes(int32_t L, int64_t T, int32_t D, int32_t N) {
 
 }  // namespace
 
+namespace rc {
+void set_last_error(const char *msg) { snprintf(g_err, sizeof g_err, "%s", msg); }
+}  // namespace rc
+
 extern "C" {
 
 const char *rc_last_error(void) { return g_err; }

@@ -87,6 +87,9 @@ cudaError_t launch_kv_project(const uint16_t *normed, const uint16_t *W, bool w_
                               const ProjectPlan &plan, float *ws, cudaStream_t stream,
                               const char **why);
 
+// Sets the message rc_last_error() returns on this host thread.
+void set_last_error(const char *msg);
+
 // Sticky device fault bits of the projection kernel (current device).
 cudaError_t read_project_faults(uint32_t *flags, bool clear);
 
