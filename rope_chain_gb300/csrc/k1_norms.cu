@@ -29,12 +29,19 @@ __device__ __forceinline__ void unpack8(const uint4 &q, float *f) {
     f[6] = bf16_lo(q.w); f[7] = bf16_hi(q.w);
 }
 
-// Sum of squares of the row this CTA holds, in the documented order.
-__device__ __forceinline__ float row_sumsq(const float (&v)[32], float *sums, int warp, int lane) {
+// Sum of squares of the row this CTA holds (its 4 packed fragments per
+// thread), in the documented order.
+__device__ __forceinline__ float row_sumsq(const uint4 (&q)[kFrags], float *sums, int warp,
+                                           int lane) {
     float p = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-        p = __fadd_rn(p, __fmul_rn(v[i], v[i]));
+    for (int k = 0; k < kFrags; ++k) {
+        float f[8];
+        unpack8(q[k], f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            p = __fadd_rn(p, __fmul_rn(f[i], f[i]));
+    }
     p = warp_butterfly_sum(p);
     if (lane == 0)
         sums[warp] = p;
@@ -46,8 +53,17 @@ __device__ __forceinline__ float row_sumsq(const float (&v)[32], float *sums, in
     return s;
 }
 
+__device__ __forceinline__ uint4 pack8(const float *y) {
+    uint4 w;
+    w.x = pack_bf16x2(y[0], y[1]);
+    w.y = pack_bf16x2(y[2], y[3]);
+    w.z = pack_bf16x2(y[4], y[5]);
+    w.w = pack_bf16x2(y[6], y[7]);
+    return w;
+}
+
 template <bool kHiddenW, bool kPreW>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 k1_context_norms(const uint16_t *__restrict__ x, int64_t T,
                  const uint16_t *__restrict__ hidden_w, const uint16_t *__restrict__ pre_w,
                  int32_t L, float eps, uint16_t *__restrict__ out)
@@ -56,63 +72,68 @@ k1_context_norms(const uint16_t *__restrict__ x, int64_t T,
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t row = blockIdx.x;
 
+    // The row (read once: streaming) and the hidden gains (shared by all
+    // rows: cached) load together.
     const uint4 *xr = reinterpret_cast<const uint4 *>(x) + row * (kHidden / 8);
-    uint4 q[kFrags];
+    const uint4 *gh = reinterpret_cast<const uint4 *>(hidden_w);
+    const uint4 *gp = reinterpret_cast<const uint4 *>(pre_w);
+    uint4 q[kFrags], hq[kFrags], pq[kFrags];
 #pragma unroll
-    for (int k = 0; k < kFrags; ++k)
-        q[k] = __ldcs(xr + k * kFragStride + tid);          // read once: stream
-    float v[32];
-#pragma unroll
-    for (int k = 0; k < kFrags; ++k)
-        unpack8(q[k], v + 8 * k);
+    for (int k = 0; k < kFrags; ++k) {
+        q[k] = __ldcs(xr + k * kFragStride + tid);
+        if (kHiddenW)
+            hq[k] = __ldg(gh + k * kFragStride + tid);
+    }
 
-    // a1: hidden norm, rounded to bf16
-    const float r = inv_rms(row_sumsq(v, sums[0], warp, lane), 0x1p-13f, eps);
-    if (kHiddenW) {
-        const uint4 *g = reinterpret_cast<const uint4 *>(hidden_w);
+    // a1: hidden norm; z = bf16((x * r) * gamma) kept packed in q
+    const float r = inv_rms(row_sumsq(q, sums[0], warp, lane), 0x1p-13f, eps);
 #pragma unroll
-        for (int k = 0; k < kFrags; ++k) {
-            float gf[8];
-            unpack8(__ldg(g + k * kFragStride + tid), gf);
+    for (int k = 0; k < kFrags; ++k) {
+        float f[8];
+        unpack8(q[k], f);
+        if (kHiddenW) {
+            float g[8];
+            unpack8(hq[k], g);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                v[8 * k + i] = round_bf16(__fmul_rn(__fmul_rn(v[8 * k + i], r), gf[i]));
-        }
-    } else {
+                f[i] = __fmul_rn(__fmul_rn(f[i], r), g[i]);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            v[i] = round_bf16(__fmul_rn(v[i], r));
+            for (int i = 0; i < 8; ++i)
+                f[i] = __fmul_rn(f[i], r);
+        }
+        q[k] = pack8(f);
+    }
+
+    // Layer 0's gains load while the second row sum is reduced.
+    if (kPreW) {
+#pragma unroll
+        for (int k = 0; k < kFrags; ++k)
+            pq[k] = __ldg(gp + k * kFragStride + tid);
     }
 
     // a2: the layers' input norms share one inverse RMS
-    const float r2 = inv_rms(row_sumsq(v, sums[1], warp, lane), 0x1p-13f, eps);
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-        v[i] = __fmul_rn(v[i], r2);
-
+    const float r2 = inv_rms(row_sumsq(q, sums[1], warp, lane), 0x1p-13f, eps);
     for (int32_t l = 0; l < L; ++l) {
         uint4 *o = reinterpret_cast<uint4 *>(out) + ((int64_t)l * T + row) * (kHidden / 8);
-        const uint4 *g = reinterpret_cast<const uint4 *>(pre_w) + (int64_t)l * (kHidden / 8);
+        const uint4 *gn = gp + (int64_t)(l + 1) * (kHidden / 8);
 #pragma unroll
         for (int k = 0; k < kFrags; ++k) {
-            float y[8];
+            float f[8];
+            unpack8(q[k], f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                f[i] = __fmul_rn(f[i], r2);
             if (kPreW) {
-                float gf[8];
-                unpack8(__ldg(g + k * kFragStride + tid), gf);
+                float g[8];
+                unpack8(pq[k], g);
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    y[i] = __fmul_rn(v[8 * k + i], gf[i]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    y[i] = v[8 * k + i];
+                    f[i] = __fmul_rn(f[i], g[i]);
+                if (l + 1 < L)                   // this fragment's gains for the next layer
+                    pq[k] = __ldg(gn + k * kFragStride + tid);
             }
-            uint4 w;
-            w.x = pack_bf16x2(y[0], y[1]);
-            w.y = pack_bf16x2(y[2], y[3]);
-            w.z = pack_bf16x2(y[4], y[5]);
-            w.w = pack_bf16x2(y[6], y[7]);
-            o[k * kFragStride + tid] = w;
+            o[k * kFragStride + tid] = pack8(f);
         }
     }
 }

@@ -9,9 +9,8 @@
 // each warp store covers 128 contiguous bytes of one head.
 //
 // Differences from the pages' kernel: 8 warps (rows) per CTA instead of one;
-// the slot is read first and a skipped row reads nothing else; a slot past
-// the cache or a position past the table skips the row and counts it in the
-// caller's error word instead of writing out of bounds.
+// a slot past the cache or a position past the table skips the row and counts
+// it in the caller's error word instead of writing out of bounds.
 #include "rc_internal.cuh"
 
 namespace rc {
@@ -36,22 +35,11 @@ k3_kv_store(const __grid_constant__ StoreLaunch p)
     const int64_t *slots = p.slots[layer];
     if (slots == nullptr)
         return;
+    // Every load first, as the pages' kernel does: the slot, the position and
+    // the row's K and V words are independent, so their latencies overlap; a
+    // skipped row wastes its K/V reads but never writes.
     const int64_t slot = __ldg(slots + row);
-    if (slot < 0)
-        return;
-    if (slot >= p.capacity) {
-        count_skip(p.err, lane);
-        return;
-    }
-    int64_t pos = 0;
-    if (kRope) {
-        pos = __ldg(p.positions + row);
-        if (pos < 0 || pos >= p.max_position) {
-            count_skip(p.err, lane);
-            return;
-        }
-    }
-
+    const int64_t pos = kRope ? __ldg(p.positions + row) : 0;
     const uint32_t *kr = reinterpret_cast<const uint32_t *>(
         p.k + (int64_t)layer * p.k_layer_stride + row * p.k_row_stride) + lane;
     const uint32_t *vr = reinterpret_cast<const uint32_t *>(
@@ -61,6 +49,12 @@ k3_kv_store(const __grid_constant__ StoreLaunch p)
     for (int h = 0; h < H; ++h) {
         kw[h] = __ldcs(kr + h * (kHeadDim / 2));
         vw[h] = __ldcs(vr + h * (kHeadDim / 2));
+    }
+    if (slot < 0)
+        return;
+    if (slot >= p.capacity || (kRope && (pos < 0 || pos >= p.max_position))) {
+        count_skip(p.err, lane);
+        return;
     }
     float c = 1.0f, s = 0.0f;
     if (kRope) {
