@@ -373,6 +373,256 @@ k2_splitk_reduce(const float *__restrict__ partial, uint16_t *__restrict__ out, 
     }
 }
 
+// ------------------------------------------------------------- CTA pairs
+//
+// k2_project_pair: the same tile pipeline on a pair of CTAs (a cluster of 2
+// on neighbouring SMs) issuing tcgen05.mma.cta_group::2 with M = 256, N = 256.
+// CTA r of the pair stages A rows m0 + 128 r ... and B columns n0 + 128 r ...
+// (half of B each), so one 256 x 256 x 64 step moves 32 KiB into each SM
+// instead of the 48 KiB a single-CTA 128 x 256 tile needs, and 6 stages fit
+// where 4 did.  The leader (rank 0) waits for both CTAs' bytes on its own
+// barriers and issues the MMAs; commits arrive on both CTAs' barriers.  Each
+// CTA's TMEM holds the accumulator of its own 128 rows.
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(addr), "r"(rank));
+    return d;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// TMA load into this CTA's smem whose bytes are counted on `bar`, a barrier
+// of the pair's leader (a shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map, int c0,
+                                                 int c1, int c2, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on `bar` (same offset) in both CTAs of the pair once the MMAs
+// issued so far by this thread have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar), "h"((uint16_t)0x3) : "memory");
+}
+
+struct PairCfg {
+    static constexpr int kStages = 6;
+    static constexpr uint32_t kBHalf = 128 * BK * 2;            // 16 KiB of B per CTA
+    static constexpr uint32_t kStageBytes = kABytes + kBHalf;    // 32 KiB per CTA
+    static constexpr uint32_t kPairTx = 2 * kStageBytes;         // counted on the leader
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 256;
+};
+
+template <bool kBmn>
+__global__ void __launch_bounds__(kThreads, 1)
+k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmArgs g)
+{
+    using C = PairCfg;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sA = smem_u32(smem);
+    const uint32_t sB = sA + S * kABytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * C::kStageBytes);
+    const uint32_t bar0 = smem_u32(bars);         // full[s] (leader), empty[s], accum
+    const uint32_t accum = bar0 + 8u * (2 * S);
+    // words[0]: TMEM base; [1]: stages the leader's MMA thread consumed;
+    // [2]: skip flag (written by the leader into both CTAs); [3]: stages the
+    // peer's loader issued (written by the peer into the leader)
+    volatile uint32_t *words = reinterpret_cast<volatile uint32_t *>(bars + 2 * S + 1);
+    const uint32_t words_addr = smem_u32((const void *)words);
+
+    const int warp = __shfl_sync(0xFFFFFFFFu, (int)(threadIdx.x >> 5), 0);
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int n0 = (blockIdx.x >> 1) * 256;        // the pair's 256 output columns
+    const int m0 = blockIdx.y * 256 + 128 * (int)rank;   // this CTA's 128 rows
+    const int nb = n0 + 128 * (int)rank;           // this CTA's half of B
+    const int l = blockIdx.z / g.splits;
+    const int split = blockIdx.z - l * g.splits;
+    const int kb0 = split * g.kb_per_split;
+    const int nkb = min(g.kb_per_split, g.kb_total - kb0);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar0 + 8u * s, 1);
+            mbar_init(bar0 + 8u * (S + s), 1);
+        }
+        mbar_init(accum, 1);
+        words[1] = 0u;
+        words[3] = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+        if (leader) {
+            // One skip decision for the pair, written into both CTAs.
+            const uint32_t skip = faulted() ? 1u : 0u;
+            words[2] = skip;
+            st_cluster_u32(map_to_rank(words_addr + 8u, 1), skip);
+        }
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(words_addr), "r"(256) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    cluster_sync();                               // barriers, skip flag and TMEM pair-wide
+    tc_fence_after();
+    const uint32_t tmem = words[0];
+    const bool skip = words[2] != 0u;
+
+    int issued = 0;
+    if (warp == 0) {
+        if (lane == 0 && !skip) {
+            for (int i = 0; i < nkb; ++i) {
+                const int s = i % S;
+                const uint32_t ph = (uint32_t)(i / S) & 1u;
+                if (!mbar_wait(bar0 + 8u * (S + s), ph ^ 1u)) {
+                    raise_fault(kFaultLoad);
+                    break;
+                }
+                const uint32_t full = map_to_rank(bar0 + 8u * s, 0);
+                if (leader)
+                    mbar_expect_tx(bar0 + 8u * s, C::kPairTx);
+                const int kc = (kb0 + i) * BK;
+                tma_load_3d_pair(sA + s * kABytes, &tmA, kc, m0, l, full);
+                if (kBmn) {
+                    tma_load_3d_pair(sB + s * C::kBHalf, &tmB, nb, kc, l, full);
+                    tma_load_3d_pair(sB + s * C::kBHalf + 8192u, &tmB, nb + 64, kc, l, full);
+                } else {
+                    tma_load_3d_pair(sB + s * C::kBHalf, &tmB, kc, nb, l, full);
+                }
+                issued = i + 1;
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            int consumed = 0;
+            if (!skip) {
+                constexpr uint32_t idesc = make_idesc(256, 256, kBmn);
+                for (int i = 0; i < nkb; ++i) {
+                    const int s = i % S;
+                    const uint32_t ph = (uint32_t)(i / S) & 1u;
+                    if (!mbar_wait(bar0 + 8u * s, ph)) {
+                        raise_fault(kFaultMma);
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a = sA + s * kABytes, b = sB + s * C::kBHalf;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(a + 32u * kk, 16u, 1024u);
+                        const uint64_t bd = kBmn ? smem_desc_sw128(b + 2048u * kk, 8192u, 1024u)
+                                                 : smem_desc_sw128(b + 32u * kk, 16u, 1024u);
+                        mma_bf16_pair(tmem, ad, bd, idesc, (i | kk) != 0 ? 1u : 0u);
+                    }
+                    mma_commit_pair(bar0 + 8u * (S + s));
+                    consumed = i + 1;
+                }
+            }
+            words[1] = (uint32_t)consumed;
+            mma_commit_pair(accum);
+        }
+        __syncwarp();
+    } else {
+        const int q = warp & 3;
+        bool ok = !skip && mbar_wait(accum, 0u);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok && !skip && lane == 0)
+            raise_fault(kFaultAccum);
+        if (ok) {
+            tc_fence_after();
+            const int row = m0 + 32 * q + lane;
+            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16);
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tbase + 32u * c, r);
+                if (row < g.T) {
+                    if (g.splits == 1) {
+                        uint4 *o = reinterpret_cast<uint4 *>(
+                            g.out + ((int64_t)l * g.T + row) * g.N + n0 + 32 * c);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            o[j] = make_uint4(pack_acc(r[8 * j], r[8 * j + 1]),
+                                              pack_acc(r[8 * j + 2], r[8 * j + 3]),
+                                              pack_acc(r[8 * j + 4], r[8 * j + 5]),
+                                              pack_acc(r[8 * j + 6], r[8 * j + 7]));
+                    } else {
+                        float4 *o = reinterpret_cast<float4 *>(
+                            g.partial + (((int64_t)split * g.L + l) * g.T + row) * g.N + n0 + 32 * c);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            o[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                               __uint_as_float(r[4 * j + 2]),
+                                               __uint_as_float(r[4 * j + 3]));
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (!leader && warp == 0 && lane == 0)
+        st_cluster_u32(map_to_rank(words_addr + 12u, 0), (uint32_t)issued);
+    cluster_sync();
+    if (leader && warp == 0 && lane == 0) {
+        // Both CTAs' loads land on the leader's barriers: after a fault, wait
+        // for every stage either CTA issued before anyone frees smem.
+        const int last = max(issued, (int)words[3]);
+        for (int i = (int)words[1]; i < last; ++i)
+            if (!mbar_wait_own(bar0 + 8u * (i % S), (uint32_t)(i / S) & 1u)) {
+                raise_fault(kFaultDrain);
+                break;
+            }
+    }
+    if (leader && warp == 1 && lane == 0 && !mbar_wait_own(accum, 0u))
+        raise_fault(kFaultDrain);
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256)
+                     : "memory");
+    }
+}
+
 // ------------------------------------------------------------------ host
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -431,6 +681,40 @@ cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, const Gemm
     return cudaGetLastError();
 }
 
+template <bool kBmn>
+cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &g,
+                        int n_pairs, int m_pairs, cudaStream_t stream) {
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(k2_project_pair<kBmn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)PairCfg::kSmem);
+        if (e != cudaSuccess)
+            return e;
+        if (dev < 64)
+            configured[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * n_pairs), (unsigned)m_pairs, (unsigned)(g.L * g.splits));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = PairCfg::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k2_project_pair<kBmn>, ma, mb, g);
+    if (e != cudaSuccess)
+        return e;
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 ProjectPlan plan_kv_project(int32_t L, int64_t T, int32_t D, int32_t N, int num_sms,
@@ -438,8 +722,11 @@ ProjectPlan plan_kv_project(int32_t L, int64_t T, int32_t D, int32_t N, int num_
 {
     ProjectPlan p{};
     p.bn = (N % 256 == 0) ? 256 : 128;
+    // CTA pairs need two 128-row halves with work and 256-wide N tiles.
+    p.pair = p.bn == 256 && T > BM;
     const int kb_total = D / BK;
-    const int64_t tiles = (int64_t)L * ((T + BM - 1) / BM) * (N / p.bn);
+    const int64_t tiles = p.pair ? 2 * (int64_t)L * ((T + 255) / 256) * (N / 256)
+                                 : (int64_t)L * ((T + BM - 1) / BM) * (N / p.bn);
     int splits = 1;
     if (tiles < num_sms) {
         splits = (int)(num_sms / tiles);
@@ -463,7 +750,8 @@ cudaError_t launch_kv_project(const uint16_t *normed, const uint16_t *W, bool w_
         *why = "tensor map of the normed rows could not be encoded";
         return cudaErrorInvalidValue;
     }
-    const bool ok_b = w_nk ? make_map(&mb, W, (uint64_t)D, (uint64_t)N, (uint64_t)L, BK, plan.bn)
+    const uint32_t b_rows = plan.pair ? 128u : (uint32_t)plan.bn;   // K-major B rows per CTA
+    const bool ok_b = w_nk ? make_map(&mb, W, (uint64_t)D, (uint64_t)N, (uint64_t)L, BK, b_rows)
                            : make_map(&mb, W, (uint64_t)N, (uint64_t)D, (uint64_t)L, 64, BK);
     if (!ok_b) {
         *why = "tensor map of the weights could not be encoded";
@@ -481,7 +769,10 @@ cudaError_t launch_kv_project(const uint16_t *normed, const uint16_t *W, bool w_
     const int n_tiles = N / plan.bn;
     const int m_tiles = (int)((T + BM - 1) / BM);
     cudaError_t e;
-    if (plan.bn == 256)
+    if (plan.pair)
+        e = w_nk ? launch_pair<false>(ma, mb, g, N / 256, (int)((T + 255) / 256), stream)
+                 : launch_pair<true>(ma, mb, g, N / 256, (int)((T + 255) / 256), stream);
+    else if (plan.bn == 256)
         e = w_nk ? launch_tile<256, false>(ma, mb, g, n_tiles, m_tiles, stream)
                  : launch_tile<256, true>(ma, mb, g, n_tiles, m_tiles, stream);
     else

@@ -71,6 +71,7 @@ cudaError_t launch_kv_store(const StoreLaunch &p, int32_t H, int32_t layers,
                             cudaStream_t stream);
 
 struct ProjectPlan {
+    bool pair;             // CTA pairs (cta_group::2, 256 x 256 tiles)
     int bn;                // 128 or 256
     int splits;            // >= 1
     int kb_per_split;      // 64-wide K blocks per split
