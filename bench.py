@@ -214,6 +214,7 @@ def run_ours(args, w):
     ws_bytes = rc.workspace_size(w.L, w.T, w.D, w.N)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    # K1 + K2 (+ the split-K reduce when it splits) + K3 (8 layers per launch)
     launches_per_step = 1 + (2 if ws_bytes else 1) + (w.L + 7) // 8
 
     def chain(ev=None):

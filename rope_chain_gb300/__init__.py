@@ -115,12 +115,18 @@ def workspace_size(L: int, T: int, D: int, N: int) -> int:
     return int(lib().rc_kv_project_workspace_size(L, T, D, N))
 
 
+def new_workspace(L: int, T: int, D: int, N: int, device) -> Optional[torch.Tensor]:
+    """A split-K workspace for these sizes (None when not needed)."""
+    n = workspace_size(L, T, D, N)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
 def kv_project(normed: torch.Tensor, W: torch.Tensor, out: Optional[torch.Tensor] = None,
                w_layout: int = RC_W_KN, workspace: Optional[torch.Tensor] = None,
                stream=None) -> torch.Tensor:
     """bf16 [L, T, N] = normed [L, T, D] x W, W [L, D, N] (RC_W_KN) or
-    [L, N, D] (RC_W_NK).  ``workspace`` (any dtype, contiguous) enables
-    split-K for small T; see workspace_size()."""
+    [L, N, D] (RC_W_NK).  ``workspace`` (any dtype, contiguous; see
+    new_workspace() and workspace_size()) enables split-K for small T."""
     _bf16(normed, "normed")
     _bf16(W, "W")
     L, T, D = normed.shape

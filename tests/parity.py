@@ -82,7 +82,7 @@ def run_gpu_chain(case: dict, dev, *, w_layout: int = rc.RC_W_KN, use_workspace:
     if use_workspace:
         nbytes = rc.workspace_size(L, T, 8192, N)
         if nbytes:
-            ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
     normed = rc.context_norms(x, hw, pw, L, case["eps"])
     kv = rc.kv_project(normed, Wd, w_layout=w_layout, workspace=ws)
     rc.kv_store_from_projection(kv, H, positions, slots, cs, caches, case["eps"], err=err)

@@ -94,10 +94,31 @@ def test_projection_within_two_ulp(T, L, D, H, layout, split):
     ws = None
     if split:
         nbytes = rc.workspace_size(L, T, D, N)
-        ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=DEV)
+        ws = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=DEV)
     out = rc.kv_project(bits_to_dev(a), bits_to_dev(Wl), w_layout=layout, workspace=ws)
     ref, ab = oracle.kv_project(a, W)
     parity.assert_projection_close(parity.host_bits(out), ref, ab)
+
+
+@pytest.mark.parametrize("L,T,H,layout", [(3, 100, 1, rc.RC_W_KN),    # single CTA, workspace
+                                           (3, 512, 8, rc.RC_W_NK),    # CTA pairs, cluster split-K
+                                           (1, 64, 8, rc.RC_W_KN)])    # single CTA, 32 splits
+def test_projection_repeated_calls_identical(L, T, H, layout):
+    # one workspace (when the plan uses one), three calls in a row: identical
+    # results within the 2-ulp rule, i.e. nothing a call leaves behind
+    # changes the next one
+    rng = np.random.default_rng(21 + T)
+    D, N = 8192, 128 * H
+    a = workloads.normal_bf16(rng, (L, T, D), 0.0, 1.0)
+    W = workloads.normal_bf16(rng, (L, D, N), 0.0, 0.02)
+    Wl = W if layout == rc.RC_W_KN else np.ascontiguousarray(W.transpose(0, 2, 1))
+    ws = rc.new_workspace(L, T, D, N, DEV)
+    a_d, w_d = bits_to_dev(a), bits_to_dev(Wl)
+    ref, ab = oracle.kv_project(a, W)
+    outs = [parity.host_bits(rc.kv_project(a_d, w_d, w_layout=layout, workspace=ws))
+            for _ in range(3)]
+    parity.assert_projection_close(outs[0], ref, ab)
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
 
 
 def test_projection_one_hot_is_exact():
@@ -113,7 +134,7 @@ def test_projection_one_hot_is_exact():
     for layout in (rc.RC_W_KN, rc.RC_W_NK):
         Wl = W if layout == rc.RC_W_KN else np.ascontiguousarray(W.transpose(0, 2, 1))
         nbytes = rc.workspace_size(L, T, D, N)
-        ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=DEV)
+        ws = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=DEV)
         out = parity.host_bits(rc.kv_project(bits_to_dev(a), bits_to_dev(Wl), w_layout=layout,
                                              workspace=ws))
         for l in range(L):

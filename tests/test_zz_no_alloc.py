@@ -29,6 +29,7 @@ def built():
 
 
 @pytest.mark.parametrize("L,T,D,H,layout", [(3, 512, 8192, 8, rc.RC_W_KN),
+                                            (3, 128, 8192, 8, rc.RC_W_KN),
                                             (1, 64, 8192, 8, rc.RC_W_KN),
                                             (2, 100, 1024, 1, rc.RC_W_NK)])
 def test_no_alloc_matches_workspace_path_twice(L, T, D, H, layout):
@@ -40,7 +41,7 @@ def test_no_alloc_matches_workspace_path_twice(L, T, D, H, layout):
     a_d, w_d = parity.dev_bf16(a, DEV), parity.dev_bf16(Wl, DEV)
     nbytes = rc.workspace_size(L, T, D, N)
     assert nbytes > 0, "this shape should split K"
-    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
     ref = rc.kv_project(a_d, w_d, w_layout=layout, workspace=ws)
     torch.cuda.synchronize()
     ref_bits = parity.host_bits(ref)
