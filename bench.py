@@ -217,14 +217,17 @@ def run_ours(args, w):
     # K1 + K2 (+ the split-K reduce when it splits) + K3 (8 layers per launch)
     launches_per_step = 1 + (2 if ws_bytes else 1) + (w.L + 7) // 8
 
-    def chain(ev=None):
+    def chain(ev=None, per_kernel=False):
+        # ev[0] / ev[3] bracket the step; with per_kernel, ev[1] / ev[2] split
+        # it per call (an event between two kernels also stops the second
+        # from launching early, so the timed steps use step events only)
         if ev:
             ev[0].record()
         rc.context_norms(x, hw, pw, w.L, w.eps, out=normed)
-        if ev:
+        if ev and per_kernel:
             ev[1].record()
         rc.kv_project(normed, W, out=kv, workspace=ws)
-        if ev:
+        if ev and per_kernel:
             ev[2].record()
         rc.kv_store_from_projection(kv, w.H, positions, slots, cs, caches, w.eps, err=err)
         if ev:
@@ -240,23 +243,28 @@ def run_ours(args, w):
     # graphs (older torch) the steps are launched eagerly instead.
     timing = "cuda graph"
     try:
-        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
-               for _ in range(args.steps)]
+        make_event = lambda: torch.cuda.Event(enable_timing=True, external=True)
+        make_event()
     except TypeError:
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        make_event = lambda: torch.cuda.Event(enable_timing=True)
         timing = "eager"
+    evs = [[make_event() for _ in range(4)] for _ in range(args.steps)]
+    kevs = [[make_event() for _ in range(4)] for _ in range(args.steps)]
 
-    def timed_steps():
+    def steps(events, per_kernel):
         for i in range(args.steps):
             flush.fill_(i & 0xFF)            # L2 flushed before every timed step (not timed)
-            chain(evs[i])
+            chain(events[i], per_kernel)
 
-    graph = None
+    graphs = None
     if timing == "cuda graph":
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            timed_steps()
-        graph.replay()                       # warm the graph itself
+        graphs = []
+        for events, per_kernel in ((evs, False), (kevs, True)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                steps(events, per_kernel)
+            g.replay()                       # warm the graph itself
+            graphs.append(g)
         torch.cuda.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
@@ -264,16 +272,23 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    if graph is not None:
-        graph.replay()
+    if graphs:
+        graphs[0].replay()                   # the timed K steps
     else:
-        timed_steps()
+        steps(evs, False)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
+    # per-kernel breakdown (for the roofline): the same K steps with an event
+    # between consecutive calls, replayed after the timed region
+    if graphs:
+        graphs[1].replay()
+    else:
+        steps(kevs, True)
+    torch.cuda.synchronize()
     step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    k_ms = [[e[j].elapsed_time(e[j + 1]) for e in evs] for j in range(3)]
+    k_ms = [[e[j].elapsed_time(e[j + 1]) for e in kevs] for j in range(3)]
     total_ms = max_over_ranks(sum(step_ms), world)
     faults = rc.read_device_faults(clear=True)
     if faults:

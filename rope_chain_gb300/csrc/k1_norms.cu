@@ -71,6 +71,8 @@ k1_context_norms(const uint16_t *__restrict__ x, int64_t T,
     __shared__ float sums[2][kThreads / 32];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t row = blockIdx.x;
+    pdl_trigger();
+    pdl_wait();
 
     // The row (read once: streaming) and the hidden gains (shared by all
     // rows: cached) load together.
@@ -146,14 +148,12 @@ cudaError_t launch_context_norms(const uint16_t *x, int64_t T, const uint16_t *h
 {
     const dim3 grid((unsigned)T), block(kThreads);
     if (hidden_w && pre_w)
-        k1_context_norms<true, true><<<grid, block, 0, stream>>>(x, T, hidden_w, pre_w, L, eps, out);
-    else if (hidden_w)
-        k1_context_norms<true, false><<<grid, block, 0, stream>>>(x, T, hidden_w, pre_w, L, eps, out);
-    else if (pre_w)
-        k1_context_norms<false, true><<<grid, block, 0, stream>>>(x, T, hidden_w, pre_w, L, eps, out);
-    else
-        k1_context_norms<false, false><<<grid, block, 0, stream>>>(x, T, hidden_w, pre_w, L, eps, out);
-    return cudaGetLastError();
+        return launch_pdl(k1_context_norms<true, true>, grid, block, 0, stream, 1, x, T, hidden_w, pre_w, L, eps, out);
+    if (hidden_w)
+        return launch_pdl(k1_context_norms<true, false>, grid, block, 0, stream, 1, x, T, hidden_w, pre_w, L, eps, out);
+    if (pre_w)
+        return launch_pdl(k1_context_norms<false, true>, grid, block, 0, stream, 1, x, T, hidden_w, pre_w, L, eps, out);
+    return launch_pdl(k1_context_norms<false, false>, grid, block, 0, stream, 1, x, T, hidden_w, pre_w, L, eps, out);
 }
 
 }  // namespace rc

@@ -211,6 +211,7 @@ k2_project(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     const int split = blockIdx.z - l * g.splits;
     const int kb0 = split * g.kb_per_split;
     const int nkb = min(g.kb_per_split, g.kb_total - kb0);
+    pdl_trigger();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -232,6 +233,7 @@ k2_project(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = words[0];
+    pdl_wait();                                   // the previous kernel's writes are visible
     const bool skip = faulted();
 
     int issued = 0;
@@ -355,6 +357,8 @@ k2_splitk_reduce(const float *__restrict__ partial, uint16_t *__restrict__ out, 
                  int splits)
 {
     const int64_t n8 = count / 8;
+    pdl_trigger();
+    pdl_wait();
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
          i += (int64_t)gridDim.x * blockDim.x) {
         const float4 *p = reinterpret_cast<const float4 *>(partial) + 2 * i;
@@ -475,6 +479,7 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const int split = blockIdx.z - l * g.splits;
     const int kb0 = split * g.kb_per_split;
     const int nkb = min(g.kb_per_split, g.kb_total - kb0);
+    pdl_trigger();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -488,7 +493,9 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
         if (leader) {
-            // One skip decision for the pair, written into both CTAs.
+            // One skip decision for the pair, written into both CTAs.  Read
+            // before pdl_wait: a fault raised by a projection still finishing
+            // just before this one can be missed, and this one then runs.
             const uint32_t skip = faulted() ? 1u : 0u;
             words[2] = skip;
             st_cluster_u32(map_to_rank(words_addr + 8u, 1), skip);
@@ -504,6 +511,7 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = words[0];
     const bool skip = words[2] != 0u;
+    pdl_wait();                                   // the previous kernel's writes are visible
 
     int issued = 0;
     if (warp == 0) {
@@ -677,8 +685,7 @@ cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, const Gemm
             configured[dev] = true;
     }
     const dim3 grid((unsigned)n_tiles, (unsigned)m_tiles, (unsigned)(g.L * g.splits));
-    k2_project<BN, kBmn><<<grid, kThreads, Cfg<BN>::kSmem, stream>>>(ma, mb, g);
-    return cudaGetLastError();
+    return launch_pdl(k2_project<BN, kBmn>, grid, dim3(kThreads), Cfg<BN>::kSmem, stream, 1, ma, mb, g);
 }
 
 template <bool kBmn>
@@ -697,22 +704,8 @@ cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const Gemm
         if (dev < 64)
             configured[dev] = true;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(2 * n_pairs), (unsigned)m_pairs, (unsigned)(g.L * g.splits));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = PairCfg::kSmem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, k2_project_pair<kBmn>, ma, mb, g);
-    if (e != cudaSuccess)
-        return e;
-    return cudaGetLastError();
+    const dim3 grid((unsigned)(2 * n_pairs), (unsigned)m_pairs, (unsigned)(g.L * g.splits));
+    return launch_pdl(k2_project_pair<kBmn>, grid, dim3(kThreads), PairCfg::kSmem, stream, 2, ma, mb, g);
 }
 
 }  // namespace
@@ -782,8 +775,8 @@ cudaError_t launch_kv_project(const uint16_t *normed, const uint16_t *W, bool w_
         return e;
     const int64_t count = (int64_t)L * T * N;
     const int64_t blocks = std::min<int64_t>((count / 8 + 255) / 256, 152 * 16);
-    k2_splitk_reduce<<<(unsigned)blocks, 256, 0, stream>>>(ws, out, count, plan.splits);
-    return cudaGetLastError();
+    return launch_pdl(k2_splitk_reduce, dim3((unsigned)blocks), dim3(256), 0, stream, 1,
+                      static_cast<const float *>(ws), out, count, (int)plan.splits);
 }
 
 cudaError_t read_project_faults(uint32_t *flags, bool clear)

@@ -30,6 +30,8 @@ k3_kv_store(const __grid_constant__ StoreLaunch p)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * kWarps + warp;
     const int layer = blockIdx.y;
+    pdl_trigger();
+    pdl_wait();
     if (row >= p.rows)
         return;
     const int64_t *slots = p.slots[layer];
@@ -99,10 +101,8 @@ template <int H>
 cudaError_t launch_h(const StoreLaunch &p, int32_t layers, cudaStream_t stream) {
     const dim3 grid((unsigned)((p.rows + kWarps - 1) / kWarps), (unsigned)layers);
     if (p.cos_sin)
-        k3_kv_store<H, true><<<grid, kWarps * 32, 0, stream>>>(p);
-    else
-        k3_kv_store<H, false><<<grid, kWarps * 32, 0, stream>>>(p);
-    return cudaGetLastError();
+        return launch_pdl(k3_kv_store<H, true>, grid, dim3(kWarps * 32), 0, stream, 1, p);
+    return launch_pdl(k3_kv_store<H, false>, grid, dim3(kWarps * 32), 0, stream, 1, p);
 }
 
 }  // namespace

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -41,6 +42,47 @@ __device__ __forceinline__ float warp_butterfly_sum(float v) {
     for (int o = 16; o >= 1; o >>= 1)
         v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
     return v;
+}
+
+// ------------------------------------------------- programmatic launches
+//
+// Every kernel of the library is launched with programmatic stream
+// serialization: it may start while the previous kernel on the stream is
+// finishing.  Each kernel lets its own dependents launch as soon as it starts
+// (pdl_trigger) and touches no global memory before pdl_wait, which returns
+// once the previous kernel has completed and its writes are visible; so only
+// launch latency and prologue work (barrier set-up, TMEM allocation) overlap.
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// cudaLaunchKernelEx with programmatic stream serialization and, when
+// cluster_x > 1, a (cluster_x, 1, 1) cluster.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, unsigned cluster_x, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    unsigned n = 1;
+    if (cluster_x > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = cluster_x;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        n = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // ------------------------------------------------------------- launches
