@@ -171,6 +171,42 @@ rc_status rc_kv_store(const uint16_t *k, const uint16_t *v,
                       int64_t rows, int32_t *err, cudaStream_t stream);
 
 /*
+ * rc_kv_project_store -- steps 3 and 4 fused (the projection and the store
+ * of [rt] ContextKV.store in one pass; the scope's "store fused into the
+ * GEMM epilogue").  The caches receive exactly the bits that
+ *   rc_kv_project(normed, W, w_layout, kv, ...) followed by
+ *   rc_kv_store(k = kv, v = kv + 64*H, row stride 128*H, layer stride
+ *               T*128*H, positions, slots, cos_sin, caches, ..., rows, err)
+ * would write with the same workspace, without the [L, T, 128*H] round trip:
+ * the key is normed from the bf16-rounded projection exactly as
+ * rc_kv_store norms it.  Where the projection is not split, CTA-pair tiles
+ * store from the GEMM epilogue; split plans store from the pass that adds
+ * the FP32 partials.
+ *
+ *   normed, W, w_layout, D        as rc_kv_project; N = 128*H
+ *   L                             1 <= L <= 64 (one launch for all layers)
+ *   T                             rows of the projection, as rc_kv_project
+ *   positions, slots, cos_sin, max_position, caches, num_blocks,
+ *   block_size, H, eps, err       as rc_kv_store (caches and cos_sin
+ *                                 16-byte aligned)
+ *   rows                          rows stored, 0 <= rows <= T
+ *   kv_out                        optional bf16 [L, T, 128*H]: also write the
+ *                                 projection; required when the plan neither
+ *                                 splits nor uses CTA pairs (T <= 128 or
+ *                                 N = 128, without a workspace)
+ *   workspace                     as rc_kv_project
+ */
+rc_status rc_kv_project_store(const uint16_t *normed, const uint16_t *W,
+                              int32_t w_layout, int32_t L, int64_t T, int32_t D,
+                              int32_t H, const int64_t *positions,
+                              const int64_t *const *slots,
+                              const uint16_t *cos_sin, int64_t max_position,
+                              uint16_t *const *caches, int32_t num_blocks,
+                              int32_t block_size, float eps, int64_t rows,
+                              int32_t *err, uint16_t *kv_out, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * rc_kv_project_no_alloc -- rc_kv_project for callers that cannot allocate.
  * The pages have no counterpart: it is an addition of this library.
  *

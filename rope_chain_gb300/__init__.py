@@ -50,6 +50,10 @@ SIGNATURES = {
     "rc_read_device_faults": ([_c.POINTER(_c.c_uint32), _c.c_int32], _c.c_int),
     "rc_kv_project_no_alloc": ([_vp, _vp, _c.c_int32, _vp, _c.c_int32, _c.c_int64, _c.c_int32,
                                 _c.c_int32, _vp], _c.c_int),
+    "rc_kv_project_store": ([_vp, _vp, _c.c_int32, _c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32,
+                             _vp, _c.POINTER(_vp), _vp, _c.c_int64, _c.POINTER(_vp), _c.c_int32,
+                             _c.c_int32, _c.c_float, _c.c_int64, _vp, _vp, _vp, _c.c_size_t, _vp],
+                            _c.c_int),
 }
 
 
@@ -202,6 +206,51 @@ def kv_store(k: torch.Tensor, v: torch.Tensor, positions: Optional[torch.Tensor]
                              v.stride(1), _ptr(positions), slot_arr, _ptr(cos_sin),
                              0 if cos_sin is None else cos_sin.shape[0], cache_arr, nb, bs, H, L,
                              eps, rows, _ptr(err), _stream(stream)))
+
+
+def kv_project_store(normed: torch.Tensor, W: torch.Tensor, H: int, positions, slots,
+                     cos_sin, caches, eps: float, rows: Optional[int] = None, err=None,
+                     kv_out: Optional[torch.Tensor] = None, w_layout: int = RC_W_KN,
+                     workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Projection and store in one pass (rc_kv_project_store): the caches get
+    the bits kv_project + kv_store_from_projection would write."""
+    _bf16(normed, "normed")
+    _bf16(W, "W")
+    L, T, D = normed.shape
+    if len(slots) != L or len(caches) != L:
+        raise ValueError("slots and caches need one entry per layer")
+    nb, h_, bs, w_ = caches[0].shape
+    if h_ != H or w_ != 2 * HEAD_DIM:
+        raise ValueError("caches must be [num_blocks, H, block_size, 128]")
+    for c in caches:
+        _bf16(c, "cache")
+        if tuple(c.shape) != (nb, h_, bs, w_):
+            raise ValueError("all caches must have one shape")
+    for sl in slots:
+        if sl is not None and (sl.dtype != torch.int64 or not sl.is_contiguous() or not sl.is_cuda):
+            raise ValueError("slots must be contiguous CUDA int64 tensors")
+    if rows is None:
+        first = next((sl for sl in slots if sl is not None), None)
+        rows = 0 if first is None else first.shape[0]
+    for sl in slots:
+        if sl is not None and sl.shape[0] < rows:
+            raise ValueError("every slot mapping needs at least `rows` entries")
+    if cos_sin is not None:
+        _bf16(cos_sin, "cos_sin")
+        if positions is None or positions.dtype != torch.int64 or not positions.is_contiguous():
+            raise ValueError("RoPE needs contiguous int64 positions")
+    if kv_out is not None:
+        _bf16(kv_out, "kv_out")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    slot_arr = (_vp * L)(*[_ptr(sl) for sl in slots])
+    cache_arr = (_vp * L)(*[c.data_ptr() for c in caches])
+    _check(lib().rc_kv_project_store(normed.data_ptr(), W.data_ptr(), w_layout, L, T, D, H,
+                                     _ptr(positions), slot_arr, _ptr(cos_sin),
+                                     0 if cos_sin is None else cos_sin.shape[0], cache_arr, nb, bs,
+                                     eps, rows, _ptr(err), _ptr(kv_out), ws_ptr, ws_bytes,
+                                     _stream(stream)))
 
 
 def split_kv(kv: torch.Tensor, H: int):

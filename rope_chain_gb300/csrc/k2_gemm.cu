@@ -439,6 +439,130 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
         " [%0], %1;" ::"r"(bar), "h"((uint16_t)0x3) : "memory");
 }
 
+// ------------------------------------------------- fused store epilogue
+//
+// With the projection and the store fused, an epilogue thread holds its row's
+// 256 accumulators = 4 heads of K or of V.  It rounds them to bf16 (the
+// projection), and for a key head computes the K-norm from those bf16 values
+// with the sum folded exactly as the store kernel's lane butterfly does it
+// (seen from lane 0: pairs (j, j+16), then +8, +4, +2, +1 partners; even
+// and odd squares separately, then even + odd), so the stored key is the
+// same bits the unfused store would write.
+
+__device__ __forceinline__ float fold32(const float (&q)[32]) {
+    float a[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        a[j] = __fadd_rn(q[j], q[j + 16]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        a[j] = __fadd_rn(a[j], a[j + 8]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        a[j] = __fadd_rn(a[j], a[j + 4]);
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+        a[j] = __fadd_rn(a[j], a[j + 2]);
+    return __fadd_rn(a[0], a[1]);
+}
+
+// The tile's store for one row (all 32 lanes call it: TMEM loads are
+// warp-collective).  tbase: this warp's TMEM lanes, column 0 of the tile.
+__device__ __forceinline__ void fused_store_tile(const FusedStore &fs, const GemmArgs &g,
+                                                 uint32_t tbase, int l, int row, int n0) {
+    const bool live = row < g.T;
+    const bool rope = fs.cos_sin != nullptr;
+    const int H = fs.H;
+    const int N = g.N;
+    bool store = false;
+    int64_t slot = 0, pos = 0;
+    if (live && row < fs.rows && fs.slots[l] != nullptr) {
+        slot = __ldg(fs.slots[l] + row);
+        if (slot >= 0) {
+            if (rope)
+                pos = __ldg(fs.positions + row);
+            if (slot >= fs.capacity || (rope && (pos < 0 || pos >= fs.max_position))) {
+                if (n0 == 0 && fs.err != nullptr)        // counted once per (row, layer)
+                    atomicAdd(fs.err, 1);
+            } else {
+                store = true;
+            }
+        }
+    }
+    uint16_t *dst_row = nullptr;
+    if (store) {
+        const uint32_t bs = (uint32_t)fs.block_size;
+        const uint32_t blk = (uint32_t)slot / bs;
+        const uint32_t page = (uint32_t)slot - blk * bs;
+        dst_row = fs.caches[l] + (((int64_t)blk * H) * bs + page) * (2 * kHeadDim);
+    }
+#pragma unroll 1
+    for (int hh = 0; hh < 4; ++hh) {
+        uint32_t r[64];
+        tmem_ld32(tbase + 64u * hh, *reinterpret_cast<uint32_t (*)[32]>(r));
+        tmem_ld32(tbase + 64u * hh + 32u, *reinterpret_cast<uint32_t (*)[32]>(r + 32));
+        uint32_t kp[32];                               // the projection, bf16 pairs
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            kp[j] = pack_acc(r[2 * j], r[2 * j + 1]);
+        if (live && fs.kv_out != nullptr) {
+            uint4 *o = reinterpret_cast<uint4 *>(fs.kv_out + ((int64_t)l * g.T + row) * N + n0 + 64 * hh);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                o[j] = make_uint4(kp[4 * j], kp[4 * j + 1], kp[4 * j + 2], kp[4 * j + 3]);
+        }
+        if (!store)
+            continue;
+        const int gidx = (n0 >> 6) + hh;               // head index within [K heads | V heads]
+        const bool is_k = gidx < H;
+        const int h = is_k ? gidx : gidx - H;
+        uint4 *dst = reinterpret_cast<uint4 *>(dst_row + (int64_t)h * fs.block_size * (2 * kHeadDim) +
+                                               (is_k ? 0 : kHeadDim));
+        if (is_k) {
+            float ev[32], od[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float k0 = bf16_lo(kp[j]), k1 = bf16_hi(kp[j]);
+                ev[j] = __fmul_rn(k0, k0);
+                od[j] = __fmul_rn(k1, k1);
+            }
+            const float rr = inv_rms(__fadd_rn(fold32(ev), fold32(od)), 0x1p-6f, fs.eps);
+            const uint4 *cs = rope ? reinterpret_cast<const uint4 *>(fs.cos_sin + pos * kHeadDim) : nullptr;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {              // 8 pairs at a time
+                uint4 cq = make_uint4(0, 0, 0, 0), sq = cq;
+                if (rope) {
+                    cq = __ldg(cs + q);                // cos of pairs 8q .. 8q+7
+                    sq = __ldg(cs + 4 + q);            // sin of the same pairs
+                }
+                const uint32_t cw[4] = {cq.x, cq.y, cq.z, cq.w}, sw[4] = {sq.x, sq.y, sq.z, sq.w};
+                uint32_t out[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const int j = 8 * q + t;
+                    float n0 = round_bf16(__fmul_rn(bf16_lo(kp[j]), rr));
+                    float n1 = round_bf16(__fmul_rn(bf16_hi(kp[j]), rr));
+                    if (rope) {
+                        const float c = (t & 1) ? bf16_hi(cw[t >> 1]) : bf16_lo(cw[t >> 1]);
+                        const float sn = (t & 1) ? bf16_hi(sw[t >> 1]) : bf16_lo(sw[t >> 1]);
+                        const float x = __fmaf_rn(n0, c, -__fmul_rn(n1, sn));
+                        const float y = __fmaf_rn(n1, c, __fmul_rn(n0, sn));
+                        n0 = x;
+                        n1 = y;
+                    }
+                    out[t] = pack_bf16x2(n0, n1);
+                }
+                dst[2 * q] = make_uint4(out[0], out[1], out[2], out[3]);
+                dst[2 * q + 1] = make_uint4(out[4], out[5], out[6], out[7]);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                dst[j] = make_uint4(kp[4 * j], kp[4 * j + 1], kp[4 * j + 2], kp[4 * j + 3]);
+        }
+    }
+}
+
 struct PairCfg {
     static constexpr int kStages = 6;
     static constexpr uint32_t kBHalf = 128 * BK * 2;            // 16 KiB of B per CTA
@@ -447,10 +571,10 @@ struct PairCfg {
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 256;
 };
 
-template <bool kBmn>
+template <bool kBmn, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
 k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const GemmArgs g)
+                const GemmArgs g, const __grid_constant__ FusedStore fs)
 {
     using C = PairCfg;
     constexpr int S = C::kStages;
@@ -572,7 +696,10 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok && !skip && lane == 0)
             raise_fault(kFaultAccum);
-        if (ok) {
+        if (ok && kFused && g.splits == 1) {
+            tc_fence_after();
+            fused_store_tile(fs, g, tmem + ((uint32_t)(32 * q) << 16), l, m0 + 32 * q + lane, n0);
+        } else if (ok) {
             tc_fence_after();
             const int row = m0 + 32 * q + lane;
             const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16);
@@ -688,24 +815,25 @@ cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, const Gemm
     return launch_pdl(k2_project<BN, kBmn>, grid, dim3(kThreads), Cfg<BN>::kSmem, stream, 1, ma, mb, g);
 }
 
-template <bool kBmn>
+template <bool kBmn, bool kFused>
 cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &g,
-                        int n_pairs, int m_pairs, cudaStream_t stream) {
+                        const FusedStore &fs, int n_pairs, int m_pairs, cudaStream_t stream) {
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
     if (dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(k2_project_pair<kBmn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)PairCfg::kSmem);
+        e = cudaFuncSetAttribute(k2_project_pair<kBmn, kFused>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PairCfg::kSmem);
         if (e != cudaSuccess)
             return e;
         if (dev < 64)
             configured[dev] = true;
     }
     const dim3 grid((unsigned)(2 * n_pairs), (unsigned)m_pairs, (unsigned)(g.L * g.splits));
-    return launch_pdl(k2_project_pair<kBmn>, grid, dim3(kThreads), PairCfg::kSmem, stream, 2, ma, mb, g);
+    return launch_pdl(k2_project_pair<kBmn, kFused>, grid, dim3(kThreads), PairCfg::kSmem, stream, 2,
+                      ma, mb, g, fs);
 }
 
 }  // namespace
@@ -734,49 +862,132 @@ ProjectPlan plan_kv_project(int32_t L, int64_t T, int32_t D, int32_t N, int num_
     return p;
 }
 
+namespace {
+
+// Tensor maps and kernel arguments of one projection.
+bool project_setup(const uint16_t *normed, const uint16_t *W, bool w_nk, uint16_t *out, int32_t L,
+                   int64_t T, int32_t D, int32_t N, const ProjectPlan &plan, float *ws,
+                   CUtensorMap *ma, CUtensorMap *mb, GemmArgs *g, const char **why) {
+    if (!make_map(ma, normed, (uint64_t)D, (uint64_t)T, (uint64_t)L, BK, BM)) {
+        *why = "tensor map of the normed rows could not be encoded";
+        return false;
+    }
+    const uint32_t b_rows = plan.pair ? 128u : (uint32_t)plan.bn;   // K-major B rows per CTA
+    const bool ok_b = w_nk ? make_map(mb, W, (uint64_t)D, (uint64_t)N, (uint64_t)L, BK, b_rows)
+                           : make_map(mb, W, (uint64_t)N, (uint64_t)D, (uint64_t)L, 64, BK);
+    if (!ok_b) {
+        *why = "tensor map of the weights could not be encoded";
+        return false;
+    }
+    g->T = (int32_t)T;
+    g->N = N;
+    g->L = L;
+    g->kb_total = D / BK;
+    g->kb_per_split = plan.kb_per_split;
+    g->splits = plan.splits;
+    g->out = out;
+    g->partial = ws;
+    return true;
+}
+
+// The GEMM kernel of a plan (no split-K reduction).
+template <bool kFused>
+cudaError_t launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &g,
+                        const FusedStore &fs, bool w_nk, const ProjectPlan &plan, int64_t T,
+                        int32_t N, cudaStream_t stream) {
+    if (plan.pair)
+        return w_nk ? launch_pair<false, kFused>(ma, mb, g, fs, N / 256, (int)((T + 255) / 256), stream)
+                    : launch_pair<true, kFused>(ma, mb, g, fs, N / 256, (int)((T + 255) / 256), stream);
+    const int n_tiles = N / plan.bn;
+    const int m_tiles = (int)((T + BM - 1) / BM);
+    if (plan.bn == 256)
+        return w_nk ? launch_tile<256, false>(ma, mb, g, n_tiles, m_tiles, stream)
+                    : launch_tile<256, true>(ma, mb, g, n_tiles, m_tiles, stream);
+    return w_nk ? launch_tile<128, false>(ma, mb, g, n_tiles, m_tiles, stream)
+                : launch_tile<128, true>(ma, mb, g, n_tiles, m_tiles, stream);
+}
+
+cudaError_t launch_reduce(const float *ws, uint16_t *out, int64_t count, int splits,
+                          cudaStream_t stream) {
+    const int64_t blocks = std::min<int64_t>((count / 8 + 255) / 256, 152 * 16);
+    return launch_pdl(k2_splitk_reduce, dim3((unsigned)blocks), dim3(256), 0, stream, 1, ws, out,
+                      count, splits);
+}
+
+}  // namespace
+
 cudaError_t launch_kv_project(const uint16_t *normed, const uint16_t *W, bool w_nk, uint16_t *out,
                               int32_t L, int64_t T, int32_t D, int32_t N, const ProjectPlan &plan,
                               float *ws, cudaStream_t stream, const char **why)
 {
     CUtensorMap ma, mb;
-    if (!make_map(&ma, normed, (uint64_t)D, (uint64_t)T, (uint64_t)L, BK, BM)) {
-        *why = "tensor map of the normed rows could not be encoded";
-        return cudaErrorInvalidValue;
-    }
-    const uint32_t b_rows = plan.pair ? 128u : (uint32_t)plan.bn;   // K-major B rows per CTA
-    const bool ok_b = w_nk ? make_map(&mb, W, (uint64_t)D, (uint64_t)N, (uint64_t)L, BK, b_rows)
-                           : make_map(&mb, W, (uint64_t)N, (uint64_t)D, (uint64_t)L, 64, BK);
-    if (!ok_b) {
-        *why = "tensor map of the weights could not be encoded";
-        return cudaErrorInvalidValue;
-    }
     GemmArgs g;
-    g.T = (int32_t)T;
-    g.N = N;
-    g.L = L;
-    g.kb_total = D / BK;
-    g.kb_per_split = plan.kb_per_split;
-    g.splits = plan.splits;
-    g.out = out;
-    g.partial = ws;
-    const int n_tiles = N / plan.bn;
-    const int m_tiles = (int)((T + BM - 1) / BM);
-    cudaError_t e;
-    if (plan.pair)
-        e = w_nk ? launch_pair<false>(ma, mb, g, N / 256, (int)((T + 255) / 256), stream)
-                 : launch_pair<true>(ma, mb, g, N / 256, (int)((T + 255) / 256), stream);
-    else if (plan.bn == 256)
-        e = w_nk ? launch_tile<256, false>(ma, mb, g, n_tiles, m_tiles, stream)
-                 : launch_tile<256, true>(ma, mb, g, n_tiles, m_tiles, stream);
-    else
-        e = w_nk ? launch_tile<128, false>(ma, mb, g, n_tiles, m_tiles, stream)
-                 : launch_tile<128, true>(ma, mb, g, n_tiles, m_tiles, stream);
+    if (!project_setup(normed, W, w_nk, out, L, T, D, N, plan, ws, &ma, &mb, &g, why))
+        return cudaErrorInvalidValue;
+    FusedStore none{};
+    cudaError_t e = launch_gemm<false>(ma, mb, g, none, w_nk, plan, T, N, stream);
     if (e != cudaSuccess || plan.splits == 1)
         return e;
-    const int64_t count = (int64_t)L * T * N;
-    const int64_t blocks = std::min<int64_t>((count / 8 + 255) / 256, 152 * 16);
-    return launch_pdl(k2_splitk_reduce, dim3((unsigned)blocks), dim3(256), 0, stream, 1,
-                      static_cast<const float *>(ws), out, count, (int)plan.splits);
+    return launch_reduce(ws, out, (int64_t)L * T * N, plan.splits, stream);
+}
+
+cudaError_t launch_kv_project_store(const uint16_t *normed, const uint16_t *W, bool w_nk,
+                                    int32_t L, int64_t T, int32_t D, int32_t N,
+                                    const ProjectPlan &plan, float *ws, const FusedStore &fs,
+                                    cudaStream_t stream, const char **why)
+{
+    CUtensorMap ma, mb;
+    GemmArgs g;
+    if (!project_setup(normed, W, w_nk, fs.kv_out, L, T, D, N, plan, ws, &ma, &mb, &g, why))
+        return cudaErrorInvalidValue;
+    cudaError_t e;
+    if (plan.splits > 1) {
+        // partials, then one pass that reduces and stores
+        e = launch_gemm<false>(ma, mb, g, fs, w_nk, plan, T, N, stream);
+        if (e != cudaSuccess)
+            return e;
+        *why = "reduce-and-store launch";
+        return launch_reduce_store(fs, ws, plan.splits, L, (int32_t)T, stream);
+    }
+    if (plan.pair)                                 // the epilogue stores
+        return launch_gemm<true>(ma, mb, g, fs, w_nk, plan, T, N, stream);
+    // single CTAs without a split: the projection lands in kv_out, then the
+    // store kernel reads it (8 layers per launch)
+    if (fs.kv_out == nullptr) {
+        *why = "this size needs kv_out (the projection is stored from it)";
+        return cudaErrorInvalidValue;
+    }
+    e = launch_gemm<false>(ma, mb, g, fs, w_nk, plan, T, N, stream);
+    if (e != cudaSuccess)
+        return e;
+    for (int32_t first = 0; first < L; first += kMaxLayersPerLaunch) {
+        const int32_t n = std::min(kMaxLayersPerLaunch, L - first);
+        StoreLaunch p{};
+        bool any = false;
+        for (int32_t i = 0; i < n; ++i) {
+            p.slots[i] = fs.slots[first + i];
+            p.caches[i] = fs.caches[first + i];
+            any = any || p.slots[i] != nullptr;
+        }
+        if (!any)
+            continue;
+        p.k = fs.kv_out + (int64_t)first * T * N;
+        p.v = p.k + 64 * fs.H;
+        p.k_layer_stride = p.v_layer_stride = T * N;
+        p.k_row_stride = p.v_row_stride = N;
+        p.positions = fs.positions;
+        p.cos_sin = fs.cos_sin;
+        p.max_position = fs.max_position;
+        p.capacity = fs.capacity;
+        p.block_size = fs.block_size;
+        p.rows = fs.rows;
+        p.eps = fs.eps;
+        p.err = fs.err;
+        e = launch_kv_store(p, fs.H, n, stream);
+        if (e != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t read_project_faults(uint32_t *flags, bool clear)

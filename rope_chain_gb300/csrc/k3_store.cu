@@ -23,6 +23,44 @@ __device__ __forceinline__ void count_skip(int32_t *err, int lane) {
         atomicAdd(err, 1);
 }
 
+// The key pair (k0, k1) = elements (2 lane, 2 lane + 1) of one head, for a
+// whole warp: weightless K-norm (sum folded as even and odd squares by xor
+// butterflies, then even + odd), the bf16 key, GPT-J RoPE with (c, s), and
+// the packed bf16 result.
+template <bool kRope>
+__device__ __forceinline__ uint32_t knorm_rope_lane(float k0, float k1, float c, float s, float eps) {
+    const float even = warp_butterfly_sum(__fmul_rn(k0, k0));
+    const float odd = warp_butterfly_sum(__fmul_rn(k1, k1));
+    const float r = inv_rms(__fadd_rn(even, odd), 0x1p-6f, eps);
+    float n0 = round_bf16(__fmul_rn(k0, r));
+    float n1 = round_bf16(__fmul_rn(k1, r));
+    if (kRope) {
+        const float x = __fmaf_rn(n0, c, -__fmul_rn(n1, s));
+        const float y = __fmaf_rn(n1, c, __fmul_rn(n0, s));
+        n0 = x;
+        n1 = y;
+    }
+    return pack_bf16x2(n0, n1);
+}
+
+// Writes one row's H heads of K' and V into its cache slot (lane = pair).
+template <int H>
+__device__ __forceinline__ void insert_row(uint16_t *cache, int64_t slot, int32_t block_size,
+                                           const uint32_t (&ko)[H], const uint32_t (&vw)[H],
+                                           int lane) {
+    // Slots of a cache fit 32 bits (checked on the host).
+    const uint32_t bs = (uint32_t)block_size;
+    const uint32_t blk = (uint32_t)slot / bs;
+    const uint32_t page = (uint32_t)slot - blk * bs;
+    uint32_t *dst = reinterpret_cast<uint32_t *>(cache) + (((int64_t)blk * H) * bs + page) * kHeadDim + lane;
+    const int64_t head_stride = (int64_t)bs * kHeadDim;      // in 4-byte words
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+        dst[h * head_stride] = ko[h];
+        dst[h * head_stride + kHeadDim / 2] = vw[h];          // V follows K
+    }
+}
+
 template <int H, bool kRope>
 __global__ void __launch_bounds__(kWarps * 32)
 k3_kv_store(const __grid_constant__ StoreLaunch p)
@@ -67,34 +105,99 @@ k3_kv_store(const __grid_constant__ StoreLaunch p)
 
     uint32_t ko[H];
 #pragma unroll
-    for (int h = 0; h < H; ++h) {
-        const float k0 = bf16_lo(kw[h]), k1 = bf16_hi(kw[h]);
-        const float even = warp_butterfly_sum(__fmul_rn(k0, k0));
-        const float odd = warp_butterfly_sum(__fmul_rn(k1, k1));
-        const float r = inv_rms(__fadd_rn(even, odd), 0x1p-6f, p.eps);
-        float n0 = round_bf16(__fmul_rn(k0, r));
-        float n1 = round_bf16(__fmul_rn(k1, r));
-        if (kRope) {
-            const float x = __fmaf_rn(n0, c, -__fmul_rn(n1, s));
-            const float y = __fmaf_rn(n1, c, __fmul_rn(n0, s));
-            n0 = x;
-            n1 = y;
-        }
-        ko[h] = pack_bf16x2(n0, n1);
-    }
+    for (int h = 0; h < H; ++h)
+        ko[h] = knorm_rope_lane<kRope>(bf16_lo(kw[h]), bf16_hi(kw[h]), c, s, p.eps);
+    insert_row<H>(p.caches[layer], slot, p.block_size, ko, vw, lane);
+}
 
-    // Slots of a cache fit 32 bits (checked on the host).
-    const uint32_t bs = (uint32_t)p.block_size;
-    const uint32_t blk = (uint32_t)slot / bs;
-    const uint32_t page = (uint32_t)slot - blk * bs;
-    uint32_t *dst = reinterpret_cast<uint32_t *>(p.caches[layer]) +
-                    (((int64_t)blk * H) * bs + page) * kHeadDim + lane;
-    const int64_t head_stride = (int64_t)bs * kHeadDim;      // in 4-byte words
+// Split-K projection finished and stored in one pass: the FP32 partials
+// [splits, L, T, 128 H] are added in split order and rounded to bf16 (the
+// same additions as the projection's reduce kernel), optionally written to
+// kv_out, and stored like k3_kv_store.  One warp per (row, layer), all rows
+// of the projection (kv_out), storing the first fs.rows.
+template <int H, bool kRope>
+__global__ void __launch_bounds__(kWarps * 32)
+k3_reduce_store(const __grid_constant__ FusedStore fs, const float *__restrict__ partial,
+                int32_t splits, int32_t L, int32_t T)
+{
+    constexpr int N = 2 * H * kHeadDim;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * kWarps + warp;
+    const int layer = blockIdx.y;
+    pdl_trigger();
+    pdl_wait();
+    if (row >= T)
+        return;
+    const int64_t *slots = fs.slots[layer];
+    const bool store = slots != nullptr && row < fs.rows;
+    int64_t slot = -1, pos = 0;
+    if (store) {
+        slot = __ldg(slots + row);
+        if (kRope)
+            pos = __ldg(fs.positions + row);
+    }
+    const int64_t plane = (int64_t)L * T * N;
+    const float *p0 = partial + ((int64_t)layer * T + row) * N + 2 * lane;
+    float2 ka[H], va[H];
 #pragma unroll
     for (int h = 0; h < H; ++h) {
-        dst[h * head_stride] = ko[h];
-        dst[h * head_stride + kHeadDim / 2] = vw[h];          // V follows K
+        ka[h] = __ldcs(reinterpret_cast<const float2 *>(p0 + h * kHeadDim));
+        va[h] = __ldcs(reinterpret_cast<const float2 *>(p0 + (H + h) * kHeadDim));
     }
+    for (int sp = 1; sp < splits; ++sp) {
+        const float *q = p0 + sp * plane;
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+            const float2 a = __ldcs(reinterpret_cast<const float2 *>(q + h * kHeadDim));
+            const float2 b = __ldcs(reinterpret_cast<const float2 *>(q + (H + h) * kHeadDim));
+            ka[h].x = __fadd_rn(ka[h].x, a.x);
+            ka[h].y = __fadd_rn(ka[h].y, a.y);
+            va[h].x = __fadd_rn(va[h].x, b.x);
+            va[h].y = __fadd_rn(va[h].y, b.y);
+        }
+    }
+    uint32_t kw[H], vw[H];
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+        kw[h] = pack_bf16x2(ka[h].x, ka[h].y);
+        vw[h] = pack_bf16x2(va[h].x, va[h].y);
+    }
+    if (fs.kv_out != nullptr) {
+        uint32_t *o = reinterpret_cast<uint32_t *>(fs.kv_out + ((int64_t)layer * T + row) * N) + lane;
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+            o[h * (kHeadDim / 2)] = kw[h];
+            o[(H + h) * (kHeadDim / 2)] = vw[h];
+        }
+    }
+    if (!store || slot < 0)
+        return;
+    if (slot >= fs.capacity || (kRope && (pos < 0 || pos >= fs.max_position))) {
+        count_skip(fs.err, lane);
+        return;
+    }
+    float c = 1.0f, s = 0.0f;
+    if (kRope) {
+        const unsigned short *cs = reinterpret_cast<const unsigned short *>(fs.cos_sin) + pos * kHeadDim;
+        c = __uint_as_float((uint32_t)__ldg(cs + lane) << 16);
+        s = __uint_as_float((uint32_t)__ldg(cs + kHeadDim / 2 + lane) << 16);
+    }
+    uint32_t ko[H];
+#pragma unroll
+    for (int h = 0; h < H; ++h)
+        ko[h] = knorm_rope_lane<kRope>(bf16_lo(kw[h]), bf16_hi(kw[h]), c, s, fs.eps);
+    insert_row<H>(fs.caches[layer], slot, fs.block_size, ko, vw, lane);
+}
+
+template <int H>
+cudaError_t launch_rs(const FusedStore &fs, const float *partial, int32_t splits, int32_t L,
+                      int32_t T, cudaStream_t stream) {
+    const dim3 grid((unsigned)((T + kWarps - 1) / kWarps), (unsigned)L);
+    if (fs.cos_sin)
+        return launch_pdl(k3_reduce_store<H, true>, grid, dim3(kWarps * 32), 0, stream, 1, fs, partial,
+                          splits, L, T);
+    return launch_pdl(k3_reduce_store<H, false>, grid, dim3(kWarps * 32), 0, stream, 1, fs, partial,
+                      splits, L, T);
 }
 
 template <int H>
@@ -106,6 +209,20 @@ cudaError_t launch_h(const StoreLaunch &p, int32_t layers, cudaStream_t stream) 
 }
 
 }  // namespace
+
+cudaError_t launch_reduce_store(const FusedStore &fs, const float *partial, int32_t splits,
+                                int32_t L, int32_t T, cudaStream_t stream)
+{
+    switch (fs.H) {
+    case 1: return launch_rs<1>(fs, partial, splits, L, T, stream);
+    case 2: return launch_rs<2>(fs, partial, splits, L, T, stream);
+    case 4: return launch_rs<4>(fs, partial, splits, L, T, stream);
+    case 8: return launch_rs<8>(fs, partial, splits, L, T, stream);
+    case 16: return launch_rs<16>(fs, partial, splits, L, T, stream);
+    case 32: return launch_rs<32>(fs, partial, splits, L, T, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
 
 cudaError_t launch_kv_store(const StoreLaunch &p, int32_t H, int32_t layers, cudaStream_t stream)
 {

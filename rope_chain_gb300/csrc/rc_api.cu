@@ -225,6 +225,86 @@ rc_status rc_kv_store(const uint16_t *k, const uint16_t *v, int64_t k_layer_stri
     return ok();
 }
 
+rc_status rc_kv_project_store(const uint16_t *normed, const uint16_t *W, int32_t w_layout,
+                              int32_t L, int64_t T, int32_t D, int32_t H,
+                              const int64_t *positions, const int64_t *const *slots,
+                              const uint16_t *cos_sin, int64_t max_position,
+                              uint16_t *const *caches, int32_t num_blocks, int32_t block_size,
+                              float eps, int64_t rows, int32_t *err, uint16_t *kv_out,
+                              void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    if (H != 1 && H != 2 && H != 4 && H != 8 && H != 16 && H != 32)
+        return fail(RC_ERR_UNSUPPORTED, "rc_kv_project_store: H=%d is not a power of two <= 32", H);
+    const int32_t N = 2 * H * rc::kHeadDim;
+    rc_status st = check_project_sizes(L, T, D, N);
+    if (st != RC_OK)
+        return st;
+    if (L > rc::kMaxFusedLayers)
+        return fail(RC_ERR_UNSUPPORTED, "rc_kv_project_store: L=%d above %d", L, rc::kMaxFusedLayers);
+    if (w_layout != RC_W_KN && w_layout != RC_W_NK)
+        return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store: unknown weight layout %d", w_layout);
+    if (!normed || !W || !slots || !caches)
+        return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store: normed, W, slots and caches must not be NULL");
+    if (!aligned(normed, 16) || !aligned(W, 16) || (kv_out && !aligned(kv_out, 16)) ||
+        (workspace && !aligned(workspace, 16)))
+        return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store: normed, W, kv_out and workspace must be 16-byte aligned");
+    if (rows < 0 || rows > T)
+        return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store: rows=%lld outside [0, T]", (long long)rows);
+    if (num_blocks < 1 || block_size < 1 || (int64_t)num_blocks * block_size >= (1LL << 31))
+        return fail(RC_ERR_INVALID_ARG,
+                    "rc_kv_project_store: need num_blocks, block_size >= 1 and num_blocks*block_size < 2^31");
+    if (cos_sin) {
+        if (!positions || !aligned(positions, 8))
+            return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store: RoPE needs 8-byte aligned positions");
+        if (max_position < 1)
+            return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store: max_position must be >= 1 with a table");
+        if (!aligned(cos_sin, 16))
+            return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store: cos_sin must be 16-byte aligned");
+    }
+    for (int32_t l = 0; l < L; ++l) {
+        if (!slots[l])
+            continue;
+        if (!aligned(slots[l], 8))
+            return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store: slots[%d] must be 8-byte aligned", l);
+        if (!caches[l] || !aligned(caches[l], 16))
+            return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store: caches[%d] must be a 16-byte aligned pointer", l);
+    }
+    if (T == 0)
+        return ok();
+    if (kv_out && overlap(kv_out, (size_t)L * T * N * 2, normed, (size_t)L * T * D * 2))
+        return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store: kv_out overlaps normed");
+    const int sms = num_sms_current();
+    if (sms <= 0)
+        return fail(RC_ERR_CUDA, "rc_kv_project_store: no current CUDA device");
+    const rc::ProjectPlan plan =
+        rc::plan_kv_project(L, T, D, N, sms, workspace ? workspace_bytes : 0);
+    if (plan.splits == 1 && !plan.pair && !kv_out)
+        return fail(RC_ERR_INVALID_ARG,
+                    "rc_kv_project_store: at these sizes the store reads the projection from kv_out; "
+                    "pass kv_out or a workspace of rc_kv_project_workspace_size() bytes");
+    rc::FusedStore fs{};
+    fs.positions = positions;
+    fs.cos_sin = cos_sin;
+    fs.max_position = max_position;
+    for (int32_t l = 0; l < L; ++l) {
+        fs.slots[l] = slots[l];
+        fs.caches[l] = caches[l];
+    }
+    fs.capacity = (int64_t)num_blocks * block_size;
+    fs.block_size = block_size;
+    fs.H = H;
+    fs.rows = (int32_t)rows;
+    fs.eps = eps;
+    fs.err = err;
+    fs.kv_out = kv_out;
+    const char *why = "launch";
+    const cudaError_t e = rc::launch_kv_project_store(normed, W, w_layout == RC_W_NK, L, T, D, N, plan,
+                                                      static_cast<float *>(workspace), fs, stream, &why);
+    if (e != cudaSuccess)
+        return cuda_fail(e, why);
+    return ok();
+}
+
 rc_status rc_read_device_faults(uint32_t *flags, int32_t clear)
 {
     if (!flags)

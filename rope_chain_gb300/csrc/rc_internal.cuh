@@ -108,6 +108,28 @@ struct StoreLaunch {
     int32_t *err;
 };
 
+// The store half of the fused projection + store (all layers in one launch).
+constexpr int kMaxFusedLayers = 64;
+struct FusedStore {
+    const int64_t *positions;
+    const uint16_t *cos_sin;         // NULL: no RoPE
+    int64_t max_position;
+    const int64_t *slots[kMaxFusedLayers];
+    uint16_t *caches[kMaxFusedLayers];
+    int64_t capacity;                // num_blocks * block_size
+    int32_t block_size;
+    int32_t H;
+    int32_t rows;                    // rows inserted (<= T)
+    float eps;
+    int32_t *err;
+    uint16_t *kv_out;                // optional bf16 [L, T, 2*H*64] copy of the projection
+};
+
+// Store from split-K partials: adds the FP32 partials [splits, L, T, N] in
+// split order, rounds to bf16 (the projection), then K-norm, RoPE and insert.
+cudaError_t launch_reduce_store(const FusedStore &fs, const float *partial, int32_t splits,
+                                int32_t L, int32_t T, cudaStream_t stream);
+
 // Store: one chunk of <= 8 layers; H in {1,2,4,8,16,32}.
 cudaError_t launch_kv_store(const StoreLaunch &p, int32_t H, int32_t layers,
                             cudaStream_t stream);
@@ -132,6 +154,14 @@ cudaError_t launch_kv_project(const uint16_t *normed, const uint16_t *W, bool w_
 
 // Sets the message rc_last_error() returns on this host thread.
 void set_last_error(const char *msg);
+
+// Projection + store: the pair kernel's epilogue stores when it does not
+// split; split plans go through launch_reduce_store; single-CTA plans that do
+// not split need fs.kv_out (projection to kv_out, then the store kernel).
+cudaError_t launch_kv_project_store(const uint16_t *normed, const uint16_t *W, bool w_nk,
+                                    int32_t L, int64_t T, int32_t D, int32_t N,
+                                    const ProjectPlan &plan, float *ws, const FusedStore &fs,
+                                    cudaStream_t stream, const char **why);
 
 // Sticky device fault bits of the projection kernel (current device).
 cudaError_t read_project_faults(uint32_t *flags, bool clear);

@@ -1,0 +1,137 @@
+"""rc_kv_project_store (projection and store in one pass) against the
+oracle: the caches bit-exact against the oracle's store fed the projection
+the same call wrote to kv_out, kv_out within the projection rule, the skip
+count equal; and the caches identical with and without kv_out and to the
+unfused calls.  Covers the three ways the call runs: the CTA-pair epilogue
+store (no split), the reduce-and-store pass (split-K), and projection to
+kv_out then the store kernel (single CTAs, no split)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rope_chain_gb300 as rc
+import workloads
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from rope_chain_gb300 import _build
+    _build.build()
+    oracle.build()
+    rc.read_device_faults(clear=True)
+    yield
+    assert rc.read_device_faults(clear=True) == 0
+
+
+def _dev(case):
+    H = case["cache_shape"][1]
+    L = len(case["slots"])
+    return dict(
+        positions=torch.from_numpy(case["positions"]).to(DEV),
+        slots=[None if s is None else torch.from_numpy(s).to(DEV) for s in case["slots"]],
+        cs=parity.dev_bf16(case["cos_sin"], DEV),
+        caches=[parity.dev_bf16(c, DEV) for c in parity.make_caches(case, L, parity.SENTINEL)],
+        err=torch.zeros(1, dtype=torch.int32, device=DEV), H=H, L=L)
+
+
+def run_fused(case, normed_d, W_d, *, workspace, kv_out, rows=None, layout=rc.RC_W_KN):
+    d = _dev(case)
+    T = normed_d.shape[1]
+    kv = torch.empty((d["L"], T, 128 * d["H"]), dtype=torch.bfloat16, device=DEV) if kv_out else None
+    ws = rc.new_workspace(d["L"], T, 8192 if normed_d.shape[2] == 8192 else normed_d.shape[2],
+                          128 * d["H"], DEV) if workspace else None
+    rc.kv_project_store(normed_d, W_d, d["H"], d["positions"], d["slots"], d["cs"], d["caches"],
+                        case["eps"], rows=rows, err=d["err"], kv_out=kv, w_layout=layout,
+                        workspace=ws)
+    torch.cuda.synchronize()
+    return ([parity.host_bits(c) for c in d["caches"]],
+            None if kv is None else parity.host_bits(kv), int(d["err"].item()))
+
+
+def check(case, normed, W, *, workspace, rows=None, layout=rc.RC_W_KN, slots=None):
+    if slots is not None:
+        case = dict(case, slots=slots)
+    Wl = W if layout == rc.RC_W_KN else np.ascontiguousarray(W.transpose(0, 2, 1))
+    nd, wd = parity.dev_bf16(normed, DEV), parity.dev_bf16(Wl, DEV)
+    caches, kv, err = run_fused(case, nd, wd, workspace=workspace, kv_out=True, rows=rows,
+                                layout=layout)
+    T = normed.shape[1]
+    rows_ = T if rows is None else rows
+    ref_caches = parity.make_caches(case, len(case["slots"]), parity.SENTINEL)
+    ref_err = oracle.kv_store_from_projection(kv, case["cache_shape"][1], case["positions"],
+                                              case["slots"], case["cos_sin"], ref_caches,
+                                              case["eps"], rows_)
+    for g, r in zip(caches, ref_caches):
+        assert np.array_equal(g, r)
+    assert err == ref_err
+    sample = None if T <= 512 else np.unique(np.r_[0, T - 1, np.linspace(0, T - 1, 200).astype(int)])
+    ref64, ab = oracle.kv_project(normed, W, rows=sample)
+    parity.assert_projection_close(kv if sample is None else kv[:, sample], ref64, ab)
+    return caches, nd, wd
+
+
+@pytest.mark.parametrize("T,L,H,workspace,rope", [
+    (300, 2, 2, False, True),      # CTA pairs, epilogue store, K and V heads in one tile
+    (512, 3, 8, False, True),      # CTA pairs, epilogue store
+    (512, 3, 8, True, True),       # CTA pairs, split-K, reduce-and-store
+    (200, 2, 16, False, False),    # CTA pairs, epilogue store, no RoPE
+    (129, 1, 32, True, True),      # H = 32, ragged rows
+    (64, 2, 8, True, True),        # single CTAs, split-K, reduce-and-store
+    (100, 2, 1, False, True),      # N = 128: single CTAs without split, kv_out then store
+    (100, 3, 4, True, False),      # single CTAs (T <= 128), split, no RoPE
+])
+def test_fused_store_bit_exact(T, L, H, workspace, rope):
+    case = workloads.random_case(500 + T + H, T=T, L=L, H=H, rope=rope, max_position=512,
+                                 num_blocks=(T + 15) // 16 + 4, block_size=16)
+    normed = oracle.context_norms(case["x"], case["hidden_w"], case["pre_w"], L, case["eps"])
+    caches, nd, wd = check(case, normed, case["W"], workspace=workspace)
+    # without kv_out (where the plan allows) the caches are the same bits
+    if not (H == 1 and not workspace):
+        c2, kv2, e2 = run_fused(case, nd, wd, workspace=workspace, kv_out=False)
+        for a, b in zip(caches, c2):
+            assert np.array_equal(a, b)
+
+
+def test_fused_rows_prefix_null_layer_and_bad_rows():
+    T, L, H = 300, 3, 8
+    case = workloads.random_case(777, T=T, L=L, H=H, max_position=64, num_blocks=24, block_size=16)
+    slots = [s.copy() for s in case["slots"]]
+    slots[1] = None
+    slots[0][5] = 24 * 16           # == capacity
+    slots[2][7] = 1 << 40
+    pos = case["positions"].copy()
+    pos[9] = 64                     # == max_position
+    case = dict(case, positions=pos)
+    normed = oracle.context_norms(case["x"], case["hidden_w"], case["pre_w"], L, case["eps"])
+    for ws in (False, True):
+        check(case, normed, case["W"], workspace=ws, rows=250, slots=slots)
+
+
+@pytest.mark.parametrize("layout", [rc.RC_W_KN, rc.RC_W_NK])
+def test_fused_matches_unfused_chain(layout):
+    # the caches of the fused call equal those of kv_project + kv_store
+    w = workloads.WORKLOADS[2]
+    case = workloads.make_inputs(w)
+    got = parity.run_gpu_chain(case, DEV, w_layout=layout)
+    normed = got["normed"]
+    W = case["W"]
+    Wl = W if layout == rc.RC_W_KN else np.ascontiguousarray(W.transpose(0, 2, 1))
+    caches, kv, err = run_fused(case, parity.dev_bf16(normed, DEV), parity.dev_bf16(Wl, DEV),
+                                workspace=True, kv_out=True, layout=layout)
+    assert np.array_equal(kv, got["kv"])
+    for a, b in zip(caches, got["caches"]):
+        assert np.array_equal(a, b)
+    assert err == got["err"]
+
+
+@pytest.mark.parametrize("index", [1, 2, 3, 4, 5])
+def test_fused_workloads(index):
+    w = workloads.WORKLOADS[index]
+    case = workloads.make_inputs(w)
+    normed = oracle.context_norms(case["x"], case["hidden_w"], case["pre_w"], w.L, w.eps)
+    check(case, normed, case["W"], workspace=True)
