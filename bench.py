@@ -214,33 +214,43 @@ def run_ours(args, w):
     ws_bytes = rc.workspace_size(w.L, w.T, w.D, w.N)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    # K1 + K2 (+ the split-K reduce when it splits) + K3 (8 layers per launch)
-    launches_per_step = 1 + (2 if ws_bytes else 1) + (w.L + 7) // 8
+    # K1 + the fused projection/store: the GEMM, plus the reduce-and-store
+    # pass when K is split (the pair kernel's epilogue stores otherwise)
+    launches_per_step = 1 + (2 if ws_bytes else 1)
 
     def chain(ev=None, per_kernel=False):
-        # ev[0] / ev[3] bracket the step; with per_kernel, ev[1] / ev[2] split
-        # it per call (an event between two kernels also stops the second
-        # from launching early, so the timed steps use step events only)
+        """One step: the norms, then projection + K-norm + RoPE + insert.
+        ev[0] / ev[2] bracket the step; with per_kernel ev[1] splits it (an
+        event between two kernels stops the second from launching early, so
+        the timed steps use step events only)."""
         if ev:
             ev[0].record()
         rc.context_norms(x, hw, pw, w.L, w.eps, out=normed)
         if ev and per_kernel:
             ev[1].record()
-        rc.kv_project(normed, W, out=kv, workspace=ws)
-        if ev and per_kernel:
-            ev[2].record()
-        rc.kv_store_from_projection(kv, w.H, positions, slots, cs, caches, w.eps, err=err)
+        rc.kv_project_store(normed, W, w.H, positions, slots, cs, caches, w.eps, err=err,
+                            workspace=ws if ws_bytes else None)
         if ev:
-            ev[3].record()
+            ev[2].record()
+
+    def chain_unfused(ev):
+        """The three calls of the boundary, an event after each (breakdown)."""
+        ev[0].record()
+        rc.context_norms(x, hw, pw, w.L, w.eps, out=normed)
+        ev[1].record()
+        rc.kv_project(normed, W, out=kv, workspace=ws if ws_bytes else None)
+        ev[2].record()
+        rc.kv_store_from_projection(kv, w.H, positions, slots, cs, caches, w.eps, err=err)
+        ev[3].record()
 
     for i in range(args.warmup):
         flush.fill_(i & 0xFF)
         chain()
+        chain_unfused([torch.cuda.Event(enable_timing=True) for _ in range(4)])
     torch.cuda.synchronize()
     # The K timed steps run as one captured CUDA graph (what a serving loop
     # does with these graph-capturable calls), each step preceded by the L2
-    # flush and bracketed per call by event nodes; without event nodes in
-    # graphs (older torch) the steps are launched eagerly instead.
+    # flush; without event nodes in graphs (older torch) they launch eagerly.
     timing = "cuda graph"
     try:
         make_event = lambda: torch.cuda.Event(enable_timing=True, external=True)
@@ -248,52 +258,53 @@ def run_ours(args, w):
     except TypeError:
         make_event = lambda: torch.cuda.Event(enable_timing=True)
         timing = "eager"
-    evs = [[make_event() for _ in range(4)] for _ in range(args.steps)]
-    kevs = [[make_event() for _ in range(4)] for _ in range(args.steps)]
+    evs = [[make_event() for _ in range(3)] for _ in range(args.steps)]
+    kevs = [[make_event() for _ in range(3)] for _ in range(args.steps)]
+    uevs = [[make_event() for _ in range(4)] for _ in range(args.steps)]
 
-    def steps(events, per_kernel):
+    def steps(kind):
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)            # L2 flushed before every timed step (not timed)
-            chain(events[i], per_kernel)
+            flush.fill_(i & 0xFF)            # L2 flushed before every step (not timed)
+            if kind == "timed":
+                chain(evs[i])
+            elif kind == "kernels":
+                chain(kevs[i], per_kernel=True)
+            else:
+                chain_unfused(uevs[i])
 
-    graphs = None
+    graphs = {}
     if timing == "cuda graph":
-        graphs = []
-        for events, per_kernel in ((evs, False), (kevs, True)):
+        for kind in ("timed", "kernels", "unfused"):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                steps(events, per_kernel)
+                steps(kind)
             g.replay()                       # warm the graph itself
-            graphs.append(g)
+            graphs[kind] = g
         torch.cuda.synchronize()
+    run = lambda kind: graphs[kind].replay() if graphs else steps(kind)
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    if graphs:
-        graphs[0].replay()                   # the timed K steps
-    else:
-        steps(evs, False)
+    run("timed")                             # the timed K steps
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    # per-kernel breakdown (for the roofline): the same K steps with an event
-    # between consecutive calls, replayed after the timed region
-    if graphs:
-        graphs[1].replay()
-    else:
-        steps(kevs, True)
+    # breakdowns (roofline figures), replayed after the timed region
+    run("kernels")
+    run("unfused")
     torch.cuda.synchronize()
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    k_ms = [[e[j].elapsed_time(e[j + 1]) for e in kevs] for j in range(3)]
+    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
     total_ms = max_over_ranks(sum(step_ms), world)
+    k1_ms = [e[0].elapsed_time(e[1]) for e in kevs]
+    ps_ms = [e[1].elapsed_time(e[2]) for e in kevs]
+    u_ms = [[e[j].elapsed_time(e[j + 1]) for e in uevs] for j in range(3)]
     faults = rc.read_device_faults(clear=True)
     if faults:
         raise RuntimeError(f"projection kernel raised fault bits {faults:#x}")
-
     # ---- end to end: pinned host inputs copied in, the status word read back
     x_h = torch.from_numpy(case["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
     pos_h = torch.from_numpy(case["positions"]).pin_memory()
@@ -330,21 +341,25 @@ def run_ours(args, w):
     peaks, peak_src = load_peaks()
     counts = algorithmic_counts(w, 2 if ws_bytes else 1)
     k3_bytes = store_bytes(w, case["slots"], w.rope)
-    k1_us = 1e3 * statistics.mean(k_ms[0])
-    k2_us = 1e3 * statistics.mean(k_ms[1])
-    k3_us = 1e3 * statistics.mean(k_ms[2])
-    hbm = peaks["hbm_gbs"]
-    tc = peaks["bf16_tflops"]
+    hbm, tc = peaks["hbm_gbs"], peaks["bf16_tflops"]
+    us = lambda ms: 1e3 * statistics.mean(ms)
+
+    def hbm_entry(nbytes, t_us):
+        return {"us": t_us, "GB/s": nbytes / t_us / 1e3, "frac": nbytes / t_us / 1e3 / hbm,
+                "bound": "hbm"}
+
+    def tc_entry(t_us):
+        return {"us": t_us, "TFLOP/s": counts["k2_flops"] / t_us / 1e6,
+                "frac": counts["k2_flops"] / t_us / 1e6 / tc, "bound": "tensor"}
+
     kern = {
-        "norms": {"us": k1_us, "GB/s": counts["k1_bytes"] / k1_us / 1e3,
-                  "frac": counts["k1_bytes"] / k1_us / 1e3 / hbm, "bound": "hbm"},
-        "project": {"us": k2_us, "TFLOP/s": counts["k2_flops"] / k2_us / 1e6,
-                    "frac": counts["k2_flops"] / k2_us / 1e6 / tc, "bound": "tensor",
-                    "split_k_workspace_bytes": ws_bytes},
-        "store": {"us": k3_us, "GB/s": k3_bytes / k3_us / 1e3, "frac": k3_bytes / k3_us / 1e3 / hbm,
-                  "bound": "hbm"},
+        "norms": hbm_entry(counts["k1_bytes"], us(k1_ms)),
+        "project_store": dict(tc_entry(us(ps_ms)), split_k_workspace_bytes=ws_bytes),
+        "unfused": {"norms": hbm_entry(counts["k1_bytes"], us(u_ms[0])),
+                    "project": tc_entry(us(u_ms[1])),
+                    "store": hbm_entry(k3_bytes, us(u_ms[2]))},
     }
-    dominant = max(kern, key=lambda k: kern[k]["us"])
+    dominant = "project_store" if kern["project_store"]["us"] >= kern["norms"]["us"] else "norms"
     d = kern[dominant]
     if d["bound"] == "tensor":
         roof = {"kernel": dominant, "bound": "tensor", "achieved": d["TFLOP/s"], "peak": tc,
@@ -361,6 +376,7 @@ def run_ours(args, w):
     rec = base_record(args, w, world)
     rec["config"]["l2"] = "flushed (512 MiB write) before every timed step"
     rec["config"]["timing"] = timing
+    rec["config"]["path"] = "rc_context_norms + rc_kv_project_store (fused projection and store)"
     rec.update({
         "value": world * w.T * args.steps / (total_ms / 1e3),
         "ms_per_step": total_ms / args.steps,

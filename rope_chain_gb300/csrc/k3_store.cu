@@ -113,17 +113,20 @@ k3_kv_store(const __grid_constant__ StoreLaunch p)
 // Split-K projection finished and stored in one pass: the FP32 partials
 // [splits, L, T, 128 H] are added in split order and rounded to bf16 (the
 // same additions as the projection's reduce kernel), optionally written to
-// kv_out, and stored like k3_kv_store.  One warp per (row, layer), all rows
-// of the projection (kv_out), storing the first fs.rows.
-template <int H, bool kRope>
+// kv_out, and stored like k3_kv_store.  One warp per (row, layer, head): the
+// K-norm needs only its head, and many splits (small T) still leave enough
+// warps; the split loop is unrolled so 8 partials are in flight per lane.
+template <bool kRope>
 __global__ void __launch_bounds__(kWarps * 32)
 k3_reduce_store(const __grid_constant__ FusedStore fs, const float *__restrict__ partial,
                 int32_t splits, int32_t L, int32_t T)
 {
-    constexpr int N = 2 * H * kHeadDim;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * kWarps + warp;
     const int layer = blockIdx.y;
+    const int h = blockIdx.z;
+    const int H = fs.H;
+    const int N = 2 * H * kHeadDim;
     pdl_trigger();
     pdl_wait();
     if (row >= T)
@@ -137,43 +140,45 @@ k3_reduce_store(const __grid_constant__ FusedStore fs, const float *__restrict__
             pos = __ldg(fs.positions + row);
     }
     const int64_t plane = (int64_t)L * T * N;
-    const float *p0 = partial + ((int64_t)layer * T + row) * N + 2 * lane;
-    float2 ka[H], va[H];
+    const float *pk = partial + ((int64_t)layer * T + row) * N + h * kHeadDim + 2 * lane;
+    const float *pv = pk + H * kHeadDim;
+    float2 ka = __ldcs(reinterpret_cast<const float2 *>(pk));
+    float2 va = __ldcs(reinterpret_cast<const float2 *>(pv));
+    int sp = 1;
+    for (; sp + 8 <= splits; sp += 8) {
+        float2 a[8], b[8];
 #pragma unroll
-    for (int h = 0; h < H; ++h) {
-        ka[h] = __ldcs(reinterpret_cast<const float2 *>(p0 + h * kHeadDim));
-        va[h] = __ldcs(reinterpret_cast<const float2 *>(p0 + (H + h) * kHeadDim));
-    }
-    for (int sp = 1; sp < splits; ++sp) {
-        const float *q = p0 + sp * plane;
+        for (int u = 0; u < 8; ++u) {
+            a[u] = __ldcs(reinterpret_cast<const float2 *>(pk + (sp + u) * plane));
+            b[u] = __ldcs(reinterpret_cast<const float2 *>(pv + (sp + u) * plane));
+        }
 #pragma unroll
-        for (int h = 0; h < H; ++h) {
-            const float2 a = __ldcs(reinterpret_cast<const float2 *>(q + h * kHeadDim));
-            const float2 b = __ldcs(reinterpret_cast<const float2 *>(q + (H + h) * kHeadDim));
-            ka[h].x = __fadd_rn(ka[h].x, a.x);
-            ka[h].y = __fadd_rn(ka[h].y, a.y);
-            va[h].x = __fadd_rn(va[h].x, b.x);
-            va[h].y = __fadd_rn(va[h].y, b.y);
+        for (int u = 0; u < 8; ++u) {
+            ka.x = __fadd_rn(ka.x, a[u].x);
+            ka.y = __fadd_rn(ka.y, a[u].y);
+            va.x = __fadd_rn(va.x, b[u].x);
+            va.y = __fadd_rn(va.y, b[u].y);
         }
     }
-    uint32_t kw[H], vw[H];
-#pragma unroll
-    for (int h = 0; h < H; ++h) {
-        kw[h] = pack_bf16x2(ka[h].x, ka[h].y);
-        vw[h] = pack_bf16x2(va[h].x, va[h].y);
+    for (; sp < splits; ++sp) {
+        const float2 a = __ldcs(reinterpret_cast<const float2 *>(pk + sp * plane));
+        const float2 b = __ldcs(reinterpret_cast<const float2 *>(pv + sp * plane));
+        ka.x = __fadd_rn(ka.x, a.x);
+        ka.y = __fadd_rn(ka.y, a.y);
+        va.x = __fadd_rn(va.x, b.x);
+        va.y = __fadd_rn(va.y, b.y);
     }
+    const uint32_t kw = pack_bf16x2(ka.x, ka.y), vw = pack_bf16x2(va.x, va.y);
     if (fs.kv_out != nullptr) {
         uint32_t *o = reinterpret_cast<uint32_t *>(fs.kv_out + ((int64_t)layer * T + row) * N) + lane;
-#pragma unroll
-        for (int h = 0; h < H; ++h) {
-            o[h * (kHeadDim / 2)] = kw[h];
-            o[(H + h) * (kHeadDim / 2)] = vw[h];
-        }
+        o[h * (kHeadDim / 2)] = kw;
+        o[(H + h) * (kHeadDim / 2)] = vw;
     }
     if (!store || slot < 0)
         return;
     if (slot >= fs.capacity || (kRope && (pos < 0 || pos >= fs.max_position))) {
-        count_skip(fs.err, lane);
+        if (h == 0)                               // once per (row, layer)
+            count_skip(fs.err, lane);
         return;
     }
     float c = 1.0f, s = 0.0f;
@@ -182,22 +187,15 @@ k3_reduce_store(const __grid_constant__ FusedStore fs, const float *__restrict__
         c = __uint_as_float((uint32_t)__ldg(cs + lane) << 16);
         s = __uint_as_float((uint32_t)__ldg(cs + kHeadDim / 2 + lane) << 16);
     }
-    uint32_t ko[H];
-#pragma unroll
-    for (int h = 0; h < H; ++h)
-        ko[h] = knorm_rope_lane<kRope>(bf16_lo(kw[h]), bf16_hi(kw[h]), c, s, fs.eps);
-    insert_row<H>(fs.caches[layer], slot, fs.block_size, ko, vw, lane);
-}
-
-template <int H>
-cudaError_t launch_rs(const FusedStore &fs, const float *partial, int32_t splits, int32_t L,
-                      int32_t T, cudaStream_t stream) {
-    const dim3 grid((unsigned)((T + kWarps - 1) / kWarps), (unsigned)L);
-    if (fs.cos_sin)
-        return launch_pdl(k3_reduce_store<H, true>, grid, dim3(kWarps * 32), 0, stream, 1, fs, partial,
-                          splits, L, T);
-    return launch_pdl(k3_reduce_store<H, false>, grid, dim3(kWarps * 32), 0, stream, 1, fs, partial,
-                      splits, L, T);
+    const uint32_t ko = knorm_rope_lane<kRope>(bf16_lo(kw), bf16_hi(kw), c, s, fs.eps);
+    // Slots of a cache fit 32 bits (checked on the host).
+    const uint32_t bs = (uint32_t)fs.block_size;
+    const uint32_t blk = (uint32_t)slot / bs;
+    const uint32_t page = (uint32_t)slot - blk * bs;
+    uint32_t *dst = reinterpret_cast<uint32_t *>(fs.caches[layer]) +
+                    (((int64_t)blk * H + h) * bs + page) * kHeadDim + lane;
+    dst[0] = ko;
+    dst[kHeadDim / 2] = vw;                       // V follows K
 }
 
 template <int H>
@@ -213,15 +211,12 @@ cudaError_t launch_h(const StoreLaunch &p, int32_t layers, cudaStream_t stream) 
 cudaError_t launch_reduce_store(const FusedStore &fs, const float *partial, int32_t splits,
                                 int32_t L, int32_t T, cudaStream_t stream)
 {
-    switch (fs.H) {
-    case 1: return launch_rs<1>(fs, partial, splits, L, T, stream);
-    case 2: return launch_rs<2>(fs, partial, splits, L, T, stream);
-    case 4: return launch_rs<4>(fs, partial, splits, L, T, stream);
-    case 8: return launch_rs<8>(fs, partial, splits, L, T, stream);
-    case 16: return launch_rs<16>(fs, partial, splits, L, T, stream);
-    case 32: return launch_rs<32>(fs, partial, splits, L, T, stream);
-    default: return cudaErrorInvalidValue;
-    }
+    const dim3 grid((unsigned)((T + kWarps - 1) / kWarps), (unsigned)L, (unsigned)fs.H);
+    if (fs.cos_sin)
+        return launch_pdl(k3_reduce_store<true>, grid, dim3(kWarps * 32), 0, stream, 1, fs, partial,
+                          splits, L, T);
+    return launch_pdl(k3_reduce_store<false>, grid, dim3(kWarps * 32), 0, stream, 1, fs, partial,
+                      splits, L, T);
 }
 
 cudaError_t launch_kv_store(const StoreLaunch &p, int32_t H, int32_t layers, cudaStream_t stream)
