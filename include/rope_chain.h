@@ -207,6 +207,42 @@ rc_status rc_kv_project_store(const uint16_t *normed, const uint16_t *W,
                               size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * rc_context_kv -- the whole chain in one call (steps 1 to 4; [rt]
+ * ContextKV.store / MuseSparkDSparkModel.precompute_and_store_context_kv),
+ * with the norms fused into the projection (the scope's "norms fused into
+ * the GEMM producer"): a row pass writes the hidden-norm output
+ * z = bf16(hidden_norm(x)) and each row's layer-norm inverse RMS r once; the
+ * projection forms each layer's operand bf16((z * r) * pre_w[l]) in shared
+ * memory (bit-identical to rc_context_norms' output) and stores as
+ * rc_kv_project_store does.  The [L, T, D] normed rows never reach memory.
+ * The caches receive exactly the bits of rc_context_norms +
+ * rc_kv_project_store with an equally split projection.
+ *
+ *   x, T, D, hidden_w, pre_w, L, eps      as rc_context_norms (D = 8192,
+ *                                         L <= 64)
+ *   W, w_layout, H                        as rc_kv_project (N = 128*H)
+ *   positions ... err, kv_out             as rc_kv_project_store
+ *   workspace   device scratch, 256-byte aligned, required: the row pass's
+ *               z and r (T*D*2 + T*4 bytes, rounded up) — or, for T <= 128
+ *               or H = 1, the normed rows [L, T, D] — followed by the split-K
+ *               partials; rc_context_kv_workspace_size() gives the bytes of
+ *               the full plan, and less space splits K less.
+ */
+rc_status rc_context_kv(const uint16_t *x, int64_t T, int32_t D,
+                        const uint16_t *hidden_w, const uint16_t *pre_w,
+                        int32_t L, float eps, const uint16_t *W,
+                        int32_t w_layout, int32_t H, const int64_t *positions,
+                        const int64_t *const *slots, const uint16_t *cos_sin,
+                        int64_t max_position, uint16_t *const *caches,
+                        int32_t num_blocks, int32_t block_size, int64_t rows,
+                        int32_t *err, uint16_t *kv_out, void *workspace,
+                        size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes of rc_context_kv for these sizes on the current device
+   (0 for unsupported sizes). */
+size_t rc_context_kv_workspace_size(int32_t L, int64_t T, int32_t D, int32_t H);
+
+/*
  * rc_kv_project_no_alloc -- rc_kv_project for callers that cannot allocate.
  * The pages have no counterpart: it is an addition of this library.
  *

@@ -50,6 +50,11 @@ SIGNATURES = {
     "rc_read_device_faults": ([_c.POINTER(_c.c_uint32), _c.c_int32], _c.c_int),
     "rc_kv_project_no_alloc": ([_vp, _vp, _c.c_int32, _vp, _c.c_int32, _c.c_int64, _c.c_int32,
                                 _c.c_int32, _vp], _c.c_int),
+    "rc_context_kv": ([_vp, _c.c_int64, _c.c_int32, _vp, _vp, _c.c_int32, _c.c_float, _vp,
+                       _c.c_int32, _c.c_int32, _vp, _c.POINTER(_vp), _vp, _c.c_int64,
+                       _c.POINTER(_vp), _c.c_int32, _c.c_int32, _c.c_int64, _vp, _vp, _vp,
+                       _c.c_size_t, _vp], _c.c_int),
+    "rc_context_kv_workspace_size": ([_c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32], _c.c_size_t),
     "rc_kv_project_store": ([_vp, _vp, _c.c_int32, _c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32,
                              _vp, _c.POINTER(_vp), _vp, _c.c_int64, _c.POINTER(_vp), _c.c_int32,
                              _c.c_int32, _c.c_float, _c.c_int64, _vp, _vp, _vp, _c.c_size_t, _vp],
@@ -251,6 +256,68 @@ def kv_project_store(normed: torch.Tensor, W: torch.Tensor, H: int, positions, s
                                      0 if cos_sin is None else cos_sin.shape[0], cache_arr, nb, bs,
                                      eps, rows, _ptr(err), _ptr(kv_out), ws_ptr, ws_bytes,
                                      _stream(stream)))
+
+
+def context_kv_workspace(L: int, T: int, H: int, device, D: int = 8192) -> torch.Tensor:
+    """A workspace for context_kv (rc_context_kv_workspace_size bytes)."""
+    n = int(lib().rc_context_kv_workspace_size(L, T, D, H))
+    if n == 0:
+        raise RopeChainError(RC_ERR_UNSUPPORTED, "no workspace size for these sizes")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def _store_operands(H, slots, caches, positions, cos_sin, rows):
+    L = len(caches)
+    nb, h_, bs, w_ = caches[0].shape
+    if h_ != H or w_ != 2 * HEAD_DIM:
+        raise ValueError("caches must be [num_blocks, H, block_size, 128]")
+    for c in caches:
+        _bf16(c, "cache")
+        if tuple(c.shape) != (nb, h_, bs, w_):
+            raise ValueError("all caches must have one shape")
+    if len(slots) != L:
+        raise ValueError("slots and caches need one entry per layer")
+    for sl in slots:
+        if sl is not None and (sl.dtype != torch.int64 or not sl.is_contiguous() or not sl.is_cuda):
+            raise ValueError("slots must be contiguous CUDA int64 tensors")
+    if rows is None:
+        first = next((sl for sl in slots if sl is not None), None)
+        rows = 0 if first is None else first.shape[0]
+    for sl in slots:
+        if sl is not None and sl.shape[0] < rows:
+            raise ValueError("every slot mapping needs at least `rows` entries")
+    if cos_sin is not None:
+        _bf16(cos_sin, "cos_sin")
+        if positions is None or positions.dtype != torch.int64 or not positions.is_contiguous():
+            raise ValueError("RoPE needs contiguous int64 positions")
+    slot_arr = (_vp * L)(*[_ptr(sl) for sl in slots])
+    cache_arr = (_vp * L)(*[c.data_ptr() for c in caches])
+    return slot_arr, cache_arr, nb, bs, rows
+
+
+def context_kv(x: torch.Tensor, hidden_w, pre_w, W: torch.Tensor, H: int, positions, slots,
+               cos_sin, caches, eps: float, workspace: torch.Tensor, rows: Optional[int] = None,
+               err=None, kv_out: Optional[torch.Tensor] = None, w_layout: int = RC_W_KN,
+               stream=None) -> None:
+    """The whole chain in one call (rc_context_kv): norms fused into the
+    projection, store fused after it.  ``workspace``: context_kv_workspace()."""
+    _bf16(x, "x")
+    _bf16(W, "W")
+    T, D = x.shape
+    L = len(caches)
+    for w_, n in ((hidden_w, "hidden_w"), (pre_w, "pre_w")):
+        if w_ is not None:
+            _bf16(w_, n)
+    if kv_out is not None:
+        _bf16(kv_out, "kv_out")
+    if not (workspace.is_cuda and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    slot_arr, cache_arr, nb, bs, rows = _store_operands(H, slots, caches, positions, cos_sin, rows)
+    _check(lib().rc_context_kv(x.data_ptr(), T, D, _ptr(hidden_w), _ptr(pre_w), L, eps,
+                               W.data_ptr(), w_layout, H, _ptr(positions), slot_arr, _ptr(cos_sin),
+                               0 if cos_sin is None else cos_sin.shape[0], cache_arr, nb, bs, rows,
+                               _ptr(err), _ptr(kv_out), workspace.data_ptr(),
+                               workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def split_kv(kv: torch.Tensor, H: int):

@@ -140,6 +140,54 @@ k1_context_norms(const uint16_t *__restrict__ x, int64_t T,
     }
 }
 
+// The row half of the norms for the fused chain: z = bf16(hidden_norm(x))
+// and r2 = the layers' shared inverse RMS of z, per row; the projection
+// forms each layer's bf16((z * r2) * gamma_l) tile itself.  Same arithmetic
+// and order as k1_context_norms.
+template <bool kHiddenW>
+__global__ void __launch_bounds__(kThreads, 4)
+k1_row_prep(const uint16_t *__restrict__ x, const uint16_t *__restrict__ hidden_w, float eps,
+            uint16_t *__restrict__ z, float *__restrict__ r2_out)
+{
+    __shared__ float sums[2][kThreads / 32];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t row = blockIdx.x;
+    pdl_trigger();
+    pdl_wait();
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x) + row * (kHidden / 8);
+    const uint4 *gh = reinterpret_cast<const uint4 *>(hidden_w);
+    uint4 q[kFrags], hq[kFrags];
+#pragma unroll
+    for (int k = 0; k < kFrags; ++k) {
+        q[k] = __ldcs(xr + k * kFragStride + tid);
+        if (kHiddenW)
+            hq[k] = __ldg(gh + k * kFragStride + tid);
+    }
+    const float r = inv_rms(row_sumsq(q, sums[0], warp, lane), 0x1p-13f, eps);
+    uint4 *zr = reinterpret_cast<uint4 *>(z) + row * (kHidden / 8);
+#pragma unroll
+    for (int k = 0; k < kFrags; ++k) {
+        float f[8];
+        unpack8(q[k], f);
+        if (kHiddenW) {
+            float g[8];
+            unpack8(hq[k], g);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                f[i] = __fmul_rn(__fmul_rn(f[i], r), g[i]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                f[i] = __fmul_rn(f[i], r);
+        }
+        q[k] = pack8(f);
+        zr[k * kFragStride + tid] = q[k];
+    }
+    const float r2 = inv_rms(row_sumsq(q, sums[1], warp, lane), 0x1p-13f, eps);
+    if (tid == 0)
+        r2_out[row] = r2;
+}
+
 }  // namespace
 
 cudaError_t launch_context_norms(const uint16_t *x, int64_t T, const uint16_t *hidden_w,
@@ -154,6 +202,15 @@ cudaError_t launch_context_norms(const uint16_t *x, int64_t T, const uint16_t *h
     if (pre_w)
         return launch_pdl(k1_context_norms<false, true>, grid, block, 0, stream, 1, x, T, hidden_w, pre_w, L, eps, out);
     return launch_pdl(k1_context_norms<false, false>, grid, block, 0, stream, 1, x, T, hidden_w, pre_w, L, eps, out);
+}
+
+cudaError_t launch_row_prep(const uint16_t *x, int64_t T, const uint16_t *hidden_w, float eps,
+                            uint16_t *z, float *r2, cudaStream_t stream)
+{
+    const dim3 grid((unsigned)T), block(kThreads);
+    if (hidden_w)
+        return launch_pdl(k1_row_prep<true>, grid, block, 0, stream, 1, x, hidden_w, eps, z, r2);
+    return launch_pdl(k1_row_prep<false>, grid, block, 0, stream, 1, x, hidden_w, eps, z, r2);
 }
 
 }  // namespace rc

@@ -84,6 +84,30 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
+// try_wait with acquire at cluster scope (arrivals released by the peer CTA).
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 0;; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok)
+            return true;
+        if ((it & 255u) == 255u && (faulted() || globaltimer() - t0 > kWaitNs))
+            return false;
+    }
+}
+
+// Arrive on a barrier of any CTA of the cluster (a shared::cluster address).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
@@ -171,6 +195,10 @@ struct GemmArgs {
     int32_t kb_total, kb_per_split, splits;
     uint16_t *out;       // bf16 [L, T, N] when splits == 1
     float *partial;      // FP32 [splits, L, T, N] when splits > 1
+    // Pair kernel forming A in shared memory (fused norms): A = z [T, D]
+    // scaled per row by row_scale and per column by col_gain [L, D] (or 1)
+    const float *row_scale;
+    const uint16_t *col_gain;
 };
 
 template <int BN>
@@ -569,9 +597,23 @@ struct PairCfg {
     static constexpr uint32_t kStageBytes = kABytes + kBHalf;    // 32 KiB per CTA
     static constexpr uint32_t kPairTx = 2 * kStageBytes;         // counted on the leader
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 256;
+    static_assert((4 * kStages + 1) * 8 + 5 * 4 <= 256, "barriers and words fit the tail");
 };
 
-template <bool kBmn, bool kFused>
+__device__ __forceinline__ void unpack8f(const uint4 &q, float *f) {
+    f[0] = bf16_lo(q.x); f[1] = bf16_hi(q.x);
+    f[2] = bf16_lo(q.y); f[3] = bf16_hi(q.y);
+    f[4] = bf16_lo(q.z); f[5] = bf16_hi(q.z);
+    f[6] = bf16_lo(q.w); f[7] = bf16_hi(q.w);
+}
+
+// kTransform: the A tile is formed in shared memory from the hidden-norm
+// output z (TMA-loaded): A = bf16((z * row_scale) * col_gain_l), the same
+// operations and roundings as the norms kernel's layer step, so the operand
+// is bit-identical to the normed rows that kernel would have written.  The
+// 4 epilogue warps do it in place (128-byte swizzled rows: logical 16-byte
+// chunk c of row r sits at chunk c ^ (r % 8)) before the epilogue.
+template <bool kBmn, bool kFused, bool kTransform>
 __global__ void __launch_bounds__(kThreads, 1)
 k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmArgs g, const __grid_constant__ FusedStore fs)
@@ -584,12 +626,16 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const uint32_t sA = smem_u32(smem);
     const uint32_t sB = sA + S * kABytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * C::kStageBytes);
-    const uint32_t bar0 = smem_u32(bars);         // full[s] (leader), empty[s], accum
-    const uint32_t accum = bar0 + 8u * (2 * S);
+    // full[s] (leader: B, and A unless kTransform), empty[s], aload[s]
+    // (kTransform: this CTA's A), ready[s] (kTransform, leader: A formed in
+    // both CTAs), accum
+    const uint32_t bar0 = smem_u32(bars);
+    const uint32_t empty0 = bar0 + 8u * S, aload0 = bar0 + 16u * S, ready0 = bar0 + 24u * S;
+    const uint32_t accum = bar0 + 32u * S;
     // words[0]: TMEM base; [1]: stages the leader's MMA thread consumed;
     // [2]: skip flag (written by the leader into both CTAs); [3]: stages the
     // peer's loader issued (written by the peer into the leader)
-    volatile uint32_t *words = reinterpret_cast<volatile uint32_t *>(bars + 2 * S + 1);
+    volatile uint32_t *words = reinterpret_cast<volatile uint32_t *>(bars + 4 * S + 1);
     const uint32_t words_addr = smem_u32((const void *)words);
 
     const int warp = __shfl_sync(0xFFFFFFFFu, (int)(threadIdx.x >> 5), 0);
@@ -608,7 +654,9 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(bar0 + 8u * s, 1);
-            mbar_init(bar0 + 8u * (S + s), 1);
+            mbar_init(empty0 + 8u * s, 1);
+            mbar_init(aload0 + 8u * s, 1);
+            mbar_init(ready0 + 8u * s, 8);         // 4 warps in each CTA of the pair
         }
         mbar_init(accum, 1);
         words[1] = 0u;
@@ -643,15 +691,20 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % S;
                 const uint32_t ph = (uint32_t)(i / S) & 1u;
-                if (!mbar_wait(bar0 + 8u * (S + s), ph ^ 1u)) {
+                if (!mbar_wait(empty0 + 8u * s, ph ^ 1u)) {
                     raise_fault(kFaultLoad);
                     break;
                 }
                 const uint32_t full = map_to_rank(bar0 + 8u * s, 0);
                 if (leader)
-                    mbar_expect_tx(bar0 + 8u * s, C::kPairTx);
+                    mbar_expect_tx(bar0 + 8u * s, kTransform ? 2u * C::kBHalf : C::kPairTx);
                 const int kc = (kb0 + i) * BK;
-                tma_load_3d_pair(sA + s * kABytes, &tmA, kc, m0, l, full);
+                if (kTransform) {
+                    mbar_expect_tx(aload0 + 8u * s, kABytes);
+                    tma_load_3d(sA + s * kABytes, &tmA, kc, m0, 0, aload0 + 8u * s);
+                } else {
+                    tma_load_3d_pair(sA + s * kABytes, &tmA, kc, m0, l, full);
+                }
                 if (kBmn) {
                     tma_load_3d_pair(sB + s * C::kBHalf, &tmB, nb, kc, l, full);
                     tma_load_3d_pair(sB + s * C::kBHalf + 8192u, &tmB, nb + 64, kc, l, full);
@@ -669,7 +722,8 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 for (int i = 0; i < nkb; ++i) {
                     const int s = i % S;
                     const uint32_t ph = (uint32_t)(i / S) & 1u;
-                    if (!mbar_wait(bar0 + 8u * s, ph)) {
+                    if (!mbar_wait(bar0 + 8u * s, ph) ||
+                        (kTransform && !mbar_wait_cluster(ready0 + 8u * s, ph))) {
                         raise_fault(kFaultMma);
                         break;
                     }
@@ -682,7 +736,7 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                                  : smem_desc_sw128(b + 32u * kk, 16u, 1024u);
                         mma_bf16_pair(tmem, ad, bd, idesc, (i | kk) != 0 ? 1u : 0u);
                     }
-                    mma_commit_pair(bar0 + 8u * (S + s));
+                    mma_commit_pair(empty0 + 8u * s);
                     consumed = i + 1;
                 }
             }
@@ -692,6 +746,54 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         __syncwarp();
     } else {
         const int q = warp & 3;
+        if (kTransform && !skip) {
+            // Form this CTA's A tiles: thread t takes logical chunk c = t % 8
+            // (8 columns) of rows t / 8 + 16 j, j < 8.
+            const int t = (int)threadIdx.x - 64;
+            const int c = t & 7, r0 = t >> 3;
+            float rs[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int row = m0 + r0 + 16 * j;
+                rs[j] = row < g.T ? __ldg(g.row_scale + row) : 0.0f;
+            }
+            const uint16_t *gain = g.col_gain ? g.col_gain + (int64_t)l * (g.kb_total * BK) : nullptr;
+            const uint32_t ready_lead = map_to_rank(ready0, 0);
+            for (int i = 0; i < nkb; ++i) {
+                const int s = i % S;
+                const uint32_t ph = (uint32_t)(i / S) & 1u;
+                if (!mbar_wait(aload0 + 8u * s, ph)) {
+                    raise_fault(kFaultLoad);
+                    break;
+                }
+                float gm[8];
+                if (gain)
+                    unpack8f(__ldg(reinterpret_cast<const uint4 *>(gain + (kb0 + i) * BK + 8 * c)), gm);
+                uint8_t *st = smem + s * kABytes;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int r = r0 + 16 * j;
+                    uint4 *p = reinterpret_cast<uint4 *>(st + r * 128 + ((c ^ (r & 7)) << 4));
+                    float f[8];
+                    unpack8f(*p, f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        f[e] = __fmul_rn(f[e], rs[j]);
+                    if (gain) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            f[e] = __fmul_rn(f[e], gm[e]);
+                    }
+                    *p = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                    pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                }
+                // generic-proxy writes, then visible to the tensor core
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_cluster(ready_lead + 8u * s);
+            }
+        }
         bool ok = !skip && mbar_wait(accum, 0u);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok && !skip && lane == 0)
@@ -736,15 +838,24 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (!leader && warp == 0 && lane == 0)
         st_cluster_u32(map_to_rank(words_addr + 12u, 0), (uint32_t)issued);
     cluster_sync();
-    if (leader && warp == 0 && lane == 0) {
-        // Both CTAs' loads land on the leader's barriers: after a fault, wait
-        // for every stage either CTA issued before anyone frees smem.
-        const int last = max(issued, (int)words[3]);
-        for (int i = (int)words[1]; i < last; ++i)
-            if (!mbar_wait_own(bar0 + 8u * (i % S), (uint32_t)(i / S) & 1u)) {
-                raise_fault(kFaultDrain);
-                break;
-            }
+    if (warp == 0 && lane == 0) {
+        if (leader) {
+            // Both CTAs' B (and A) loads land on the leader's barriers: after
+            // a fault, wait for every stage either CTA issued before anyone
+            // frees smem.
+            const int last = max(issued, (int)words[3]);
+            for (int i = (int)words[1]; i < last; ++i)
+                if (!mbar_wait_own(bar0 + 8u * (i % S), (uint32_t)(i / S) & 1u)) {
+                    raise_fault(kFaultDrain);
+                    break;
+                }
+        }
+        if (kTransform)                               // this CTA's own A loads
+            for (int i = max(0, issued - S); i < issued; ++i)
+                if (!mbar_wait_own(aload0 + 8u * (i % S), (uint32_t)(i / S) & 1u)) {
+                    raise_fault(kFaultDrain);
+                    break;
+                }
     }
     if (leader && warp == 1 && lane == 0 && !mbar_wait_own(accum, 0u))
         raise_fault(kFaultDrain);
@@ -815,7 +926,7 @@ cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, const Gemm
     return launch_pdl(k2_project<BN, kBmn>, grid, dim3(kThreads), Cfg<BN>::kSmem, stream, 1, ma, mb, g);
 }
 
-template <bool kBmn, bool kFused>
+template <bool kBmn, bool kFused, bool kTransform>
 cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &g,
                         const FusedStore &fs, int n_pairs, int m_pairs, cudaStream_t stream) {
     static bool configured[64] = {};
@@ -824,7 +935,7 @@ cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const Gemm
     if (e != cudaSuccess)
         return e;
     if (dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(k2_project_pair<kBmn, kFused>,
+        e = cudaFuncSetAttribute(k2_project_pair<kBmn, kFused, kTransform>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PairCfg::kSmem);
         if (e != cudaSuccess)
             return e;
@@ -832,8 +943,8 @@ cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const Gemm
             configured[dev] = true;
     }
     const dim3 grid((unsigned)(2 * n_pairs), (unsigned)m_pairs, (unsigned)(g.L * g.splits));
-    return launch_pdl(k2_project_pair<kBmn, kFused>, grid, dim3(kThreads), PairCfg::kSmem, stream, 2,
-                      ma, mb, g, fs);
+    return launch_pdl(k2_project_pair<kBmn, kFused, kTransform>, grid, dim3(kThreads), PairCfg::kSmem,
+                      stream, 2, ma, mb, g, fs);
 }
 
 }  // namespace
@@ -887,6 +998,8 @@ bool project_setup(const uint16_t *normed, const uint16_t *W, bool w_nk, uint16_
     g->splits = plan.splits;
     g->out = out;
     g->partial = ws;
+    g->row_scale = nullptr;
+    g->col_gain = nullptr;
     return true;
 }
 
@@ -896,8 +1009,8 @@ cudaError_t launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const Gemm
                         const FusedStore &fs, bool w_nk, const ProjectPlan &plan, int64_t T,
                         int32_t N, cudaStream_t stream) {
     if (plan.pair)
-        return w_nk ? launch_pair<false, kFused>(ma, mb, g, fs, N / 256, (int)((T + 255) / 256), stream)
-                    : launch_pair<true, kFused>(ma, mb, g, fs, N / 256, (int)((T + 255) / 256), stream);
+        return w_nk ? launch_pair<false, kFused, false>(ma, mb, g, fs, N / 256, (int)((T + 255) / 256), stream)
+                    : launch_pair<true, kFused, false>(ma, mb, g, fs, N / 256, (int)((T + 255) / 256), stream);
     const int n_tiles = N / plan.bn;
     const int m_tiles = (int)((T + BM - 1) / BM);
     if (plan.bn == 256)
@@ -988,6 +1101,41 @@ cudaError_t launch_kv_project_store(const uint16_t *normed, const uint16_t *W, b
             return e;
     }
     return cudaSuccess;
+}
+
+cudaError_t launch_context_kv(const uint16_t *x, int64_t T, const uint16_t *hidden_w,
+                              const uint16_t *pre_w, float eps, const uint16_t *W, bool w_nk,
+                              int32_t L, int32_t N, const ProjectPlan &plan, uint16_t *z, float *r2,
+                              float *ws, const FusedStore &fs, cudaStream_t stream, const char **why)
+{
+    constexpr int D = kHidden;
+    cudaError_t e = launch_row_prep(x, T, hidden_w, eps, z, r2, stream);
+    if (e != cudaSuccess) {
+        *why = "row prep launch";
+        return e;
+    }
+    CUtensorMap ma, mb;
+    GemmArgs g;
+    if (!project_setup(z, W, w_nk, fs.kv_out, L, T, D, N, plan, ws, &ma, &mb, &g, why))
+        return cudaErrorInvalidValue;
+    // A is z [T, D] (one "layer"), formed per layer in shared memory
+    if (!make_map(&ma, z, (uint64_t)D, (uint64_t)T, 1, BK, BM)) {
+        *why = "tensor map of the hidden-norm rows could not be encoded";
+        return cudaErrorInvalidValue;
+    }
+    g.row_scale = r2;
+    g.col_gain = pre_w;
+    const int n_pairs = N / 256, m_pairs = (int)((T + 255) / 256);
+    *why = "fused projection launch";
+    if (plan.splits == 1)
+        return w_nk ? launch_pair<false, true, true>(ma, mb, g, fs, n_pairs, m_pairs, stream)
+                    : launch_pair<true, true, true>(ma, mb, g, fs, n_pairs, m_pairs, stream);
+    e = w_nk ? launch_pair<false, false, true>(ma, mb, g, fs, n_pairs, m_pairs, stream)
+             : launch_pair<true, false, true>(ma, mb, g, fs, n_pairs, m_pairs, stream);
+    if (e != cudaSuccess)
+        return e;
+    *why = "reduce-and-store launch";
+    return launch_reduce_store(fs, ws, plan.splits, L, (int32_t)T, stream);
 }
 
 cudaError_t read_project_faults(uint32_t *flags, bool clear)

@@ -225,6 +225,76 @@ rc_status rc_kv_store(const uint16_t *k, const uint16_t *v, int64_t k_layer_stri
     return ok();
 }
 
+}  // extern "C"
+
+namespace {
+
+// Checks the store operands of the fused calls and fills a FusedStore.
+rc_status fused_store_args(const char *fn, int32_t L, int64_t T, int32_t H,
+                           const int64_t *positions, const int64_t *const *slots,
+                           const uint16_t *cos_sin, int64_t max_position, uint16_t *const *caches,
+                           int32_t num_blocks, int32_t block_size, float eps, int64_t rows,
+                           int32_t *err, uint16_t *kv_out, rc::FusedStore *fs)
+{
+    if (L > rc::kMaxFusedLayers)
+        return fail(RC_ERR_UNSUPPORTED, "%s: L=%d above %d", fn, L, rc::kMaxFusedLayers);
+    if (!slots || !caches)
+        return fail(RC_ERR_INVALID_ARG, "%s: slots and caches must not be NULL", fn);
+    if (kv_out && !aligned(kv_out, 16))
+        return fail(RC_ERR_INVALID_ARG, "%s: kv_out must be 16-byte aligned", fn);
+    if (rows < 0 || rows > T)
+        return fail(RC_ERR_INVALID_ARG, "%s: rows=%lld outside [0, T]", fn, (long long)rows);
+    if (num_blocks < 1 || block_size < 1 || (int64_t)num_blocks * block_size >= (1LL << 31))
+        return fail(RC_ERR_INVALID_ARG,
+                    "%s: need num_blocks, block_size >= 1 and num_blocks*block_size < 2^31", fn);
+    if (cos_sin) {
+        if (!positions || !aligned(positions, 8))
+            return fail(RC_ERR_INVALID_ARG, "%s: RoPE needs 8-byte aligned positions", fn);
+        if (max_position < 1)
+            return fail(RC_ERR_INVALID_ARG, "%s: max_position must be >= 1 with a table", fn);
+        if (!aligned(cos_sin, 16))
+            return fail(RC_ERR_INVALID_ARG, "%s: cos_sin must be 16-byte aligned", fn);
+    }
+    *fs = rc::FusedStore{};
+    for (int32_t l = 0; l < L; ++l) {
+        if (slots[l]) {
+            if (!aligned(slots[l], 8))
+                return fail(RC_ERR_INVALID_ARG, "%s: slots[%d] must be 8-byte aligned", fn, l);
+            if (!caches[l] || !aligned(caches[l], 16))
+                return fail(RC_ERR_INVALID_ARG, "%s: caches[%d] must be a 16-byte aligned pointer", fn, l);
+        }
+        fs->slots[l] = slots[l];
+        fs->caches[l] = caches[l];
+    }
+    fs->positions = positions;
+    fs->cos_sin = cos_sin;
+    fs->max_position = max_position;
+    fs->capacity = (int64_t)num_blocks * block_size;
+    fs->block_size = block_size;
+    fs->H = H;
+    fs->rows = (int32_t)rows;
+    fs->eps = eps;
+    fs->err = err;
+    fs->kv_out = kv_out;
+    return RC_OK;
+}
+
+bool supported_heads(int32_t H) {
+    return H == 1 || H == 2 || H == 4 || H == 8 || H == 16 || H == 32;
+}
+
+size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+// Bytes the whole-chain call keeps ahead of the split-K partials.
+size_t context_kv_fixed_bytes(bool pair, int32_t L, int64_t T, int32_t D) {
+    return pair ? round256((size_t)T * D * 2) + round256((size_t)T * 4)
+                : round256((size_t)L * T * D * 2);
+}
+
+}  // namespace
+
+extern "C" {
+
 rc_status rc_kv_project_store(const uint16_t *normed, const uint16_t *W, int32_t w_layout,
                               int32_t L, int64_t T, int32_t D, int32_t H,
                               const int64_t *positions, const int64_t *const *slots,
@@ -233,73 +303,120 @@ rc_status rc_kv_project_store(const uint16_t *normed, const uint16_t *W, int32_t
                               float eps, int64_t rows, int32_t *err, uint16_t *kv_out,
                               void *workspace, size_t workspace_bytes, cudaStream_t stream)
 {
-    if (H != 1 && H != 2 && H != 4 && H != 8 && H != 16 && H != 32)
-        return fail(RC_ERR_UNSUPPORTED, "rc_kv_project_store: H=%d is not a power of two <= 32", H);
+    const char *fn = "rc_kv_project_store";
+    if (!supported_heads(H))
+        return fail(RC_ERR_UNSUPPORTED, "%s: H=%d is not a power of two <= 32", fn, H);
     const int32_t N = 2 * H * rc::kHeadDim;
     rc_status st = check_project_sizes(L, T, D, N);
     if (st != RC_OK)
         return st;
-    if (L > rc::kMaxFusedLayers)
-        return fail(RC_ERR_UNSUPPORTED, "rc_kv_project_store: L=%d above %d", L, rc::kMaxFusedLayers);
     if (w_layout != RC_W_KN && w_layout != RC_W_NK)
-        return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store: unknown weight layout %d", w_layout);
-    if (!normed || !W || !slots || !caches)
-        return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store: normed, W, slots and caches must not be NULL");
-    if (!aligned(normed, 16) || !aligned(W, 16) || (kv_out && !aligned(kv_out, 16)) ||
-        (workspace && !aligned(workspace, 16)))
-        return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store: normed, W, kv_out and workspace must be 16-byte aligned");
-    if (rows < 0 || rows > T)
-        return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store: rows=%lld outside [0, T]", (long long)rows);
-    if (num_blocks < 1 || block_size < 1 || (int64_t)num_blocks * block_size >= (1LL << 31))
-        return fail(RC_ERR_INVALID_ARG,
-                    "rc_kv_project_store: need num_blocks, block_size >= 1 and num_blocks*block_size < 2^31");
-    if (cos_sin) {
-        if (!positions || !aligned(positions, 8))
-            return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store: RoPE needs 8-byte aligned positions");
-        if (max_position < 1)
-            return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store: max_position must be >= 1 with a table");
-        if (!aligned(cos_sin, 16))
-            return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store: cos_sin must be 16-byte aligned");
-    }
-    for (int32_t l = 0; l < L; ++l) {
-        if (!slots[l])
-            continue;
-        if (!aligned(slots[l], 8))
-            return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store: slots[%d] must be 8-byte aligned", l);
-        if (!caches[l] || !aligned(caches[l], 16))
-            return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store: caches[%d] must be a 16-byte aligned pointer", l);
-    }
+        return fail(RC_ERR_INVALID_ARG, "%s: unknown weight layout %d", fn, w_layout);
+    if (!normed || !W)
+        return fail(RC_ERR_INVALID_ARG, "%s: normed and W must not be NULL", fn);
+    if (!aligned(normed, 16) || !aligned(W, 16) || (workspace && !aligned(workspace, 16)))
+        return fail(RC_ERR_INVALID_ARG, "%s: normed, W and workspace must be 16-byte aligned", fn);
+    rc::FusedStore fs;
+    st = fused_store_args(fn, L, T, H, positions, slots, cos_sin, max_position, caches, num_blocks,
+                          block_size, eps, rows, err, kv_out, &fs);
+    if (st != RC_OK)
+        return st;
     if (T == 0)
         return ok();
     if (kv_out && overlap(kv_out, (size_t)L * T * N * 2, normed, (size_t)L * T * D * 2))
-        return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store: kv_out overlaps normed");
+        return fail(RC_ERR_INVALID_ARG, "%s: kv_out overlaps normed", fn);
     const int sms = num_sms_current();
     if (sms <= 0)
-        return fail(RC_ERR_CUDA, "rc_kv_project_store: no current CUDA device");
+        return fail(RC_ERR_CUDA, "%s: no current CUDA device", fn);
     const rc::ProjectPlan plan =
         rc::plan_kv_project(L, T, D, N, sms, workspace ? workspace_bytes : 0);
     if (plan.splits == 1 && !plan.pair && !kv_out)
         return fail(RC_ERR_INVALID_ARG,
-                    "rc_kv_project_store: at these sizes the store reads the projection from kv_out; "
-                    "pass kv_out or a workspace of rc_kv_project_workspace_size() bytes");
-    rc::FusedStore fs{};
-    fs.positions = positions;
-    fs.cos_sin = cos_sin;
-    fs.max_position = max_position;
-    for (int32_t l = 0; l < L; ++l) {
-        fs.slots[l] = slots[l];
-        fs.caches[l] = caches[l];
-    }
-    fs.capacity = (int64_t)num_blocks * block_size;
-    fs.block_size = block_size;
-    fs.H = H;
-    fs.rows = (int32_t)rows;
-    fs.eps = eps;
-    fs.err = err;
-    fs.kv_out = kv_out;
+                    "%s: at these sizes the store reads the projection from kv_out; "
+                    "pass kv_out or a workspace of rc_kv_project_workspace_size() bytes", fn);
     const char *why = "launch";
     const cudaError_t e = rc::launch_kv_project_store(normed, W, w_layout == RC_W_NK, L, T, D, N, plan,
                                                       static_cast<float *>(workspace), fs, stream, &why);
+    if (e != cudaSuccess)
+        return cuda_fail(e, why);
+    return ok();
+}
+
+size_t rc_context_kv_workspace_size(int32_t L, int64_t T, int32_t D, int32_t H)
+{
+    if (!supported_heads(H) || D != rc::kHidden || L < 1 || L > rc::kMaxFusedLayers)
+        return 0;
+    const int32_t N = 2 * H * rc::kHeadDim;
+    if (check_project_sizes(L, T, D, N) != RC_OK || T == 0)
+        return 0;
+    const int sms = num_sms_current();
+    if (sms <= 0)
+        return 0;
+    const rc::ProjectPlan plan = rc::plan_kv_project(L, T, D, N, sms, SIZE_MAX);
+    return context_kv_fixed_bytes(plan.pair, L, T, D) + plan.workspace;
+}
+
+rc_status rc_context_kv(const uint16_t *x, int64_t T, int32_t D, const uint16_t *hidden_w,
+                        const uint16_t *pre_w, int32_t L, float eps, const uint16_t *W,
+                        int32_t w_layout, int32_t H, const int64_t *positions,
+                        const int64_t *const *slots, const uint16_t *cos_sin, int64_t max_position,
+                        uint16_t *const *caches, int32_t num_blocks, int32_t block_size,
+                        int64_t rows, int32_t *err, uint16_t *kv_out, void *workspace,
+                        size_t workspace_bytes, cudaStream_t stream)
+{
+    const char *fn = "rc_context_kv";
+    if (D != rc::kHidden)
+        return fail(RC_ERR_UNSUPPORTED, "%s: D=%d, the row norm takes D=8192", fn, D);
+    if (!supported_heads(H))
+        return fail(RC_ERR_UNSUPPORTED, "%s: H=%d is not a power of two <= 32", fn, H);
+    const int32_t N = 2 * H * rc::kHeadDim;
+    rc_status st = check_project_sizes(L, T, D, N);
+    if (st != RC_OK)
+        return st;
+    if (w_layout != RC_W_KN && w_layout != RC_W_NK)
+        return fail(RC_ERR_INVALID_ARG, "%s: unknown weight layout %d", fn, w_layout);
+    if (!x || !W || !workspace)
+        return fail(RC_ERR_INVALID_ARG, "%s: x, W and workspace must not be NULL", fn);
+    if (!aligned(x, 16) || !aligned(W, 16) || !aligned(workspace, 256) ||
+        (hidden_w && !aligned(hidden_w, 16)) || (pre_w && !aligned(pre_w, 16)))
+        return fail(RC_ERR_INVALID_ARG,
+                    "%s: x, W and weights must be 16-byte aligned, workspace 256-byte aligned", fn);
+    rc::FusedStore fs;
+    st = fused_store_args(fn, L, T, H, positions, slots, cos_sin, max_position, caches, num_blocks,
+                          block_size, eps, rows, err, kv_out, &fs);
+    if (st != RC_OK)
+        return st;
+    if (T == 0)
+        return ok();
+    const int sms = num_sms_current();
+    if (sms <= 0)
+        return fail(RC_ERR_CUDA, "%s: no current CUDA device", fn);
+    const bool pair = rc::plan_kv_project(L, T, D, N, sms, 0).pair;
+    const size_t fixed = context_kv_fixed_bytes(pair, L, T, D);
+    if (workspace_bytes < fixed)
+        return fail(RC_ERR_INVALID_ARG, "%s: the workspace needs at least %zu bytes (%zu given)", fn,
+                    fixed, workspace_bytes);
+    char *wsb = static_cast<char *>(workspace);
+    float *partials = reinterpret_cast<float *>(wsb + fixed);
+    const rc::ProjectPlan plan = rc::plan_kv_project(L, T, D, N, sms, workspace_bytes - fixed);
+    const char *why = "launch";
+    cudaError_t e;
+    if (plan.pair) {
+        uint16_t *z = reinterpret_cast<uint16_t *>(wsb);
+        float *r2 = reinterpret_cast<float *>(wsb + round256((size_t)T * D * 2));
+        e = rc::launch_context_kv(x, T, hidden_w, pre_w, eps, W, w_layout == RC_W_NK, L, N, plan, z,
+                                  r2, partials, fs, stream, &why);
+    } else {
+        if (plan.splits == 1 && !kv_out)
+            return fail(RC_ERR_INVALID_ARG,
+                        "%s: at these sizes the store reads the projection from kv_out; pass kv_out "
+                        "or a workspace of rc_context_kv_workspace_size() bytes", fn);
+        uint16_t *normed = reinterpret_cast<uint16_t *>(wsb);
+        e = rc::launch_context_norms(x, T, hidden_w, pre_w, L, eps, normed, stream);
+        if (e == cudaSuccess)
+            e = rc::launch_kv_project_store(normed, W, w_layout == RC_W_NK, L, T, D, N, plan, partials,
+                                            fs, stream, &why);
+    }
     if (e != cudaSuccess)
         return cuda_fail(e, why);
     return ok();

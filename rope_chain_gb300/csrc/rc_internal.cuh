@@ -92,6 +92,11 @@ cudaError_t launch_context_norms(const uint16_t *x, int64_t T, const uint16_t *h
                                  const uint16_t *pre_w, int32_t L, float eps,
                                  uint16_t *out, cudaStream_t stream);
 
+// Row prep for the fused chain: z = bf16 [T, 8192] hidden-norm output and
+// r2 [T] = the layers' shared inverse RMS of z.
+cudaError_t launch_row_prep(const uint16_t *x, int64_t T, const uint16_t *hidden_w, float eps,
+                            uint16_t *z, float *r2, cudaStream_t stream);
+
 struct StoreLaunch {
     const uint16_t *k;               // layer 0 of this chunk
     const uint16_t *v;
@@ -162,6 +167,13 @@ cudaError_t launch_kv_project_store(const uint16_t *normed, const uint16_t *W, b
                                     int32_t L, int64_t T, int32_t D, int32_t N,
                                     const ProjectPlan &plan, float *ws, const FusedStore &fs,
                                     cudaStream_t stream, const char **why);
+
+// The whole chain for CTA-pair plans: row prep (z, r2), then the projection
+// forming each layer's normed tile in shared memory, with the store fused.
+cudaError_t launch_context_kv(const uint16_t *x, int64_t T, const uint16_t *hidden_w,
+                              const uint16_t *pre_w, float eps, const uint16_t *W, bool w_nk,
+                              int32_t L, int32_t N, const ProjectPlan &plan, uint16_t *z, float *r2,
+                              float *ws, const FusedStore &fs, cudaStream_t stream, const char **why);
 
 // Sticky device fault bits of the projection kernel (current device).
 cudaError_t read_project_faults(uint32_t *flags, bool clear);
