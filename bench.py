@@ -213,32 +213,55 @@ def run_ours(args, w):
     kv = torch.empty((w.L, w.T, w.N), dtype=torch.bfloat16, device=dev)
     ws_bytes = rc.workspace_size(w.L, w.T, w.D, w.N)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    cws = rc.context_kv_workspace(w.L, w.T, w.H, dev)   # the whole-chain call's workspace
+    z = torch.empty((w.T, w.D), dtype=torch.bfloat16, device=dev)
+    r2 = torch.empty((w.T,), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    # K1 + the fused projection/store: the GEMM, plus the reduce-and-store
-    # pass when K is split (the pair kernel's epilogue stores otherwise)
-    launches_per_step = 1 + (2 if ws_bytes else 1)
+    pair = w.T > 128 and w.N % 256 == 0                  # CTA-pair plans
+    split = ws_bytes > 0
+    # norms (or row pass) + GEMM + (reduce-and-store when K is split; the
+    # pair epilogue stores otherwise; single CTAs without split: store kernel)
+    launches_per_step = 2 + (1 if split else (0 if pair else (w.L + 7) // 8))
 
-    def chain(ev=None, per_kernel=False):
-        """One step: the norms, then projection + K-norm + RoPE + insert.
-        ev[0] / ev[2] bracket the step; with per_kernel ev[1] splits it (an
-        event between two kernels stops the second from launching early, so
-        the timed steps use step events only)."""
+    whole = args.path == "whole"
+
+    def chain(ev=None):
+        """One step through the public calls (ev[0] / ev[2] bracket it):
+        "store" path: rc_context_norms, then rc_kv_project_store (projection
+        with the store fused); "whole" path: rc_context_kv (the norms formed
+        inside the projection as well)."""
         if ev:
             ev[0].record()
-        rc.context_norms(x, hw, pw, w.L, w.eps, out=normed)
-        if ev and per_kernel:
-            ev[1].record()
-        rc.kv_project_store(normed, W, w.H, positions, slots, cs, caches, w.eps, err=err,
-                            workspace=ws if ws_bytes else None)
+        if whole:
+            rc.context_kv(x, hw, pw, W, w.H, positions, slots, cs, caches, w.eps, cws, err=err)
+        else:
+            rc.context_norms(x, hw, pw, w.L, w.eps, out=normed)
+            rc.kv_project_store(normed, W, w.H, positions, slots, cs, caches, w.eps, err=err,
+                                workspace=ws if split else None)
         if ev:
             ev[2].record()
+
+    def chain_split(ev):
+        """The same work as chain(), an event between its kernels (breakdown)."""
+        ev[0].record()
+        if whole and pair:
+            rc.context_rows(x, hw, w.eps, z=z, r2=r2)
+            ev[1].record()
+            rc.context_kv_from_rows(z, r2, pw, W, w.H, positions, slots, cs, caches, w.eps, err=err,
+                                    workspace=ws if split else None)
+        else:
+            rc.context_norms(x, hw, pw, w.L, w.eps, out=normed)
+            ev[1].record()
+            rc.kv_project_store(normed, W, w.H, positions, slots, cs, caches, w.eps, err=err,
+                                kv_out=kv, workspace=ws if split else None)
+        ev[2].record()
 
     def chain_unfused(ev):
         """The three calls of the boundary, an event after each (breakdown)."""
         ev[0].record()
         rc.context_norms(x, hw, pw, w.L, w.eps, out=normed)
         ev[1].record()
-        rc.kv_project(normed, W, out=kv, workspace=ws if ws_bytes else None)
+        rc.kv_project(normed, W, out=kv, workspace=ws if split else None)
         ev[2].record()
         rc.kv_store_from_projection(kv, w.H, positions, slots, cs, caches, w.eps, err=err)
         ev[3].record()
@@ -246,6 +269,7 @@ def run_ours(args, w):
     for i in range(args.warmup):
         flush.fill_(i & 0xFF)
         chain()
+        chain_split([torch.cuda.Event(enable_timing=True) for _ in range(3)])
         chain_unfused([torch.cuda.Event(enable_timing=True) for _ in range(4)])
     torch.cuda.synchronize()
     # The K timed steps run as one captured CUDA graph (what a serving loop
@@ -268,7 +292,7 @@ def run_ours(args, w):
             if kind == "timed":
                 chain(evs[i])
             elif kind == "kernels":
-                chain(kevs[i], per_kernel=True)
+                chain_split(kevs[i])
             else:
                 chain_unfused(uevs[i])
 
@@ -352,14 +376,19 @@ def run_ours(args, w):
         return {"us": t_us, "TFLOP/s": counts["k2_flops"] / t_us / 1e6,
                 "frac": counts["k2_flops"] / t_us / 1e6 / tc, "bound": "tensor"}
 
+    rows_bytes = 2 * w.T * w.D * 2 + 2 * w.D + 4 * w.T   # read x, write z, gains, r2
+    fused_norms = whole and pair
     kern = {
-        "norms": hbm_entry(counts["k1_bytes"], us(k1_ms)),
-        "project_store": dict(tc_entry(us(ps_ms)), split_k_workspace_bytes=ws_bytes),
+        "row_pass" if fused_norms else "norms": hbm_entry(rows_bytes if fused_norms else counts["k1_bytes"],
+                                                          us(k1_ms)),
+        "project_store": dict(tc_entry(us(ps_ms)), split_k_workspace_bytes=ws_bytes,
+                              norms_fused=fused_norms),
         "unfused": {"norms": hbm_entry(counts["k1_bytes"], us(u_ms[0])),
                     "project": tc_entry(us(u_ms[1])),
                     "store": hbm_entry(k3_bytes, us(u_ms[2]))},
     }
-    dominant = "project_store" if kern["project_store"]["us"] >= kern["norms"]["us"] else "norms"
+    first = "row_pass" if fused_norms else "norms"
+    dominant = "project_store" if kern["project_store"]["us"] >= kern[first]["us"] else first
     d = kern[dominant]
     if d["bound"] == "tensor":
         roof = {"kernel": dominant, "bound": "tensor", "achieved": d["TFLOP/s"], "peak": tc,
@@ -376,7 +405,9 @@ def run_ours(args, w):
     rec = base_record(args, w, world)
     rec["config"]["l2"] = "flushed (512 MiB write) before every timed step"
     rec["config"]["timing"] = timing
-    rec["config"]["path"] = "rc_context_norms + rc_kv_project_store (fused projection and store)"
+    rec["config"]["path"] = ("rc_context_kv (row pass; projection forming the normed rows in shared "
+                             "memory, store fused)" if whole else
+                             "rc_context_norms + rc_kv_project_store (projection with the store fused)")
     rec.update({
         "value": world * w.T * args.steps / (total_ms / 1e3),
         "ms_per_step": total_ms / args.steps,
@@ -399,6 +430,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", default="store", choices=["store", "whole"],
+                    help="store: norms + fused projection/store; whole: rc_context_kv")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

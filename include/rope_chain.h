@@ -243,6 +243,31 @@ rc_status rc_context_kv(const uint16_t *x, int64_t T, int32_t D,
 size_t rc_context_kv_workspace_size(int32_t L, int64_t T, int32_t D, int32_t H);
 
 /*
+ * rc_context_kv in two calls.  rc_context_rows is the row pass: per row t,
+ *   z[t]  = bf16(hidden_norm(x[t]))          bf16 [T, 8192], 16-byte aligned
+ *   r2[t] = 1/sqrt(fma(sum z[t]^2, 1/D, eps)) FP32 [T] (the layer norms'
+ *                                            inverse RMS, shared by all layers)
+ * in the order and roundings of rc_context_norms.  rc_context_kv_from_rows
+ * then projects and stores from (z, r2, pre_w): each layer's operand
+ * bf16((z * r2) * pre_w[l]) is formed in shared memory.  It takes
+ * T > 128 and H >= 2 (CTA-pair tiles) only; `workspace` holds the split-K
+ * partials (rc_kv_project_workspace_size() bytes; may be NULL).
+ */
+rc_status rc_context_rows(const uint16_t *x, int64_t T, int32_t D,
+                          const uint16_t *hidden_w, float eps, uint16_t *z,
+                          float *r2, cudaStream_t stream);
+rc_status rc_context_kv_from_rows(const uint16_t *z, const float *r2, int64_t T,
+                                  int32_t D, const uint16_t *pre_w, int32_t L,
+                                  float eps, const uint16_t *W, int32_t w_layout,
+                                  int32_t H, const int64_t *positions,
+                                  const int64_t *const *slots,
+                                  const uint16_t *cos_sin, int64_t max_position,
+                                  uint16_t *const *caches, int32_t num_blocks,
+                                  int32_t block_size, int64_t rows, int32_t *err,
+                                  uint16_t *kv_out, void *workspace,
+                                  size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * rc_kv_project_no_alloc -- rc_kv_project for callers that cannot allocate.
  * The pages have no counterpart: it is an addition of this library.
  *

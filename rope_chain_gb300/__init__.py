@@ -54,6 +54,11 @@ SIGNATURES = {
                        _c.c_int32, _c.c_int32, _vp, _c.POINTER(_vp), _vp, _c.c_int64,
                        _c.POINTER(_vp), _c.c_int32, _c.c_int32, _c.c_int64, _vp, _vp, _vp,
                        _c.c_size_t, _vp], _c.c_int),
+    "rc_context_rows": ([_vp, _c.c_int64, _c.c_int32, _vp, _c.c_float, _vp, _vp, _vp], _c.c_int),
+    "rc_context_kv_from_rows": ([_vp, _vp, _c.c_int64, _c.c_int32, _vp, _c.c_int32, _c.c_float, _vp,
+                                 _c.c_int32, _c.c_int32, _vp, _c.POINTER(_vp), _vp, _c.c_int64,
+                                 _c.POINTER(_vp), _c.c_int32, _c.c_int32, _c.c_int64, _vp, _vp,
+                                 _vp, _c.c_size_t, _vp], _c.c_int),
     "rc_context_kv_workspace_size": ([_c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32], _c.c_size_t),
     "rc_kv_project_store": ([_vp, _vp, _c.c_int32, _c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32,
                              _vp, _c.POINTER(_vp), _vp, _c.c_int64, _c.POINTER(_vp), _c.c_int32,
@@ -318,6 +323,45 @@ def context_kv(x: torch.Tensor, hidden_w, pre_w, W: torch.Tensor, H: int, positi
                                0 if cos_sin is None else cos_sin.shape[0], cache_arr, nb, bs, rows,
                                _ptr(err), _ptr(kv_out), workspace.data_ptr(),
                                workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def context_rows(x: torch.Tensor, hidden_w, eps: float, z: Optional[torch.Tensor] = None,
+                 r2: Optional[torch.Tensor] = None, stream=None):
+    """The row pass of context_kv: (z bf16 [T, 8192], r2 float32 [T])."""
+    _bf16(x, "x")
+    T, D = x.shape
+    if z is None:
+        z = torch.empty((T, D), dtype=torch.bfloat16, device=x.device)
+    if r2 is None:
+        r2 = torch.empty((T,), dtype=torch.float32, device=x.device)
+    if hidden_w is not None:
+        _bf16(hidden_w, "hidden_w")
+    _check(lib().rc_context_rows(x.data_ptr(), T, D, _ptr(hidden_w), eps, z.data_ptr(),
+                                 r2.data_ptr(), _stream(stream)))
+    return z, r2
+
+
+def context_kv_from_rows(z: torch.Tensor, r2: torch.Tensor, pre_w, W: torch.Tensor, H: int,
+                         positions, slots, cos_sin, caches, eps: float, rows=None, err=None,
+                         kv_out=None, workspace=None, w_layout: int = RC_W_KN, stream=None) -> None:
+    """The projection and store of context_kv from its row pass."""
+    _bf16(z, "z")
+    _bf16(W, "W")
+    T, D = z.shape
+    L = len(caches)
+    if pre_w is not None:
+        _bf16(pre_w, "pre_w")
+    if kv_out is not None:
+        _bf16(kv_out, "kv_out")
+    slot_arr, cache_arr, nb, bs, rows = _store_operands(H, slots, caches, positions, cos_sin, rows)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check(lib().rc_context_kv_from_rows(z.data_ptr(), r2.data_ptr(), T, D, _ptr(pre_w), L, eps,
+                                         W.data_ptr(), w_layout, H, _ptr(positions), slot_arr,
+                                         _ptr(cos_sin), 0 if cos_sin is None else cos_sin.shape[0],
+                                         cache_arr, nb, bs, rows, _ptr(err), _ptr(kv_out), ws_ptr,
+                                         ws_bytes, _stream(stream)))
 
 
 def split_kv(kv: torch.Tensor, H: int):

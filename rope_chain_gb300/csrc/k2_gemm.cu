@@ -84,28 +84,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
-// try_wait with acquire at cluster scope (arrivals released by the peer CTA).
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
-    const unsigned long long t0 = globaltimer();
-    for (uint32_t it = 0;; ++it) {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (ok)
-            return true;
-        if ((it & 255u) == 255u && (faulted() || globaltimer() - t0 > kWaitNs))
-            return false;
-    }
+// Arrive on a barrier of this CTA.
+__device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 // Arrive on a barrier of any CTA of the cluster (a shared::cluster address).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
@@ -596,9 +582,23 @@ struct PairCfg {
     static constexpr uint32_t kBHalf = 128 * BK * 2;            // 16 KiB of B per CTA
     static constexpr uint32_t kStageBytes = kABytes + kBHalf;    // 32 KiB per CTA
     static constexpr uint32_t kPairTx = 2 * kStageBytes;         // counted on the leader
-    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 256;
-    static_assert((4 * kStages + 1) * 8 + 5 * 4 <= 256, "barriers and words fit the tail");
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 512;
+    static_assert((5 * kStages + 1) * 8 + 5 * 4 <= 512, "barriers and words fit the tail");
 };
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4 &v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
 
 __device__ __forceinline__ void unpack8f(const uint4 &q, float *f) {
     f[0] = bf16_lo(q.x); f[1] = bf16_hi(q.x);
@@ -613,8 +613,16 @@ __device__ __forceinline__ void unpack8f(const uint4 &q, float *f) {
 // is bit-identical to the normed rows that kernel would have written.  The
 // 4 epilogue warps do it in place (128-byte swizzled rows: logical 16-byte
 // chunk c of row r sits at chunk c ^ (r % 8)) before the epilogue.
+// Threads of the pair kernel: producer warp, MMA warp, 4 epilogue warps
+// (with kTransform: kFormGroups groups of 4 forming warps taking stages in
+// turn, so several stages are formed at once; warps 2-5 also run the
+// epilogue).
+constexpr int kFormGroups = 3;
+template <bool kTransform>
+constexpr int pair_threads() { return kTransform ? 64 + 128 * kFormGroups : kThreads; }
+
 template <bool kBmn, bool kFused, bool kTransform>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(pair_threads<kTransform>(), 1)
 k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmArgs g, const __grid_constant__ FusedStore fs)
 {
@@ -627,15 +635,16 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const uint32_t sB = sA + S * kABytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * C::kStageBytes);
     // full[s] (leader: B, and A unless kTransform), empty[s], aload[s]
-    // (kTransform: this CTA's A), ready[s] (kTransform, leader: A formed in
-    // both CTAs), accum
+    // (kTransform: this CTA's A), ready[s] (kTransform: this CTA's A is
+    // formed), peer[s] (kTransform, leader: the peer's A is formed), accum
     const uint32_t bar0 = smem_u32(bars);
     const uint32_t empty0 = bar0 + 8u * S, aload0 = bar0 + 16u * S, ready0 = bar0 + 24u * S;
-    const uint32_t accum = bar0 + 32u * S;
+    const uint32_t peer0 = bar0 + 32u * S;
+    const uint32_t accum = bar0 + 40u * S;
     // words[0]: TMEM base; [1]: stages the leader's MMA thread consumed;
     // [2]: skip flag (written by the leader into both CTAs); [3]: stages the
     // peer's loader issued (written by the peer into the leader)
-    volatile uint32_t *words = reinterpret_cast<volatile uint32_t *>(bars + 4 * S + 1);
+    volatile uint32_t *words = reinterpret_cast<volatile uint32_t *>(bars + 5 * S + 1);
     const uint32_t words_addr = smem_u32((const void *)words);
 
     const int warp = __shfl_sync(0xFFFFFFFFu, (int)(threadIdx.x >> 5), 0);
@@ -656,7 +665,8 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             mbar_init(bar0 + 8u * s, 1);
             mbar_init(empty0 + 8u * s, 1);
             mbar_init(aload0 + 8u * s, 1);
-            mbar_init(ready0 + 8u * s, 8);         // 4 warps in each CTA of the pair
+            mbar_init(ready0 + 8u * s, 4);         // the 4 forming warps of the stage's group
+            mbar_init(peer0 + 8u * s, 1);          // forwarded by the peer's warp 1
         }
         mbar_init(accum, 1);
         words[1] = 0u;
@@ -723,7 +733,8 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     const int s = i % S;
                     const uint32_t ph = (uint32_t)(i / S) & 1u;
                     if (!mbar_wait(bar0 + 8u * s, ph) ||
-                        (kTransform && !mbar_wait_cluster(ready0 + 8u * s, ph))) {
+                        (kTransform && (!mbar_wait(ready0 + 8u * s, ph) ||
+                                        !mbar_wait(peer0 + 8u * s, ph)))) {
                         raise_fault(kFaultMma);
                         break;
                     }
@@ -742,14 +753,28 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             }
             words[1] = (uint32_t)consumed;
             mma_commit_pair(accum);
+        } else if (kTransform && lane == 0 && !skip) {
+            // The peer's idle MMA thread forwards "A formed" to the leader, so
+            // the forming warps never pay for a cluster-scope release.
+            const uint32_t peer_lead = map_to_rank(peer0, 0);
+            for (int i = 0; i < nkb; ++i) {
+                const int s = i % S;
+                if (!mbar_wait(ready0 + 8u * s, (uint32_t)(i / S) & 1u)) {
+                    raise_fault(kFaultMma);
+                    break;
+                }
+                mbar_arrive_cluster(peer_lead + 8u * s);
+            }
         }
         __syncwarp();
     } else {
         const int q = warp & 3;
         if (kTransform && !skip) {
-            // Form this CTA's A tiles: thread t takes logical chunk c = t % 8
-            // (8 columns) of rows t / 8 + 16 j, j < 8.
-            const int t = (int)threadIdx.x - 64;
+            // Form this CTA's A tiles: group grp (warps 2 + 4 grp ...) forms
+            // the stages i with i % kFormGroups == grp; thread t of a group
+            // takes logical chunk c = t % 8 (8 columns) of rows t / 8 + 16 j.
+            const int grp = ((int)threadIdx.x - 64) >> 7;
+            const int t = ((int)threadIdx.x - 64) & 127;
             const int c = t & 7, r0 = t >> 3;
             float rs[8];
 #pragma unroll
@@ -758,8 +783,7 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 rs[j] = row < g.T ? __ldg(g.row_scale + row) : 0.0f;
             }
             const uint16_t *gain = g.col_gain ? g.col_gain + (int64_t)l * (g.kb_total * BK) : nullptr;
-            const uint32_t ready_lead = map_to_rank(ready0, 0);
-            for (int i = 0; i < nkb; ++i) {
+            for (int i = grp; i < nkb; i += kFormGroups) {
                 const int s = i % S;
                 const uint32_t ph = (uint32_t)(i / S) & 1u;
                 if (!mbar_wait(aload0 + 8u * s, ph)) {
@@ -769,13 +793,20 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 float gm[8];
                 if (gain)
                     unpack8f(__ldg(reinterpret_cast<const uint4 *>(gain + (kb0 + i) * BK + 8 * c)), gm);
-                uint8_t *st = smem + s * kABytes;
+                // all 8 rows' chunks in flight, then formed, then written back
+                const uint32_t st = sA + s * kABytes;
+                uint32_t addr[8];
+                uint4 v[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int r = r0 + 16 * j;
-                    uint4 *p = reinterpret_cast<uint4 *>(st + r * 128 + ((c ^ (r & 7)) << 4));
+                    addr[j] = st + r * 128 + ((c ^ (r & 7)) << 4);
+                    v[j] = ld_shared_v4(addr[j]);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
                     float f[8];
-                    unpack8f(*p, f);
+                    unpack8f(v[j], f);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         f[e] = __fmul_rn(f[e], rs[j]);
@@ -784,19 +815,22 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         for (int e = 0; e < 8; ++e)
                             f[e] = __fmul_rn(f[e], gm[e]);
                     }
-                    *p = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                                    pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                    v[j] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                      pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
                 }
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(addr[j], v[j]);
                 // generic-proxy writes, then visible to the tensor core
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive_cluster(ready_lead + 8u * s);
+                    mbar_arrive_local(ready0 + 8u * s);
             }
         }
-        bool ok = !skip && mbar_wait(accum, 0u);
+        bool ok = warp < 6 && !skip && mbar_wait(accum, 0u);
         ok = __all_sync(0xFFFFFFFFu, ok);
-        if (!ok && !skip && lane == 0)
+        if (!ok && !skip && warp < 6 && lane == 0)
             raise_fault(kFaultAccum);
         if (ok && kFused && g.splits == 1) {
             tc_fence_after();
@@ -943,8 +977,8 @@ cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const Gemm
             configured[dev] = true;
     }
     const dim3 grid((unsigned)(2 * n_pairs), (unsigned)m_pairs, (unsigned)(g.L * g.splits));
-    return launch_pdl(k2_project_pair<kBmn, kFused, kTransform>, grid, dim3(kThreads), PairCfg::kSmem,
-                      stream, 2, ma, mb, g, fs);
+    return launch_pdl(k2_project_pair<kBmn, kFused, kTransform>, grid,
+                      dim3(pair_threads<kTransform>()), PairCfg::kSmem, stream, 2, ma, mb, g, fs);
 }
 
 }  // namespace
@@ -1103,17 +1137,12 @@ cudaError_t launch_kv_project_store(const uint16_t *normed, const uint16_t *W, b
     return cudaSuccess;
 }
 
-cudaError_t launch_context_kv(const uint16_t *x, int64_t T, const uint16_t *hidden_w,
-                              const uint16_t *pre_w, float eps, const uint16_t *W, bool w_nk,
-                              int32_t L, int32_t N, const ProjectPlan &plan, uint16_t *z, float *r2,
-                              float *ws, const FusedStore &fs, cudaStream_t stream, const char **why)
+cudaError_t launch_kv_from_rows(const uint16_t *z, const float *r2, int64_t T,
+                                const uint16_t *pre_w, const uint16_t *W, bool w_nk, int32_t L,
+                                int32_t N, const ProjectPlan &plan, float *ws, const FusedStore &fs,
+                                cudaStream_t stream, const char **why)
 {
     constexpr int D = kHidden;
-    cudaError_t e = launch_row_prep(x, T, hidden_w, eps, z, r2, stream);
-    if (e != cudaSuccess) {
-        *why = "row prep launch";
-        return e;
-    }
     CUtensorMap ma, mb;
     GemmArgs g;
     if (!project_setup(z, W, w_nk, fs.kv_out, L, T, D, N, plan, ws, &ma, &mb, &g, why))
@@ -1130,8 +1159,8 @@ cudaError_t launch_context_kv(const uint16_t *x, int64_t T, const uint16_t *hidd
     if (plan.splits == 1)
         return w_nk ? launch_pair<false, true, true>(ma, mb, g, fs, n_pairs, m_pairs, stream)
                     : launch_pair<true, true, true>(ma, mb, g, fs, n_pairs, m_pairs, stream);
-    e = w_nk ? launch_pair<false, false, true>(ma, mb, g, fs, n_pairs, m_pairs, stream)
-             : launch_pair<true, false, true>(ma, mb, g, fs, n_pairs, m_pairs, stream);
+    cudaError_t e = w_nk ? launch_pair<false, false, true>(ma, mb, g, fs, n_pairs, m_pairs, stream)
+                         : launch_pair<true, false, true>(ma, mb, g, fs, n_pairs, m_pairs, stream);
     if (e != cudaSuccess)
         return e;
     *why = "reduce-and-store launch";

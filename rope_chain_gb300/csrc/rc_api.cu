@@ -404,8 +404,10 @@ rc_status rc_context_kv(const uint16_t *x, int64_t T, int32_t D, const uint16_t 
     if (plan.pair) {
         uint16_t *z = reinterpret_cast<uint16_t *>(wsb);
         float *r2 = reinterpret_cast<float *>(wsb + round256((size_t)T * D * 2));
-        e = rc::launch_context_kv(x, T, hidden_w, pre_w, eps, W, w_layout == RC_W_NK, L, N, plan, z,
-                                  r2, partials, fs, stream, &why);
+        e = rc::launch_row_prep(x, T, hidden_w, eps, z, r2, stream);
+        if (e == cudaSuccess)
+            e = rc::launch_kv_from_rows(z, r2, T, pre_w, W, w_layout == RC_W_NK, L, N, plan, partials,
+                                        fs, stream, &why);
     } else {
         if (plan.splits == 1 && !kv_out)
             return fail(RC_ERR_INVALID_ARG,
@@ -417,6 +419,75 @@ rc_status rc_context_kv(const uint16_t *x, int64_t T, int32_t D, const uint16_t 
             e = rc::launch_kv_project_store(normed, W, w_layout == RC_W_NK, L, T, D, N, plan, partials,
                                             fs, stream, &why);
     }
+    if (e != cudaSuccess)
+        return cuda_fail(e, why);
+    return ok();
+}
+
+rc_status rc_context_rows(const uint16_t *x, int64_t T, int32_t D, const uint16_t *hidden_w,
+                          float eps, uint16_t *z, float *r2, cudaStream_t stream)
+{
+    const char *fn = "rc_context_rows";
+    if (D != rc::kHidden)
+        return fail(RC_ERR_UNSUPPORTED, "%s: D=%d, the row norm takes D=8192", fn, D);
+    if (T < 0 || T > 0x7FFFFFFFLL)
+        return fail(RC_ERR_INVALID_ARG, "%s: T=%lld outside [0, 2^31)", fn, (long long)T);
+    if (!x || !z || !r2)
+        return fail(RC_ERR_INVALID_ARG, "%s: x, z and r2 must not be NULL", fn);
+    if (!aligned(x, 16) || !aligned(z, 16) || !aligned(r2, 4) || (hidden_w && !aligned(hidden_w, 16)))
+        return fail(RC_ERR_INVALID_ARG, "%s: x, z and hidden_w must be 16-byte aligned", fn);
+    if (T > 0 && overlap(x, (size_t)T * D * 2, z, (size_t)T * D * 2))
+        return fail(RC_ERR_INVALID_ARG, "%s: z overlaps x", fn);
+    if (T == 0)
+        return ok();
+    const cudaError_t e = rc::launch_row_prep(x, T, hidden_w, eps, z, r2, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "rc_context_rows launch");
+    return ok();
+}
+
+rc_status rc_context_kv_from_rows(const uint16_t *z, const float *r2, int64_t T, int32_t D,
+                                  const uint16_t *pre_w, int32_t L, float eps, const uint16_t *W,
+                                  int32_t w_layout, int32_t H, const int64_t *positions,
+                                  const int64_t *const *slots, const uint16_t *cos_sin,
+                                  int64_t max_position, uint16_t *const *caches,
+                                  int32_t num_blocks, int32_t block_size, int64_t rows,
+                                  int32_t *err, uint16_t *kv_out, void *workspace,
+                                  size_t workspace_bytes, cudaStream_t stream)
+{
+    const char *fn = "rc_context_kv_from_rows";
+    if (D != rc::kHidden)
+        return fail(RC_ERR_UNSUPPORTED, "%s: D=%d, the rows are 8192 wide", fn, D);
+    if (!supported_heads(H))
+        return fail(RC_ERR_UNSUPPORTED, "%s: H=%d is not a power of two <= 32", fn, H);
+    const int32_t N = 2 * H * rc::kHeadDim;
+    rc_status st = check_project_sizes(L, T, D, N);
+    if (st != RC_OK)
+        return st;
+    if (w_layout != RC_W_KN && w_layout != RC_W_NK)
+        return fail(RC_ERR_INVALID_ARG, "%s: unknown weight layout %d", fn, w_layout);
+    if (!z || !r2 || !W)
+        return fail(RC_ERR_INVALID_ARG, "%s: z, r2 and W must not be NULL", fn);
+    if (!aligned(z, 16) || !aligned(W, 16) || !aligned(r2, 4) || (pre_w && !aligned(pre_w, 16)) ||
+        (workspace && !aligned(workspace, 16)))
+        return fail(RC_ERR_INVALID_ARG, "%s: z, W, pre_w and workspace must be 16-byte aligned", fn);
+    rc::FusedStore fs;
+    st = fused_store_args(fn, L, T, H, positions, slots, cos_sin, max_position, caches, num_blocks,
+                          block_size, eps, rows, err, kv_out, &fs);
+    if (st != RC_OK)
+        return st;
+    if (T == 0)
+        return ok();
+    const int sms = num_sms_current();
+    if (sms <= 0)
+        return fail(RC_ERR_CUDA, "%s: no current CUDA device", fn);
+    const rc::ProjectPlan plan = rc::plan_kv_project(L, T, D, N, sms, workspace ? workspace_bytes : 0);
+    if (!plan.pair)
+        return fail(RC_ERR_UNSUPPORTED,
+                    "%s: needs T > 128 and H >= 2 (CTA-pair tiles); use rc_context_kv", fn);
+    const char *why = "launch";
+    const cudaError_t e = rc::launch_kv_from_rows(z, r2, T, pre_w, W, w_layout == RC_W_NK, L, N, plan,
+                                                  static_cast<float *>(workspace), fs, stream, &why);
     if (e != cudaSuccess)
         return cuda_fail(e, why);
     return ok();

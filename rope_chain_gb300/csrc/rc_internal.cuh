@@ -168,12 +168,13 @@ cudaError_t launch_kv_project_store(const uint16_t *normed, const uint16_t *W, b
                                     const ProjectPlan &plan, float *ws, const FusedStore &fs,
                                     cudaStream_t stream, const char **why);
 
-// The whole chain for CTA-pair plans: row prep (z, r2), then the projection
-// forming each layer's normed tile in shared memory, with the store fused.
-cudaError_t launch_context_kv(const uint16_t *x, int64_t T, const uint16_t *hidden_w,
-                              const uint16_t *pre_w, float eps, const uint16_t *W, bool w_nk,
-                              int32_t L, int32_t N, const ProjectPlan &plan, uint16_t *z, float *r2,
-                              float *ws, const FusedStore &fs, cudaStream_t stream, const char **why);
+// The chain after the row pass, for CTA-pair plans: the projection forming
+// each layer's normed tile from (z, r2, pre_w) in shared memory, with the
+// store fused (epilogue, or the reduce-and-store pass when K is split).
+cudaError_t launch_kv_from_rows(const uint16_t *z, const float *r2, int64_t T,
+                                const uint16_t *pre_w, const uint16_t *W, bool w_nk, int32_t L,
+                                int32_t N, const ProjectPlan &plan, float *ws, const FusedStore &fs,
+                                cudaStream_t stream, const char **why);
 
 // Sticky device fault bits of the projection kernel (current device).
 cudaError_t read_project_faults(uint32_t *flags, bool clear);

@@ -115,3 +115,39 @@ def test_whole_chain_workloads(index):
     T = w.T
     sample = None if T <= 512 else np.unique(np.r_[0, T - 1, np.linspace(0, T - 1, 256).astype(int)])
     check_against_oracle(case, got, normed=ref["normed"], sample=sample)
+
+
+@pytest.mark.parametrize("hw,pw", [(True, True), (False, True), (True, False)])
+def test_two_phase_rows_then_projection(hw, pw):
+    T, L, H = 384, 3, 8
+    case = workloads.random_case(4242, T=T, L=L, H=H, max_position=512, num_blocks=(T + 15) // 16 + 3,
+                                 block_size=16, hidden_weighted=hw, pre_weighted=pw)
+    x = parity.dev_bf16(case["x"], DEV)
+    z, r2 = rc.context_rows(x, parity.dev_bf16(case["hidden_w"], DEV), case["eps"])
+    torch.cuda.synchronize()
+    # (z, r2) reproduce the oracle's normed rows: bf16((z * r2) * gamma_l) in
+    # binary32, one rounding per operation, as the layer step is defined
+    zf = (parity.host_bits(z).astype(np.uint32) << 16).view(np.float32)
+    r2h = r2.cpu().numpy().astype(np.float32)
+    ref = oracle.context_norms(case["x"], case["hidden_w"], case["pre_w"], L, case["eps"])
+    for l in range(L):
+        y = zf * r2h[:, None]
+        if pw:
+            y = y * ((case["pre_w"][l].astype(np.uint32) << 16).view(np.float32))[None, :]
+        assert np.array_equal(workloads.to_bf16_bits(y), ref[l])
+    # rows + from_rows == the one-call chain
+    whole = run_whole(case)
+    caches = [parity.dev_bf16(c, DEV) for c in parity.make_caches(case, L, parity.SENTINEL)]
+    kv = torch.empty((L, T, 128 * H), dtype=torch.bfloat16, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = rc.new_workspace(L, T, 8192, 128 * H, DEV)
+    rc.context_kv_from_rows(z, r2, parity.dev_bf16(case["pre_w"], DEV), parity.dev_bf16(case["W"], DEV),
+                            H, torch.from_numpy(case["positions"]).to(DEV),
+                            [torch.from_numpy(s).to(DEV) for s in case["slots"]],
+                            parity.dev_bf16(case["cos_sin"], DEV), caches, case["eps"], err=err,
+                            kv_out=kv, workspace=ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(parity.host_bits(kv), whole["kv"])
+    for a, b in zip(caches, whole["caches"]):
+        assert np.array_equal(parity.host_bits(a), b)
+    assert int(err.item()) == whole["err"]
