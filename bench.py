@@ -31,6 +31,17 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_FLUSH_BYTES = 512 << 20          # > 129 MB L2: written between timed steps
 
 
+# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
+# capture of this bench command (dram__bytes_read.sum + dram__bytes_write.sum,
+# summed over the kernels the timed call launches); keyed by (workload, path,
+# kernel).  An entry is removed whenever one of its kernels changes.
+# workload 2, store path, project_store = k2_project_pair (75.73 MB read,
+# 3.76 MB written) + k3_reduce_store (18.97 MB read, cache rows stay in L2).
+NCU_TRAFFIC = {
+    (2, "store", "project_store"): 75.73e6 + 3.76e6 + 18.97e6,
+}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -390,13 +401,14 @@ def run_ours(args, w):
     first = "row_pass" if fused_norms else "norms"
     dominant = "project_store" if kern["project_store"]["us"] >= kern[first]["us"] else first
     d = kern[dominant]
+    traffic = NCU_TRAFFIC.get((args.workload, args.path, dominant))
     if d["bound"] == "tensor":
         roof = {"kernel": dominant, "bound": "tensor", "achieved": d["TFLOP/s"], "peak": tc,
-                "unit": "TFLOP/s", "frac": d["frac"], "traffic": None,
+                "unit": "TFLOP/s", "frac": d["frac"], "traffic": traffic,
                 "peak_source": f"bf16_tflops (burst) of {peak_src}"}
     else:
         roof = {"kernel": dominant, "bound": "hbm", "achieved": d["GB/s"], "peak": hbm,
-                "unit": "GB/s", "frac": d["frac"], "traffic": None,
+                "unit": "GB/s", "frac": d["frac"], "traffic": traffic,
                 "peak_source": f"hbm_gbs of {peak_src}"}
     import oracle
     oracle.build()
