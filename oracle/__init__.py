@@ -47,6 +47,14 @@ _i32p = ctypes.POINTER(ctypes.c_int32)
 _c = ctypes
 
 
+class _Norm(ctypes.Structure):
+    """rco_norm: one norm's weight (bf16 or FP32 bits), scale side, gain
+    center and eps."""
+    _fields_ = [("weight", ctypes.c_void_p), ("fp32", ctypes.c_int32),
+                ("input_scale", ctypes.c_int32), ("center", ctypes.c_float),
+                ("eps", ctypes.c_float)]
+
+
 def lib():
     global _lib
     if _lib is None:
@@ -65,6 +73,9 @@ def lib():
             "rco_context_norms": ([_u16p, _c.c_int64, _c.c_int32, _u16p, _u16p,
                                    _c.c_int32, _c.c_float, _u16p, _c.c_int32],
                                   _c.c_int32),
+            "rco_context_norms_ex": ([_u16p, _c.c_int64, _c.c_int32, _c.POINTER(_Norm),
+                                      _c.POINTER(_Norm), _c.c_int32, _u16p, _c.c_int32],
+                                     _c.c_int32),
             "rco_kv_project": ([_u16p, _u16p, _c.c_int32, _c.c_int32, _c.c_int64,
                                 _c.c_int32, _c.c_int32, _i64p, _c.c_int64, _f64p,
                                 _f64p, _c.c_int32], _c.c_int32),
@@ -158,6 +169,39 @@ def context_norms(x: np.ndarray, hidden_w: Optional[np.ndarray],
     return out
 
 
+def _norm(weight: Optional[np.ndarray], input_scale: bool, center: float, eps: float,
+          shape) -> _Norm:
+    if weight is None:
+        return _Norm(None, 0, 0, 0.0, eps)
+    assert weight.shape == shape and weight.flags["C_CONTIGUOUS"]
+    if weight.dtype == np.float32:
+        fp32 = 1
+    elif weight.dtype == np.uint16:
+        fp32 = 0
+    else:
+        raise TypeError("norm weights are bf16 bits (uint16) or float32")
+    return _Norm(weight.ctypes.data, fp32, int(bool(input_scale)), center, eps)
+
+
+def context_norms_ex(x: np.ndarray, L: int, *, hidden_w: Optional[np.ndarray] = None,
+                     pre_w: Optional[np.ndarray] = None, hidden_eps: float,
+                     pre_eps: float, hidden_center: float = 0.0, pre_center: float = 0.0,
+                     hidden_input_scale: bool = False, pre_input_scale: bool = False,
+                     threads: int = 0) -> np.ndarray:
+    """``context_norms`` with every option of the norms kernel: weights as
+    bf16 bits (uint16) or float32, each norm's eps and gain center, and
+    whether each weight scales the norm's input (else its output)."""
+    T, D = x.shape
+    out = np.empty((L, T, D), dtype=np.uint16)
+    h = _norm(hidden_w, hidden_input_scale, hidden_center, hidden_eps, (D,))
+    p = _norm(pre_w, pre_input_scale, pre_center, pre_eps, (L, D))
+    rc = lib().rco_context_norms_ex(_p(x, _u16p), T, D, ctypes.byref(h), ctypes.byref(p), L,
+                                    _p(out, _u16p), threads)
+    if rc != 0:
+        raise ValueError("oracle: unsupported context_norms_ex arguments")
+    return out
+
+
 def kv_project(normed: np.ndarray, W: np.ndarray, rows: Optional[np.ndarray] = None,
                w_nd: bool = False, with_abs: bool = True, threads: int = 0):
     """float64 [L, R, N] projection of the selected rows (all rows when
@@ -214,6 +258,15 @@ def kv_store_from_projection(kv: np.ndarray, H: int, positions, slots, cos_sin,
     L, T, N = kv.shape
     assert N == 128 * H
     flat = np.ascontiguousarray(kv).reshape(-1)
+    if not np.isscalar(rows):
+        # per-layer row counts ([rt] _slot_groups: each layer inserts the
+        # first len(slots[l]) rows): one layer at a time
+        err = 0
+        for l in range(L):
+            k_l = flat[l * T * N:]
+            err += kv_store(k_l, k_l[64 * H:], T * N, N, T * N, N, positions, [slots[l]],
+                            cos_sin, [caches[l]], H, eps, int(rows[l]), threads)
+        return err
     v_view = flat[64 * H:]          # a view: V starts 64*H elements into a row
     return kv_store(flat, v_view, T * N, N, T * N, N, positions, slots, cos_sin,
                     caches, H, eps, rows, threads)

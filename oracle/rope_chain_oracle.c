@@ -28,11 +28,19 @@
  *       restated without NVIDIA's internals; the inverse RMS here is the
  *       correctly rounded 1 / sqrt(v) (IEEE sqrt, then IEEE divide) with
  *       v = fma(S, 1/width, eps) as the pages write it.
- *   R3  Norm gains scale the output, center 0: y = (x * r) * gamma
- *       ([bnd] boundary_fragments order); a weightless norm is y = x * r.
+ *   R3  Norm gains scale the output unless the norm is input-scaled (R7):
+ *       y = (x * r) * gamma ([bnd] boundary_fragments order); a weightless
+ *       norm is y = x * r.
  *   R4  NaN rounds to the canonical bf16 NaN 0x7FFF.
  *   R5  A slot >= num_blocks*block_size, or (with RoPE) a position outside
  *       [0, max_position), skips its row and counts it in *err.
+ *   R6  A gain center is added to the weight only when it is non-zero: the
+ *       stock norm with center 0 multiplies by the weight itself, so a -0.0
+ *       weight keeps its sign ([ctx] _ContextNormsKernel adds it always).
+ *   R7  An input-scale weight multiplies the input before the sum of
+ *       squares and nothing after it, in the order of [bnd]
+ *       boundary_fragments; the hidden norm's output is still rounded to
+ *       bf16 before the layer norm reads it.
  *
  * Parity pins: every function here is checked by the "not gpu" tests
  * against closed forms, invariants, brute force or library routines.
@@ -243,6 +251,91 @@ int32_t rco_context_norms(const uint16_t *x, int64_t T, int32_t D,
                     y = y * rco_f32(g[c]);
                 o[c] = rco_bf16_rn(y);
             }
+        }
+        free(v);
+    }
+    return 0;
+}
+
+/* One norm of the chain with every option [ctx] ContextNorms binds
+   (ContextNormConstants and the call's eps and gain centers):
+     weight       NULL (weightless), else [D] (hidden) or [L, D] (pre);
+     fp32         the weight's dtype: 1 FP32, 0 BF16;
+     input_scale  1: the weight scales the input before the norm, 0: the
+                  norm's output (R3);
+     center       the gain center, added to each weight element (R6);
+     eps          this norm's own eps. */
+typedef struct {
+    const void *weight;
+    int32_t fp32;
+    int32_t input_scale;
+    float center;
+    float eps;
+} rco_norm;
+
+/* gamma_c of the weight row at `offset` (R6: the center is added only when non-zero, so
+   that a center of 0 leaves the weight's bits, -0.0 included, unchanged). */
+static float norm_gain(const rco_norm *n, int64_t offset, int32_t c)
+{
+    float g;
+    if (n->fp32)
+        g = ((const float *)n->weight)[offset + c];
+    else
+        g = rco_f32(((const uint16_t *)n->weight)[offset + c]);
+    if (n->center != 0.0f)
+        g = g + n->center;
+    return g;
+}
+
+/* The RMSNorm of one 8192-wide row v (binary32 values) as [bnd]
+   boundary_fragments writes each of its two norms: with an input-scale
+   weight u = gamma * v first, else u = v; S = sum of squares of u (R1);
+   r = 1 / sqrt(fma(S, 2^-13, eps)) (R2); y = u * r, times gamma when the
+   weight scales the output.  `offset` selects the weight row. */
+static void norm_row(const float *v, const rco_norm *n, int64_t offset, float *y)
+{
+    const int weighted = n->weight != NULL;
+    const int pre_scale = weighted && n->input_scale;
+    float *u = y;                         /* y doubles as the scaled input */
+    for (int c = 0; c < RCO_D; ++c)
+        u[c] = pre_scale ? norm_gain(n, offset, c) * v[c] : v[c];
+    const float r = rco_inv_rms(rco_row_sumsq(u), 1.0f / 8192.0f, n->eps);
+    for (int c = 0; c < RCO_D; ++c) {
+        float t = u[c] * r;
+        if (weighted && !pre_scale)
+            t = t * norm_gain(n, offset, c);
+        y[c] = t;
+    }
+}
+
+/* rco_context_norms with every variant of ContextNormConstants: the hidden
+   norm (weight [D]) of each row, rounded to bf16, then each layer's input
+   norm (weight row l of [L, D]) of that, stacked at out[l, t, :] in bf16.
+   Each norm has its own eps, gain center, weight dtype and scale side.
+   Returns 0, or 1 for unsupported arguments. */
+int32_t rco_context_norms_ex(const uint16_t *x, int64_t T, int32_t D,
+                             const rco_norm *hidden, const rco_norm *pre,
+                             int32_t L, uint16_t *out, int32_t threads)
+{
+    if (D != RCO_D || T < 0 || L < 1 || !x || !out || !hidden || !pre)
+        return 1;
+#pragma omp parallel for schedule(static) num_threads(pick_threads(threads))
+    for (int64_t t = 0; t < T; ++t) {
+        float *v = (float *)malloc(3 * RCO_D * sizeof(float));
+        float *z = v + RCO_D, *y = z + RCO_D;
+        const uint16_t *xr = x + t * (int64_t)RCO_D;
+        for (int c = 0; c < RCO_D; ++c)
+            v[c] = rco_f32(xr[c]);
+        /* a1: the hidden norm, its output rounded to bf16 */
+        norm_row(v, hidden, 0, y);
+        for (int c = 0; c < RCO_D; ++c)
+            z[c] = rco_f32(rco_bf16_rn(y[c]));
+        /* a2: layer l's input norm of z, stacked at [l, t] */
+        for (int32_t l = 0; l < L; ++l) {
+            norm_row(z, pre, (int64_t)l * RCO_D, y);
+            uint16_t *o = out + ((int64_t)l * T + t) * RCO_D;
+            for (int c = 0; c < RCO_D; ++c)
+                o[c] = rco_bf16_rn(y[c]);
         }
         free(v);
     }
