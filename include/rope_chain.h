@@ -89,6 +89,50 @@ rc_status rc_context_norms(const uint16_t *x, int64_t T, int32_t D,
                            cudaStream_t stream);
 
 /*
+ * rc_context_norms_ex -- steps 1 and 2 with every option of [ctx]
+ * ContextNormConstants and ContextNorms: each norm's weight absent, bf16 or
+ * FP32; the weight scaling the norm's input (before the sum of squares) or
+ * its output; a gain center added to each weight element; and each norm's
+ * own eps ([ctx] ContextNorms takes hidden_eps and pre_eps).
+ *
+ * For one norm with weight w, gamma_c = w_c + center (w_c itself when the
+ * center is 0, so a -0.0 weight keeps its sign), and
+ *   input scale:   u_c = gamma_c * v_c,  y_c = u_c * r(u)
+ *   output scale:  y_c = (v_c * r(v)) * gamma_c
+ *   no weight:     y_c = v_c * r(v)
+ * with r(u) = 1 / sqrt(fma(sum_c u_c^2, 1/D, eps)) in the order of
+ * rc_context_norms ([bnd] boundary_fragments writes both scale sides in this
+ * order).  z = bf16(hidden norm of x); out[l, t] = bf16(layer l's norm of z),
+ * an input-scale layer weight giving each layer its own r.
+ *
+ *   x, T, D, L, out   as rc_context_norms
+ *   hidden, pre       HOST pointers to the two norms' parameters, read during
+ *                     the call; hidden->weight is [D], pre->weight [L, D]
+ *                     (device, 16-byte aligned, NULL exactly when
+ *                     weight_dtype is RC_NORM_NONE; input_scale and
+ *                     gain_center of a weightless norm are ignored)
+ * Errors: RC_ERR_INVALID_ARG for a NULL or misaligned pointer, an unknown
+ * weight_dtype or a weight/dtype mismatch; RC_ERR_UNSUPPORTED for D != 8192.
+ */
+typedef enum {
+    RC_NORM_NONE = 0,   /* weightless norm */
+    RC_NORM_BF16 = 1,   /* bf16 weight (uint16_t bit patterns) */
+    RC_NORM_F32 = 2     /* FP32 weight */
+} rc_norm_weight;
+
+typedef struct {
+    const void *weight;     /* device pointer, or NULL with RC_NORM_NONE */
+    int32_t weight_dtype;   /* rc_norm_weight */
+    int32_t input_scale;    /* non-zero: the weight scales the norm's input */
+    float gain_center;      /* added to each weight element when non-zero */
+    float eps;              /* this norm's eps */
+} rc_norm_params;
+
+rc_status rc_context_norms_ex(const uint16_t *x, int64_t T, int32_t D,
+                              const rc_norm_params *hidden, const rc_norm_params *pre,
+                              int32_t L, uint16_t *out, cudaStream_t stream);
+
+/*
  * rc_kv_project -- step 3.  [rt] ContextKV._project
  * (torch.bmm(per_layer, stacked_kv_weight.transpose(1, 2))).
  *
@@ -171,6 +215,26 @@ rc_status rc_kv_store(const uint16_t *k, const uint16_t *v,
                       int64_t rows, int32_t *err, cudaStream_t stream);
 
 /*
+ * rc_kv_store_rows -- rc_kv_store with a row count per layer ([rt]
+ * _slot_groups: each layer's slot mapping has its own length and layer l
+ * inserts its first len(slots[l]) rows; the pages issue one store call per
+ * run of consecutive layers of equal length, here one launch takes up to 8
+ * layers of any lengths).
+ *
+ *   layer_rows    HOST array of L row counts, each 0 <= layer_rows[l] < 2^31;
+ *                 slots[l] and k, v hold at least layer_rows[l] rows
+ *   other arguments as rc_kv_store (positions holds max_l layer_rows[l] rows)
+ */
+rc_status rc_kv_store_rows(const uint16_t *k, const uint16_t *v,
+                           int64_t k_layer_stride, int64_t k_row_stride,
+                           int64_t v_layer_stride, int64_t v_row_stride,
+                           const int64_t *positions, const int64_t *const *slots,
+                           const uint16_t *cos_sin, int64_t max_position,
+                           uint16_t *const *caches, int32_t num_blocks,
+                           int32_t block_size, int32_t H, int32_t L, float eps,
+                           const int64_t *layer_rows, int32_t *err, cudaStream_t stream);
+
+/*
  * rc_kv_project_store -- steps 3 and 4 fused (the projection and the store
  * of [rt] ContextKV.store in one pass; the scope's "store fused into the
  * GEMM epilogue").  The caches receive exactly the bits that
@@ -205,6 +269,23 @@ rc_status rc_kv_project_store(const uint16_t *normed, const uint16_t *W,
                               int32_t block_size, float eps, int64_t rows,
                               int32_t *err, uint16_t *kv_out, void *workspace,
                               size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * rc_kv_project_store_rows -- rc_kv_project_store with a row count per
+ * layer, as rc_kv_store_rows: layer l stores its first layer_rows[l] rows.
+ *
+ *   layer_rows    HOST array of L row counts, each 0 <= layer_rows[l] <= T
+ *   other arguments as rc_kv_project_store
+ */
+rc_status rc_kv_project_store_rows(const uint16_t *normed, const uint16_t *W,
+                                   int32_t w_layout, int32_t L, int64_t T, int32_t D,
+                                   int32_t H, const int64_t *positions,
+                                   const int64_t *const *slots,
+                                   const uint16_t *cos_sin, int64_t max_position,
+                                   uint16_t *const *caches, int32_t num_blocks,
+                                   int32_t block_size, float eps, const int64_t *layer_rows,
+                                   int32_t *err, uint16_t *kv_out, void *workspace,
+                                   size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * rc_context_kv -- the whole chain in one call (steps 1 to 4; [rt]

@@ -64,7 +64,28 @@ SIGNATURES = {
                              _vp, _c.POINTER(_vp), _vp, _c.c_int64, _c.POINTER(_vp), _c.c_int32,
                              _c.c_int32, _c.c_float, _c.c_int64, _vp, _vp, _vp, _c.c_size_t, _vp],
                             _c.c_int),
+    "rc_kv_project_store_rows": ([_vp, _vp, _c.c_int32, _c.c_int32, _c.c_int64, _c.c_int32,
+                                  _c.c_int32, _vp, _c.POINTER(_vp), _vp, _c.c_int64,
+                                  _c.POINTER(_vp), _c.c_int32, _c.c_int32, _c.c_float,
+                                  _c.POINTER(_c.c_int64), _vp, _vp, _vp, _c.c_size_t, _vp],
+                                 _c.c_int),
+    "rc_kv_store_rows": ([_vp, _vp, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _vp,
+                          _c.POINTER(_vp), _vp, _c.c_int64, _c.POINTER(_vp), _c.c_int32, _c.c_int32,
+                          _c.c_int32, _c.c_int32, _c.c_float, _c.POINTER(_c.c_int64), _vp, _vp],
+                         _c.c_int),
 }
+
+
+class NormParams(ctypes.Structure):
+    """rc_norm_params: one norm's weight (device pointer), its dtype
+    (RC_NORM_*), scale side, gain center and eps."""
+    _fields_ = [("weight", _vp), ("weight_dtype", _c.c_int32), ("input_scale", _c.c_int32),
+                ("gain_center", _c.c_float), ("eps", _c.c_float)]
+
+
+RC_NORM_NONE, RC_NORM_BF16, RC_NORM_F32 = 0, 1, 2
+SIGNATURES["rc_context_norms_ex"] = ([_vp, _c.c_int64, _c.c_int32, _c.POINTER(NormParams),
+                                      _c.POINTER(NormParams), _c.c_int32, _vp, _vp], _c.c_int)
 
 
 def lib():
@@ -122,6 +143,70 @@ def context_norms(x: torch.Tensor, hidden_w: Optional[torch.Tensor],
     _check(lib().rc_context_norms(x.data_ptr(), T, D, _ptr(hidden_w), _ptr(pre_w), L, eps,
                                   out.data_ptr(), _stream(stream)))
     return out
+
+
+def _norm_params(w: Optional[torch.Tensor], input_scale: bool, center: float, eps: float,
+                 name: str) -> NormParams:
+    if w is None:
+        return NormParams(None, RC_NORM_NONE, 0, 0.0, eps)
+    if not w.is_cuda or not w.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if w.dtype == torch.bfloat16:
+        dt = RC_NORM_BF16
+    elif w.dtype == torch.float32:
+        dt = RC_NORM_F32
+    else:
+        raise TypeError(f"{name} must be bfloat16 or float32")
+    return NormParams(w.data_ptr(), dt, int(bool(input_scale)), center, eps)
+
+
+def context_norms_ex(x: torch.Tensor, L: int, *, hidden_w: Optional[torch.Tensor] = None,
+                     pre_w: Optional[torch.Tensor] = None, hidden_eps: float, pre_eps: float,
+                     hidden_center: float = 0.0, pre_center: float = 0.0,
+                     hidden_input_scale: bool = False, pre_input_scale: bool = False,
+                     out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """context_norms with every norm option (rc_context_norms_ex): weights
+    bf16 or float32 ([8192] hidden, [L, 8192] layers), each norm's eps and
+    gain center, and whether each weight scales the norm's input."""
+    _bf16(x, "x")
+    T, D = x.shape
+    if out is None:
+        out = torch.empty((L, T, D), dtype=torch.bfloat16, device=x.device)
+    _bf16(out, "out")
+    if hidden_w is not None and tuple(hidden_w.shape) != (D,):
+        raise ValueError("hidden_w must be [8192]")
+    if pre_w is not None and tuple(pre_w.shape) != (L, D):
+        raise ValueError("pre_w must be [L, 8192]")
+    h = _norm_params(hidden_w, hidden_input_scale, hidden_center, hidden_eps, "hidden_w")
+    p = _norm_params(pre_w, pre_input_scale, pre_center, pre_eps, "pre_w")
+    _check(lib().rc_context_norms_ex(x.data_ptr(), T, D, ctypes.byref(h), ctypes.byref(p), L,
+                                     out.data_ptr(), _stream(stream)))
+    return out
+
+
+def _layer_rows(slots, rows):
+    """(rows, per-layer row counts or None): an int applies to every layer; a
+    sequence gives each layer its count; None takes each layer's slot-mapping
+    length (0 for a None layer), collapsing to one count when they agree."""
+    if rows is None:
+        lens = [0 if sl is None else int(sl.shape[0]) for sl in slots]
+        live = {n for n, sl in zip(lens, slots) if sl is not None}
+        if len(live) <= 1:
+            return (live.pop() if live else 0), None
+        return 0, lens
+    if isinstance(rows, int):
+        return rows, None
+    lens = [int(r) for r in rows]
+    if len(lens) != len(slots):
+        raise ValueError("rows needs one count per layer")
+    return 0, lens
+
+
+def _check_slot_lengths(slots, rows, per_layer):
+    for i, sl in enumerate(slots):
+        need = rows if per_layer is None else per_layer[i]
+        if sl is not None and sl.shape[0] < need:
+            raise ValueError(f"slots[{i}] has fewer than its {need} rows")
 
 
 def workspace_size(L: int, T: int, D: int, N: int) -> int:
@@ -200,22 +285,22 @@ def kv_store(k: torch.Tensor, v: torch.Tensor, positions: Optional[torch.Tensor]
     for s in slots:
         if s is not None and (s.dtype != torch.int64 or not s.is_contiguous() or not s.is_cuda):
             raise ValueError("slots must be contiguous CUDA int64 tensors")
-    if rows is None:
-        first = next((s for s in slots if s is not None), None)
-        rows = 0 if first is None else first.shape[0]
-    for s in slots:
-        if s is not None and s.shape[0] < rows:
-            raise ValueError("every slot mapping needs at least `rows` entries")
+    rows, per_layer = _layer_rows(slots, rows)
+    _check_slot_lengths(slots, rows, per_layer)
     if cos_sin is not None:
         _bf16(cos_sin, "cos_sin")
         if positions is None or positions.dtype != torch.int64 or not positions.is_contiguous():
             raise ValueError("RoPE needs contiguous int64 positions")
     slot_arr = (_vp * L)(*[_ptr(s) for s in slots])
     cache_arr = (_vp * L)(*[c.data_ptr() for c in caches])
-    _check(lib().rc_kv_store(k.data_ptr(), v.data_ptr(), k.stride(0), k.stride(1), v.stride(0),
-                             v.stride(1), _ptr(positions), slot_arr, _ptr(cos_sin),
-                             0 if cos_sin is None else cos_sin.shape[0], cache_arr, nb, bs, H, L,
-                             eps, rows, _ptr(err), _stream(stream)))
+    args = (k.data_ptr(), v.data_ptr(), k.stride(0), k.stride(1), v.stride(0), v.stride(1),
+            _ptr(positions), slot_arr, _ptr(cos_sin), 0 if cos_sin is None else cos_sin.shape[0],
+            cache_arr, nb, bs, H, L, eps)
+    if per_layer is None:
+        _check(lib().rc_kv_store(*args, rows, _ptr(err), _stream(stream)))
+    else:
+        _check(lib().rc_kv_store_rows(*args, (_c.c_int64 * L)(*per_layer), _ptr(err),
+                                      _stream(stream)))
 
 
 def kv_project_store(normed: torch.Tensor, W: torch.Tensor, H: int, positions, slots,
@@ -239,12 +324,8 @@ def kv_project_store(normed: torch.Tensor, W: torch.Tensor, H: int, positions, s
     for sl in slots:
         if sl is not None and (sl.dtype != torch.int64 or not sl.is_contiguous() or not sl.is_cuda):
             raise ValueError("slots must be contiguous CUDA int64 tensors")
-    if rows is None:
-        first = next((sl for sl in slots if sl is not None), None)
-        rows = 0 if first is None else first.shape[0]
-    for sl in slots:
-        if sl is not None and sl.shape[0] < rows:
-            raise ValueError("every slot mapping needs at least `rows` entries")
+    rows, per_layer = _layer_rows(slots, rows)
+    _check_slot_lengths(slots, rows, per_layer)
     if cos_sin is not None:
         _bf16(cos_sin, "cos_sin")
         if positions is None or positions.dtype != torch.int64 or not positions.is_contiguous():
@@ -256,11 +337,13 @@ def kv_project_store(normed: torch.Tensor, W: torch.Tensor, H: int, positions, s
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     slot_arr = (_vp * L)(*[_ptr(sl) for sl in slots])
     cache_arr = (_vp * L)(*[c.data_ptr() for c in caches])
-    _check(lib().rc_kv_project_store(normed.data_ptr(), W.data_ptr(), w_layout, L, T, D, H,
-                                     _ptr(positions), slot_arr, _ptr(cos_sin),
-                                     0 if cos_sin is None else cos_sin.shape[0], cache_arr, nb, bs,
-                                     eps, rows, _ptr(err), _ptr(kv_out), ws_ptr, ws_bytes,
-                                     _stream(stream)))
+    head = (normed.data_ptr(), W.data_ptr(), w_layout, L, T, D, H, _ptr(positions), slot_arr,
+            _ptr(cos_sin), 0 if cos_sin is None else cos_sin.shape[0], cache_arr, nb, bs, eps)
+    tail = (_ptr(err), _ptr(kv_out), ws_ptr, ws_bytes, _stream(stream))
+    if per_layer is None:
+        _check(lib().rc_kv_project_store(*head, rows, *tail))
+    else:
+        _check(lib().rc_kv_project_store_rows(*head, (_c.c_int64 * L)(*per_layer), *tail))
 
 
 def context_kv_workspace(L: int, T: int, H: int, device, D: int = 8192) -> torch.Tensor:

@@ -66,7 +66,7 @@ template <bool kHiddenW, bool kPreW>
 __global__ void __launch_bounds__(kThreads, 4)
 k1_context_norms(const uint16_t *__restrict__ x, int64_t T,
                  const uint16_t *__restrict__ hidden_w, const uint16_t *__restrict__ pre_w,
-                 int32_t L, float eps, uint16_t *__restrict__ out)
+                 int32_t L, float hidden_eps, float pre_eps, uint16_t *__restrict__ out)
 {
     __shared__ float sums[2][kThreads / 32];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -88,7 +88,7 @@ k1_context_norms(const uint16_t *__restrict__ x, int64_t T,
     }
 
     // a1: hidden norm; z = bf16((x * r) * gamma) kept packed in q
-    const float r = inv_rms(row_sumsq(q, sums[0], warp, lane), 0x1p-13f, eps);
+    const float r = inv_rms(row_sumsq(q, sums[0], warp, lane), 0x1p-13f, hidden_eps);
 #pragma unroll
     for (int k = 0; k < kFrags; ++k) {
         float f[8];
@@ -115,7 +115,7 @@ k1_context_norms(const uint16_t *__restrict__ x, int64_t T,
     }
 
     // a2: the layers' input norms share one inverse RMS
-    const float r2 = inv_rms(row_sumsq(q, sums[1], warp, lane), 0x1p-13f, eps);
+    const float r2 = inv_rms(row_sumsq(q, sums[1], warp, lane), 0x1p-13f, pre_eps);
     for (int32_t l = 0; l < L; ++l) {
         uint4 *o = reinterpret_cast<uint4 *>(out) + ((int64_t)l * T + row) * (kHidden / 8);
         const uint4 *gn = gp + (int64_t)(l + 1) * (kHidden / 8);
@@ -188,20 +188,186 @@ k1_row_prep(const uint16_t *__restrict__ x, const uint16_t *__restrict__ hidden_
         r2_out[row] = r2;
 }
 
+// ------------------------------------------------------------ variants
+//
+// Every option of the pages' ContextNormConstants and ContextNorms: each
+// norm's weight may be absent, bf16 or FP32, may scale the norm's input
+// (before the sum of squares) or its output, has a gain center added to
+// each element when non-zero, and its own eps.  With an input-scale layer
+// weight the layers' inverse RMS differs per layer, so each layer takes its
+// own row sum.  Same thread mapping, order of sums and roundings as
+// k1_context_norms; the options are uniform over the grid, so the branches
+// on them do not diverge.
+
+constexpr int kVals = kFrags * 8;     // values per thread
+
+// Fragment k's 8 gains of weight row `row` (its columns 2048 k + 8 t + i).
+__device__ __forceinline__ void load_gains(const NormDesc &n, int64_t row, int k, int tid,
+                                           float (&g)[8]) {
+    const int64_t col = row * kHidden + (int64_t)k * 2048 + 8 * tid;
+    if (n.fp32) {
+        const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(n.w) + col);
+        const float4 a = __ldg(p), b = __ldg(p + 1);
+        g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w;
+        g[4] = b.x; g[5] = b.y; g[6] = b.z; g[7] = b.w;
+    } else {
+        unpack8(__ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(n.w) + col)), g);
+    }
+    if (n.center != 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            g[i] = __fadd_rn(g[i], n.center);
+    }
+}
+
+// Sum of squares of the row held as v (fragment-major), in the order of
+// row_sumsq.
+__device__ __forceinline__ float row_sumsq_f(const float (&v)[kVals], float *sums, int warp,
+                                             int lane) {
+    float p = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kVals; ++j)
+        p = __fadd_rn(p, __fmul_rn(v[j], v[j]));
+    p = warp_butterfly_sum(p);
+    if (lane == 0)
+        sums[warp] = p;
+    __syncthreads();
+    float s = sums[0];
+#pragma unroll
+    for (int w = 1; w < kThreads / 32; ++w)
+        s = __fadd_rn(s, sums[w]);
+    return s;
+}
+
+// One RMSNorm of the row in v, in place: an input-scale weight multiplies
+// first (gamma * v), then S, r = 1 / sqrt(fma(S, 2^-13, eps)), v * r, and an
+// output-scale weight multiplies last.  `sums` alternates between two
+// buffers so that consecutive norms need one barrier each.
+__device__ __forceinline__ void norm_row(float (&v)[kVals], const NormDesc &n, int64_t wrow,
+                                         float (&sums)[2][kThreads / 32], int &buf, int tid,
+                                         int warp, int lane) {
+    const bool weighted = n.w != nullptr;
+    const bool in_scale = weighted && n.input_scale;
+    if (in_scale) {
+#pragma unroll
+        for (int k = 0; k < kFrags; ++k) {
+            float g[8];
+            load_gains(n, wrow, k, tid, g);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                v[8 * k + i] = __fmul_rn(g[i], v[8 * k + i]);
+        }
+    }
+    const float r = inv_rms(row_sumsq_f(v, sums[buf], warp, lane), 0x1p-13f, n.eps);
+    buf ^= 1;
+#pragma unroll
+    for (int k = 0; k < kFrags; ++k) {
+        float g[8];
+        if (weighted && !in_scale)
+            load_gains(n, wrow, k, tid, g);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float y = __fmul_rn(v[8 * k + i], r);
+            if (weighted && !in_scale)
+                y = __fmul_rn(y, g[i]);
+            v[8 * k + i] = y;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+k1_context_norms_ex(const uint16_t *__restrict__ x, int64_t T, const NormDesc hidden,
+                    const NormDesc pre, int32_t L, uint16_t *__restrict__ out)
+{
+    __shared__ float sums[2][kThreads / 32];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t row = blockIdx.x;
+    int buf = 0;
+    pdl_trigger();
+    pdl_wait();
+
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x) + row * (kHidden / 8);
+    float v[kVals];
+#pragma unroll
+    for (int k = 0; k < kFrags; ++k) {
+        float f[8];
+        unpack8(__ldcs(xr + k * kFragStride + tid), f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            v[8 * k + i] = f[i];
+    }
+    // a1: the hidden norm, rounded to bf16 (kept packed)
+    norm_row(v, hidden, 0, sums, buf, tid, warp, lane);
+    uint4 z[kFrags];
+#pragma unroll
+    for (int k = 0; k < kFrags; ++k)
+        z[k] = pack8(&v[8 * k]);
+
+    // a2: with an output-scale (or no) layer weight one inverse RMS serves
+    // every layer
+    const bool per_layer = pre.w != nullptr && pre.input_scale;
+    float r2 = 0.0f;
+    if (!per_layer) {
+#pragma unroll
+        for (int k = 0; k < kFrags; ++k)
+            unpack8(z[k], &v[8 * k]);
+        r2 = inv_rms(row_sumsq_f(v, sums[buf], warp, lane), 0x1p-13f, pre.eps);
+        buf ^= 1;
+    }
+    for (int32_t l = 0; l < L; ++l) {
+#pragma unroll
+        for (int k = 0; k < kFrags; ++k)
+            unpack8(z[k], &v[8 * k]);
+        if (per_layer) {
+            norm_row(v, pre, l, sums, buf, tid, warp, lane);
+        } else {
+#pragma unroll
+            for (int k = 0; k < kFrags; ++k) {
+                float g[8];
+                if (pre.w != nullptr)
+                    load_gains(pre, l, k, tid, g);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float y = __fmul_rn(v[8 * k + i], r2);
+                    if (pre.w != nullptr)
+                        y = __fmul_rn(y, g[i]);
+                    v[8 * k + i] = y;
+                }
+            }
+        }
+        uint4 *o = reinterpret_cast<uint4 *>(out) + ((int64_t)l * T + row) * (kHidden / 8);
+#pragma unroll
+        for (int k = 0; k < kFrags; ++k)
+            o[k * kFragStride + tid] = pack8(&v[8 * k]);
+    }
+}
+
 }  // namespace
 
+cudaError_t launch_context_norms_ex(const uint16_t *x, int64_t T, const NormDesc &hidden,
+                                    const NormDesc &pre, int32_t L, uint16_t *out,
+                                    cudaStream_t stream)
+{
+    return launch_pdl(k1_context_norms_ex, dim3((unsigned)T), dim3(kThreads), 0, stream, 1, x, T,
+                      hidden, pre, L, out);
+}
+
 cudaError_t launch_context_norms(const uint16_t *x, int64_t T, const uint16_t *hidden_w,
-                                 const uint16_t *pre_w, int32_t L, float eps,
+                                 const uint16_t *pre_w, int32_t L, float hidden_eps, float pre_eps,
                                  uint16_t *out, cudaStream_t stream)
 {
     const dim3 grid((unsigned)T), block(kThreads);
     if (hidden_w && pre_w)
-        return launch_pdl(k1_context_norms<true, true>, grid, block, 0, stream, 1, x, T, hidden_w, pre_w, L, eps, out);
+        return launch_pdl(k1_context_norms<true, true>, grid, block, 0, stream, 1, x, T, hidden_w,
+                          pre_w, L, hidden_eps, pre_eps, out);
     if (hidden_w)
-        return launch_pdl(k1_context_norms<true, false>, grid, block, 0, stream, 1, x, T, hidden_w, pre_w, L, eps, out);
+        return launch_pdl(k1_context_norms<true, false>, grid, block, 0, stream, 1, x, T, hidden_w,
+                          pre_w, L, hidden_eps, pre_eps, out);
     if (pre_w)
-        return launch_pdl(k1_context_norms<false, true>, grid, block, 0, stream, 1, x, T, hidden_w, pre_w, L, eps, out);
-    return launch_pdl(k1_context_norms<false, false>, grid, block, 0, stream, 1, x, T, hidden_w, pre_w, L, eps, out);
+        return launch_pdl(k1_context_norms<false, true>, grid, block, 0, stream, 1, x, T, hidden_w,
+                          pre_w, L, hidden_eps, pre_eps, out);
+    return launch_pdl(k1_context_norms<false, false>, grid, block, 0, stream, 1, x, T, hidden_w,
+                      pre_w, L, hidden_eps, pre_eps, out);
 }
 
 cudaError_t launch_row_prep(const uint16_t *x, int64_t T, const uint16_t *hidden_w, float eps,

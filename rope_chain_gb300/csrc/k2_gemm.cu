@@ -490,7 +490,7 @@ __device__ __forceinline__ void fused_store_tile(const FusedStore &fs, const Gem
     const int N = g.N;
     bool store = false;
     int64_t slot = 0, pos = 0;
-    if (live && row < fs.rows && fs.slots[l] != nullptr) {
+    if (live && row < fs.rows[l] && fs.slots[l] != nullptr) {
         slot = __ldg(fs.slots[l] + row);
         if (slot >= 0) {
             if (rope)
@@ -1112,9 +1112,12 @@ cudaError_t launch_kv_project_store(const uint16_t *normed, const uint16_t *W, b
         StoreLaunch p{};
         bool any = false;
         for (int32_t i = 0; i < n; ++i) {
-            p.slots[i] = fs.slots[first + i];
+            p.slots[i] = fs.rows[first + i] > 0 ? fs.slots[first + i] : nullptr;
             p.caches[i] = fs.caches[first + i];
+            p.rows[i] = fs.rows[first + i];
             any = any || p.slots[i] != nullptr;
+            if (p.slots[i])
+                p.grid_rows = std::max(p.grid_rows, p.rows[i]);
         }
         if (!any)
             continue;
@@ -1127,7 +1130,6 @@ cudaError_t launch_kv_project_store(const uint16_t *normed, const uint16_t *W, b
         p.max_position = fs.max_position;
         p.capacity = fs.capacity;
         p.block_size = fs.block_size;
-        p.rows = fs.rows;
         p.eps = fs.eps;
         p.err = fs.err;
         e = launch_kv_store(p, fs.H, n, stream);

@@ -70,7 +70,7 @@ k3_kv_store(const __grid_constant__ StoreLaunch p)
     const int layer = blockIdx.y;
     pdl_trigger();
     pdl_wait();
-    if (row >= p.rows)
+    if (row >= p.rows[layer])
         return;
     const int64_t *slots = p.slots[layer];
     if (slots == nullptr)
@@ -132,7 +132,7 @@ k3_reduce_store(const __grid_constant__ FusedStore fs, const float *__restrict__
     if (row >= T)
         return;
     const int64_t *slots = fs.slots[layer];
-    const bool store = slots != nullptr && row < fs.rows;
+    const bool store = slots != nullptr && row < fs.rows[layer];
     int64_t slot = -1, pos = 0;
     if (store) {
         slot = __ldg(slots + row);
@@ -200,7 +200,7 @@ k3_reduce_store(const __grid_constant__ FusedStore fs, const float *__restrict__
 
 template <int H>
 cudaError_t launch_h(const StoreLaunch &p, int32_t layers, cudaStream_t stream) {
-    const dim3 grid((unsigned)((p.rows + kWarps - 1) / kWarps), (unsigned)layers);
+    const dim3 grid((unsigned)((p.grid_rows + kWarps - 1) / kWarps), (unsigned)layers);
     if (p.cos_sin)
         return launch_pdl(k3_kv_store<H, true>, grid, dim3(kWarps * 32), 0, stream, 1, p);
     return launch_pdl(k3_kv_store<H, false>, grid, dim3(kWarps * 32), 0, stream, 1, p);

@@ -68,6 +68,101 @@ rc_status check_project_sizes(int32_t L, int64_t T, int32_t D, int32_t N) {
 
 }  // namespace
 
+namespace {
+
+// rc_kv_store and rc_kv_store_rows: layer l inserts layer_rows[l] rows
+// (`rows` for every layer when layer_rows is NULL).
+rc_status kv_store_impl(const char *fn, const uint16_t *k, const uint16_t *v,
+                        int64_t k_layer_stride, int64_t k_row_stride, int64_t v_layer_stride,
+                        int64_t v_row_stride, const int64_t *positions,
+                        const int64_t *const *slots, const uint16_t *cos_sin,
+                        int64_t max_position, uint16_t *const *caches, int32_t num_blocks,
+                        int32_t block_size, int32_t H, int32_t L, float eps,
+                        const int64_t *layer_rows, int64_t rows, int32_t *err,
+                        cudaStream_t stream)
+{
+    if (H != 1 && H != 2 && H != 4 && H != 8 && H != 16 && H != 32)
+        return fail(RC_ERR_UNSUPPORTED, "%s: H=%d is not a power of two <= 32", fn, H);
+    if (L < 1 || L > 4096)
+        return fail(RC_ERR_INVALID_ARG, "%s: L=%d outside [1, 4096]", fn, L);
+    int64_t max_rows = 0;
+    for (int32_t l = 0; l < L; ++l) {
+        const int64_t r = layer_rows ? layer_rows[l] : rows;
+        if (r < 0 || r > 0x7FFFFFFFLL)
+            return fail(RC_ERR_INVALID_ARG, "%s: rows of layer %d = %lld outside [0, 2^31)", fn, l,
+                        (long long)r);
+        max_rows = std::max(max_rows, r);
+    }
+    if (num_blocks < 1 || block_size < 1 || (int64_t)num_blocks * block_size >= (1LL << 31))
+        return fail(RC_ERR_INVALID_ARG,
+                    "%s: need num_blocks, block_size >= 1 and num_blocks*block_size < 2^31", fn);
+    if (!k || !v || !slots || !caches)
+        return fail(RC_ERR_INVALID_ARG, "%s: k, v, slots and caches must not be NULL", fn);
+    if (!aligned(k, 4) || !aligned(v, 4))
+        return fail(RC_ERR_INVALID_ARG, "%s: k and v must be 4-byte aligned", fn);
+    if (k_layer_stride < 0 || k_row_stride < 0 || v_layer_stride < 0 || v_row_stride < 0 ||
+        (k_layer_stride | k_row_stride | v_layer_stride | v_row_stride) & 1)
+        return fail(RC_ERR_INVALID_ARG, "%s: strides must be even and non-negative", fn);
+    if (cos_sin) {
+        if (!positions || !aligned(positions, 8))
+            return fail(RC_ERR_INVALID_ARG, "%s: RoPE needs 8-byte aligned positions", fn);
+        if (max_position < 1)
+            return fail(RC_ERR_INVALID_ARG, "%s: max_position must be >= 1 with a table", fn);
+        if (!aligned(cos_sin, 2))
+            return fail(RC_ERR_INVALID_ARG, "%s: cos_sin must be 2-byte aligned", fn);
+    }
+    for (int32_t l = 0; l < L; ++l) {
+        if (!slots[l])
+            continue;
+        if (!aligned(slots[l], 8))
+            return fail(RC_ERR_INVALID_ARG, "%s: slots[%d] must be 8-byte aligned", fn, l);
+        if (!caches[l] || !aligned(caches[l], 4))
+            return fail(RC_ERR_INVALID_ARG, "%s: caches[%d] must be a 4-byte aligned pointer", fn, l);
+    }
+    if (max_rows == 0)
+        return ok();
+
+    // Layers go to the GPU in chunks of at most 8 (the pointer tables are
+    // kernel parameters); a chunk whose layers all lack slots is skipped.
+    for (int32_t first = 0; first < L; first += rc::kMaxLayersPerLaunch) {
+        const int32_t n = std::min(rc::kMaxLayersPerLaunch, L - first);
+        rc::StoreLaunch p{};
+        bool any = false;
+        int64_t chunk_rows = 0;
+        for (int32_t i = 0; i < n; ++i) {
+            const int64_t r = layer_rows ? layer_rows[first + i] : rows;
+            p.slots[i] = r > 0 ? slots[first + i] : nullptr;
+            p.caches[i] = caches[first + i];
+            p.rows[i] = (int32_t)r;
+            any = any || p.slots[i] != nullptr;
+            if (p.slots[i])
+                chunk_rows = std::max(chunk_rows, r);
+        }
+        if (!any)
+            continue;
+        p.k = k + first * k_layer_stride;
+        p.v = v + first * v_layer_stride;
+        p.k_layer_stride = k_layer_stride;
+        p.k_row_stride = k_row_stride;
+        p.v_layer_stride = v_layer_stride;
+        p.v_row_stride = v_row_stride;
+        p.positions = positions;
+        p.cos_sin = cos_sin;
+        p.max_position = max_position;
+        p.capacity = (int64_t)num_blocks * block_size;
+        p.block_size = block_size;
+        p.grid_rows = (int32_t)chunk_rows;
+        p.eps = eps;
+        p.err = err;
+        const cudaError_t e = rc::launch_kv_store(p, H, n, stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, fn);
+    }
+    return ok();
+}
+
+}  // namespace
+
 namespace rc {
 void set_last_error(const char *msg) { snprintf(g_err, sizeof g_err, "%s", msg); }
 }  // namespace rc
@@ -98,9 +193,64 @@ rc_status rc_context_norms(const uint16_t *x, int64_t T, int32_t D, const uint16
         return fail(RC_ERR_INVALID_ARG, "rc_context_norms: out overlaps x");
     if (T == 0)
         return ok();
-    const cudaError_t e = rc::launch_context_norms(x, T, hidden_w, pre_w, L, eps, out, stream);
+    const cudaError_t e = rc::launch_context_norms(x, T, hidden_w, pre_w, L, eps, eps, out, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "rc_context_norms launch");
+    return ok();
+}
+
+rc_status rc_context_norms_ex(const uint16_t *x, int64_t T, int32_t D,
+                              const rc_norm_params *hidden, const rc_norm_params *pre, int32_t L,
+                              uint16_t *out, cudaStream_t stream)
+{
+    const char *fn = "rc_context_norms_ex";
+    if (D != rc::kHidden)
+        return fail(RC_ERR_UNSUPPORTED, "%s: D=%d, the row norm takes D=8192", fn, D);
+    if (T < 0 || T > 0x7FFFFFFFLL)
+        return fail(RC_ERR_INVALID_ARG, "%s: T=%lld outside [0, 2^31)", fn, (long long)T);
+    if (L < 1 || L > 64)
+        return fail(RC_ERR_INVALID_ARG, "%s: L=%d outside [1, 64]", fn, L);
+    if (!x || !out || !hidden || !pre)
+        return fail(RC_ERR_INVALID_ARG, "%s: x, out, hidden and pre must not be NULL", fn);
+    if (!aligned(x, 16) || !aligned(out, 16))
+        return fail(RC_ERR_INVALID_ARG, "%s: x and out must be 16-byte aligned", fn);
+    rc::NormDesc d[2];
+    const rc_norm_params *np[2] = {hidden, pre};
+    for (int i = 0; i < 2; ++i) {
+        const rc_norm_params &n = *np[i];
+        const char *which = i ? "pre" : "hidden";
+        if (n.weight_dtype != RC_NORM_NONE && n.weight_dtype != RC_NORM_BF16 &&
+            n.weight_dtype != RC_NORM_F32)
+            return fail(RC_ERR_INVALID_ARG, "%s: %s weight_dtype=%d unknown", fn, which, n.weight_dtype);
+        if ((n.weight_dtype == RC_NORM_NONE) != (n.weight == nullptr))
+            return fail(RC_ERR_INVALID_ARG, "%s: %s weight must be NULL exactly when weight_dtype is "
+                        "RC_NORM_NONE", fn, which);
+        if (n.weight && !aligned(n.weight, 16))
+            return fail(RC_ERR_INVALID_ARG, "%s: %s weight must be 16-byte aligned", fn, which);
+        d[i].w = n.weight;
+        d[i].fp32 = n.weight_dtype == RC_NORM_F32;
+        d[i].input_scale = n.weight != nullptr && n.input_scale != 0;   // weightless: ignored
+        d[i].center = n.gain_center;
+        d[i].eps = n.eps;
+    }
+    const size_t xbytes = (size_t)T * D * 2, obytes = (size_t)L * T * D * 2;
+    if (T > 0 && overlap(x, xbytes, out, obytes))
+        return fail(RC_ERR_INVALID_ARG, "%s: out overlaps x", fn);
+    if (T == 0)
+        return ok();
+    // bf16 output-scale weights without a center take the default kernel
+    const auto plain = [](const rc::NormDesc &n) {
+        return n.w == nullptr || (!n.fp32 && !n.input_scale && n.center == 0.0f);
+    };
+    cudaError_t e;
+    if (plain(d[0]) && plain(d[1]))
+        e = rc::launch_context_norms(x, T, static_cast<const uint16_t *>(d[0].w),
+                                     static_cast<const uint16_t *>(d[1].w), L, d[0].eps, d[1].eps,
+                                     out, stream);
+    else
+        e = rc::launch_context_norms_ex(x, T, d[0], d[1], L, out, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "rc_context_norms_ex launch");
     return ok();
 }
 
@@ -156,73 +306,23 @@ rc_status rc_kv_store(const uint16_t *k, const uint16_t *v, int64_t k_layer_stri
                       int32_t num_blocks, int32_t block_size, int32_t H, int32_t L, float eps,
                       int64_t rows, int32_t *err, cudaStream_t stream)
 {
-    if (H != 1 && H != 2 && H != 4 && H != 8 && H != 16 && H != 32)
-        return fail(RC_ERR_UNSUPPORTED, "rc_kv_store: H=%d is not a power of two <= 32", H);
-    if (L < 1 || L > 4096)
-        return fail(RC_ERR_INVALID_ARG, "rc_kv_store: L=%d outside [1, 4096]", L);
-    if (rows < 0 || rows > 0x7FFFFFFFLL)
-        return fail(RC_ERR_INVALID_ARG, "rc_kv_store: rows=%lld outside [0, 2^31)", (long long)rows);
-    if (num_blocks < 1 || block_size < 1 || (int64_t)num_blocks * block_size >= (1LL << 31))
-        return fail(RC_ERR_INVALID_ARG,
-                    "rc_kv_store: need num_blocks, block_size >= 1 and num_blocks*block_size < 2^31");
-    if (!k || !v || !slots || !caches)
-        return fail(RC_ERR_INVALID_ARG, "rc_kv_store: k, v, slots and caches must not be NULL");
-    if (!aligned(k, 4) || !aligned(v, 4))
-        return fail(RC_ERR_INVALID_ARG, "rc_kv_store: k and v must be 4-byte aligned");
-    if (k_layer_stride < 0 || k_row_stride < 0 || v_layer_stride < 0 || v_row_stride < 0 ||
-        (k_layer_stride | k_row_stride | v_layer_stride | v_row_stride) & 1)
-        return fail(RC_ERR_INVALID_ARG, "rc_kv_store: strides must be even and non-negative");
-    if (cos_sin) {
-        if (!positions || !aligned(positions, 8))
-            return fail(RC_ERR_INVALID_ARG, "rc_kv_store: RoPE needs 8-byte aligned positions");
-        if (max_position < 1)
-            return fail(RC_ERR_INVALID_ARG, "rc_kv_store: max_position must be >= 1 with a table");
-        if (!aligned(cos_sin, 2))
-            return fail(RC_ERR_INVALID_ARG, "rc_kv_store: cos_sin must be 2-byte aligned");
-    }
-    for (int32_t l = 0; l < L; ++l) {
-        if (!slots[l])
-            continue;
-        if (!aligned(slots[l], 8))
-            return fail(RC_ERR_INVALID_ARG, "rc_kv_store: slots[%d] must be 8-byte aligned", l);
-        if (!caches[l] || !aligned(caches[l], 4))
-            return fail(RC_ERR_INVALID_ARG, "rc_kv_store: caches[%d] must be a 4-byte aligned pointer", l);
-    }
-    if (rows == 0)
-        return ok();
+    return kv_store_impl("rc_kv_store", k, v, k_layer_stride, k_row_stride, v_layer_stride,
+                         v_row_stride, positions, slots, cos_sin, max_position, caches, num_blocks,
+                         block_size, H, L, eps, nullptr, rows, err, stream);
+}
 
-    // Layers go to the GPU in chunks of at most 8 (the pointer tables are
-    // kernel parameters); a chunk whose layers all lack slots is skipped.
-    for (int32_t first = 0; first < L; first += rc::kMaxLayersPerLaunch) {
-        const int32_t n = std::min(rc::kMaxLayersPerLaunch, L - first);
-        rc::StoreLaunch p{};
-        bool any = false;
-        for (int32_t i = 0; i < n; ++i) {
-            p.slots[i] = slots[first + i];
-            p.caches[i] = caches[first + i];
-            any = any || p.slots[i] != nullptr;
-        }
-        if (!any)
-            continue;
-        p.k = k + first * k_layer_stride;
-        p.v = v + first * v_layer_stride;
-        p.k_layer_stride = k_layer_stride;
-        p.k_row_stride = k_row_stride;
-        p.v_layer_stride = v_layer_stride;
-        p.v_row_stride = v_row_stride;
-        p.positions = positions;
-        p.cos_sin = cos_sin;
-        p.max_position = max_position;
-        p.capacity = (int64_t)num_blocks * block_size;
-        p.block_size = block_size;
-        p.rows = (int32_t)rows;
-        p.eps = eps;
-        p.err = err;
-        const cudaError_t e = rc::launch_kv_store(p, H, n, stream);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "rc_kv_store launch");
-    }
-    return ok();
+rc_status rc_kv_store_rows(const uint16_t *k, const uint16_t *v, int64_t k_layer_stride,
+                           int64_t k_row_stride, int64_t v_layer_stride, int64_t v_row_stride,
+                           const int64_t *positions, const int64_t *const *slots,
+                           const uint16_t *cos_sin, int64_t max_position, uint16_t *const *caches,
+                           int32_t num_blocks, int32_t block_size, int32_t H, int32_t L, float eps,
+                           const int64_t *layer_rows, int32_t *err, cudaStream_t stream)
+{
+    if (!layer_rows)
+        return fail(RC_ERR_INVALID_ARG, "rc_kv_store_rows: layer_rows must not be NULL");
+    return kv_store_impl("rc_kv_store_rows", k, v, k_layer_stride, k_row_stride, v_layer_stride,
+                         v_row_stride, positions, slots, cos_sin, max_position, caches, num_blocks,
+                         block_size, H, L, eps, layer_rows, 0, err, stream);
 }
 
 }  // extern "C"
@@ -234,7 +334,8 @@ rc_status fused_store_args(const char *fn, int32_t L, int64_t T, int32_t H,
                            const int64_t *positions, const int64_t *const *slots,
                            const uint16_t *cos_sin, int64_t max_position, uint16_t *const *caches,
                            int32_t num_blocks, int32_t block_size, float eps, int64_t rows,
-                           int32_t *err, uint16_t *kv_out, rc::FusedStore *fs)
+                           int32_t *err, uint16_t *kv_out, rc::FusedStore *fs,
+                           const int64_t *layer_rows = nullptr)
 {
     if (L > rc::kMaxFusedLayers)
         return fail(RC_ERR_UNSUPPORTED, "%s: L=%d above %d", fn, L, rc::kMaxFusedLayers);
@@ -242,8 +343,14 @@ rc_status fused_store_args(const char *fn, int32_t L, int64_t T, int32_t H,
         return fail(RC_ERR_INVALID_ARG, "%s: slots and caches must not be NULL", fn);
     if (kv_out && !aligned(kv_out, 16))
         return fail(RC_ERR_INVALID_ARG, "%s: kv_out must be 16-byte aligned", fn);
-    if (rows < 0 || rows > T)
-        return fail(RC_ERR_INVALID_ARG, "%s: rows=%lld outside [0, T]", fn, (long long)rows);
+    if (L < 1)
+        return fail(RC_ERR_INVALID_ARG, "%s: L=%d below 1", fn, L);
+    for (int32_t l = 0; l < L; ++l) {
+        const int64_t r = layer_rows ? layer_rows[l] : rows;
+        if (r < 0 || r > T)
+            return fail(RC_ERR_INVALID_ARG, "%s: rows=%lld (layer %d) outside [0, T]", fn,
+                        (long long)r, l);
+    }
     if (num_blocks < 1 || block_size < 1 || (int64_t)num_blocks * block_size >= (1LL << 31))
         return fail(RC_ERR_INVALID_ARG,
                     "%s: need num_blocks, block_size >= 1 and num_blocks*block_size < 2^31", fn);
@@ -272,7 +379,8 @@ rc_status fused_store_args(const char *fn, int32_t L, int64_t T, int32_t H,
     fs->capacity = (int64_t)num_blocks * block_size;
     fs->block_size = block_size;
     fs->H = H;
-    fs->rows = (int32_t)rows;
+    for (int32_t l = 0; l < L; ++l)
+        fs->rows[l] = (int32_t)(layer_rows ? layer_rows[l] : rows);
     fs->eps = eps;
     fs->err = err;
     fs->kv_out = kv_out;
@@ -293,17 +401,18 @@ size_t context_kv_fixed_bytes(bool pair, int32_t L, int64_t T, int32_t D) {
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-rc_status rc_kv_project_store(const uint16_t *normed, const uint16_t *W, int32_t w_layout,
-                              int32_t L, int64_t T, int32_t D, int32_t H,
-                              const int64_t *positions, const int64_t *const *slots,
-                              const uint16_t *cos_sin, int64_t max_position,
-                              uint16_t *const *caches, int32_t num_blocks, int32_t block_size,
-                              float eps, int64_t rows, int32_t *err, uint16_t *kv_out,
-                              void *workspace, size_t workspace_bytes, cudaStream_t stream)
+// rc_kv_project_store and rc_kv_project_store_rows.
+rc_status kv_project_store_impl(const char *fn, const uint16_t *normed, const uint16_t *W,
+                                int32_t w_layout, int32_t L, int64_t T, int32_t D, int32_t H,
+                                const int64_t *positions, const int64_t *const *slots,
+                                const uint16_t *cos_sin, int64_t max_position,
+                                uint16_t *const *caches, int32_t num_blocks, int32_t block_size,
+                                float eps, const int64_t *layer_rows, int64_t rows, int32_t *err,
+                                uint16_t *kv_out, void *workspace, size_t workspace_bytes,
+                                cudaStream_t stream)
 {
-    const char *fn = "rc_kv_project_store";
     if (!supported_heads(H))
         return fail(RC_ERR_UNSUPPORTED, "%s: H=%d is not a power of two <= 32", fn, H);
     const int32_t N = 2 * H * rc::kHeadDim;
@@ -318,7 +427,7 @@ rc_status rc_kv_project_store(const uint16_t *normed, const uint16_t *W, int32_t
         return fail(RC_ERR_INVALID_ARG, "%s: normed, W and workspace must be 16-byte aligned", fn);
     rc::FusedStore fs;
     st = fused_store_args(fn, L, T, H, positions, slots, cos_sin, max_position, caches, num_blocks,
-                          block_size, eps, rows, err, kv_out, &fs);
+                          block_size, eps, rows, err, kv_out, &fs, layer_rows);
     if (st != RC_OK)
         return st;
     if (T == 0)
@@ -340,6 +449,40 @@ rc_status rc_kv_project_store(const uint16_t *normed, const uint16_t *W, int32_t
     if (e != cudaSuccess)
         return cuda_fail(e, why);
     return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+rc_status rc_kv_project_store(const uint16_t *normed, const uint16_t *W, int32_t w_layout,
+                              int32_t L, int64_t T, int32_t D, int32_t H,
+                              const int64_t *positions, const int64_t *const *slots,
+                              const uint16_t *cos_sin, int64_t max_position,
+                              uint16_t *const *caches, int32_t num_blocks, int32_t block_size,
+                              float eps, int64_t rows, int32_t *err, uint16_t *kv_out,
+                              void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    return kv_project_store_impl("rc_kv_project_store", normed, W, w_layout, L, T, D, H, positions,
+                                 slots, cos_sin, max_position, caches, num_blocks, block_size, eps,
+                                 nullptr, rows, err, kv_out, workspace, workspace_bytes, stream);
+}
+
+rc_status rc_kv_project_store_rows(const uint16_t *normed, const uint16_t *W, int32_t w_layout,
+                                   int32_t L, int64_t T, int32_t D, int32_t H,
+                                   const int64_t *positions, const int64_t *const *slots,
+                                   const uint16_t *cos_sin, int64_t max_position,
+                                   uint16_t *const *caches, int32_t num_blocks, int32_t block_size,
+                                   float eps, const int64_t *layer_rows, int32_t *err,
+                                   uint16_t *kv_out, void *workspace, size_t workspace_bytes,
+                                   cudaStream_t stream)
+{
+    if (!layer_rows)
+        return fail(RC_ERR_INVALID_ARG, "rc_kv_project_store_rows: layer_rows must not be NULL");
+    return kv_project_store_impl("rc_kv_project_store_rows", normed, W, w_layout, L, T, D, H,
+                                 positions, slots, cos_sin, max_position, caches, num_blocks,
+                                 block_size, eps, layer_rows, 0, err, kv_out, workspace,
+                                 workspace_bytes, stream);
 }
 
 size_t rc_context_kv_workspace_size(int32_t L, int64_t T, int32_t D, int32_t H)
@@ -414,7 +557,7 @@ rc_status rc_context_kv(const uint16_t *x, int64_t T, int32_t D, const uint16_t 
                         "%s: at these sizes the store reads the projection from kv_out; pass kv_out "
                         "or a workspace of rc_context_kv_workspace_size() bytes", fn);
         uint16_t *normed = reinterpret_cast<uint16_t *>(wsb);
-        e = rc::launch_context_norms(x, T, hidden_w, pre_w, L, eps, normed, stream);
+        e = rc::launch_context_norms(x, T, hidden_w, pre_w, L, eps, eps, normed, stream);
         if (e == cudaSuccess)
             e = rc::launch_kv_project_store(normed, W, w_layout == RC_W_NK, L, T, D, N, plan, partials,
                                             fs, stream, &why);

@@ -87,10 +87,26 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
 
 // ------------------------------------------------------------- launches
 
-// Norms: grid of T CTAs x 256 threads; returns the launch error.
+// Norms: grid of T CTAs x 256 threads; returns the launch error.  bf16
+// output-scale weights (or none), gain center 0.
 cudaError_t launch_context_norms(const uint16_t *x, int64_t T, const uint16_t *hidden_w,
-                                 const uint16_t *pre_w, int32_t L, float eps,
+                                 const uint16_t *pre_w, int32_t L, float hidden_eps, float pre_eps,
                                  uint16_t *out, cudaStream_t stream);
+
+// One norm of the variant kernel: weight NULL (weightless), bf16 or FP32
+// ([8192] hidden, [L, 8192] layers), whether it scales the input, its gain
+// center (added when non-zero) and eps.
+struct NormDesc {
+    const void *w;
+    int32_t fp32;
+    int32_t input_scale;
+    float center;
+    float eps;
+};
+
+cudaError_t launch_context_norms_ex(const uint16_t *x, int64_t T, const NormDesc &hidden,
+                                    const NormDesc &pre, int32_t L, uint16_t *out,
+                                    cudaStream_t stream);
 
 // Row prep for the fused chain: z = bf16 [T, 8192] hidden-norm output and
 // r2 [T] = the layers' shared inverse RMS of z.
@@ -108,7 +124,8 @@ struct StoreLaunch {
     uint16_t *caches[kMaxLayersPerLaunch];
     int64_t capacity;                // num_blocks * block_size
     int32_t block_size;
-    int32_t rows;
+    int32_t rows[kMaxLayersPerLaunch];   // rows inserted per layer of the chunk
+    int32_t grid_rows;               // rows the grid covers (max over the chunk)
     float eps;
     int32_t *err;
 };
@@ -124,7 +141,7 @@ struct FusedStore {
     int64_t capacity;                // num_blocks * block_size
     int32_t block_size;
     int32_t H;
-    int32_t rows;                    // rows inserted (<= T)
+    int32_t rows[kMaxFusedLayers];   // rows inserted per layer (<= T)
     float eps;
     int32_t *err;
     uint16_t *kv_out;                // optional bf16 [L, T, 2*H*64] copy of the projection

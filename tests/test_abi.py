@@ -117,3 +117,66 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(rc, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         rc.lib()
+
+
+def _norm(weight=None, dtype=0, input_scale=0, center=0.0, eps=1e-6):
+    return rc.NormParams(weight, dtype, input_scale, center, eps)
+
+
+def test_norms_ex_rejections(lib):
+    x, o = 0x10000, 0x200000
+    call = lambda h, p, D=8192, T=4, L=1: lib.rc_context_norms_ex(
+        A(x), T, D, None if h is None else ctypes.byref(h), None if p is None else ctypes.byref(p),
+        L, A(o), None)
+    none = _norm()
+    assert call(none, none, D=4096) == rc.RC_ERR_UNSUPPORTED
+    assert call(None, none) == rc.RC_ERR_INVALID_ARG
+    assert call(_norm(dtype=5), none) == rc.RC_ERR_INVALID_ARG
+    assert "weight_dtype" in last(lib)
+    assert call(_norm(dtype=rc.RC_NORM_BF16), none) == rc.RC_ERR_INVALID_ARG     # dtype, no weight
+    assert call(none, _norm(weight=0x4000)) == rc.RC_ERR_INVALID_ARG             # weight, no dtype
+    assert call(none, _norm(weight=0x4008, dtype=rc.RC_NORM_F32)) == rc.RC_ERR_INVALID_ARG
+    assert "aligned" in last(lib)
+    assert call(none, none, L=0) == rc.RC_ERR_INVALID_ARG
+    # input_scale and a center on a weightless norm are ignored; T == 0 is empty
+    assert call(_norm(input_scale=1, center=1.0), _norm(weight=0x4000, dtype=rc.RC_NORM_F32),
+                T=0) == rc.RC_OK
+
+
+def _store_rows(lib, layer_rows, **over):
+    arg = dict(k=A(0x1000), v=A(0x1080), kls=1024, krs=128, vls=1024, vrs=128, positions=A(0x4000),
+               slots=[A(0x8000), A(0x9000)], cos=None, maxpos=0,
+               caches=[A(0x100000), A(0x200000)], nb=4, bs=16, H=8, L=2, eps=1e-6, err=None)
+    arg.update(over)
+    L = arg["L"]
+    slots = (ctypes.c_void_p * L)(*arg["slots"][:L])
+    caches = (ctypes.c_void_p * L)(*arg["caches"][:L])
+    rows = None if layer_rows is None else (ctypes.c_int64 * L)(*layer_rows)
+    return lib.rc_kv_store_rows(arg["k"], arg["v"], arg["kls"], arg["krs"], arg["vls"],
+                                arg["vrs"], arg["positions"], slots, arg["cos"], arg["maxpos"],
+                                caches, arg["nb"], arg["bs"], arg["H"], L, arg["eps"], rows,
+                                arg["err"], None)
+
+
+def test_store_rows_rejections(lib):
+    assert _store_rows(lib, None) == rc.RC_ERR_INVALID_ARG
+    assert "layer_rows" in last(lib)
+    assert _store_rows(lib, [4, -1]) == rc.RC_ERR_INVALID_ARG
+    assert "layer 1" in last(lib)
+    assert _store_rows(lib, [4, 1 << 31]) == rc.RC_ERR_INVALID_ARG
+    assert _store_rows(lib, [4, 2], H=5) == rc.RC_ERR_UNSUPPORTED
+    assert _store_rows(lib, [0, 0]) == rc.RC_OK            # nothing to insert: no launch
+
+
+def test_project_store_rows_rejections(lib):
+    a, w = 0x100000, 0x4000000
+    slots = (ctypes.c_void_p * 2)(A(0x8000), A(0x9000))
+    caches = (ctypes.c_void_p * 2)(A(0x1000000), A(0x2000000))
+    call = lambda rows, T=8: lib.rc_kv_project_store_rows(
+        A(a), A(w), 0, 2, T, 8192, 8, None, slots, None, 0, caches, 4, 16, 1e-6,
+        None if rows is None else (ctypes.c_int64 * 2)(*rows), None, None, None, 0, None)
+    assert call(None) == rc.RC_ERR_INVALID_ARG
+    assert call([8, 9]) == rc.RC_ERR_INVALID_ARG
+    assert "outside [0, T]" in last(lib)
+    assert call([-1, 0]) == rc.RC_ERR_INVALID_ARG
+    assert call([0, 0], T=0) == rc.RC_OK
