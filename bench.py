@@ -35,11 +35,7 @@ L2_FLUSH_BYTES = 512 << 20          # > 129 MB L2: written between timed steps
 # capture of this bench command (dram__bytes_read.sum + dram__bytes_write.sum,
 # summed over the kernels the timed call launches); keyed by (workload, path,
 # kernel).  An entry is removed whenever one of its kernels changes.
-# workload 2, store path, project_store = k2_project_pair (75.73 MB read,
-# 3.76 MB written) + k3_reduce_store (18.97 MB read, cache rows stay in L2).
-NCU_TRAFFIC = {
-    (2, "store", "project_store"): 75.73e6 + 3.76e6 + 18.97e6,
-}
+NCU_TRAFFIC = {}
 
 
 def load_peaks():

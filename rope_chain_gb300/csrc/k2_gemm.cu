@@ -577,6 +577,10 @@ __device__ __forceinline__ void fused_store_tile(const FusedStore &fs, const Gem
     }
 }
 
+// Staging rows of one epilogue warp: 32 rows of 144 bytes (FP32) or 80
+// bytes (bf16), placed in the first pipeline stage.
+constexpr uint32_t kStageRowsBytes = 32u * 144u;
+
 struct PairCfg {
     static constexpr int kStages = 6;
     static constexpr uint32_t kBHalf = 128 * BK * 2;            // 16 KiB of B per CTA
@@ -584,6 +588,7 @@ struct PairCfg {
     static constexpr uint32_t kPairTx = 2 * kStageBytes;         // counted on the leader
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 512;
     static_assert((5 * kStages + 1) * 8 + 5 * 4 <= 512, "barriers and words fit the tail");
+    static_assert(4 * kStageRowsBytes <= (uint32_t)kStages * kABytes, "staging rows fit the A stages");
 };
 
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
@@ -836,33 +841,57 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             tc_fence_after();
             fused_store_tile(fs, g, tmem + ((uint32_t)(32 * q) << 16), l, m0 + 32 * q + lane, n0);
         } else if (ok) {
+            // Each thread holds one row's 32 accumulators per TMEM load; they
+            // pass through this warp's staging rows in shared memory (the
+            // pipeline stages are idle once the accumulator is complete) so
+            // that every global store instruction writes whole 128-byte (FP32)
+            // or 64-byte (bf16) row segments instead of 32 scattered pieces.
             tc_fence_after();
-            const int row = m0 + 32 * q + lane;
             const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16);
+            const uint32_t stage = sA + (uint32_t)q * kStageRowsBytes;
+            const int row0 = m0 + 32 * q;
 #pragma unroll 1
             for (int c = 0; c < 8; ++c) {
                 uint32_t r[32];
                 tmem_ld32(tbase + 32u * c, r);
-                if (row < g.T) {
-                    if (g.splits == 1) {
-                        uint4 *o = reinterpret_cast<uint4 *>(
-                            g.out + ((int64_t)l * g.T + row) * g.N + n0 + 32 * c);
+                if (g.splits == 1) {
+                    // bf16: 64 bytes per row, rows 80 bytes apart (conflict-free)
+                    const uint32_t w = stage + (uint32_t)lane * 80u;
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            o[j] = make_uint4(pack_acc(r[8 * j], r[8 * j + 1]),
-                                              pack_acc(r[8 * j + 2], r[8 * j + 3]),
-                                              pack_acc(r[8 * j + 4], r[8 * j + 5]),
-                                              pack_acc(r[8 * j + 6], r[8 * j + 7]));
-                    } else {
-                        float4 *o = reinterpret_cast<float4 *>(
-                            g.partial + (((int64_t)split * g.L + l) * g.T + row) * g.N + n0 + 32 * c);
+                    for (int j = 0; j < 4; ++j)
+                        st_shared_v4(w + 16u * j, make_uint4(pack_acc(r[8 * j], r[8 * j + 1]),
+                                                             pack_acc(r[8 * j + 2], r[8 * j + 3]),
+                                                             pack_acc(r[8 * j + 4], r[8 * j + 5]),
+                                                             pack_acc(r[8 * j + 6], r[8 * j + 7])));
+                    __syncwarp();
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            o[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                               __uint_as_float(r[4 * j + 2]),
-                                               __uint_as_float(r[4 * j + 3]));
+                    for (int i = 0; i < 4; ++i) {
+                        const int rr = (lane >> 2) + 8 * i, piece = lane & 3;
+                        const uint4 v = ld_shared_v4(stage + (uint32_t)rr * 80u + 16u * piece);
+                        const int row = row0 + rr;
+                        if (row < g.T)
+                            *reinterpret_cast<uint4 *>(g.out + ((int64_t)l * g.T + row) * g.N + n0 +
+                                                       32 * c + 8 * piece) = v;
+                    }
+                } else {
+                    // FP32 partials: 128 bytes per row, rows 144 bytes apart
+                    const uint32_t w = stage + (uint32_t)lane * 144u;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(w + 16u * j, make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2],
+                                                             r[4 * j + 3]));
+                    __syncwarp();
+                    float *base = g.partial + ((int64_t)split * g.L + l) * g.T * g.N + n0 + 32 * c;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int rr = (lane >> 3) + 4 * i, piece = lane & 7;
+                        const uint4 v = ld_shared_v4(stage + (uint32_t)rr * 144u + 16u * piece);
+                        const int row = row0 + rr;
+                        if (row < g.T)
+                            *reinterpret_cast<uint4 *>(base + (int64_t)row * g.N + 4 * piece) = v;
                     }
                 }
+                __syncwarp();                        // reads done before the next chunk's writes
             }
         }
     }
