@@ -19,10 +19,9 @@
 // raises a sticky fault bit, skips its remaining work, drains its own copies
 // and frees its TMEM.
 #include "rc_internal.cuh"
+#include "rc_tcgen05.cuh"
 
-#include <cuda.h>      // CUtensorMap and the tensor-map encoder's types
 #include <algorithm>
-#include <mutex>
 
 namespace rc {
 
@@ -34,19 +33,8 @@ constexpr int BM = 128;
 constexpr int BK = 64;                    // one 128-byte swizzle row of bf16
 constexpr int kThreads = 192;
 constexpr uint32_t kABytes = BM * BK * 2; // 16 KiB per stage
-constexpr unsigned long long kWaitNs = 1000000000ull;   // 1 s per wait
 
 enum : unsigned { kFaultLoad = 1u, kFaultMma = 2u, kFaultAccum = 4u, kFaultDrain = 8u };
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long globaltimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
 
 __device__ __forceinline__ bool faulted() {
     return *reinterpret_cast<volatile unsigned int *>(&g_project_faults) != 0u;
@@ -54,126 +42,10 @@ __device__ __forceinline__ bool faulted() {
 
 __device__ __forceinline__ void raise_fault(unsigned bit) { atomicOr(&g_project_faults, bit); }
 
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0u;
-}
-
-// Wait for the phase with `parity` to complete; false after kWaitNs or when
-// another CTA has already raised a fault.
+// Wait for the phase with `parity` to complete; false after the time limit
+// or when another CTA of any projection has already raised a fault.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    if (mbar_try(bar, parity))
-        return true;
-    const unsigned long long t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try(bar, parity))
-            return true;
-        if ((it & 255u) == 0u && (faulted() || globaltimer() - t0 > kWaitNs))
-            return false;
-    }
-}
-
-// Arrive on a barrier of this CTA.
-__device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-// Arrive on a barrier of any CTA of the cluster (a shared::cluster address).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
-                                            int c2, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 family layout:
-// start >> 4 in bits 0-13, leading byte offset >> 4 in 16-29, stride byte
-// offset >> 4 in 32-45, version 1 at bit 46, swizzle mode 2 in bits 61-63).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-// Instruction descriptor of kind::f16: FP32 accumulator, BF16 A and B,
-// A K-major, B K-major or MN-major, N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t make_idesc(int m, int n, bool b_mn) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn ? 1u : 0u) << 16) |
-           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                 ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Same as mbar_wait but ignores other CTAs' faults: used to drain this
-// CTA's own copies and MMAs before it frees its smem and TMEM.
-__device__ __forceinline__ bool mbar_wait_own(uint32_t bar, uint32_t parity) {
-    const unsigned long long t0 = globaltimer();
-    for (uint32_t it = 0;; ++it) {
-        if (mbar_try(bar, parity))
-            return true;
-        if ((it & 255u) == 255u && globaltimer() - t0 > kWaitNs)
-            return false;
-    }
+    return mbar_wait_flag(bar, parity, &g_project_faults);
 }
 
 struct GemmArgs {
@@ -591,20 +463,6 @@ struct PairCfg {
     static_assert(4 * kStageRowsBytes <= (uint32_t)kStages * kABytes, "staging rows fit the A stages");
 };
 
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4 &v) {
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-
 __device__ __forceinline__ void unpack8f(const uint4 &q, float *f) {
     f[0] = bf16_lo(q.x); f[1] = bf16_hi(q.x);
     f[2] = bf16_lo(q.y); f[3] = bf16_hi(q.y);
@@ -933,41 +791,6 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 }
 
 // ------------------------------------------------------------------ host
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
-// A rank-3 bf16 tensor map, innermost dimension first, 128-byte swizzle.
-bool make_map(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
-              uint32_t box0, uint32_t box1) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc)
-        return false;
-    const cuuint64_t dims[3] = {d0, d1, d2};
-    const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};   // bytes, dims 1 and 2
-    const cuuint32_t box[3] = {box0, box1, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 template <int BN, bool kBmn>
 cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &g,
