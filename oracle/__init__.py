@@ -76,6 +76,9 @@ def lib():
             "rco_context_norms_ex": ([_u16p, _c.c_int64, _c.c_int32, _c.POINTER(_Norm),
                                       _c.POINTER(_Norm), _c.c_int32, _u16p, _c.c_int32],
                                      _c.c_int32),
+            "rco_qkv_front_post": ([_u16p, _c.c_int32, _c.c_int32, _c.c_int32, _i64p, _u16p,
+                                    _c.c_int64, _i64p, _u16p, _c.c_int32, _c.c_int32, _c.c_float,
+                                    _u16p, _i32p], _c.c_int32),
             "rco_kv_project": ([_u16p, _u16p, _c.c_int32, _c.c_int32, _c.c_int64,
                                 _c.c_int32, _c.c_int32, _i64p, _c.c_int64, _f64p,
                                 _f64p, _c.c_int32], _c.c_int32),
@@ -270,3 +273,33 @@ def kv_store_from_projection(kv: np.ndarray, H: int, positions, slots, cos_sin,
     v_view = flat[64 * H:]          # a view: V starts 64*H elements into a row
     return kv_store(flat, v_view, T * N, N, T * N, N, positions, slots, cos_sin,
                     caches, H, eps, rows, threads)
+
+
+def qkv_front_post(raw: np.ndarray, num_heads: int, num_kv_heads: int,
+                   positions: Optional[np.ndarray], cos_sin: Optional[np.ndarray],
+                   slots: Optional[np.ndarray], cache: Optional[np.ndarray], eps: float):
+    """The decode QKV front after its projection (reading R8): returns
+    (out bf16 [M, Nqkv], skipped-row count); ``cache`` (bf16 [num_blocks,
+    num_kv_heads, block_size, 128]) is updated in place."""
+    M, N = raw.shape
+    assert N == 64 * (2 * num_heads + 2 * num_kv_heads)
+    out = np.empty_like(raw)
+    err = np.zeros(1, dtype=np.int32)
+    nb, bs = (cache.shape[0], cache.shape[2]) if cache is not None else (1, 1)
+    max_pos = cos_sin.shape[0] if cos_sin is not None else 0
+    rc = lib().rco_qkv_front_post(_p(np.ascontiguousarray(raw), _u16p), M, num_heads, num_kv_heads,
+                                  _p(positions, _i64p), _p(cos_sin, _u16p), max_pos,
+                                  _p(slots, _i64p), _p(cache, _u16p), nb, bs, eps,
+                                  _p(out, _u16p), _p(err, _i32p))
+    if rc != 0:
+        raise ValueError("oracle: unsupported qkv_front_post arguments")
+    return out, int(err[0])
+
+
+def qkv_project(hidden: np.ndarray, W: np.ndarray, threads: int = 0):
+    """float64 projection of the decode QKV front: hidden [M, D] x W^T with W
+    the nn.Linear weight [Nqkv, D]; returns (sum, sum of |products|)."""
+    M, D = hidden.shape
+    out, ab = kv_project(hidden.reshape(1, M, D), W.reshape(1, *W.shape), w_nd=True,
+                         threads=threads)
+    return out[0], ab[0]

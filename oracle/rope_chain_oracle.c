@@ -37,6 +37,17 @@
  *   R6  A gain center is added to the weight only when it is non-zero: the
  *       stock norm with center 0 multiplies by the weight itself, so a -0.0
  *       weight keeps its sign ([ctx] _ContextNormsKernel adds it always).
+ *   R8  The decode QKV front ([rt] _fused_qkv_projection, _attention,
+ *       may_fuse_qkv_front): its output row is [Q | K | V | O-gate] with
+ *       q_size = 64 * num_heads and kv_size = 64 * num_kv_heads (the split
+ *       _attention makes); the QK-norm of every Q and K head is the same
+ *       weightless 64-wide RMSNorm as the context K-norm (same order, same
+ *       eps), then GPT-J RoPE on Q and K; K and V go into the cache as the
+ *       context store inserts them; V and the gate pass through.  A row whose
+ *       slot is past the cache or whose position is outside the table is
+ *       counted in *err and inserts nothing; its Q and K are normed but not
+ *       rotated when the position is out of range.  A negative slot inserts
+ *       nothing and is not an error.
  *   R7  An input-scale weight multiplies the input before the sum of
  *       squares and nothing after it, in the order of [bnd]
  *       boundary_fragments; the hidden norm's output is still rounded to
@@ -492,5 +503,84 @@ int32_t rco_kv_store(const uint16_t *k, const uint16_t *v,
     }
     if (err)
         *err += (int32_t)skipped;
+    return 0;
+}
+
+/* ---------------------------------------------------------- decode front */
+
+/* The QKV front after its projection (R8; [rt] _fused_qkv_projection and
+   _attention): raw is the bf16 projection [M, Nqkv] of M decode tokens,
+   Nqkv = 64 * (2 * num_heads + 2 * num_kv_heads), columns [Q | K | V | gate].
+     out[m, Q and K heads] = RoPE(bf16(head * r)), r the head's weightless
+                             inverse RMS (rco_head_sumsq order, eps), RoPE at
+                             positions[m] from cos_sin when it is not NULL;
+     out[m, V and gate]    = raw[m, V and gate];
+     cache[s / bs, h, s % bs, 0:64]   = out[m, K head h],
+     cache[s / bs, h, s % bs, 64:128] = raw[m, V head h]   for s = slots[m] >= 0;
+   a row whose slot is >= num_blocks * block_size or (with a table) whose
+   position is outside [0, max_position) adds one to *err and inserts
+   nothing (R8).  slots may be NULL (nothing inserted).
+   cache is bf16 [num_blocks, num_kv_heads, block_size, 128].  Returns 0, or 1
+   for unsupported arguments. */
+int32_t rco_qkv_front_post(const uint16_t *raw, int32_t M, int32_t num_heads, int32_t num_kv_heads,
+                           const int64_t *positions, const uint16_t *cos_sin, int64_t max_position,
+                           const int64_t *slots, uint16_t *cache, int32_t num_blocks,
+                           int32_t block_size, float eps, uint16_t *out, int32_t *err)
+{
+    if (!raw || !out || M < 0 || num_heads < 1 || num_kv_heads < 1 || num_blocks < 1 ||
+        block_size < 1 || (cos_sin && !positions) || (slots && !cache))
+        return 1;
+    const int32_t q_size = RCO_HEAD * num_heads, kv_size = RCO_HEAD * num_kv_heads;
+    const int32_t N = 2 * q_size + 2 * kv_size;
+    const int64_t capacity = (int64_t)num_blocks * block_size;
+    const float inv_hd = 1.0f / 64.0f;
+    for (int32_t m = 0; m < M; ++m) {
+        const uint16_t *rr = raw + (int64_t)m * N;
+        uint16_t *o = out + (int64_t)m * N;
+        int64_t pos = 0;
+        int bad_pos = 0;
+        if (cos_sin) {
+            pos = positions[m];
+            bad_pos = pos < 0 || pos >= max_position;
+        }
+        const int rotate = cos_sin != NULL && !bad_pos;
+        const int64_t s = slots ? slots[m] : -1;
+        const int bad_slot = s >= capacity;
+        if ((bad_pos || bad_slot) && err)
+            *err += 1;
+        const int insert = s >= 0 && !bad_slot && !bad_pos;
+        /* Q and K heads: QK-norm, then RoPE */
+        for (int32_t h = 0; h < num_heads + num_kv_heads; ++h) {
+            const int32_t c0 = h * RCO_HEAD;
+            float kf[RCO_HEAD];
+            for (int e = 0; e < RCO_HEAD; ++e)
+                kf[e] = rco_f32(rr[c0 + e]);
+            float r = rco_inv_rms(rco_head_sumsq(kf), inv_hd, eps);
+            for (int j = 0; j < RCO_HEAD / 2; ++j) {
+                float n0 = rco_f32(rco_bf16_rn(kf[2 * j] * r));
+                float n1 = rco_f32(rco_bf16_rn(kf[2 * j + 1] * r));
+                if (rotate) {
+                    float c = rco_f32(cos_sin[pos * RCO_HEAD + j]);
+                    float sn = rco_f32(cos_sin[pos * RCO_HEAD + RCO_HEAD / 2 + j]);
+                    float xo, yo;
+                    rco_rope(n0, n1, c, sn, &xo, &yo);
+                    n0 = xo;
+                    n1 = yo;
+                }
+                o[c0 + 2 * j] = rco_bf16_rn(n0);
+                o[c0 + 2 * j + 1] = rco_bf16_rn(n1);
+            }
+        }
+        /* V and the gate pass through */
+        memcpy(o + q_size + kv_size, rr + q_size + kv_size, (size_t)(kv_size + q_size) * sizeof(uint16_t));
+        if (insert) {
+            const int64_t blk = s / block_size, page = s % block_size;
+            for (int32_t h = 0; h < num_kv_heads; ++h) {
+                uint16_t *dst = cache + ((blk * num_kv_heads + h) * block_size + page) * (2 * RCO_HEAD);
+                memcpy(dst, o + q_size + h * RCO_HEAD, RCO_HEAD * sizeof(uint16_t));
+                memcpy(dst + RCO_HEAD, rr + q_size + kv_size + h * RCO_HEAD, RCO_HEAD * sizeof(uint16_t));
+            }
+        }
+    }
     return 0;
 }
