@@ -375,12 +375,54 @@ rc_status rc_kv_project_no_alloc(const uint16_t *normed, const uint16_t *W,
                                  int64_t T, int32_t D, int32_t N,
                                  cudaStream_t stream);
 
-/* Sticky fault bits raised on the device by the projection kernel when one
-   of its bounded waits gives up (bit 0: load pipeline, bit 1: tensor-core
-   pipeline, bit 2: accumulator, bit 3: drain).  A kernel that sees a raised
-   bit skips its work, so after a fault every projection is wrong until the
-   bits are cleared.  Reads (and with clear != 0 resets) the bits of the
-   current device; synchronises the device.  No page counterpart. */
+/*
+ * rc_qkv_front -- the decode QKV front of one draft layer on 1 to 16 tokens:
+ * QKV projection, QK-norm, GPT-J RoPE and KV insert in one kernel ([rt]
+ * _fused_qkv_projection, _attention, may_fuse_qkv_front; the pages' kernel
+ * source is not among them, so its arithmetic is read from what they state).
+ *
+ *   proj[m, n] = bf16(sum_k hidden[m, k] * W[n, k])   FP32 accumulation
+ * Each output row is [Q | K | V | O-gate]: q_size = 64*num_heads columns of
+ * Q, kv_size = 64*num_kv_heads of K, kv_size of V, q_size of the gate
+ * (_attention's split).  Then, per token m:
+ *   out[m, Q and K heads] = per 64-wide head: bf16(head * r) with r the
+ *       weightless inverse RMS 1/sqrt(fma(sum e^2, 1/64, eps)) (the context
+ *       K-norm's lane-pair order), then GPT-J RoPE at positions[m] from
+ *       cos_sin (cos_sin may be NULL: no rotation), rounded to bf16;
+ *   out[m, V and gate]    = proj;
+ *   cache[s/bs, h, s%bs, 0:64] = out[m, K head h] and [64:128] = V head h,
+ *       for s = slots[m] >= 0.
+ * A token whose slot is >= num_blocks*block_size, or (with a table) whose
+ * position is outside [0, max_position), adds one to *err and inserts
+ * nothing; with a bad position its Q and K are normed but not rotated.
+ *
+ *   hidden      bf16 [M, D] contiguous, 16-byte aligned
+ *   M           tokens, 0 <= M <= 16 (0: nothing launched); else RC_ERR_UNSUPPORTED
+ *   D           a positive multiple of 64
+ *   W           bf16 [Nqkv, D] (the nn.Linear weight), Nqkv = 64*(2*num_heads +
+ *               2*num_kv_heads), 16-byte aligned
+ *   positions   int64 [M] (read with a table), 8-byte aligned
+ *   slots       int64 [M] slot mapping, or NULL (nothing inserted)
+ *   cache       bf16 [num_blocks, num_kv_heads, block_size, 128], 4-byte
+ *               aligned; num_blocks*block_size < 2^31
+ *   out         bf16 [M, Nqkv], 16-byte aligned, overlapping no input
+ *   raw_out     optional bf16 [M, Nqkv]: also write the projection itself
+ *   err         optional device int32 counter
+ * Bit 8 and up of rc_read_device_faults are this kernel's fault bits.
+ */
+rc_status rc_qkv_front(const uint16_t *hidden, int32_t M, int32_t D, const uint16_t *W,
+                       int32_t num_heads, int32_t num_kv_heads, const int64_t *positions,
+                       const uint16_t *cos_sin, int64_t max_position, const int64_t *slots,
+                       uint16_t *cache, int32_t num_blocks, int32_t block_size, float eps,
+                       uint16_t *out, uint16_t *raw_out, int32_t *err, cudaStream_t stream);
+
+/* Sticky fault bits raised on the device when a bounded wait gives up: bits
+   0-3 by the projection kernels, bits 8-11 by the QKV front (per kernel:
+   load pipeline, tensor-core pipeline, accumulator, drain).  A kernel that
+   sees a raised bit of its own kind skips its work, so after a fault its
+   outputs are wrong until the bits are cleared.  Reads (and with clear != 0
+   resets) the bits of the current device; synchronises the device.  No
+   page counterpart. */
 rc_status rc_read_device_faults(uint32_t *flags, int32_t clear);
 
 #ifdef __cplusplus

@@ -84,6 +84,9 @@ class NormParams(ctypes.Structure):
 
 
 RC_NORM_NONE, RC_NORM_BF16, RC_NORM_F32 = 0, 1, 2
+SIGNATURES["rc_qkv_front"] = ([_vp, _c.c_int32, _c.c_int32, _vp, _c.c_int32, _c.c_int32, _vp, _vp,
+                               _c.c_int64, _vp, _vp, _c.c_int32, _c.c_int32, _c.c_float, _vp, _vp,
+                               _vp, _vp], _c.c_int)
 SIGNATURES["rc_context_norms_ex"] = ([_vp, _c.c_int64, _c.c_int32, _c.POINTER(NormParams),
                                       _c.POINTER(NormParams), _c.c_int32, _vp, _vp], _c.c_int)
 
@@ -470,6 +473,46 @@ def context_kv_chain(x, hidden_w, pre_w, W, positions, slots, cos_sin, caches, e
     kv = kv_project(normed, W, out=kv, workspace=workspace, stream=stream)
     kv_store_from_projection(kv, H, positions, slots, cos_sin, caches, eps, err=err, stream=stream)
     return normed, kv
+
+
+def qkv_front(hidden: torch.Tensor, W: torch.Tensor, num_heads: int, num_kv_heads: int,
+              positions: Optional[torch.Tensor], cos_sin: Optional[torch.Tensor],
+              slots: Optional[torch.Tensor], cache: Optional[torch.Tensor], eps: float,
+              out: Optional[torch.Tensor] = None, raw_out: Optional[torch.Tensor] = None,
+              err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The decode QKV front of one layer (rc_qkv_front): hidden bf16 [M, D]
+    (M <= 16), W bf16 [Nqkv, D]; returns out bf16 [M, Nqkv] = [Q | K | V |
+    gate] with Q and K normed and rotated, and inserts K and V into ``cache``
+    (bf16 [num_blocks, num_kv_heads, block_size, 128]) at ``slots``."""
+    _bf16(hidden, "hidden")
+    _bf16(W, "W")
+    M, D = hidden.shape
+    N = HEAD_DIM * (2 * num_heads + 2 * num_kv_heads)
+    if tuple(W.shape) != (N, D):
+        raise ValueError(f"W must be [{N}, {D}] for these head counts")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=hidden.device)
+    _bf16(out, "out")
+    if raw_out is not None:
+        _bf16(raw_out, "raw_out")
+    nb = bs = 0
+    if slots is not None:
+        if slots.dtype != torch.int64 or not slots.is_contiguous() or slots.shape[0] < M:
+            raise ValueError("slots must be contiguous int64 [M]")
+        _bf16(cache, "cache")
+        nb, h_, bs, w_ = cache.shape
+        if h_ != num_kv_heads or w_ != 2 * HEAD_DIM:
+            raise ValueError("cache must be [num_blocks, num_kv_heads, block_size, 128]")
+    if cos_sin is not None:
+        _bf16(cos_sin, "cos_sin")
+        if positions is None or positions.dtype != torch.int64 or not positions.is_contiguous():
+            raise ValueError("RoPE needs contiguous int64 positions")
+    _check(lib().rc_qkv_front(hidden.data_ptr(), M, D, W.data_ptr(), num_heads, num_kv_heads,
+                              _ptr(positions), _ptr(cos_sin),
+                              0 if cos_sin is None else cos_sin.shape[0], _ptr(slots),
+                              _ptr(cache) if slots is not None else None, nb, bs, eps,
+                              out.data_ptr(), _ptr(raw_out), _ptr(err), _stream(stream)))
+    return out
 
 
 def read_device_faults(clear: bool = True) -> int:

@@ -16,7 +16,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "librope_chain.so")
-SOURCES = ["rc_api.cu", "k1_norms.cu", "k2_gemm.cu", "k3_store.cu", "rc_project_static.cu"]
+SOURCES = ["rc_api.cu", "k1_norms.cu", "k2_gemm.cu", "k3_store.cu", "k4_qkv_front.cu",
+           "rc_project_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # --fmad=false: no multiply-add is fused unless the source asks for it.
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "--fmad=false", "-Xcompiler", "-fPIC",

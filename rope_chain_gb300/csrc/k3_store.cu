@@ -23,26 +23,6 @@ __device__ __forceinline__ void count_skip(int32_t *err, int lane) {
         atomicAdd(err, 1);
 }
 
-// The key pair (k0, k1) = elements (2 lane, 2 lane + 1) of one head, for a
-// whole warp: weightless K-norm (sum folded as even and odd squares by xor
-// butterflies, then even + odd), the bf16 key, GPT-J RoPE with (c, s), and
-// the packed bf16 result.
-template <bool kRope>
-__device__ __forceinline__ uint32_t knorm_rope_lane(float k0, float k1, float c, float s, float eps) {
-    const float even = warp_butterfly_sum(__fmul_rn(k0, k0));
-    const float odd = warp_butterfly_sum(__fmul_rn(k1, k1));
-    const float r = inv_rms(__fadd_rn(even, odd), 0x1p-6f, eps);
-    float n0 = round_bf16(__fmul_rn(k0, r));
-    float n1 = round_bf16(__fmul_rn(k1, r));
-    if (kRope) {
-        const float x = __fmaf_rn(n0, c, -__fmul_rn(n1, s));
-        const float y = __fmaf_rn(n1, c, __fmul_rn(n0, s));
-        n0 = x;
-        n1 = y;
-    }
-    return pack_bf16x2(n0, n1);
-}
-
 // Writes one row's H heads of K' and V into its cache slot (lane = pair).
 template <int H>
 __device__ __forceinline__ void insert_row(uint16_t *cache, int64_t slot, int32_t block_size,

@@ -640,9 +640,68 @@ rc_status rc_read_device_faults(uint32_t *flags, int32_t clear)
 {
     if (!flags)
         return fail(RC_ERR_INVALID_ARG, "rc_read_device_faults: flags must not be NULL");
-    const cudaError_t e = rc::read_project_faults(flags, clear != 0);
+    uint32_t project = 0, front = 0;
+    cudaError_t e = rc::read_project_faults(&project, clear != 0);
+    if (e == cudaSuccess)
+        e = rc::read_front_faults(&front, clear != 0);
     if (e != cudaSuccess)
         return cuda_fail(e, "rc_read_device_faults");
+    *flags = project | (front << 8);
+    return ok();
+}
+
+rc_status rc_qkv_front(const uint16_t *hidden, int32_t M, int32_t D, const uint16_t *W,
+                       int32_t num_heads, int32_t num_kv_heads, const int64_t *positions,
+                       const uint16_t *cos_sin, int64_t max_position, const int64_t *slots,
+                       uint16_t *cache, int32_t num_blocks, int32_t block_size, float eps,
+                       uint16_t *out, uint16_t *raw_out, int32_t *err, cudaStream_t stream)
+{
+    const char *fn = "rc_qkv_front";
+    if (M < 0 || M > 16)
+        return fail(RC_ERR_UNSUPPORTED, "%s: M=%d outside [0, 16] (the decode front takes 1 to 16 "
+                    "tokens)", fn, M);
+    if (D < 64 || D % 64 != 0)
+        return fail(RC_ERR_UNSUPPORTED, "%s: D=%d is not a positive multiple of 64", fn, D);
+    if (num_heads < 1 || num_kv_heads < 1 || num_heads > 4096 || num_kv_heads > 4096)
+        return fail(RC_ERR_INVALID_ARG, "%s: num_heads=%d, num_kv_heads=%d outside [1, 4096]", fn,
+                    num_heads, num_kv_heads);
+    if (!hidden || !W || !out)
+        return fail(RC_ERR_INVALID_ARG, "%s: hidden, W and out must not be NULL", fn);
+    if (!aligned(hidden, 16) || !aligned(W, 16) || !aligned(out, 16) || (raw_out && !aligned(raw_out, 16)))
+        return fail(RC_ERR_INVALID_ARG, "%s: hidden, W, out and raw_out must be 16-byte aligned", fn);
+    if (cos_sin) {
+        if (!positions || !aligned(positions, 8))
+            return fail(RC_ERR_INVALID_ARG, "%s: RoPE needs 8-byte aligned positions", fn);
+        if (max_position < 1)
+            return fail(RC_ERR_INVALID_ARG, "%s: max_position must be >= 1 with a table", fn);
+        if (!aligned(cos_sin, 2))
+            return fail(RC_ERR_INVALID_ARG, "%s: cos_sin must be 2-byte aligned", fn);
+    }
+    if (slots) {
+        if (!aligned(slots, 8) || !cache || !aligned(cache, 4))
+            return fail(RC_ERR_INVALID_ARG, "%s: slots need 8-byte alignment and a 4-byte aligned "
+                        "cache", fn);
+        if (num_blocks < 1 || block_size < 1 || (int64_t)num_blocks * block_size >= (1LL << 31))
+            return fail(RC_ERR_INVALID_ARG,
+                        "%s: need num_blocks, block_size >= 1 and num_blocks*block_size < 2^31", fn);
+    }
+    const int64_t N = 64LL * (2 * num_heads + 2 * num_kv_heads);
+    if (overlap(out, (size_t)M * N * 2, W, (size_t)N * D * 2) ||
+        overlap(out, (size_t)M * N * 2, hidden, (size_t)M * D * 2) ||
+        (raw_out && overlap(raw_out, (size_t)M * N * 2, out, (size_t)M * N * 2)))
+        return fail(RC_ERR_INVALID_ARG, "%s: out (or raw_out) overlaps an input or the other output", fn);
+    if (M == 0)
+        return ok();
+    const int sms = num_sms_current();
+    if (sms <= 0)
+        return fail(RC_ERR_CUDA, "%s: no current CUDA device", fn);
+    const char *why = "launch";
+    const cudaError_t e = rc::launch_qkv_front(hidden, M, D, W, num_heads, num_kv_heads, positions,
+                                               cos_sin, max_position, slots, cache,
+                                               slots ? num_blocks : 1, slots ? block_size : 1, eps,
+                                               out, raw_out, err, sms, stream, &why);
+    if (e != cudaSuccess)
+        return cuda_fail(e, why);
     return ok();
 }
 

@@ -44,6 +44,26 @@ __device__ __forceinline__ float warp_butterfly_sum(float v) {
     return v;
 }
 
+// The key pair (k0, k1) = elements (2 lane, 2 lane + 1) of one head, for a
+// whole warp: weightless K-norm (sum folded as even and odd squares by xor
+// butterflies, then even + odd), the bf16 key, GPT-J RoPE with (c, s), and
+// the packed bf16 result.
+template <bool kRope>
+__device__ __forceinline__ uint32_t knorm_rope_lane(float k0, float k1, float c, float s, float eps) {
+    const float even = warp_butterfly_sum(__fmul_rn(k0, k0));
+    const float odd = warp_butterfly_sum(__fmul_rn(k1, k1));
+    const float r = inv_rms(__fadd_rn(even, odd), 0x1p-6f, eps);
+    float n0 = round_bf16(__fmul_rn(k0, r));
+    float n1 = round_bf16(__fmul_rn(k1, r));
+    if (kRope) {
+        const float x = __fmaf_rn(n0, c, -__fmul_rn(n1, s));
+        const float y = __fmaf_rn(n1, c, __fmul_rn(n0, s));
+        n0 = x;
+        n1 = y;
+    }
+    return pack_bf16x2(n0, n1);
+}
+
 // ------------------------------------------------- programmatic launches
 //
 // Every kernel of the library is launched with programmatic stream
@@ -195,5 +215,16 @@ cudaError_t launch_kv_from_rows(const uint16_t *z, const float *r2, int64_t T,
 
 // Sticky device fault bits of the projection kernel (current device).
 cudaError_t read_project_faults(uint32_t *flags, bool clear);
+
+// The decode QKV front (1 to 16 tokens): projection, QK-norm, RoPE, insert.
+cudaError_t launch_qkv_front(const uint16_t *hidden, int32_t M, int32_t D, const uint16_t *W,
+                             int32_t num_heads, int32_t num_kv_heads, const int64_t *positions,
+                             const uint16_t *cos_sin, int64_t max_position, const int64_t *slots,
+                             uint16_t *cache, int32_t num_blocks, int32_t block_size, float eps,
+                             uint16_t *out, uint16_t *raw, int32_t *err, int num_sms,
+                             cudaStream_t stream, const char **why);
+
+// Sticky device fault bits of the QKV front kernel (current device).
+cudaError_t read_front_faults(uint32_t *flags, bool clear);
 
 }  // namespace rc

@@ -180,3 +180,22 @@ def test_project_store_rows_rejections(lib):
     assert "outside [0, T]" in last(lib)
     assert call([-1, 0]) == rc.RC_ERR_INVALID_ARG
     assert call([0, 0], T=0) == rc.RC_OK
+
+
+def test_qkv_front_rejections(lib):
+    h, w, o = 0x10000, 0x1000000, 0x8000000
+    call = lambda M=4, D=8192, nh=4, nkv=2, hidden=A(h), W=A(w), out=A(o), raw=None, slots=None, \
+        cache=None, cos=None, pos=None, maxpos=0, nb=0, bs=0: lib.rc_qkv_front(
+        hidden, M, D, W, nh, nkv, pos, cos, maxpos, slots, cache, nb, bs, 1e-6, out, raw, None, None)
+    assert call(M=17) == rc.RC_ERR_UNSUPPORTED
+    assert "16" in last(lib)
+    assert call(D=100) == rc.RC_ERR_UNSUPPORTED
+    assert call(nh=0) == rc.RC_ERR_INVALID_ARG
+    assert call(hidden=None) == rc.RC_ERR_INVALID_ARG
+    assert call(out=A(o + 8)) == rc.RC_ERR_INVALID_ARG
+    assert call(cos=A(0x4000), maxpos=8) == rc.RC_ERR_INVALID_ARG          # no positions
+    assert call(slots=A(0x5000)) == rc.RC_ERR_INVALID_ARG                  # no cache
+    assert call(slots=A(0x5000), cache=A(0x6000), nb=1 << 20, bs=1 << 11) == rc.RC_ERR_INVALID_ARG
+    assert call(out=A(w + 64)) == rc.RC_ERR_INVALID_ARG                    # out overlaps W
+    assert "overlaps" in last(lib)
+    assert call(M=0) == rc.RC_OK
