@@ -335,23 +335,6 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
 // and odd squares separately, then even + odd), so the stored key is the
 // same bits the unfused store would write.
 
-__device__ __forceinline__ float fold32(const float (&q)[32]) {
-    float a[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-        a[j] = __fadd_rn(q[j], q[j + 16]);
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        a[j] = __fadd_rn(a[j], a[j + 8]);
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-        a[j] = __fadd_rn(a[j], a[j + 4]);
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-        a[j] = __fadd_rn(a[j], a[j + 2]);
-    return __fadd_rn(a[0], a[1]);
-}
-
 // The tile's store for one row (all 32 lanes call it: TMEM loads are
 // warp-collective).  tbase: this warp's TMEM lanes, column 0 of the tile.
 __device__ __forceinline__ void fused_store_tile(const FusedStore &fs, const GemmArgs &g,

@@ -90,6 +90,130 @@ k3_kv_store(const __grid_constant__ StoreLaunch p)
     insert_row<H>(p.caches[layer], slot, p.block_size, ko, vw, lane);
 }
 
+// The same store with one thread per key head.  A warp takes the 32 (row,
+// head) keys of 32 / H consecutive rows of one layer: it copies their K and
+// V into shared memory with coalesced 16-byte asynchronous copies (all in
+// flight at once, no registers held), each lane then reads one whole key
+// head (64 bf16), folds its sum of squares in registers in the butterfly's
+// order (knorm_rope_head: the same bits as the lane version, without
+// shuffles, and the square root and divide done once per head instead of
+// once per lane), and K' and V leave for the cache with 16-byte stores, 8
+// lanes per 128-byte half row.  Needs k, v and the caches 16-byte aligned
+// and row / layer strides in multiples of 8 elements.
+//
+// Shared memory per warp: K and V of 32 heads, 8 chunks of 16 bytes each
+// (logical chunk c of head e sits at chunk c ^ (e % 8), so the row-wise fill
+// and the head-wise read are both free of bank conflicts), and with RoPE the
+// 128-byte table rows of the warp's rows.
+constexpr int kHeadsWarps = 4;
+
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *src, bool valid) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                 ::"r"(d), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+
+template <int H, bool kRope>
+__global__ void __launch_bounds__(kHeadsWarps * 32)
+k3_kv_store_heads(const __grid_constant__ StoreLaunch p)
+{
+    constexpr int R = 32 / H;                     // rows per warp
+    __shared__ uint4 ktile[kHeadsWarps][32][8];
+    __shared__ uint4 vtile[kHeadsWarps][32][8];
+    __shared__ uint4 cstile[kHeadsWarps][kRope ? R : 1][8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int layer = blockIdx.y;
+    const int64_t row0 = ((int64_t)blockIdx.x * kHeadsWarps + warp) * R;
+    pdl_trigger();
+    pdl_wait();
+    const int64_t nrows = p.rows[layer];
+    const int64_t *slots = p.slots[layer];
+    if (slots == nullptr || row0 >= nrows)
+        return;
+    // chunk i of this lane: key e = 4 i + lane / 8 (row e / H, head e % H),
+    // 16-byte piece lane % 8 of its 64 elements; rows past the layer's count
+    // are zero-filled without a read
+    const int piece = lane & 7;
+    const uint16_t *kl = p.k + (int64_t)layer * p.k_layer_stride;
+    const uint16_t *vl = p.v + (int64_t)layer * p.v_layer_stride;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = 4 * i + (lane >> 3);
+        const int64_t row = row0 + e / H;
+        const bool live = row < nrows;
+        const int64_t r = live ? row : row0;
+        const int h = e % H;
+        cp_async16(&ktile[warp][e][piece ^ (e & 7)], kl + r * p.k_row_stride + h * kHeadDim + 8 * piece, live);
+        cp_async16(&vtile[warp][e][piece ^ (e & 7)], vl + r * p.v_row_stride + h * kHeadDim + 8 * piece, live);
+    }
+    // this lane's key: row row0 + lane / H, head lane % H
+    const int64_t my_row = row0 + lane / H;
+    int64_t slot = -1, pos = 0;
+    if (my_row < nrows) {
+        slot = __ldg(slots + my_row);
+        if (kRope)
+            pos = __ldg(p.positions + my_row);
+    }
+    bool ok = slot >= 0;
+    if (ok && (slot >= p.capacity || (kRope && (pos < 0 || pos >= p.max_position)))) {
+        if (lane % H == 0)                        // counted once per (row, layer)
+            count_skip(p.err, 0);
+        ok = false;
+    }
+    if (kRope) {
+        // table row of warp row r: logical chunk c in cstile[r][c ^ (r % 8)];
+        // the lane of head 0 of each row hands its position to the copiers
+        const int64_t tpos = ok ? pos : 0;
+#pragma unroll
+        for (int i = 0; i < (R * 8 + 31) / 32; ++i) {
+            const int c = 32 * i + lane;
+            const int r = c >> 3;
+            const int64_t rp = __shfl_sync(0xFFFFFFFFu, tpos, (r * H) & 31);
+            if (c < R * 8)
+                cp_async16(&cstile[warp][r][(c ^ r) & 7], p.cos_sin + rp * kHeadDim + 8 * (c & 7), true);
+        }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    int64_t dst = -1;                             // the key's cache row (element offset)
+    if (ok) {
+        // Slots of a cache fit 32 bits (checked on the host).
+        const uint32_t bs = (uint32_t)p.block_size;
+        const uint32_t blk = (uint32_t)slot / bs;
+        const uint32_t page = (uint32_t)slot - blk * bs;
+        dst = (((int64_t)blk * H + lane % H) * bs + page) * (2 * kHeadDim);
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncwarp();
+    uint16_t *cache = p.caches[layer];
+    // V (a bit copy) leaves first
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = 4 * i + (lane >> 3);
+        const int64_t d = __shfl_sync(0xFFFFFFFFu, dst, e);
+        if (d >= 0)
+            reinterpret_cast<uint4 *>(cache + d + kHeadDim)[piece] = vtile[warp][e][piece ^ (e & 7)];
+    }
+    __syncwarp();                                 // keeps V's registers apart from the head's
+    uint32_t w[32];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint4 q = ktile[warp][lane][j ^ (lane & 7)];
+        w[4 * j] = q.x; w[4 * j + 1] = q.y; w[4 * j + 2] = q.z; w[4 * j + 3] = q.w;
+    }
+    knorm_rope_head<kRope>(w, cstile[warp][kRope ? lane / H : 0], (lane / H) & 7, p.eps);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        ktile[warp][lane][j ^ (lane & 7)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = 4 * i + (lane >> 3);
+        const int64_t d = __shfl_sync(0xFFFFFFFFu, dst, e);
+        if (d >= 0)
+            reinterpret_cast<uint4 *>(cache + d)[piece] = ktile[warp][e][piece ^ (e & 7)];
+    }
+}
+
 // Split-K projection finished and stored in one pass: the FP32 partials
 // [splits, L, T, 128 H] are added in split order and rounded to bf16 (the
 // same additions as the projection's reduce kernel), optionally written to
@@ -97,7 +221,7 @@ k3_kv_store(const __grid_constant__ StoreLaunch p)
 // K-norm needs only its head, and many splits (small T) still leave enough
 // warps; the split loop is unrolled so 8 partials are in flight per lane.
 template <bool kRope>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, 6)
 k3_reduce_store(const __grid_constant__ FusedStore fs, const float *__restrict__ partial,
                 int32_t splits, int32_t L, int32_t T)
 {
@@ -124,29 +248,37 @@ k3_reduce_store(const __grid_constant__ FusedStore fs, const float *__restrict__
     const float *pv = pk + H * kHeadDim;
     float2 ka = __ldcs(reinterpret_cast<const float2 *>(pk));
     float2 va = __ldcs(reinterpret_cast<const float2 *>(pv));
-    int sp = 1;
-    for (; sp + 8 <= splits; sp += 8) {
-        float2 a[8], b[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            a[u] = __ldcs(reinterpret_cast<const float2 *>(pk + (sp + u) * plane));
-            b[u] = __ldcs(reinterpret_cast<const float2 *>(pv + (sp + u) * plane));
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            ka.x = __fadd_rn(ka.x, a[u].x);
-            ka.y = __fadd_rn(ka.y, a[u].y);
-            va.x = __fadd_rn(va.x, b[u].x);
-            va.y = __fadd_rn(va.y, b[u].y);
-        }
+    // the table row is fetched while the partials are in flight (row 0 for
+    // rows that are not stored)
+    float c = 1.0f, s = 0.0f;
+    const bool in_range = store && slot >= 0 && slot < fs.capacity &&
+                          (!kRope || (pos >= 0 && pos < fs.max_position));
+    if (kRope) {
+        const unsigned short *cs = reinterpret_cast<const unsigned short *>(fs.cos_sin) +
+                                   (in_range ? pos : 0) * kHeadDim;
+        c = __uint_as_float((uint32_t)__ldg(cs + lane) << 16);
+        s = __uint_as_float((uint32_t)__ldg(cs + kHeadDim / 2 + lane) << 16);
     }
-    for (; sp < splits; ++sp) {
-        const float2 a = __ldcs(reinterpret_cast<const float2 *>(pk + sp * plane));
-        const float2 b = __ldcs(reinterpret_cast<const float2 *>(pv + sp * plane));
-        ka.x = __fadd_rn(ka.x, a.x);
-        ka.y = __fadd_rn(ka.y, a.y);
-        va.x = __fadd_rn(va.x, b.x);
-        va.y = __fadd_rn(va.y, b.y);
+    // Splits 1 .. splits-1 in batches of 4 whose loads are all issued before
+    // the first add; the adds stay in split order.
+    for (int sp = 1; sp < splits; sp += 4) {
+        float2 a[4], b[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (sp + u < splits) {
+                a[u] = __ldcs(reinterpret_cast<const float2 *>(pk + (sp + u) * plane));
+                b[u] = __ldcs(reinterpret_cast<const float2 *>(pv + (sp + u) * plane));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (sp + u < splits) {
+                ka.x = __fadd_rn(ka.x, a[u].x);
+                ka.y = __fadd_rn(ka.y, a[u].y);
+                va.x = __fadd_rn(va.x, b[u].x);
+                va.y = __fadd_rn(va.y, b[u].y);
+            }
+        }
     }
     const uint32_t kw = pack_bf16x2(ka.x, ka.y), vw = pack_bf16x2(va.x, va.y);
     if (fs.kv_out != nullptr) {
@@ -156,16 +288,10 @@ k3_reduce_store(const __grid_constant__ FusedStore fs, const float *__restrict__
     }
     if (!store || slot < 0)
         return;
-    if (slot >= fs.capacity || (kRope && (pos < 0 || pos >= fs.max_position))) {
+    if (!in_range) {
         if (h == 0)                               // once per (row, layer)
             count_skip(fs.err, lane);
         return;
-    }
-    float c = 1.0f, s = 0.0f;
-    if (kRope) {
-        const unsigned short *cs = reinterpret_cast<const unsigned short *>(fs.cos_sin) + pos * kHeadDim;
-        c = __uint_as_float((uint32_t)__ldg(cs + lane) << 16);
-        s = __uint_as_float((uint32_t)__ldg(cs + kHeadDim / 2 + lane) << 16);
     }
     const uint32_t ko = knorm_rope_lane<kRope>(bf16_lo(kw), bf16_hi(kw), c, s, fs.eps);
     // Slots of a cache fit 32 bits (checked on the host).
@@ -178,12 +304,33 @@ k3_reduce_store(const __grid_constant__ FusedStore fs, const float *__restrict__
     dst[kHeadDim / 2] = vw;                       // V follows K
 }
 
+// 16-byte access to K, V, the table and every cache of the chunk.
+bool vector_ok(const StoreLaunch &p, int32_t layers) {
+    const auto a16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+    if (!a16(p.k) || !a16(p.v) || (p.cos_sin && !a16(p.cos_sin)))
+        return false;
+    if ((p.k_layer_stride | p.k_row_stride | p.v_layer_stride | p.v_row_stride) & 7)
+        return false;
+    for (int32_t i = 0; i < layers; ++i)
+        if (p.slots[i] && !a16(p.caches[i]))
+            return false;
+    return true;
+}
+
 template <int H>
 cudaError_t launch_h(const StoreLaunch &p, int32_t layers, cudaStream_t stream) {
+    const dim3 block(kWarps * 32);
+    if (vector_ok(p, layers)) {
+        constexpr int rows_per_cta = kHeadsWarps * (32 / H);
+        const dim3 grid((unsigned)((p.grid_rows + rows_per_cta - 1) / rows_per_cta), (unsigned)layers);
+        if (p.cos_sin)
+            return launch_pdl(k3_kv_store_heads<H, true>, grid, dim3(kHeadsWarps * 32), 0, stream, 1, p);
+        return launch_pdl(k3_kv_store_heads<H, false>, grid, dim3(kHeadsWarps * 32), 0, stream, 1, p);
+    }
     const dim3 grid((unsigned)((p.grid_rows + kWarps - 1) / kWarps), (unsigned)layers);
     if (p.cos_sin)
-        return launch_pdl(k3_kv_store<H, true>, grid, dim3(kWarps * 32), 0, stream, 1, p);
-    return launch_pdl(k3_kv_store<H, false>, grid, dim3(kWarps * 32), 0, stream, 1, p);
+        return launch_pdl(k3_kv_store<H, true>, grid, block, 0, stream, 1, p);
+    return launch_pdl(k3_kv_store<H, false>, grid, block, 0, stream, 1, p);
 }
 
 }  // namespace

@@ -64,6 +64,85 @@ __device__ __forceinline__ uint32_t knorm_rope_lane(float k0, float k1, float c,
     return pack_bf16x2(n0, n1);
 }
 
+// The head's sum over 32 pair values in the order of the lane butterfly seen
+// from lane 0: (j, j+16), then partners +8, +4, +2, +1.  Every lane of the
+// butterfly ends with these bits (IEEE addition commutes), so one thread
+// holding the whole head reproduces the warp's sum exactly.
+__device__ __forceinline__ float fold32(const float (&q)[32]) {
+    float a[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        a[j] = __fadd_rn(q[j], q[j + 16]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        a[j] = __fadd_rn(a[j], a[j + 8]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        a[j] = __fadd_rn(a[j], a[j + 4]);
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+        a[j] = __fadd_rn(a[j], a[j + 2]);
+    return __fadd_rn(a[0], a[1]);
+}
+
+// fold32 of the squares of the low (hi = false) or high halves of 32 packed
+// bf16 pairs, its first level taken as the squares are formed.
+template <bool kHi>
+__device__ __forceinline__ float fold32_squares(const uint32_t (&w)[32]) {
+    float a[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const float x = kHi ? bf16_hi(w[j]) : bf16_lo(w[j]);
+        const float y = kHi ? bf16_hi(w[j + 16]) : bf16_lo(w[j + 16]);
+        a[j] = __fadd_rn(__fmul_rn(x, x), __fmul_rn(y, y));
+    }
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) {
+#pragma unroll
+        for (int j = 0; j < o; ++j)
+            a[j] = __fadd_rn(a[j], a[j + o]);
+    }
+    return a[0];
+}
+
+// One whole key head in one thread: w[j] holds pair j = elements (2j, 2j+1)
+// as packed bf16.  Weightless K-norm (even squares and odd squares each
+// folded as fold32 does, then even + odd), the bf16 key, GPT-J RoPE with the
+// table row cs (cos of pairs 0..31 in logical chunks 0..3, sin in chunks
+// 4..7, 8 bf16 per 16-byte chunk; logical chunk c stored at c ^ swz), packed
+// back into w.  The same operations, in the same order, as knorm_rope_lane.
+template <bool kRope>
+__device__ __forceinline__ void knorm_rope_head(uint32_t (&w)[32], const uint4 *cs, int swz,
+                                                float eps) {
+    const float even = fold32_squares<false>(w);
+    const float odd = fold32_squares<true>(w);
+    const float r = inv_rms(__fadd_rn(even, odd), 0x1p-6f, eps);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {                 // 8 pairs per table chunk
+        uint4 c4 = make_uint4(0, 0, 0, 0), s4 = c4;
+        if (kRope) {
+            c4 = cs[q ^ swz];
+            s4 = cs[(4 + q) ^ swz];
+        }
+        const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w}, sw[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int j = 8 * q + t;
+            float n0 = round_bf16(__fmul_rn(bf16_lo(w[j]), r));
+            float n1 = round_bf16(__fmul_rn(bf16_hi(w[j]), r));
+            if (kRope) {
+                const float c = (t & 1) ? bf16_hi(cw[t >> 1]) : bf16_lo(cw[t >> 1]);
+                const float s = (t & 1) ? bf16_hi(sw[t >> 1]) : bf16_lo(sw[t >> 1]);
+                const float x = __fmaf_rn(n0, c, -__fmul_rn(n1, s));
+                const float y = __fmaf_rn(n1, c, __fmul_rn(n0, s));
+                n0 = x;
+                n1 = y;
+            }
+            w[j] = pack_bf16x2(n0, n1);
+        }
+    }
+}
+
 // ------------------------------------------------- programmatic launches
 //
 // Every kernel of the library is launched with programmatic stream

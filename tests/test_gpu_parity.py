@@ -173,6 +173,38 @@ def _compare_store(case, kv, rows, slots=None):
     return e
 
 
+@pytest.mark.parametrize("H", [1, 8, 32])
+@pytest.mark.parametrize("rope", [True, False])
+def test_store_unaligned_views(H, rope):
+    """K and V views that are only 4-byte aligned (row stride 128 H + 6
+    elements, K starting 2 elements in) take the lane-per-pair kernel; the
+    aligned views of the other store tests take the lane-per-head kernel.
+    Both must write the oracle's bits."""
+    L, T = 2, 45
+    case = workloads.random_case(260 + H, T=T, L=L, H=H, rope=rope, max_position=96,
+                                 num_blocks=8, block_size=16)
+    rng = np.random.default_rng(31 + H)
+    kv = workloads.normal_bf16(rng, (L, T, 128 * H), 0.0, 0.7)
+    buf = np.zeros((L, T, 128 * H + 6), dtype=np.uint16)
+    buf[:, :, 2:2 + 128 * H] = kv
+    bd = bits_to_dev(buf)
+    k = bd[:, :, 2:2 + 64 * H].unflatten(2, (H, 64))
+    v = bd[:, :, 2 + 64 * H:2 + 128 * H].unflatten(2, (H, 64))
+    assert k.data_ptr() % 16 != 0
+    caches_d = [bits_to_dev(c) for c in parity.make_caches(case, L, parity.SENTINEL)]
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    slots = case["slots"]
+    rc.kv_store(k, v, torch.from_numpy(case["positions"]).to(DEV),
+                [torch.from_numpy(s).to(DEV) for s in slots], bits_to_dev(case["cos_sin"]),
+                caches_d, case["eps"], rows=T, err=err)
+    caches = parity.make_caches(case, L, parity.SENTINEL)
+    e = oracle.kv_store_from_projection(kv, H, case["positions"], slots, case["cos_sin"], caches,
+                                        case["eps"], T)
+    for g, r in zip(caches_d, caches):
+        assert np.array_equal(parity.host_bits(g), r)
+    assert int(err.item()) == e
+
+
 @pytest.mark.parametrize("L", [9, 17])
 def test_store_layer_chunks_null_layers_and_rows_prefix(L):
     T, H = 50, 4
