@@ -35,7 +35,12 @@ L2_FLUSH_BYTES = 512 << 20          # > 129 MB L2: written between timed steps
 # capture of this bench command (dram__bytes_read.sum + dram__bytes_write.sum,
 # summed over the kernels the timed call launches); keyed by (workload, path,
 # kernel).  An entry is removed whenever one of its kernels changes.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # rc_kv_project_store at workload 2: k2_project_pair (75.67 MB read,
+    # 0.88 MB written) + k3_reduce_store (18.99 MB read); ncu with its default
+    # cache flush before each launch.
+    (2, "store", "project_store"): 95_530_176,
+}
 
 
 def load_peaks():
@@ -431,6 +436,167 @@ def run_ours(args, w):
     print(json.dumps(rec))
 
 
+FRONT_METRIC = "decode QKV front tokens/s (one draft layer, W streamed from HBM); W GB/s vs GB300 peak"
+
+
+def front_bytes(M: int, D: int, N: int, nkv: int, live: int) -> int:
+    """Algorithmic bytes of one decode front call: W once, the hidden rows,
+    the output rows, positions and slots, a table row per token, and K and V
+    of every live token into the cache."""
+    return 2 * N * D + 2 * M * D + 2 * M * N + 16 * M + 128 * M + live * 256 * nkv
+
+
+def oracle_front_seconds(case, M: int) -> float:
+    import numpy as np
+    import oracle
+    cache = np.zeros(case["cache_shape"], dtype=np.uint16)
+    t0 = time.perf_counter()
+    ref64, _ = oracle.qkv_project(case["hidden"], case["W"])
+    raw = oracle.bf16_rn_f64_array(ref64)
+    oracle.qkv_front_post(raw, case["num_heads"], case["num_kv_heads"], case["positions"],
+                          case["cos_sin"], case["slots"], cache, case["eps"])
+    return time.perf_counter() - t0
+
+
+def front_record(args, case, world, M):
+    N, D = case["W"].shape
+    return {"metric": FRONT_METRIC, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded)",
+            "config": {"workload": f"decode QKV front: M={M} tokens, D={D}, {case['num_heads']} query "
+                                   f"heads, {case['num_kv_heads']} KV heads, W [{N}, {D}], RoPE, "
+                                   "paged insert",
+                       "M": M, "D": D, "Nqkv": N, "num_heads": case["num_heads"],
+                       "num_kv_heads": case["num_kv_heads"],
+                       "parallelism": f"replicas x{world} (no collective)"}}
+
+
+def run_front(args):
+    """--path front: the decode QKV front (rc_qkv_front) on M tokens."""
+    import numpy as np
+    import workloads
+    rank, world, local = dist_env()
+    M = args.tokens
+    case = workloads.front_case(3000 + M, M)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import oracle
+        oracle.build()
+        for _ in range(args.warmup):
+            oracle_front_seconds(case, M)
+        total = sum(oracle_front_seconds(case, M) for _ in range(args.steps))
+        value = M * args.steps / total
+        rec = front_record(args, case, world, M)
+        rec.update({"impl": "reference", "value": value, "ms_per_step": 1e3 * total / args.steps,
+                    "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.max_threads(),
+                                     "kind": "oracle", "sample": f"all {M} tokens per step"},
+                    "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 0}})
+        rec["dtype"] = "f32 (f64 projection)"
+        print(json.dumps(rec))
+        return
+    import torch
+    import rope_chain_gb300 as rc
+    from rope_chain_gb300 import _build
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0 or not os.path.exists(rc.LIB_PATH):
+        _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    rc.lib()
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    hidden, W, cs = bf(case["hidden"]), bf(case["W"]), bf(case["cos_sin"])
+    N, D = case["W"].shape
+    positions = torch.from_numpy(case["positions"]).to(dev)
+    slots = torch.from_numpy(case["slots"]).to(dev)
+    cache = torch.zeros(case["cache_shape"], dtype=torch.bfloat16, device=dev)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    nh, nkv, eps = case["num_heads"], case["num_kv_heads"], case["eps"]
+    call = lambda: rc.qkv_front(hidden, W, nh, nkv, positions, cs, slots, cache, eps, out=out, err=err)
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        call()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True, external=True),
+            torch.cuda.Event(enable_timing=True, external=True)) for _ in range(args.steps)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            evs[i][0].record()
+            call()
+            evs[i][1].record()
+    g.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_us = [a.elapsed_time(b) * 1e3 for a, b in evs]
+    total_ms = max_over_ranks(sum(step_us) / 1e3, world)
+    if rc.read_device_faults(clear=True):
+        raise RuntimeError("QKV front raised fault bits")
+    # end to end: hidden rows in from pinned memory, the output rows back
+    h_h = torch.from_numpy(case["hidden"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    o_h = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    for i in range(args.warmup + args.steps):
+        flush.fill_(i & 0xFF)
+        ev = e2e_evs[i - args.warmup] if i >= args.warmup else None
+        if ev:
+            ev[0].record()
+        hidden.copy_(h_h, non_blocking=True)
+        call()
+        o_h.copy_(out, non_blocking=True)
+        if ev:
+            ev[1].record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_evs), world)
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    nbytes = front_bytes(M, D, N, nkv, int((case["slots"] >= 0).sum()))
+    t_us = statistics.mean(step_us)
+    import oracle
+    oracle.build()
+    cpu_s = oracle_front_seconds(case, M)
+    rec = front_record(args, case, world, M)
+    rec["config"]["l2"] = "flushed (512 MiB write) before every timed step; W (151 MB) exceeds L2"
+    rec["config"]["timing"] = "cuda graph"
+    rec.update({
+        "value": world * M * args.steps / (total_ms / 1e3),
+        "ms_per_step": total_ms / args.steps,
+        "roofline": {"kernel": "k4_qkv_front", "bound": "hbm", "achieved": nbytes / t_us / 1e3,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": nbytes / t_us / 1e3 / peaks["hbm_gbs"],
+                     "traffic": NCU_TRAFFIC.get(("front", M, "k4_qkv_front")),
+                     "peak_source": f"hbm_gbs of {peak_src}"},
+        "kernels": {"qkv_front": {"us": t_us, "GB/s": nbytes / t_us / 1e3, "bytes": nbytes}},
+        "cpu_baseline": {"value": M / cpu_s, "unit": "tokens/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": f"all {M} tokens, once"},
+        "e2e": {"value": world * M * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": M * D * 2, "d2h_bytes_per_step": M * N * 2},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    })
+    print(json.dumps(rec))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -438,11 +604,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--path", default="store", choices=["store", "whole"],
-                    help="store: norms + fused projection/store; whole: rc_context_kv")
+    ap.add_argument("--path", default="store", choices=["store", "whole", "front"],
+                    help="store: norms + fused projection/store; whole: rc_context_kv; "
+                         "front: the decode QKV front (rc_qkv_front)")
+    ap.add_argument("--tokens", type=int, default=16, choices=range(1, 17), metavar="1..16",
+                    help="tokens of the decode QKV front (--path front)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.path == "front":
+        run_front(args)
+        return
     import workloads
     w = workloads.WORKLOADS[args.workload]
     if args.impl == "reference":

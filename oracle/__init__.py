@@ -278,7 +278,7 @@ def kv_store_from_projection(kv: np.ndarray, H: int, positions, slots, cos_sin,
 def qkv_front_post(raw: np.ndarray, num_heads: int, num_kv_heads: int,
                    positions: Optional[np.ndarray], cos_sin: Optional[np.ndarray],
                    slots: Optional[np.ndarray], cache: Optional[np.ndarray], eps: float):
-    """The decode QKV front after its projection (reading R8): returns
+    """The decode QKV front after its projection (reading R15): returns
     (out bf16 [M, Nqkv], skipped-row count); ``cache`` (bf16 [num_blocks,
     num_kv_heads, block_size, 128]) is updated in place."""
     M, N = raw.shape

@@ -28,16 +28,16 @@
  *       restated without NVIDIA's internals; the inverse RMS here is the
  *       correctly rounded 1 / sqrt(v) (IEEE sqrt, then IEEE divide) with
  *       v = fma(S, 1/width, eps) as the pages write it.
- *   R3  Norm gains scale the output unless the norm is input-scaled (R7):
+ *   R3  Norm gains scale the output unless the norm is input-scaled (R14):
  *       y = (x * r) * gamma ([bnd] boundary_fragments order); a weightless
  *       norm is y = x * r.
  *   R4  NaN rounds to the canonical bf16 NaN 0x7FFF.
  *   R5  A slot >= num_blocks*block_size, or (with RoPE) a position outside
  *       [0, max_position), skips its row and counts it in *err.
- *   R6  A gain center is added to the weight only when it is non-zero: the
+ *   R13 A gain center is added to the weight only when it is non-zero: the
  *       stock norm with center 0 multiplies by the weight itself, so a -0.0
  *       weight keeps its sign ([ctx] _ContextNormsKernel adds it always).
- *   R8  The decode QKV front ([rt] _fused_qkv_projection, _attention,
+ *   R15 The decode QKV front ([rt] _fused_qkv_projection, _attention,
  *       may_fuse_qkv_front): its output row is [Q | K | V | O-gate] with
  *       q_size = 64 * num_heads and kv_size = 64 * num_kv_heads (the split
  *       _attention makes); the QK-norm of every Q and K head is the same
@@ -48,7 +48,7 @@
  *       counted in *err and inserts nothing; its Q and K are normed but not
  *       rotated when the position is out of range.  A negative slot inserts
  *       nothing and is not an error.
- *   R7  An input-scale weight multiplies the input before the sum of
+ *   R14 An input-scale weight multiplies the input before the sum of
  *       squares and nothing after it, in the order of [bnd]
  *       boundary_fragments; the hidden norm's output is still rounded to
  *       bf16 before the layer norm reads it.
@@ -274,7 +274,7 @@ int32_t rco_context_norms(const uint16_t *x, int64_t T, int32_t D,
      fp32         the weight's dtype: 1 FP32, 0 BF16;
      input_scale  1: the weight scales the input before the norm, 0: the
                   norm's output (R3);
-     center       the gain center, added to each weight element (R6);
+     center       the gain center, added to each weight element (R13);
      eps          this norm's own eps. */
 typedef struct {
     const void *weight;
@@ -284,7 +284,7 @@ typedef struct {
     float eps;
 } rco_norm;
 
-/* gamma_c of the weight row at `offset` (R6: the center is added only when non-zero, so
+/* gamma_c of the weight row at `offset` (R13: the center is added only when non-zero, so
    that a center of 0 leaves the weight's bits, -0.0 included, unchanged). */
 static float norm_gain(const rco_norm *n, int64_t offset, int32_t c)
 {
@@ -508,7 +508,7 @@ int32_t rco_kv_store(const uint16_t *k, const uint16_t *v,
 
 /* ---------------------------------------------------------- decode front */
 
-/* The QKV front after its projection (R8; [rt] _fused_qkv_projection and
+/* The QKV front after its projection (R15; [rt] _fused_qkv_projection and
    _attention): raw is the bf16 projection [M, Nqkv] of M decode tokens,
    Nqkv = 64 * (2 * num_heads + 2 * num_kv_heads), columns [Q | K | V | gate].
      out[m, Q and K heads] = RoPE(bf16(head * r)), r the head's weightless
@@ -519,7 +519,7 @@ int32_t rco_kv_store(const uint16_t *k, const uint16_t *v,
      cache[s / bs, h, s % bs, 64:128] = raw[m, V head h]   for s = slots[m] >= 0;
    a row whose slot is >= num_blocks * block_size or (with a table) whose
    position is outside [0, max_position) adds one to *err and inserts
-   nothing (R8).  slots may be NULL (nothing inserted).
+   nothing (R15).  slots may be NULL (nothing inserted).
    cache is bf16 [num_blocks, num_kv_heads, block_size, 128].  Returns 0, or 1
    for unsupported arguments. */
 int32_t rco_qkv_front_post(const uint16_t *raw, int32_t M, int32_t num_heads, int32_t num_kv_heads,

@@ -217,18 +217,23 @@ k3_kv_store_heads(const __grid_constant__ StoreLaunch p)
 // Split-K projection finished and stored in one pass: the FP32 partials
 // [splits, L, T, 128 H] are added in split order and rounded to bf16 (the
 // same additions as the projection's reduce kernel), optionally written to
-// kv_out, and stored like k3_kv_store.  One warp per (row, layer, head): the
-// K-norm needs only its head, and many splits (small T) still leave enough
-// warps; the split loop is unrolled so 8 partials are in flight per lane.
+// kv_out, and stored like k3_kv_store.  One warp per (row, layer), 4 warps
+// per CTA, so a whole workload's rows are resident in about one wave; lane
+// j holds pair (2j, 2j+1) of each head.  Heads go in groups of kRsHeads,
+// and the partials of up to kRsSplits splits of a group (K and V) are all in
+// flight before the first add; the adds stay in split order.
+constexpr int kRsWarps = 4;
+constexpr int kRsHeads = 8;
+constexpr int kRsSplits = 3;
+
 template <bool kRope>
-__global__ void __launch_bounds__(kWarps * 32, 6)
+__global__ void __launch_bounds__(kRsWarps * 32, 3)
 k3_reduce_store(const __grid_constant__ FusedStore fs, const float *__restrict__ partial,
                 int32_t splits, int32_t L, int32_t T)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * kWarps + warp;
+    const int64_t row = (int64_t)blockIdx.x * kRsWarps + warp;
     const int layer = blockIdx.y;
-    const int h = blockIdx.z;
     const int H = fs.H;
     const int N = 2 * H * kHeadDim;
     pdl_trigger();
@@ -244,64 +249,81 @@ k3_reduce_store(const __grid_constant__ FusedStore fs, const float *__restrict__
             pos = __ldg(fs.positions + row);
     }
     const int64_t plane = (int64_t)L * T * N;
-    const float *pk = partial + ((int64_t)layer * T + row) * N + h * kHeadDim + 2 * lane;
-    const float *pv = pk + H * kHeadDim;
-    float2 ka = __ldcs(reinterpret_cast<const float2 *>(pk));
-    float2 va = __ldcs(reinterpret_cast<const float2 *>(pv));
-    // the table row is fetched while the partials are in flight (row 0 for
-    // rows that are not stored)
-    float c = 1.0f, s = 0.0f;
+    const float *prow = partial + ((int64_t)layer * T + row) * N + 2 * lane;
     const bool in_range = store && slot >= 0 && slot < fs.capacity &&
                           (!kRope || (pos >= 0 && pos < fs.max_position));
+    if (store && slot >= 0 && !in_range && lane == 0)   // once per (row, layer)
+        count_skip(fs.err, 0);
+    // the table row (row 0 for rows that are not stored)
+    float c = 1.0f, s = 0.0f;
     if (kRope) {
         const unsigned short *cs = reinterpret_cast<const unsigned short *>(fs.cos_sin) +
                                    (in_range ? pos : 0) * kHeadDim;
         c = __uint_as_float((uint32_t)__ldg(cs + lane) << 16);
         s = __uint_as_float((uint32_t)__ldg(cs + kHeadDim / 2 + lane) << 16);
     }
-    // Splits 1 .. splits-1 in batches of 4 whose loads are all issued before
-    // the first add; the adds stay in split order.
-    for (int sp = 1; sp < splits; sp += 4) {
-        float2 a[4], b[4];
+    uint32_t *dst_row = nullptr;
+    if (in_range) {
+        // Slots of a cache fit 32 bits (checked on the host).
+        const uint32_t bs = (uint32_t)fs.block_size;
+        const uint32_t blk = (uint32_t)slot / bs;
+        const uint32_t page = (uint32_t)slot - blk * bs;
+        dst_row = reinterpret_cast<uint32_t *>(fs.caches[layer]) +
+                  (((int64_t)blk * H) * bs + page) * kHeadDim + lane;
+    }
+    uint32_t *kvo = fs.kv_out ? reinterpret_cast<uint32_t *>(fs.kv_out + ((int64_t)layer * T + row) * N) + lane
+                              : nullptr;
+    for (int h0 = 0; h0 < H; h0 += kRsHeads) {
+        const int nh = min(kRsHeads, H - h0);
+        float2 ka[kRsHeads], va[kRsHeads];
+        for (int sp = 0; sp < splits; sp += kRsSplits) {
+            float2 a[kRsSplits][kRsHeads], b[kRsSplits][kRsHeads];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            if (sp + u < splits) {
-                a[u] = __ldcs(reinterpret_cast<const float2 *>(pk + (sp + u) * plane));
-                b[u] = __ldcs(reinterpret_cast<const float2 *>(pv + (sp + u) * plane));
+            for (int u = 0; u < kRsSplits; ++u) {
+#pragma unroll
+                for (int q = 0; q < kRsHeads; ++q) {
+                    if (sp + u < splits && q < nh) {
+                        const float *pk = prow + (sp + u) * plane + (h0 + q) * kHeadDim;
+                        a[u][q] = __ldcs(reinterpret_cast<const float2 *>(pk));
+                        b[u][q] = __ldcs(reinterpret_cast<const float2 *>(pk + H * kHeadDim));
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kRsSplits; ++u) {
+#pragma unroll
+                for (int q = 0; q < kRsHeads; ++q) {
+                    if (sp + u < splits && q < nh) {
+                        if (sp + u == 0) {
+                            ka[q] = a[u][q];
+                            va[q] = b[u][q];
+                        } else {
+                            ka[q].x = __fadd_rn(ka[q].x, a[u][q].x);
+                            ka[q].y = __fadd_rn(ka[q].y, a[u][q].y);
+                            va[q].x = __fadd_rn(va[q].x, b[u][q].x);
+                            va[q].y = __fadd_rn(va[q].y, b[u][q].y);
+                        }
+                    }
+                }
             }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            if (sp + u < splits) {
-                ka.x = __fadd_rn(ka.x, a[u].x);
-                ka.y = __fadd_rn(ka.y, a[u].y);
-                va.x = __fadd_rn(va.x, b[u].x);
-                va.y = __fadd_rn(va.y, b[u].y);
+        for (int q = 0; q < kRsHeads; ++q) {
+            if (q < nh) {
+                const int h = h0 + q;
+                const uint32_t kw = pack_bf16x2(ka[q].x, ka[q].y), vw = pack_bf16x2(va[q].x, va[q].y);
+                if (kvo) {
+                    kvo[h * (kHeadDim / 2)] = kw;
+                    kvo[(H + h) * (kHeadDim / 2)] = vw;
+                }
+                if (in_range) {
+                    uint32_t *dst = dst_row + (int64_t)h * fs.block_size * kHeadDim;
+                    dst[0] = knorm_rope_lane<kRope>(bf16_lo(kw), bf16_hi(kw), c, s, fs.eps);
+                    dst[kHeadDim / 2] = vw;           // V follows K
+                }
             }
         }
     }
-    const uint32_t kw = pack_bf16x2(ka.x, ka.y), vw = pack_bf16x2(va.x, va.y);
-    if (fs.kv_out != nullptr) {
-        uint32_t *o = reinterpret_cast<uint32_t *>(fs.kv_out + ((int64_t)layer * T + row) * N) + lane;
-        o[h * (kHeadDim / 2)] = kw;
-        o[(H + h) * (kHeadDim / 2)] = vw;
-    }
-    if (!store || slot < 0)
-        return;
-    if (!in_range) {
-        if (h == 0)                               // once per (row, layer)
-            count_skip(fs.err, lane);
-        return;
-    }
-    const uint32_t ko = knorm_rope_lane<kRope>(bf16_lo(kw), bf16_hi(kw), c, s, fs.eps);
-    // Slots of a cache fit 32 bits (checked on the host).
-    const uint32_t bs = (uint32_t)fs.block_size;
-    const uint32_t blk = (uint32_t)slot / bs;
-    const uint32_t page = (uint32_t)slot - blk * bs;
-    uint32_t *dst = reinterpret_cast<uint32_t *>(fs.caches[layer]) +
-                    (((int64_t)blk * H + h) * bs + page) * kHeadDim + lane;
-    dst[0] = ko;
-    dst[kHeadDim / 2] = vw;                       // V follows K
 }
 
 // 16-byte access to K, V, the table and every cache of the chunk.
@@ -338,11 +360,11 @@ cudaError_t launch_h(const StoreLaunch &p, int32_t layers, cudaStream_t stream) 
 cudaError_t launch_reduce_store(const FusedStore &fs, const float *partial, int32_t splits,
                                 int32_t L, int32_t T, cudaStream_t stream)
 {
-    const dim3 grid((unsigned)((T + kWarps - 1) / kWarps), (unsigned)L, (unsigned)fs.H);
+    const dim3 grid((unsigned)((T + kRsWarps - 1) / kRsWarps), (unsigned)L);
     if (fs.cos_sin)
-        return launch_pdl(k3_reduce_store<true>, grid, dim3(kWarps * 32), 0, stream, 1, fs, partial,
+        return launch_pdl(k3_reduce_store<true>, grid, dim3(kRsWarps * 32), 0, stream, 1, fs, partial,
                           splits, L, T);
-    return launch_pdl(k3_reduce_store<false>, grid, dim3(kWarps * 32), 0, stream, 1, fs, partial,
+    return launch_pdl(k3_reduce_store<false>, grid, dim3(kRsWarps * 32), 0, stream, 1, fs, partial,
                       splits, L, T);
 }
 

@@ -199,3 +199,30 @@ def random_case(seed: int, T: int, L: int, H: int, *, rope: bool = True,
     return dict(x=x, hidden_w=hidden_w, pre_w=pre_w, W=W, positions=positions,
                 slots=slots, cos_sin=cos_sin, eps=eps,
                 cache_shape=(num_blocks, H, block_size, 2 * HEAD_DIM))
+
+
+# Decode QKV front (one draft layer, 1 to 16 tokens): the hidden width and
+# KV head count of the context workloads (D = 8192, 8 KV heads of 64), 64
+# query heads, so W is [64 * (2 * 64 + 2 * 8), 8192] = [9216, 8192].
+FRONT = dict(D=HIDDEN, num_heads=64, num_kv_heads=8, max_position=8192, num_blocks=64,
+             block_size=16, eps=1e-6)
+
+
+def front_case(seed: int, M: int, *, D: int = FRONT["D"], num_heads: int = FRONT["num_heads"],
+               num_kv_heads: int = FRONT["num_kv_heads"],
+               max_position: int = FRONT["max_position"], num_blocks: int = FRONT["num_blocks"],
+               block_size: int = FRONT["block_size"], eps: float = FRONT["eps"]) -> dict:
+    """Operands of one decode QKV front call, drawn in the order hidden
+    N(0, 1), W N(0, 0.02) ([Nqkv, D], the nn.Linear layout), positions
+    uniform in [0, max_position), slots distinct in [0, num_blocks *
+    block_size)."""
+    rng = np.random.default_rng(seed)
+    N = HEAD_DIM * (2 * num_heads + 2 * num_kv_heads)
+    hidden = normal_bf16(rng, (M, D), 0.0, 1.0)
+    W = normal_bf16(rng, (N, D), 0.0, 0.02)
+    positions = rng.integers(0, max_position, size=M, dtype=np.int64)
+    slots = rng.choice(num_blocks * block_size, size=M, replace=False).astype(np.int64)
+    return dict(hidden=hidden, W=W, positions=positions, slots=slots,
+                cos_sin=cos_sin_table(max_position), num_heads=num_heads,
+                num_kv_heads=num_kv_heads, eps=eps,
+                cache_shape=(num_blocks, num_kv_heads, block_size, 2 * HEAD_DIM))
