@@ -79,6 +79,8 @@ def check(case, normed, W, *, workspace, rows=None, layout=rc.RC_W_KN, slots=Non
     (300, 2, 2, False, True),      # CTA pairs, epilogue store, K and V heads in one tile
     (512, 3, 8, False, True),      # CTA pairs, epilogue store
     (512, 3, 8, True, True),       # CTA pairs, split-K, reduce-and-store
+    (256, 3, 8, True, True),       # CTA pairs, 6 splits
+    (200, 1, 2, True, False),      # CTA pairs, 32 splits of 4 K blocks, ragged rows
     (200, 2, 16, False, False),    # CTA pairs, epilogue store, no RoPE
     (129, 1, 32, True, True),      # H = 32, ragged rows
     (64, 2, 8, True, True),        # single CTAs, split-K, reduce-and-store
@@ -135,3 +137,4 @@ def test_fused_workloads(index):
     case = workloads.make_inputs(w)
     normed = oracle.context_norms(case["x"], case["hidden_w"], case["pre_w"], w.L, w.eps)
     check(case, normed, case["W"], workspace=True)
+
