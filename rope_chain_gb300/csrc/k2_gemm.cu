@@ -773,6 +773,280 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
 }
 
+// ------------------------------------------------- persistent CTA pairs
+//
+// k2_project_pair_persistent: the pair kernel for plans that do not split
+// K, with one CTA pair per two SMs taking output tiles t, t + P, t + 2P, ...
+// (P pairs; consecutive tiles share A rows and W columns in L2).  The TMA
+// ring runs on across tiles, and TMEM holds two 256-column accumulators:
+// while the epilogue warps of both CTAs store tile j from one, the MMA
+// thread already accumulates tile j + 1 into the other, so the epilogue and
+// the per-CTA set-up and pipeline fill no longer sit between mainloops.
+// The epilogue (bf16 rows or the fused store) is the pair kernel's.
+
+struct PersistCfg {
+    static constexpr int kStages = PairCfg::kStages;
+    static constexpr uint32_t kStageBytes = PairCfg::kStageBytes;
+    static constexpr uint32_t kStagingBytes = 4u * 32u * 80u;   // bf16 rows of 4 epilogue warps
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kStagingBytes + 512;
+    static_assert((2 * kStages + 5) * 8 + 4 * 4 <= 512, "barriers and words fit the tail");
+};
+
+// Arrive on a barrier of any CTA of the cluster, releasing at cluster scope.
+__device__ __forceinline__ void mbar_arrive_release_cluster(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Bounded wait on a barrier that other CTAs of the cluster arrive on.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 0;; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok)
+            return true;
+        if ((it & 255u) == 255u && (faulted() || globaltimer() - t0 > kWaitNs))
+            return false;
+    }
+}
+
+// This warp's 32 rows of a tile as bf16, through the warp's staging rows:
+// 64 bytes per row, rows 80 bytes apart (conflict-free), so each global
+// store instruction writes whole 64-byte row segments.
+__device__ __forceinline__ void write_bf16_rows(const GemmArgs &g, uint32_t tbase, uint32_t stage,
+                                                int row0, int l, int n0, int lane) {
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tbase + 32u * c, r);
+        const uint32_t w = stage + (uint32_t)lane * 80u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            st_shared_v4(w + 16u * j, make_uint4(pack_acc(r[8 * j], r[8 * j + 1]),
+                                                 pack_acc(r[8 * j + 2], r[8 * j + 3]),
+                                                 pack_acc(r[8 * j + 4], r[8 * j + 5]),
+                                                 pack_acc(r[8 * j + 6], r[8 * j + 7])));
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int rr = (lane >> 2) + 8 * i, piece = lane & 3;
+            const uint4 v = ld_shared_v4(stage + (uint32_t)rr * 80u + 16u * piece);
+            const int row = row0 + rr;
+            if (row < g.T)
+                *reinterpret_cast<uint4 *>(g.out + ((int64_t)l * g.T + row) * g.N + n0 + 32 * c +
+                                           8 * piece) = v;
+        }
+        __syncwarp();                                  // reads done before the next chunk's writes
+    }
+}
+
+template <bool kBmn, bool kFused>
+__global__ void __launch_bounds__(kThreads, 1)
+k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB, const GemmArgs g,
+                           const __grid_constant__ FusedStore fs, int n_pairs, int m_pairs)
+{
+    using C = PersistCfg;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sA = smem_u32(smem);
+    const uint32_t sB = sA + S * kABytes;
+    const uint32_t sStage = sA + S * C::kStageBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * C::kStageBytes + C::kStagingBytes);
+    // full[s], empty[s], afull[2] (accumulator b complete), aempty[2]
+    // (leader: both CTAs' epilogues are done with accumulator b), done
+    const uint32_t bar0 = smem_u32(bars);
+    const uint32_t empty0 = bar0 + 8u * S, afull0 = bar0 + 16u * S, aempty0 = afull0 + 16u;
+    const uint32_t done = aempty0 + 16u;
+    // words[0]: TMEM base; [1]: stages the leader's MMA thread consumed;
+    // [2]: skip flag (written by the leader into both CTAs); [3]: stages the
+    // peer's loader issued (written by the peer into the leader)
+    volatile uint32_t *words = reinterpret_cast<volatile uint32_t *>(bars + 2 * S + 5);
+    const uint32_t words_addr = smem_u32((const void *)words);
+
+    const int warp = __shfl_sync(0xFFFFFFFFu, (int)(threadIdx.x >> 5), 0);
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair_id = (int)(blockIdx.x >> 1), num_pairs = (int)(gridDim.x >> 1);
+    const int num_tiles = g.L * m_pairs * n_pairs;
+    const int nkb = g.kb_total;
+    pdl_trigger();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar0 + 8u * s, 1);
+            mbar_init(empty0 + 8u * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(afull0 + 8u * b, 1);
+            mbar_init(aempty0 + 8u * b, 8);        // 4 epilogue warps in each CTA of the pair
+        }
+        mbar_init(done, 1);
+        words[1] = 0u;
+        words[3] = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+        if (leader) {
+            const uint32_t skip = faulted() ? 1u : 0u;
+            words[2] = skip;
+            st_cluster_u32(map_to_rank(words_addr + 8u, 1), skip);
+        }
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(words_addr), "r"(512) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    cluster_sync();                               // barriers, skip flag and TMEM pair-wide
+    tc_fence_after();
+    const uint32_t tmem = words[0];
+    const bool skip = words[2] != 0u;
+    pdl_wait();                                   // the previous kernel's writes are visible
+
+    int issued = 0;
+    if (warp == 0) {
+        if (lane == 0 && !skip) {
+            int it = 0;
+            bool ok = true;
+            for (int t = pair_id; t < num_tiles && ok; t += num_pairs) {
+                const int np = t % n_pairs, rest = t / n_pairs;
+                const int mp = rest % m_pairs, l = rest / m_pairs;
+                const int m0 = mp * 256 + 128 * (int)rank;
+                const int nb = np * 256 + 128 * (int)rank;
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const int s = it % S;
+                    const uint32_t ph = (uint32_t)(it / S) & 1u;
+                    if (!mbar_wait(empty0 + 8u * s, ph ^ 1u)) {
+                        raise_fault(kFaultLoad);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full = map_to_rank(bar0 + 8u * s, 0);
+                    if (leader)
+                        mbar_expect_tx(bar0 + 8u * s, PairCfg::kPairTx);
+                    const int kc = kb * BK;
+                    tma_load_3d_pair(sA + s * kABytes, &tmA, kc, m0, l, full);
+                    if (kBmn) {
+                        tma_load_3d_pair(sB + s * PairCfg::kBHalf, &tmB, nb, kc, l, full);
+                        tma_load_3d_pair(sB + s * PairCfg::kBHalf + 8192u, &tmB, nb + 64, kc, l, full);
+                    } else {
+                        tma_load_3d_pair(sB + s * PairCfg::kBHalf, &tmB, kc, nb, l, full);
+                    }
+                    issued = it + 1;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            int consumed = 0;
+            if (!skip) {
+                constexpr uint32_t idesc = make_idesc(256, 256, kBmn);
+                int it = 0, j = 0;
+                bool ok = true;
+                for (int t = pair_id; t < num_tiles && ok; t += num_pairs, ++j) {
+                    const int b = j & 1;
+                    // both epilogues are done reading accumulator b (tile j - 2)
+                    if (!mbar_wait_cluster(aempty0 + 8u * b, ((uint32_t)(j >> 1) & 1u) ^ 1u)) {
+                        raise_fault(kFaultMma);
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem + 256u * (uint32_t)b;
+                    for (int kb = 0; kb < nkb; ++kb, ++it) {
+                        const int s = it % S;
+                        const uint32_t ph = (uint32_t)(it / S) & 1u;
+                        if (!mbar_wait(bar0 + 8u * s, ph)) {
+                            raise_fault(kFaultMma);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a = sA + s * kABytes, bb = sB + s * PairCfg::kBHalf;
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            const uint64_t ad = smem_desc_sw128(a + 32u * kk, 16u, 1024u);
+                            const uint64_t bd = kBmn ? smem_desc_sw128(bb + 2048u * kk, 8192u, 1024u)
+                                                     : smem_desc_sw128(bb + 32u * kk, 16u, 1024u);
+                            mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        }
+                        mma_commit_pair(empty0 + 8u * s);
+                        consumed = it + 1;
+                    }
+                    if (ok)
+                        mma_commit_pair(afull0 + 8u * b);   // accumulator b holds tile j
+                }
+            }
+            words[1] = (uint32_t)consumed;
+            mma_commit_pair(done);
+        }
+        __syncwarp();
+    } else {
+        const int q = warp & 3;
+        const uint32_t stage = sStage + (uint32_t)q * (32u * 80u);
+        int j = 0;
+        for (int t = pair_id; t < num_tiles && !skip; t += num_pairs, ++j) {
+            const int b = j & 1;
+            bool ok = mbar_wait(afull0 + 8u * b, (uint32_t)(j >> 1) & 1u);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) {
+                if (lane == 0)
+                    raise_fault(kFaultAccum);
+                break;
+            }
+            tc_fence_after();
+            const int np = t % n_pairs, rest = t / n_pairs;
+            const int mp = rest % m_pairs, l = rest / m_pairs;
+            const int m0 = mp * 256 + 128 * (int)rank, n0 = np * 256;
+            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + 256u * (uint32_t)b;
+            if (kFused)
+                fused_store_tile(fs, g, tbase, l, m0 + 32 * q + lane, n0);
+            else
+                write_bf16_rows(g, tbase, stage, m0 + 32 * q, l, n0, lane);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_release_cluster(map_to_rank(aempty0 + 8u * b, 0));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (!leader && warp == 0 && lane == 0)
+        st_cluster_u32(map_to_rank(words_addr + 12u, 0), (uint32_t)issued);
+    cluster_sync();
+    if (warp == 0 && lane == 0 && leader) {
+        // Both CTAs' loads land on the leader's barriers: after a fault, wait
+        // for every stage either CTA issued before anyone frees smem.
+        const int last = max(issued, (int)words[3]);
+        for (int i = (int)words[1]; i < last; ++i)
+            if (!mbar_wait_own(bar0 + 8u * (i % S), (uint32_t)(i / S) & 1u)) {
+                raise_fault(kFaultDrain);
+                break;
+            }
+    }
+    if (leader && warp == 1 && lane == 0 && !mbar_wait_own(done, 0u))
+        raise_fault(kFaultDrain);
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512)
+                     : "memory");
+    }
+}
+
 // ------------------------------------------------------------------ host
 
 template <int BN, bool kBmn>
@@ -814,6 +1088,34 @@ cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const Gemm
     const dim3 grid((unsigned)(2 * n_pairs), (unsigned)m_pairs, (unsigned)(g.L * g.splits));
     return launch_pdl(k2_project_pair<kBmn, kFused, kTransform>, grid,
                       dim3(pair_threads<kTransform>()), PairCfg::kSmem, stream, 2, ma, mb, g, fs);
+}
+
+// One CTA pair per two SMs (fewer when there are fewer tiles).
+template <bool kBmn, bool kFused>
+cudaError_t launch_pair_persistent(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &g,
+                                   const FusedStore &fs, int n_pairs, int m_pairs,
+                                   cudaStream_t stream) {
+    static int sms[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    int n_sms = dev < 64 ? sms[dev] : 0;
+    if (n_sms == 0) {
+        e = cudaFuncSetAttribute(k2_project_pair_persistent<kBmn, kFused>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PersistCfg::kSmem);
+        if (e != cudaSuccess)
+            return e;
+        e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return e;
+        if (dev < 64)
+            sms[dev] = n_sms;
+    }
+    const int64_t tiles = (int64_t)g.L * m_pairs * n_pairs;
+    const int pairs = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, n_sms / 2));
+    return launch_pdl(k2_project_pair_persistent<kBmn, kFused>, dim3((unsigned)(2 * pairs)),
+                      dim3(kThreads), PersistCfg::kSmem, stream, 2, ma, mb, g, fs, n_pairs, m_pairs);
 }
 
 }  // namespace
@@ -877,6 +1179,9 @@ template <bool kFused>
 cudaError_t launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &g,
                         const FusedStore &fs, bool w_nk, const ProjectPlan &plan, int64_t T,
                         int32_t N, cudaStream_t stream) {
+    if (plan.pair && plan.splits == 1)         // persistent pairs, epilogue under the next mainloop
+        return w_nk ? launch_pair_persistent<false, kFused>(ma, mb, g, fs, N / 256, (int)((T + 255) / 256), stream)
+                    : launch_pair_persistent<true, kFused>(ma, mb, g, fs, N / 256, (int)((T + 255) / 256), stream);
     if (plan.pair)
         return w_nk ? launch_pair<false, kFused, false>(ma, mb, g, fs, N / 256, (int)((T + 255) / 256), stream)
                     : launch_pair<true, kFused, false>(ma, mb, g, fs, N / 256, (int)((T + 255) / 256), stream);
