@@ -362,13 +362,29 @@ def run_ours(args, w):
         flush.fill_(i & 0xFF)
         e2e_step(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
     torch.cuda.synchronize()
-    e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
+    # The end-to-end steps (copies from pinned host memory, the calls, the
+    # status word back) run as one captured graph too when event nodes are
+    # available, as a serving loop would issue them; eagerly otherwise.
+    e2e_evs = [(make_event(), make_event()) for _ in range(args.steps)]
+
+    def e2e_steps():
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            e2e_step(*e2e_evs[i])
+
+    e2e_graph = None
+    if graphs:
+        e2e_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(e2e_graph):
+            e2e_steps()
+        e2e_graph.replay()                   # warm the graph itself
+        torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    for i in range(args.steps):
-        flush.fill_(i & 0xFF)
-        e2e_step(*e2e_evs[i])
+    if e2e_graph is not None:
+        e2e_graph.replay()
+    else:
+        e2e_steps()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_evs), world)
 
@@ -429,7 +445,7 @@ def run_ours(args, w):
         "cpu_baseline": {"value": R / cpu_s, "unit": "rows/s", "cores": oracle.max_threads(),
                          "kind": "oracle", "sample": f"first {R} rows of the workload, whole chain, once"},
         "e2e": {"value": world * w.T * args.steps / (e2e_ms / 1e3), "unit": "rows/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4, "timing": timing},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     })
@@ -553,11 +569,7 @@ def run_front(args):
     # end to end: hidden rows in from pinned memory, the output rows back
     h_h = torch.from_numpy(case["hidden"].view(np.int16)).view(torch.bfloat16).pin_memory()
     o_h = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
-    e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-    for i in range(args.warmup + args.steps):
-        flush.fill_(i & 0xFF)
-        ev = e2e_evs[i - args.warmup] if i >= args.warmup else None
+    def e2e_step(ev=None):
         if ev:
             ev[0].record()
         hidden.copy_(h_h, non_blocking=True)
@@ -565,6 +577,24 @@ def run_front(args):
         o_h.copy_(out, non_blocking=True)
         if ev:
             ev[1].record()
+
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        e2e_step()
+    torch.cuda.synchronize()
+    # as one captured graph, like the timed device steps
+    e2e_evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(args.steps)]
+    ge = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ge):
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            e2e_step(e2e_evs[i])
+    ge.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ge.replay()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_evs), world)
     if rank != 0:
@@ -590,7 +620,8 @@ def run_front(args):
         "cpu_baseline": {"value": M / cpu_s, "unit": "tokens/s", "cores": oracle.max_threads(),
                          "kind": "oracle", "sample": f"all {M} tokens, once"},
         "e2e": {"value": world * M * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": M * D * 2, "d2h_bytes_per_step": M * N * 2},
+                "h2d_bytes_per_step": M * D * 2, "d2h_bytes_per_step": M * N * 2,
+                "timing": "cuda graph"},
         "gpu_launches": args.steps,
         "clocks": clocks,
     })
