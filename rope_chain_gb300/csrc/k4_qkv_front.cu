@@ -51,7 +51,18 @@ constexpr uint32_t kBBytes = kTok * kBK * 2;    // 2 KiB
 constexpr uint32_t kRedStride = 80;             // bytes per column of the DSMEM partial
 constexpr uint32_t kRedBytes = kBM * kRedStride;
 constexpr uint32_t kStgBytes = kTok * kBM * 2;  // bf16 [16 tokens][128 columns]
-constexpr size_t kSmem = 1024 + (size_t)kStages * (kABytes + kBBytes) + kRedBytes + kStgBytes + 256;
+// per token: position, slot, and its cos|sin table row (64 bf16)
+constexpr uint32_t kTokBytes = kTok * 8 * 2 + kTok * kHeadDim * 2;
+constexpr size_t kSmem = 1024 + (size_t)kStages * (kABytes + kBBytes) + kRedBytes + kStgBytes +
+                         kTokBytes + 256;
+
+// Per-token operands of the epilogue, fetched while the weight streams.
+struct TokenInfo {
+    int64_t pos[kTok];
+    int64_t slot[kTok];
+    uint16_t cs[kTok][kHeadDim];       // the token's table row: cos 0..31, sin 32..63
+};
+static_assert(sizeof(TokenInfo) == kTokBytes, "token block size");
 
 enum : unsigned { kFaultLoad = 1u, kFaultMma = 2u, kFaultAccum = 4u, kFaultDrain = 8u };
 
@@ -121,9 +132,10 @@ struct FrontArgs {
 };
 
 // One (token, head) of the epilogue, a whole warp: lane j holds the pair
-// (2j, 2j+1) of head column block `col` of token m.
-__device__ __forceinline__ void front_head(const FrontArgs &a, int m, int col, uint32_t word,
-                                           int lane) {
+// (2j, 2j+1) of head column block `col` of token m; tk holds the token's
+// position, slot and table row.
+__device__ __forceinline__ void front_head(const FrontArgs &a, const TokenInfo &tk, int m, int col,
+                                           uint32_t word, int lane) {
     const int gh = col >> 6;                        // head index in [Q | K | V | gate]
     const int nq = a.num_heads, nkv = a.num_kv_heads;
     const int64_t at = (int64_t)m * a.N + col;
@@ -132,10 +144,10 @@ __device__ __forceinline__ void front_head(const FrontArgs &a, int m, int col, u
     int64_t pos = 0;
     bool bad_pos = false;
     if (a.cos_sin != nullptr) {
-        pos = __ldg(a.positions + m);
+        pos = tk.pos[m];
         bad_pos = pos < 0 || pos >= a.max_position;
     }
-    const int64_t slot = a.slots != nullptr ? __ldg(a.slots + m) : -1;
+    const int64_t slot = a.slots != nullptr ? tk.slot[m] : -1;
     const bool insert = slot >= 0 && slot < a.capacity && !bad_pos;
     uint32_t *dst = nullptr;
     if (insert && gh >= nq && gh < nq + 2 * nkv) {
@@ -150,9 +162,8 @@ __device__ __forceinline__ void front_head(const FrontArgs &a, int m, int col, u
     uint32_t o = word;
     if (gh < nq + nkv) {                            // Q or K: QK-norm, then RoPE
         if (a.cos_sin != nullptr && !bad_pos) {
-            const unsigned short *cs = reinterpret_cast<const unsigned short *>(a.cos_sin) + pos * kHeadDim;
-            const float c = __uint_as_float((uint32_t)__ldg(cs + lane) << 16);
-            const float s = __uint_as_float((uint32_t)__ldg(cs + kHeadDim / 2 + lane) << 16);
+            const float c = __uint_as_float((uint32_t)tk.cs[m][lane] << 16);
+            const float s = __uint_as_float((uint32_t)tk.cs[m][kHeadDim / 2 + lane] << 16);
             o = knorm_rope_lane<true>(bf16_lo(word), bf16_hi(word), c, s, a.eps);
         } else {
             o = knorm_rope_lane<false>(bf16_lo(word), bf16_hi(word), 1.0f, 0.0f, a.eps);
@@ -174,8 +185,10 @@ k4_qkv_front(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     const uint32_t sB = sA + kStages * kABytes;
     const uint32_t sRed = sB + kStages * kBBytes;   // the upper K half's FP32 partial
     const uint32_t sStg = sRed + kRedBytes;         // bf16 [16 tokens][128 columns]
+    const uint32_t sTok = sStg + kStgBytes;         // TokenInfo
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * (kABytes + kBBytes) + kRedBytes +
-                                                  kStgBytes);
+                                                  kStgBytes + kTokBytes);
+    TokenInfo &tk = *reinterpret_cast<TokenInfo *>(smem + (sTok - sA));
     const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8u * kStages;
     const uint32_t accum = full0 + 16u * kStages;
     // words[0]: TMEM base; [1]: the partner's partial is valid (set by rank 1
@@ -268,6 +281,24 @@ k4_qkv_front(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     const int q = warp & 3;
     uint32_t acc[16];
     if (warp >= 2) {
+        // While the weight streams: each token's position, slot and table
+        // row into shared memory for the epilogue (the CTA that stores)
+        if (rank == 0 && !skip) {
+            for (int m = warp - 2; m < a.M; m += 4) {
+                const int64_t pos = a.cos_sin != nullptr ? __ldg(a.positions + m) : 0;
+                if (lane == 0) {
+                    tk.pos[m] = pos;
+                    tk.slot[m] = a.slots != nullptr ? __ldg(a.slots + m) : -1;
+                }
+                if (a.cos_sin != nullptr) {
+                    const bool bad = pos < 0 || pos >= a.max_position;
+                    const unsigned short *row =
+                        reinterpret_cast<const unsigned short *>(a.cos_sin) + (bad ? 0 : pos) * kHeadDim;
+                    tk.cs[m][lane] = __ldg(row + lane);
+                    tk.cs[m][kHeadDim / 2 + lane] = __ldg(row + kHeadDim / 2 + lane);
+                }
+            }
+        }
         bool ok = !skip && mbar_wait(accum, 0u);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok && !skip && lane == 0)
@@ -326,19 +357,20 @@ k4_qkv_front(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CU
     }
     if (store)
         __syncthreads();                            // the staging tile is complete
-    if (store && warp >= 2) {
-        for (int item = q; item < kTok * (kBM / kHeadDim); item += 4) {
+    if (store) {
+        // all six warps take (token, head) items
+        for (int item = warp; item < kTok * (kBM / kHeadDim); item += kThreads / 32) {
             const int m = item >> 1, hh = item & 1;
             if (m >= a.M)
                 break;
             const uint32_t word = reinterpret_cast<const uint32_t *>(stg + m * kBM + hh * kHeadDim)[lane];
-            front_head(a, m, n0 + hh * kHeadDim, word, lane);
+            front_head(a, tk, m, n0 + hh * kHeadDim, word, lane);
             if (n0 == 0 && hh == 0 && lane == 0 && a.err != nullptr) {
                 // one count per token: the tile of column 0
-                const int64_t slot = a.slots != nullptr ? __ldg(a.slots + m) : -1;
+                const int64_t slot = a.slots != nullptr ? tk.slot[m] : -1;
                 bool bad = slot >= a.capacity;
                 if (a.cos_sin != nullptr) {
-                    const int64_t pos = __ldg(a.positions + m);
+                    const int64_t pos = tk.pos[m];
                     bad = bad || pos < 0 || pos >= a.max_position;
                 }
                 if (bad)
