@@ -236,6 +236,19 @@ def run_ours(args, w):
     launches_per_step = 2 + (1 if split else (0 if pair else (w.L + 7) // 8))
 
     whole = args.path == "whole"
+    variants = args.path == "variants"
+    if variants:
+        # the norm options and per-layer slot lengths: FP32 gains, the hidden
+        # gain scaling the input, a layer gain centre of 1, separate eps,
+        # layer l storing T - l * T / (2 L) rows
+        hw32 = None if hw is None else hw.float()
+        pw32 = None if pw is None else pw.float()
+        layer_rows = [w.T - l * (w.T // (2 * w.L)) for l in range(w.L)]
+
+    def norms_variant():
+        rc.context_norms_ex(x, w.L, hidden_w=hw32, pre_w=pw32, hidden_eps=w.eps,
+                            pre_eps=10.0 * w.eps, pre_center=1.0, hidden_input_scale=True,
+                            out=normed)
 
     def chain(ev=None):
         """One step through the public calls (ev[0] / ev[2] bracket it):
@@ -246,6 +259,10 @@ def run_ours(args, w):
             ev[0].record()
         if whole:
             rc.context_kv(x, hw, pw, W, w.H, positions, slots, cs, caches, w.eps, cws, err=err)
+        elif variants:
+            norms_variant()
+            rc.kv_project_store(normed, W, w.H, positions, slots, cs, caches, w.eps, rows=layer_rows,
+                                err=err, workspace=ws if split else None)
         else:
             rc.context_norms(x, hw, pw, w.L, w.eps, out=normed)
             rc.kv_project_store(normed, W, w.H, positions, slots, cs, caches, w.eps, err=err,
@@ -261,6 +278,11 @@ def run_ours(args, w):
             ev[1].record()
             rc.context_kv_from_rows(z, r2, pw, W, w.H, positions, slots, cs, caches, w.eps, err=err,
                                     workspace=ws if split else None)
+        elif variants:
+            norms_variant()
+            ev[1].record()
+            rc.kv_project_store(normed, W, w.H, positions, slots, cs, caches, w.eps, rows=layer_rows,
+                                err=err, kv_out=kv, workspace=ws if split else None)
         else:
             rc.context_norms(x, hw, pw, w.L, w.eps, out=normed)
             ev[1].record()
@@ -406,6 +428,8 @@ def run_ours(args, w):
 
     rows_bytes = 2 * w.T * w.D * 2 + 2 * w.D + 4 * w.T   # read x, write z, gains, r2
     fused_norms = whole and pair
+    if variants:                              # FP32 gains: 4 bytes per weight
+        counts["k1_bytes"] += 2 * w.D * ((1 if w.hidden_weighted else 0) + (w.L if w.pre_weighted else 0))
     kern = {
         "row_pass" if fused_norms else "norms": hbm_entry(rows_bytes if fused_norms else counts["k1_bytes"],
                                                           us(k1_ms)),
@@ -436,6 +460,9 @@ def run_ours(args, w):
     rec["config"]["timing"] = timing
     rec["config"]["path"] = ("rc_context_kv (row pass; projection forming the normed rows in shared "
                              "memory, store fused)" if whole else
+                             "rc_context_norms_ex (FP32 gains, hidden gain on the input, layer "
+                             "gain centre 1, separate eps) + rc_kv_project_store_rows (per-layer "
+                             "slot lengths)" if variants else
                              "rc_context_norms + rc_kv_project_store (projection with the store fused)")
     rec.update({
         "value": world * w.T * args.steps / (total_ms / 1e3),
@@ -635,9 +662,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--path", default="store", choices=["store", "whole", "front"],
-                    help="store: norms + fused projection/store; whole: rc_context_kv; "
-                         "front: the decode QKV front (rc_qkv_front)")
+    ap.add_argument("--path", default="store", choices=["store", "whole", "variants", "front"],
+                    help="store: norms + fused projection/store; whole: rc_context_kv; variants: "
+                         "the norm options and per-layer slot lengths; front: the decode QKV "
+                         "front (rc_qkv_front)")
     ap.add_argument("--tokens", type=int, default=16, choices=range(1, 17), metavar="1..16",
                     help="tokens of the decode QKV front (--path front)")
     args = ap.parse_args()

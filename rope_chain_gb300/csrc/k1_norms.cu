@@ -199,8 +199,6 @@ k1_row_prep(const uint16_t *__restrict__ x, const uint16_t *__restrict__ hidden_
 // k1_context_norms; the options are uniform over the grid, so the branches
 // on them do not diverge.
 
-constexpr int kVals = kFrags * 8;     // values per thread
-
 // Fragment k's 8 gains of weight row `row` (its columns 2048 k + 8 t + i).
 __device__ __forceinline__ void load_gains(const NormDesc &n, int64_t row, int k, int tid,
                                            float (&g)[8]) {
@@ -220,62 +218,77 @@ __device__ __forceinline__ void load_gains(const NormDesc &n, int64_t row, int k
     }
 }
 
-// Sum of squares of the row held as v (fragment-major), in the order of
-// row_sumsq.
-__device__ __forceinline__ float row_sumsq_f(const float (&v)[kVals], float *sums, int warp,
-                                             int lane) {
+// One fragment (8 values) of a norm's input: the packed bf16 values, times
+// the fragment's gains when the weight scales the input.
+__device__ __forceinline__ void norm_input(const uint4 &q, const NormDesc &n, int64_t wrow, int k,
+                                           int tid, float (&f)[8]) {
+    unpack8(q, f);
+    if (n.w != nullptr && n.input_scale) {
+        float g[8];
+        load_gains(n, wrow, k, tid, g);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            f[i] = __fmul_rn(g[i], f[i]);
+    }
+}
+
+// Inverse RMS of a norm of the row held packed in q: sum of squares of its
+// inputs in the order of row_sumsq (each thread's 32 values in (k, i)
+// order, an xor butterfly per warp, the 8 warp sums left to right), then
+// 1 / sqrt(fma(S, 2^-13, eps)).  `sums` alternates between two buffers so
+// that consecutive norms need one barrier each.
+__device__ __forceinline__ float norm_scale(const uint4 (&q)[kFrags], const NormDesc &n, int64_t wrow,
+                                            float (&sums)[2][kThreads / 32], int &buf, int tid,
+                                            int warp, int lane) {
     float p = 0.0f;
 #pragma unroll
-    for (int j = 0; j < kVals; ++j)
-        p = __fadd_rn(p, __fmul_rn(v[j], v[j]));
+    for (int k = 0; k < kFrags; ++k) {
+        float f[8];
+        norm_input(q[k], n, wrow, k, tid, f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            p = __fadd_rn(p, __fmul_rn(f[i], f[i]));
+    }
     p = warp_butterfly_sum(p);
     if (lane == 0)
-        sums[warp] = p;
+        sums[buf][warp] = p;
     __syncthreads();
-    float s = sums[0];
+    float s = sums[buf][0];
 #pragma unroll
     for (int w = 1; w < kThreads / 32; ++w)
-        s = __fadd_rn(s, sums[w]);
-    return s;
-}
-
-// One RMSNorm of the row in v, in place: an input-scale weight multiplies
-// first (gamma * v), then S, r = 1 / sqrt(fma(S, 2^-13, eps)), v * r, and an
-// output-scale weight multiplies last.  `sums` alternates between two
-// buffers so that consecutive norms need one barrier each.
-__device__ __forceinline__ void norm_row(float (&v)[kVals], const NormDesc &n, int64_t wrow,
-                                         float (&sums)[2][kThreads / 32], int &buf, int tid,
-                                         int warp, int lane) {
-    const bool weighted = n.w != nullptr;
-    const bool in_scale = weighted && n.input_scale;
-    if (in_scale) {
-#pragma unroll
-        for (int k = 0; k < kFrags; ++k) {
-            float g[8];
-            load_gains(n, wrow, k, tid, g);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                v[8 * k + i] = __fmul_rn(g[i], v[8 * k + i]);
-        }
-    }
-    const float r = inv_rms(row_sumsq_f(v, sums[buf], warp, lane), 0x1p-13f, n.eps);
+        s = __fadd_rn(s, sums[buf][w]);
     buf ^= 1;
-#pragma unroll
-    for (int k = 0; k < kFrags; ++k) {
-        float g[8];
-        if (weighted && !in_scale)
-            load_gains(n, wrow, k, tid, g);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float y = __fmul_rn(v[8 * k + i], r);
-            if (weighted && !in_scale)
-                y = __fmul_rn(y, g[i]);
-            v[8 * k + i] = y;
-        }
-    }
+    return inv_rms(s, 0x1p-13f, n.eps);
 }
 
-__global__ void __launch_bounds__(kThreads)
+// Fragment k of a norm's output: (input * r), times the gains when the
+// weight scales the output, packed to bf16.
+__device__ __forceinline__ uint4 norm_output(const uint4 &q, const NormDesc &n, int64_t wrow, int k,
+                                             int tid, float r) {
+    float f[8];
+    norm_input(q, n, wrow, k, tid, f);
+    const bool out_scale = n.w != nullptr && !n.input_scale;
+    float g[8];
+    if (out_scale)
+        load_gains(n, wrow, k, tid, g);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        f[i] = __fmul_rn(f[i], r);
+        if (out_scale)
+            f[i] = __fmul_rn(f[i], g[i]);
+    }
+    return pack8(f);
+}
+
+// Both norms with every option: each weight bf16, FP32 or absent, scaling
+// the norm's input (gamma * x, before the sum of squares) or its output,
+// a gain center added when non-zero, its own eps.  With an input-scale
+// layer weight the layers' inverse RMS differs per layer, so each layer
+// takes its own row sum.  Same thread mapping, order of sums and roundings
+// as k1_context_norms; the row stays packed and each fragment is formed on
+// its own (few live registers); the options are uniform over the grid, so
+// the branches on them do not diverge.
+__global__ void __launch_bounds__(kThreads, 4)
 k1_context_norms_ex(const uint16_t *__restrict__ x, int64_t T, const NormDesc hidden,
                     const NormDesc pre, int32_t L, uint16_t *__restrict__ out)
 {
@@ -287,58 +300,32 @@ k1_context_norms_ex(const uint16_t *__restrict__ x, int64_t T, const NormDesc hi
     pdl_wait();
 
     const uint4 *xr = reinterpret_cast<const uint4 *>(x) + row * (kHidden / 8);
-    float v[kVals];
+    uint4 q[kFrags];
 #pragma unroll
-    for (int k = 0; k < kFrags; ++k) {
-        float f[8];
-        unpack8(__ldcs(xr + k * kFragStride + tid), f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            v[8 * k + i] = f[i];
-    }
-    // a1: the hidden norm, rounded to bf16 (kept packed)
-    norm_row(v, hidden, 0, sums, buf, tid, warp, lane);
+    for (int k = 0; k < kFrags; ++k)
+        q[k] = __ldcs(xr + k * kFragStride + tid);
+    // a1: the hidden norm, rounded to bf16 (z kept packed in q)
+    const float r = norm_scale(q, hidden, 0, sums, buf, tid, warp, lane);
     uint4 z[kFrags];
 #pragma unroll
     for (int k = 0; k < kFrags; ++k)
-        z[k] = pack8(&v[8 * k]);
+        z[k] = norm_output(q[k], hidden, 0, k, tid, r);
 
     // a2: with an output-scale (or no) layer weight one inverse RMS serves
     // every layer
     const bool per_layer = pre.w != nullptr && pre.input_scale;
     float r2 = 0.0f;
     if (!per_layer) {
-#pragma unroll
-        for (int k = 0; k < kFrags; ++k)
-            unpack8(z[k], &v[8 * k]);
-        r2 = inv_rms(row_sumsq_f(v, sums[buf], warp, lane), 0x1p-13f, pre.eps);
-        buf ^= 1;
+        NormDesc plain = pre;
+        plain.w = nullptr;                       // the sum is of z itself
+        r2 = norm_scale(z, plain, 0, sums, buf, tid, warp, lane);
     }
     for (int32_t l = 0; l < L; ++l) {
-#pragma unroll
-        for (int k = 0; k < kFrags; ++k)
-            unpack8(z[k], &v[8 * k]);
-        if (per_layer) {
-            norm_row(v, pre, l, sums, buf, tid, warp, lane);
-        } else {
-#pragma unroll
-            for (int k = 0; k < kFrags; ++k) {
-                float g[8];
-                if (pre.w != nullptr)
-                    load_gains(pre, l, k, tid, g);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    float y = __fmul_rn(v[8 * k + i], r2);
-                    if (pre.w != nullptr)
-                        y = __fmul_rn(y, g[i]);
-                    v[8 * k + i] = y;
-                }
-            }
-        }
+        const float rl = per_layer ? norm_scale(z, pre, l, sums, buf, tid, warp, lane) : r2;
         uint4 *o = reinterpret_cast<uint4 *>(out) + ((int64_t)l * T + row) * (kHidden / 8);
 #pragma unroll
         for (int k = 0; k < kFrags; ++k)
-            o[k * kFragStride + tid] = pack8(&v[8 * k]);
+            o[k * kFragStride + tid] = norm_output(z[k], pre, l, k, tid, rl);
     }
 }
 
