@@ -21,6 +21,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kFrags = 4;             // 16-byte fragments per thread
 constexpr int kFragStride = 256;      // uint4 units between a thread's fragments
+constexpr int64_t kTwoRowsFrom = 16384;   // rows from which a CTA takes two
 
 __device__ __forceinline__ void unpack8(const uint4 &q, float *f) {
     f[0] = bf16_lo(q.x); f[1] = bf16_hi(q.x);
@@ -136,6 +137,134 @@ k1_context_norms(const uint16_t *__restrict__ x, int64_t T,
                     pq[k] = __ldg(gn + k * kFragStride + tid);
             }
             o[k * kFragStride + tid] = pack8(f);
+        }
+    }
+}
+
+// The same norms with two rows per CTA: each thread holds its 32 columns of
+// both rows, so every gain fragment is read once for the two rows (half the
+// gain traffic), and each row's sums keep row_sumsq's order.  Used when
+// there are enough rows to fill the GPU with half as many CTAs.
+template <bool kHiddenW, bool kPreW>
+__global__ void __launch_bounds__(kThreads, 2)
+k1_context_norms2(const uint16_t *__restrict__ x, int64_t T,
+                  const uint16_t *__restrict__ hidden_w, const uint16_t *__restrict__ pre_w,
+                  int32_t L, float hidden_eps, float pre_eps, uint16_t *__restrict__ out)
+{
+    __shared__ float sums[2][2][kThreads / 32];    // [norm][row of the pair][warp]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t row0 = 2 * (int64_t)blockIdx.x;
+    const bool two = row0 + 1 < T;
+    pdl_trigger();
+    pdl_wait();
+
+    const uint4 *xa = reinterpret_cast<const uint4 *>(x) + row0 * (kHidden / 8);
+    const uint4 *xb = xa + kHidden / 8;
+    const uint4 *gh = reinterpret_cast<const uint4 *>(hidden_w);
+    const uint4 *gp = reinterpret_cast<const uint4 *>(pre_w);
+    uint4 a[kFrags], b[kFrags], hq[kFrags], pq[kFrags];
+#pragma unroll
+    for (int k = 0; k < kFrags; ++k) {
+        a[k] = __ldcs(xa + k * kFragStride + tid);
+        b[k] = two ? __ldcs(xb + k * kFragStride + tid) : make_uint4(0, 0, 0, 0);
+        if (kHiddenW)
+            hq[k] = __ldg(gh + k * kFragStride + tid);
+    }
+
+    // one norm's inverse RMS for both rows, each in row_sumsq's order
+    auto pair_scale = [&](float (&sbuf)[2][kThreads / 32], float eps, float &ra, float &rb) {
+        float pa = 0.0f, pb = 0.0f;
+#pragma unroll
+        for (int k = 0; k < kFrags; ++k) {
+            float fa[8], fb[8];
+            unpack8(a[k], fa);
+            unpack8(b[k], fb);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                pa = __fadd_rn(pa, __fmul_rn(fa[i], fa[i]));
+                pb = __fadd_rn(pb, __fmul_rn(fb[i], fb[i]));
+            }
+        }
+        pa = warp_butterfly_sum(pa);
+        pb = warp_butterfly_sum(pb);
+        if (lane == 0) {
+            sbuf[0][warp] = pa;
+            sbuf[1][warp] = pb;
+        }
+        __syncthreads();
+        float sa = sbuf[0][0], sb = sbuf[1][0];
+#pragma unroll
+        for (int w = 1; w < kThreads / 32; ++w) {
+            sa = __fadd_rn(sa, sbuf[0][w]);
+            sb = __fadd_rn(sb, sbuf[1][w]);
+        }
+        ra = inv_rms(sa, 0x1p-13f, eps);
+        rb = inv_rms(sb, 0x1p-13f, eps);
+    };
+
+    // a1: hidden norm; z = bf16((x * r) * gamma) kept packed in a and b
+    float ra, rb;
+    pair_scale(sums[0], hidden_eps, ra, rb);
+#pragma unroll
+    for (int k = 0; k < kFrags; ++k) {
+        float fa[8], fb[8];
+        unpack8(a[k], fa);
+        unpack8(b[k], fb);
+        if (kHiddenW) {
+            float g[8];
+            unpack8(hq[k], g);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                fa[i] = __fmul_rn(__fmul_rn(fa[i], ra), g[i]);
+                fb[i] = __fmul_rn(__fmul_rn(fb[i], rb), g[i]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                fa[i] = __fmul_rn(fa[i], ra);
+                fb[i] = __fmul_rn(fb[i], rb);
+            }
+        }
+        a[k] = pack8(fa);
+        b[k] = pack8(fb);
+    }
+    if (kPreW) {
+#pragma unroll
+        for (int k = 0; k < kFrags; ++k)
+            pq[k] = __ldg(gp + k * kFragStride + tid);
+    }
+
+    // a2: the layers' input norms share one inverse RMS per row
+    float r2a, r2b;
+    pair_scale(sums[1], pre_eps, r2a, r2b);
+    for (int32_t l = 0; l < L; ++l) {
+        uint4 *oa = reinterpret_cast<uint4 *>(out) + ((int64_t)l * T + row0) * (kHidden / 8);
+        uint4 *ob = oa + kHidden / 8;
+        const uint4 *gn = gp + (int64_t)(l + 1) * (kHidden / 8);
+#pragma unroll
+        for (int k = 0; k < kFrags; ++k) {
+            float fa[8], fb[8];
+            unpack8(a[k], fa);
+            unpack8(b[k], fb);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                fa[i] = __fmul_rn(fa[i], r2a);
+                fb[i] = __fmul_rn(fb[i], r2b);
+            }
+            if (kPreW) {
+                float g[8];
+                unpack8(pq[k], g);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    fa[i] = __fmul_rn(fa[i], g[i]);
+                    fb[i] = __fmul_rn(fb[i], g[i]);
+                }
+                if (l + 1 < L)                   // this fragment's gains for the next layer
+                    pq[k] = __ldg(gn + k * kFragStride + tid);
+            }
+            oa[k * kFragStride + tid] = pack8(fa);
+            if (two)
+                ob[k * kFragStride + tid] = pack8(fb);
         }
     }
 }
@@ -343,7 +472,22 @@ cudaError_t launch_context_norms(const uint16_t *x, int64_t T, const uint16_t *h
                                  const uint16_t *pre_w, int32_t L, float hidden_eps, float pre_eps,
                                  uint16_t *out, cudaStream_t stream)
 {
-    const dim3 grid((unsigned)T), block(kThreads);
+    const dim3 block(kThreads);
+    if (T >= kTwoRowsFrom) {                       // two rows per CTA
+        const dim3 grid2((unsigned)((T + 1) / 2));
+        if (hidden_w && pre_w)
+            return launch_pdl(k1_context_norms2<true, true>, grid2, block, 0, stream, 1, x, T,
+                              hidden_w, pre_w, L, hidden_eps, pre_eps, out);
+        if (hidden_w)
+            return launch_pdl(k1_context_norms2<true, false>, grid2, block, 0, stream, 1, x, T,
+                              hidden_w, pre_w, L, hidden_eps, pre_eps, out);
+        if (pre_w)
+            return launch_pdl(k1_context_norms2<false, true>, grid2, block, 0, stream, 1, x, T,
+                              hidden_w, pre_w, L, hidden_eps, pre_eps, out);
+        return launch_pdl(k1_context_norms2<false, false>, grid2, block, 0, stream, 1, x, T,
+                          hidden_w, pre_w, L, hidden_eps, pre_eps, out);
+    }
+    const dim3 grid((unsigned)T);
     if (hidden_w && pre_w)
         return launch_pdl(k1_context_norms<true, true>, grid, block, 0, stream, 1, x, T, hidden_w,
                           pre_w, L, hidden_eps, pre_eps, out);
