@@ -22,6 +22,7 @@ constexpr int kThreads = 256;
 constexpr int kFrags = 4;             // 16-byte fragments per thread
 constexpr int kFragStride = 256;      // uint4 units between a thread's fragments
 constexpr int64_t kTwoRowsFrom = 16384;   // rows from which a CTA takes two
+constexpr int64_t kExTwoRowsFrom = 16384; // the same for the norm-options kernel
 
 __device__ __forceinline__ void unpack8(const uint4 &q, float *f) {
     f[0] = bf16_lo(q.x); f[1] = bf16_hi(q.x);
@@ -347,66 +348,82 @@ __device__ __forceinline__ void load_gains(const NormDesc &n, int64_t row, int k
     }
 }
 
-// One fragment (8 values) of a norm's input: the packed bf16 values, times
-// the fragment's gains when the weight scales the input.
-__device__ __forceinline__ void norm_input(const uint4 &q, const NormDesc &n, int64_t wrow, int k,
-                                           int tid, float (&f)[8]) {
-    unpack8(q, f);
-    if (n.w != nullptr && n.input_scale) {
-        float g[8];
-        load_gains(n, wrow, k, tid, g);
+// Inverse RMS of one norm of R rows held packed in q (row j in q[j]): the
+// sum of squares of each row's inputs (the packed bf16 values, times the
+// gains when the weight scales the input) in the order of row_sumsq -- each
+// thread's 32 values in (k, i) order, an xor butterfly per warp, the 8 warp
+// sums left to right -- then 1 / sqrt(fma(S, 2^-13, eps)).  Each gain
+// fragment is loaded once for the R rows.  `sums` alternates between two
+// buffers so that consecutive norms need one barrier each.
+template <int R>
+__device__ __forceinline__ void norm_scale(const uint4 (&q)[R][kFrags], const NormDesc &n,
+                                           int64_t wrow, float (&sums)[2][R][kThreads / 32],
+                                           int &buf, int tid, int warp, int lane, float (&r)[R]) {
+    const bool in_scale = n.w != nullptr && n.input_scale;
+    float p[R];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            f[i] = __fmul_rn(g[i], f[i]);
-    }
-}
-
-// Inverse RMS of a norm of the row held packed in q: sum of squares of its
-// inputs in the order of row_sumsq (each thread's 32 values in (k, i)
-// order, an xor butterfly per warp, the 8 warp sums left to right), then
-// 1 / sqrt(fma(S, 2^-13, eps)).  `sums` alternates between two buffers so
-// that consecutive norms need one barrier each.
-__device__ __forceinline__ float norm_scale(const uint4 (&q)[kFrags], const NormDesc &n, int64_t wrow,
-                                            float (&sums)[2][kThreads / 32], int &buf, int tid,
-                                            int warp, int lane) {
-    float p = 0.0f;
+    for (int j = 0; j < R; ++j)
+        p[j] = 0.0f;
 #pragma unroll
     for (int k = 0; k < kFrags; ++k) {
-        float f[8];
-        norm_input(q[k], n, wrow, k, tid, f);
+        float g[8];
+        if (in_scale)
+            load_gains(n, wrow, k, tid, g);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            p = __fadd_rn(p, __fmul_rn(f[i], f[i]));
+        for (int j = 0; j < R; ++j) {
+            float f[8];
+            unpack8(q[j][k], f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (in_scale)
+                    f[i] = __fmul_rn(g[i], f[i]);
+                p[j] = __fadd_rn(p[j], __fmul_rn(f[i], f[i]));
+            }
+        }
     }
-    p = warp_butterfly_sum(p);
-    if (lane == 0)
-        sums[buf][warp] = p;
-    __syncthreads();
-    float s = sums[buf][0];
 #pragma unroll
-    for (int w = 1; w < kThreads / 32; ++w)
-        s = __fadd_rn(s, sums[buf][w]);
+    for (int j = 0; j < R; ++j) {
+        p[j] = warp_butterfly_sum(p[j]);
+        if (lane == 0)
+            sums[buf][j][warp] = p[j];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        float s = sums[buf][j][0];
+#pragma unroll
+        for (int w = 1; w < kThreads / 32; ++w)
+            s = __fadd_rn(s, sums[buf][j][w]);
+        r[j] = inv_rms(s, 0x1p-13f, n.eps);
+    }
     buf ^= 1;
-    return inv_rms(s, 0x1p-13f, n.eps);
 }
 
-// Fragment k of a norm's output: (input * r), times the gains when the
-// weight scales the output, packed to bf16.
-__device__ __forceinline__ uint4 norm_output(const uint4 &q, const NormDesc &n, int64_t wrow, int k,
-                                             int tid, float r) {
-    float f[8];
-    norm_input(q, n, wrow, k, tid, f);
-    const bool out_scale = n.w != nullptr && !n.input_scale;
+// Fragment k of one norm's output for R rows: (input * r), times the gains
+// when the weight scales the output, packed to bf16 (the gain fragment read
+// once for the R rows).
+template <int R>
+__device__ __forceinline__ void norm_output(const uint4 (&q)[R][kFrags], const NormDesc &n,
+                                            int64_t wrow, int k, int tid, const float (&r)[R],
+                                            uint4 (&o)[R]) {
+    const bool weighted = n.w != nullptr;
     float g[8];
-    if (out_scale)
+    if (weighted)
         load_gains(n, wrow, k, tid, g);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        f[i] = __fmul_rn(f[i], r);
-        if (out_scale)
-            f[i] = __fmul_rn(f[i], g[i]);
+    for (int j = 0; j < R; ++j) {
+        float f[8];
+        unpack8(q[j][k], f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (weighted && n.input_scale)
+                f[i] = __fmul_rn(g[i], f[i]);
+            f[i] = __fmul_rn(f[i], r[j]);
+            if (weighted && !n.input_scale)
+                f[i] = __fmul_rn(f[i], g[i]);
+        }
+        o[j] = pack8(f);
     }
-    return pack8(f);
 }
 
 // Both norms with every option: each weight bf16, FP32 or absent, scaling
@@ -414,47 +431,108 @@ __device__ __forceinline__ uint4 norm_output(const uint4 &q, const NormDesc &n, 
 // a gain center added when non-zero, its own eps.  With an input-scale
 // layer weight the layers' inverse RMS differs per layer, so each layer
 // takes its own row sum.  Same thread mapping, order of sums and roundings
-// as k1_context_norms; the row stays packed and each fragment is formed on
-// its own (few live registers); the options are uniform over the grid, so
-// the branches on them do not diverge.
-__global__ void __launch_bounds__(kThreads, 4)
+// as k1_context_norms; R rows per CTA (two for large T: each gain fragment
+// is then read once for both rows); the rows stay packed and each fragment
+// is formed on its own (few live registers); the options are uniform over
+// the grid, so the branches on them do not diverge.
+template <int R>
+__global__ void __launch_bounds__(kThreads, R == 1 ? 4 : 2)
 k1_context_norms_ex(const uint16_t *__restrict__ x, int64_t T, const NormDesc hidden,
                     const NormDesc pre, int32_t L, uint16_t *__restrict__ out)
 {
-    __shared__ float sums[2][kThreads / 32];
+    __shared__ float sums[2][R][kThreads / 32];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t row = blockIdx.x;
+    const int64_t row0 = (int64_t)blockIdx.x * R;
     int buf = 0;
     pdl_trigger();
     pdl_wait();
 
-    const uint4 *xr = reinterpret_cast<const uint4 *>(x) + row * (kHidden / 8);
-    uint4 q[kFrags];
+    uint4 q[R][kFrags];
 #pragma unroll
-    for (int k = 0; k < kFrags; ++k)
-        q[k] = __ldcs(xr + k * kFragStride + tid);
-    // a1: the hidden norm, rounded to bf16 (z kept packed in q)
-    const float r = norm_scale(q, hidden, 0, sums, buf, tid, warp, lane);
-    uint4 z[kFrags];
+    for (int j = 0; j < R; ++j) {
+        const bool live = row0 + j < T;             // a missing last row reads as zeros
+        const uint4 *xr = reinterpret_cast<const uint4 *>(x) + (row0 + j) * (kHidden / 8);
 #pragma unroll
-    for (int k = 0; k < kFrags; ++k)
-        z[k] = norm_output(q[k], hidden, 0, k, tid, r);
+        for (int k = 0; k < kFrags; ++k)
+            q[j][k] = live ? __ldcs(xr + k * kFragStride + tid) : make_uint4(0, 0, 0, 0);
+    }
+    // a1: the hidden norm, rounded to bf16 (z kept packed)
+    float r[R];
+    norm_scale<R>(q, hidden, 0, sums, buf, tid, warp, lane, r);
+    uint4 z[R][kFrags];
+#pragma unroll
+    for (int k = 0; k < kFrags; ++k) {
+        uint4 o[R];
+        norm_output<R>(q, hidden, 0, k, tid, r, o);
+#pragma unroll
+        for (int j = 0; j < R; ++j)
+            z[j][k] = o[j];
+    }
 
     // a2: with an output-scale (or no) layer weight one inverse RMS serves
     // every layer
     const bool per_layer = pre.w != nullptr && pre.input_scale;
-    float r2 = 0.0f;
+    float r2[R];
     if (!per_layer) {
         NormDesc plain = pre;
         plain.w = nullptr;                       // the sum is of z itself
-        r2 = norm_scale(z, plain, 0, sums, buf, tid, warp, lane);
+        norm_scale<R>(z, plain, 0, sums, buf, tid, warp, lane, r2);
     }
-    for (int32_t l = 0; l < L; ++l) {
-        const float rl = per_layer ? norm_scale(z, pre, l, sums, buf, tid, warp, lane) : r2;
-        uint4 *o = reinterpret_cast<uint4 *>(out) + ((int64_t)l * T + row) * (kHidden / 8);
+    if (per_layer || R == 1) {
+        // each layer's fragment gains read where they are used (with one row
+        // per CTA this keeps the registers, and so the occupancy, of the
+        // plain kernel)
+        for (int32_t l = 0; l < L; ++l) {
+            float rl[R];
+            if (per_layer) {
+                norm_scale<R>(z, pre, l, sums, buf, tid, warp, lane, rl);
+            } else {
+#pragma unroll
+                for (int j = 0; j < R; ++j)
+                    rl[j] = r2[j];
+            }
+#pragma unroll
+            for (int k = 0; k < kFrags; ++k) {
+                uint4 o[R];
+                norm_output<R>(z, pre, l, k, tid, rl, o);
+#pragma unroll
+                for (int j = 0; j < R; ++j)
+                    if (row0 + j < T)
+                        reinterpret_cast<uint4 *>(out)[((int64_t)l * T + row0 + j) * (kHidden / 8) +
+                                                       k * kFragStride + tid] = o[j];
+            }
+        }
+        return;
+    }
+    // two rows, output-scale (or no) layer weight: (z * r2) * gamma_l, each
+    // fragment's gains for layer l + 1 fetched while layer l is stored
+    const bool weighted = pre.w != nullptr;
+    float g[kFrags][8];
+    if (weighted) {
 #pragma unroll
         for (int k = 0; k < kFrags; ++k)
-            o[k * kFragStride + tid] = norm_output(z[k], pre, l, k, tid, rl);
+            load_gains(pre, 0, k, tid, g[k]);
+    }
+    for (int32_t l = 0; l < L; ++l) {
+#pragma unroll
+        for (int k = 0; k < kFrags; ++k) {
+#pragma unroll
+            for (int j = 0; j < R; ++j) {
+                float f[8];
+                unpack8(z[j][k], f);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    f[i] = __fmul_rn(f[i], r2[j]);
+                    if (weighted)
+                        f[i] = __fmul_rn(f[i], g[k][i]);
+                }
+                if (row0 + j < T)
+                    reinterpret_cast<uint4 *>(out)[((int64_t)l * T + row0 + j) * (kHidden / 8) +
+                                                   k * kFragStride + tid] = pack8(f);
+            }
+            if (weighted && l + 1 < L)
+                load_gains(pre, l + 1, k, tid, g[k]);
+        }
     }
 }
 
@@ -464,7 +542,10 @@ cudaError_t launch_context_norms_ex(const uint16_t *x, int64_t T, const NormDesc
                                     const NormDesc &pre, int32_t L, uint16_t *out,
                                     cudaStream_t stream)
 {
-    return launch_pdl(k1_context_norms_ex, dim3((unsigned)T), dim3(kThreads), 0, stream, 1, x, T,
+    if (T >= kExTwoRowsFrom)                     // two rows per CTA
+        return launch_pdl(k1_context_norms_ex<2>, dim3((unsigned)((T + 1) / 2)), dim3(kThreads), 0,
+                          stream, 1, x, T, hidden, pre, L, out);
+    return launch_pdl(k1_context_norms_ex<1>, dim3((unsigned)T), dim3(kThreads), 0, stream, 1, x, T,
                       hidden, pre, L, out);
 }
 
