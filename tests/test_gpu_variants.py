@@ -177,6 +177,7 @@ def test_store_per_layer_rows(T, L, H, rows):
 
 @pytest.mark.parametrize("T,L,H,workspace,rows", [
     (300, 3, 8, False, [300, 120, 0]),       # CTA pairs, epilogue store
+    (300, 9, 2, False, [300, 299, 1, 150, 0, 64, 65, 300, 7]),   # persistent pairs, 9 layers
     (512, 3, 8, True, [1, 512, 400]),        # CTA pairs, split-K, reduce-and-store
     (100, 2, 1, False, [100, 3]),            # single CTAs: kv_out, then the store kernel
     (257, 10, 2, True, [257, 0, 5, 256, 100, 1, 2, 3, 250, 257]),
