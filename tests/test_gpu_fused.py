@@ -80,7 +80,7 @@ def check(case, normed, W, *, workspace, rows=None, layout=rc.RC_W_KN, slots=Non
     (512, 3, 8, False, True),      # CTA pairs, epilogue store
     (512, 3, 8, True, True),       # CTA pairs, split-K, reduce-and-store
     (256, 3, 8, True, True),       # CTA pairs, 6 splits
-    (200, 1, 2, True, False),      # CTA pairs, 32 splits of 4 K blocks, ragged rows
+    (200, 1, 2, True, False),      # CTA pairs, 16 splits of 8 K blocks, ragged rows
     (200, 2, 16, False, False),    # CTA pairs, epilogue store, no RoPE
     (1000, 10, 4, False, True),    # persistent pairs: 80 tiles over at most 76 pairs (both accumulators)
     (129, 1, 32, True, True),      # H = 32, ragged rows

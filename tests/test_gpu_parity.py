@@ -102,7 +102,7 @@ def test_projection_within_two_ulp(T, L, D, H, layout, split):
 
 @pytest.mark.parametrize("L,T,H,layout", [(3, 100, 1, rc.RC_W_KN),    # single CTA, workspace
                                            (3, 512, 8, rc.RC_W_NK),    # CTA pairs, cluster split-K
-                                           (1, 64, 8, rc.RC_W_KN)])    # single CTA, 32 splits
+                                           (1, 64, 8, rc.RC_W_KN)])    # single CTA, 16 splits
 def test_projection_repeated_calls_identical(L, T, H, layout):
     # one workspace (when the plan uses one), three calls in a row: identical
     # results within the 2-ulp rule, i.e. nothing a call leaves behind
