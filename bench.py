@@ -455,6 +455,8 @@ def run_ours(args, w):
     oracle.build()
     R = cpu_sample_rows(w)
     cpu_s = oracle_chain_rows(case, w, R)
+    R1 = min(w.T, 32)
+    cpu1_s = oracle_chain_rows(case, w, R1, threads=1)
     rec = base_record(args, w, world)
     rec["config"]["l2"] = "flushed (512 MiB write) before every timed step"
     rec["config"]["timing"] = timing
@@ -470,7 +472,9 @@ def run_ours(args, w):
         "roofline": roof,
         "kernels": kern,
         "cpu_baseline": {"value": R / cpu_s, "unit": "rows/s", "cores": oracle.max_threads(),
-                         "kind": "oracle", "sample": f"first {R} rows of the workload, whole chain, once"},
+                         "kind": "oracle", "sample": f"first {R} rows of the workload, whole chain, once",
+                         "one_core": {"value": R1 / cpu1_s, "unit": "rows/s", "cores": 1,
+                                      "sample": f"first {R1} rows, whole chain, once"}},
         "e2e": {"value": world * w.T * args.steps / (e2e_ms / 1e3), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4, "timing": timing},
         "gpu_launches": launches_per_step * args.steps,
