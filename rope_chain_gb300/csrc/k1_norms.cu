@@ -22,7 +22,7 @@ constexpr int kThreads = 256;
 constexpr int kFrags = 4;             // 16-byte fragments per thread
 constexpr int kFragStride = 256;      // uint4 units between a thread's fragments
 constexpr int64_t kTwoRowsFrom = 16384;   // rows from which a CTA takes two
-constexpr int64_t kExTwoRowsFrom = 16384; // the same for the norm-options kernel
+constexpr int64_t kExTwoRowsFrom = 16384; // the same for the norm-options kernel (weights staged)
 
 __device__ __forceinline__ void unpack8(const uint4 &q, float *f) {
     f[0] = bf16_lo(q.x); f[1] = bf16_hi(q.x);
@@ -431,12 +431,12 @@ __device__ __forceinline__ void norm_output(const uint4 (&q)[R][kFrags], const N
 // a gain center added when non-zero, its own eps.  With an input-scale
 // layer weight the layers' inverse RMS differs per layer, so each layer
 // takes its own row sum.  Same thread mapping, order of sums and roundings
-// as k1_context_norms; R rows per CTA (two for large T: each gain fragment
-// is then read once for both rows); the rows stay packed and each fragment
-// is formed on its own (few live registers); the options are uniform over
-// the grid, so the branches on them do not diverge.
+// as k1_context_norms; R rows per CTA (run with one; the helpers take R for
+// the staged kernel below); the rows stay packed and each fragment is formed
+// on its own (few live registers); the options are uniform over the grid,
+// so the branches on them do not diverge.
 template <int R>
-__global__ void __launch_bounds__(kThreads, R == 1 ? 4 : 2)
+__global__ void __launch_bounds__(kThreads, 4)
 k1_context_norms_ex(const uint16_t *__restrict__ x, int64_t T, const NormDesc hidden,
                     const NormDesc pre, int32_t L, uint16_t *__restrict__ out)
 {
@@ -478,62 +478,244 @@ k1_context_norms_ex(const uint16_t *__restrict__ x, int64_t T, const NormDesc hi
         plain.w = nullptr;                       // the sum is of z itself
         norm_scale<R>(z, plain, 0, sums, buf, tid, warp, lane, r2);
     }
-    if (per_layer || R == 1) {
-        // each layer's fragment gains read where they are used (with one row
-        // per CTA this keeps the registers, and so the occupancy, of the
-        // plain kernel)
-        for (int32_t l = 0; l < L; ++l) {
-            float rl[R];
-            if (per_layer) {
-                norm_scale<R>(z, pre, l, sums, buf, tid, warp, lane, rl);
-            } else {
-#pragma unroll
-                for (int j = 0; j < R; ++j)
-                    rl[j] = r2[j];
-            }
-#pragma unroll
-            for (int k = 0; k < kFrags; ++k) {
-                uint4 o[R];
-                norm_output<R>(z, pre, l, k, tid, rl, o);
-#pragma unroll
-                for (int j = 0; j < R; ++j)
-                    if (row0 + j < T)
-                        reinterpret_cast<uint4 *>(out)[((int64_t)l * T + row0 + j) * (kHidden / 8) +
-                                                       k * kFragStride + tid] = o[j];
-            }
-        }
-        return;
-    }
-    // two rows, output-scale (or no) layer weight: (z * r2) * gamma_l, each
-    // fragment's gains for layer l + 1 fetched while layer l is stored
-    const bool weighted = pre.w != nullptr;
-    float g[kFrags][8];
-    if (weighted) {
-#pragma unroll
-        for (int k = 0; k < kFrags; ++k)
-            load_gains(pre, 0, k, tid, g[k]);
-    }
+    // each layer's fragment gains read where they are used (this keeps the
+    // registers, and so the occupancy, of the plain kernel)
     for (int32_t l = 0; l < L; ++l) {
+        float rl[R];
+        if (per_layer) {
+            norm_scale<R>(z, pre, l, sums, buf, tid, warp, lane, rl);
+        } else {
+#pragma unroll
+            for (int j = 0; j < R; ++j)
+                rl[j] = r2[j];
+        }
 #pragma unroll
         for (int k = 0; k < kFrags; ++k) {
+            uint4 o[R];
+            norm_output<R>(z, pre, l, k, tid, rl, o);
 #pragma unroll
-            for (int j = 0; j < R; ++j) {
-                float f[8];
-                unpack8(z[j][k], f);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    f[i] = __fmul_rn(f[i], r2[j]);
-                    if (weighted)
-                        f[i] = __fmul_rn(f[i], g[k][i]);
-                }
+            for (int j = 0; j < R; ++j)
                 if (row0 + j < T)
                     reinterpret_cast<uint4 *>(out)[((int64_t)l * T + row0 + j) * (kHidden / 8) +
-                                                   k * kFragStride + tid] = pack8(f);
-            }
-            if (weighted && l + 1 < L)
-                load_gains(pre, l + 1, k, tid, g[k]);
+                                                   k * kFragStride + tid] = o[j];
         }
     }
+}
+
+// ---- the same kernel with each weight row staged in shared memory
+//
+// With FP32 gains a layer's weight row is 32 KiB, and L of them do not stay
+// in L1, so reading each fragment's gains from global memory once per CTA
+// costs as much L2 traffic as the rows themselves.  Here the CTA copies each
+// weight row into shared memory once (cp.async, two buffers: the next
+// layer's row lands while this layer is stored) and R rows share it; no gain
+// is held in registers across the layer loop.  Same arithmetic and order.
+
+constexpr int kGainBytes = kHidden * 4;          // one FP32 weight row
+
+// Start copying weight row `row` of n into dst (a no-op without a weight);
+// always commits one group, so the group count is the same for every option.
+__device__ __forceinline__ void stage_gains(const NormDesc &n, int64_t row, uint8_t *dst, int tid) {
+    if (n.w != nullptr) {
+        const int bytes = n.fp32 ? kHidden * 4 : kHidden * 2;
+        const uint8_t *src = static_cast<const uint8_t *>(n.w) + row * bytes;
+        for (int o = 16 * tid; o < bytes; o += 16 * kThreads) {
+            const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst + o));
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src + o) : "memory");
+        }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void staged_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Fragment k's 8 gains (columns 2048 k + 8 t + i) from a staged weight row.
+__device__ __forceinline__ void smem_gains(const NormDesc &n, const uint8_t *row, int k, int tid,
+                                           float (&g)[8]) {
+    const int col = k * 2048 + 8 * tid;
+    if (n.fp32) {
+        const float4 *p = reinterpret_cast<const float4 *>(row) + col / 4;
+        const float4 a = p[0], b = p[1];
+        g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w;
+        g[4] = b.x; g[5] = b.y; g[6] = b.z; g[7] = b.w;
+    } else {
+        unpack8(*reinterpret_cast<const uint4 *>(row + 2 * col), g);
+    }
+    if (n.center != 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            g[i] = __fadd_rn(g[i], n.center);
+    }
+}
+
+// norm_scale with the weight row (when the weight scales the input) staged.
+template <int R>
+__device__ __forceinline__ void staged_scale(const uint4 (&q)[R][kFrags], const NormDesc &n,
+                                             const uint8_t *grow, float (&sums)[2][R][kThreads / 32],
+                                             int &buf, int tid, int warp, int lane, float (&r)[R]) {
+    const bool in_scale = n.w != nullptr && n.input_scale;
+    float p[R];
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+        p[j] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kFrags; ++k) {
+        float g[8];
+        if (in_scale)
+            smem_gains(n, grow, k, tid, g);
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            float f[8];
+            unpack8(q[j][k], f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (in_scale)
+                    f[i] = __fmul_rn(g[i], f[i]);
+                p[j] = __fadd_rn(p[j], __fmul_rn(f[i], f[i]));
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        p[j] = warp_butterfly_sum(p[j]);
+        if (lane == 0)
+            sums[buf][j][warp] = p[j];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        float s = sums[buf][j][0];
+#pragma unroll
+        for (int w = 1; w < kThreads / 32; ++w)
+            s = __fadd_rn(s, sums[buf][j][w]);
+        r[j] = inv_rms(s, 0x1p-13f, n.eps);
+    }
+    buf ^= 1;
+}
+
+// norm_output with the weight row staged.
+template <int R>
+__device__ __forceinline__ void staged_output(const uint4 (&q)[R][kFrags], const NormDesc &n,
+                                              const uint8_t *grow, int k, int tid, const float (&r)[R],
+                                              uint4 (&o)[R]) {
+    const bool weighted = n.w != nullptr;
+    float g[8];
+    if (weighted)
+        smem_gains(n, grow, k, tid, g);
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        float f[8];
+        unpack8(q[j][k], f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (weighted && n.input_scale)
+                f[i] = __fmul_rn(g[i], f[i]);
+            f[i] = __fmul_rn(f[i], r[j]);
+            if (weighted && !n.input_scale)
+                f[i] = __fmul_rn(f[i], g[i]);
+        }
+        o[j] = pack8(f);
+    }
+}
+
+// Buffer 0 holds the hidden weight, then layers 1, 3, ...; buffer 1 layers
+// 0, 2, ...  Copy groups: [hidden], [layer 0], then one per later layer,
+// issued at the top of the previous layer once every thread is past the
+// buffer's last reader (the barrier after the wait).
+template <int R>
+__global__ void __launch_bounds__(kThreads, 2)
+k1_context_norms_exs(const uint16_t *__restrict__ x, int64_t T, const NormDesc hidden,
+                     const NormDesc pre, int32_t L, uint16_t *__restrict__ out)
+{
+    extern __shared__ __align__(16) uint8_t gstage[];   // [2][kGainBytes]
+    __shared__ float sums[2][R][kThreads / 32];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t row0 = (int64_t)blockIdx.x * R;
+    int buf = 0;
+    pdl_trigger();
+    pdl_wait();
+    stage_gains(hidden, 0, gstage, tid);
+    stage_gains(pre, 0, gstage + kGainBytes, tid);
+
+    uint4 q[R][kFrags];
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        const bool live = row0 + j < T;             // missing last rows read as zeros
+        const uint4 *xr = reinterpret_cast<const uint4 *>(x) + (row0 + j) * (kHidden / 8);
+#pragma unroll
+        for (int k = 0; k < kFrags; ++k)
+            q[j][k] = live ? __ldcs(xr + k * kFragStride + tid) : make_uint4(0, 0, 0, 0);
+    }
+    staged_wait<1>();                               // the hidden weight (this thread's part)
+    __syncthreads();
+    // a1: the hidden norm, rounded to bf16 (z kept packed, in place of x)
+    float r[R];
+    staged_scale<R>(q, hidden, gstage, sums, buf, tid, warp, lane, r);
+#pragma unroll
+    for (int k = 0; k < kFrags; ++k) {
+        uint4 o[R];
+        staged_output<R>(q, hidden, gstage, k, tid, r, o);
+#pragma unroll
+        for (int j = 0; j < R; ++j)
+            q[j][k] = o[j];
+    }
+    // a2: one inverse RMS for every layer unless the layer weight scales the input
+    const bool per_layer = pre.w != nullptr && pre.input_scale;
+    float r2[R];
+    if (!per_layer) {
+        NormDesc plain = pre;
+        plain.w = nullptr;                          // the sum is of z itself
+        staged_scale<R>(q, plain, nullptr, sums, buf, tid, warp, lane, r2);
+    }
+    for (int32_t l = 0; l < L; ++l) {
+        staged_wait<0>();                           // layer l's row (this thread's part)
+        __syncthreads();                            // ... everyone's; the other buffer is free
+        if (l + 1 < L)
+            stage_gains(pre, l + 1, gstage + ((l + 2) & 1) * kGainBytes, tid);
+        const uint8_t *grow = gstage + ((l + 1) & 1) * kGainBytes;
+        float rl[R];
+        if (per_layer) {
+            staged_scale<R>(q, pre, grow, sums, buf, tid, warp, lane, rl);
+        } else {
+#pragma unroll
+            for (int j = 0; j < R; ++j)
+                rl[j] = r2[j];
+        }
+#pragma unroll
+        for (int k = 0; k < kFrags; ++k) {
+            uint4 o[R];
+            staged_output<R>(q, pre, grow, k, tid, rl, o);
+#pragma unroll
+            for (int j = 0; j < R; ++j)
+                if (row0 + j < T)
+                    reinterpret_cast<uint4 *>(out)[((int64_t)l * T + row0 + j) * (kHidden / 8) +
+                                                   k * kFragStride + tid] = o[j];
+        }
+    }
+    staged_wait<0>();                               // no copy outlives the CTA
+}
+
+template <int R>
+cudaError_t launch_exs(const uint16_t *x, int64_t T, const NormDesc &hidden, const NormDesc &pre,
+                       int32_t L, uint16_t *out, cudaStream_t stream) {
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(k1_context_norms_exs<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 2 * kGainBytes);
+        if (e != cudaSuccess)
+            return e;
+        if (dev < 64)
+            configured[dev] = true;
+    }
+    return launch_pdl(k1_context_norms_exs<R>, dim3((unsigned)((T + R - 1) / R)), dim3(kThreads),
+                      (size_t)(2 * kGainBytes), stream, 1, x, T, hidden, pre, L, out);
 }
 
 }  // namespace
@@ -542,9 +724,8 @@ cudaError_t launch_context_norms_ex(const uint16_t *x, int64_t T, const NormDesc
                                     const NormDesc &pre, int32_t L, uint16_t *out,
                                     cudaStream_t stream)
 {
-    if (T >= kExTwoRowsFrom)                     // two rows per CTA
-        return launch_pdl(k1_context_norms_ex<2>, dim3((unsigned)((T + 1) / 2)), dim3(kThreads), 0,
-                          stream, 1, x, T, hidden, pre, L, out);
+    if (T >= kExTwoRowsFrom)                     // two rows per CTA, weights staged
+        return launch_exs<2>(x, T, hidden, pre, L, out, stream);
     return launch_pdl(k1_context_norms_ex<1>, dim3((unsigned)T), dim3(kThreads), 0, stream, 1, x, T,
                       hidden, pre, L, out);
 }

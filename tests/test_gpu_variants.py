@@ -89,6 +89,32 @@ def test_norm_variants_shapes(T, L):
     assert np.array_equal(parity.host_bits(out), ref)
 
 
+@pytest.mark.parametrize("T", [4099, 16387])
+@pytest.mark.parametrize("hidden,pre,center", [
+    (("f32", True), ("f32", False), 1.0),     # one r for every layer, FP32 gains staged
+    (("bf16", False), ("f32", True), 0.0),    # input-scale layer weight: r per layer
+    (("none", False), ("bf16", False), -0.5),
+    (("none", False), ("none", False), 0.0),
+])
+def test_norm_variants_many_rows(T, hidden, pre, center):
+    # row counts that take the kernels holding several rows per CTA (odd,
+    # and 3 mod 4: the last CTA is ragged)
+    (hk, hin), (pk, pin) = hidden, pre
+    rng = np.random.default_rng(T + int(8 * center))
+    L = 3
+    x = workloads.to_bf16_bits(rng.standard_normal((T, D)).astype(np.float32))
+    hw = _weight(rng, hk, (D,))
+    pw = _weight(rng, pk, (L, D))
+    kw = dict(hidden_eps=1e-6, pre_eps=1e-5, pre_center=center, hidden_input_scale=hin,
+              pre_input_scale=pin)
+    ref = oracle.context_norms_ex(x, L, hidden_w=hw, pre_w=pw, **kw)
+    out = rc.context_norms_ex(parity.dev_bf16(x, DEV), L, hidden_w=_dev_w(hw), pre_w=_dev_w(pw),
+                              **kw)
+    torch.cuda.synchronize()
+    got = parity.host_bits(out)
+    assert np.array_equal(got, ref), f"{int((got != ref).sum())} elements differ"
+
+
 def test_plain_options_equal_context_norms():
     # bf16 output-scale weights without a center and with one eps: the same
     # bits as rc_context_norms
