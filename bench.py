@@ -230,10 +230,21 @@ def run_ours(args, w):
     r2 = torch.empty((w.T,), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     pair = w.T > 128 and w.N % 256 == 0                  # CTA-pair plans
-    split = ws_bytes > 0
+    use_ws = ws_bytes > 0
+    # With CTA pairs the library splits K when the tiles need fewer CTAs
+    # than the GPU has SMs, and otherwise (persistent pairs) uses the
+    # workspace for a split-K launch of the last layer's final row blocks.
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    pair_ctas = 2 * w.L * ((w.T + 255) // 256) * (w.N // 256)
+    tail = use_ws and pair and pair_ctas >= sms
+    split = use_ws and not tail
     # norms (or row pass) + GEMM + (reduce-and-store when K is split; the
-    # pair epilogue stores otherwise; single CTAs without split: store kernel)
+    # pair epilogue stores otherwise, plus the tail's split GEMM and
+    # reduce-and-store; single CTAs without split: store kernel).  The
+    # whole-chain call's forming projection takes every tile itself.
     launches_per_step = 2 + (1 if split else (0 if pair else (w.L + 7) // 8))
+    if tail and args.path != "whole":
+        launches_per_step += 2
 
     whole = args.path == "whole"
     variants = args.path == "variants"
@@ -262,11 +273,11 @@ def run_ours(args, w):
         elif variants:
             norms_variant()
             rc.kv_project_store(normed, W, w.H, positions, slots, cs, caches, w.eps, rows=layer_rows,
-                                err=err, workspace=ws if split else None)
+                                err=err, workspace=ws if use_ws else None)
         else:
             rc.context_norms(x, hw, pw, w.L, w.eps, out=normed)
             rc.kv_project_store(normed, W, w.H, positions, slots, cs, caches, w.eps, err=err,
-                                workspace=ws if split else None)
+                                workspace=ws if use_ws else None)
         if ev:
             ev[2].record()
 
@@ -277,17 +288,17 @@ def run_ours(args, w):
             rc.context_rows(x, hw, w.eps, z=z, r2=r2)
             ev[1].record()
             rc.context_kv_from_rows(z, r2, pw, W, w.H, positions, slots, cs, caches, w.eps, err=err,
-                                    workspace=ws if split else None)
+                                    workspace=ws if use_ws else None)
         elif variants:
             norms_variant()
             ev[1].record()
             rc.kv_project_store(normed, W, w.H, positions, slots, cs, caches, w.eps, rows=layer_rows,
-                                err=err, kv_out=kv, workspace=ws if split else None)
+                                err=err, kv_out=kv, workspace=ws if use_ws else None)
         else:
             rc.context_norms(x, hw, pw, w.L, w.eps, out=normed)
             ev[1].record()
             rc.kv_project_store(normed, W, w.H, positions, slots, cs, caches, w.eps, err=err,
-                                kv_out=kv, workspace=ws if split else None)
+                                kv_out=kv, workspace=ws if use_ws else None)
         ev[2].record()
 
     def chain_unfused(ev):
@@ -295,7 +306,7 @@ def run_ours(args, w):
         ev[0].record()
         rc.context_norms(x, hw, pw, w.L, w.eps, out=normed)
         ev[1].record()
-        rc.kv_project(normed, W, out=kv, workspace=ws if split else None)
+        rc.kv_project(normed, W, out=kv, workspace=ws if use_ws else None)
         ev[2].record()
         rc.kv_store_from_projection(kv, w.H, positions, slots, cs, caches, w.eps, err=err)
         ev[3].record()
@@ -434,7 +445,7 @@ def run_ours(args, w):
         "row_pass" if fused_norms else "norms": hbm_entry(rows_bytes if fused_norms else counts["k1_bytes"],
                                                           us(k1_ms)),
         "project_store": dict(tc_entry(us(ps_ms)), split_k_workspace_bytes=ws_bytes,
-                              norms_fused=fused_norms),
+                              tail_split=bool(tail and not fused_norms), norms_fused=fused_norms),
         "unfused": {"norms": hbm_entry(counts["k1_bytes"], us(u_ms[0])),
                     "project": tc_entry(us(u_ms[1])),
                     "store": hbm_entry(k3_bytes, us(u_ms[2]))},

@@ -152,8 +152,11 @@ rc_status rc_context_norms_ex(const uint16_t *x, int64_t T, int32_t D,
  *              size in bytes; NULL/0 runs without split-K.  For few output
  *              tiles the K dimension is split across CTAs and the FP32
  *              partial sums are added in split order by a second kernel
- *              (deterministic for a given workspace size).  The bytes that
- *              give the full split are rc_kv_project_workspace_size().
+ *              (deterministic for a given workspace size).  With many
+ *              tiles whose last round would leave most SMs idle, the last
+ *              layer's final row blocks are split the same way in a launch
+ *              of their own.  The bytes that give the full split are
+ *              rc_kv_project_workspace_size().
  */
 rc_status rc_kv_project(const uint16_t *normed, const uint16_t *W,
                         int32_t w_layout, uint16_t *out, int32_t L, int64_t T,
@@ -161,7 +164,7 @@ rc_status rc_kv_project(const uint16_t *normed, const uint16_t *W,
                         size_t workspace_bytes, cudaStream_t stream);
 
 /* Workspace bytes rc_kv_project uses at most for these sizes on the current
-   device (0 when it would not split).  Host-only apart from one device
+   device (0 when it would split nothing).  Host-only apart from one device
    attribute query; returns 0 for invalid sizes. */
 size_t rc_kv_project_workspace_size(int32_t L, int64_t T, int32_t D, int32_t N);
 

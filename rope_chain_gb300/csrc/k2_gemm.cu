@@ -850,7 +850,8 @@ template <bool kBmn, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
 k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, const GemmArgs g,
-                           const __grid_constant__ FusedStore fs, int n_pairs, int m_pairs)
+                           const __grid_constant__ FusedStore fs, int n_pairs, int m_pairs,
+                           int tile_limit)
 {
     using C = PersistCfg;
     constexpr int S = C::kStages;
@@ -877,7 +878,8 @@ k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
     const uint32_t rank = cluster_ctarank();
     const bool leader = rank == 0;
     const int pair_id = (int)(blockIdx.x >> 1), num_pairs = (int)(gridDim.x >> 1);
-    const int num_tiles = g.L * m_pairs * n_pairs;
+    // the first tile_limit tiles (the rest, if any, are another launch's)
+    const int num_tiles = min(g.L * m_pairs * n_pairs, tile_limit);
     const int nkb = g.kb_total;
     pdl_trigger();
 
@@ -1093,7 +1095,7 @@ cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const Gemm
 // One CTA pair per two SMs (fewer when there are fewer tiles).
 template <bool kBmn, bool kFused>
 cudaError_t launch_pair_persistent(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &g,
-                                   const FusedStore &fs, int n_pairs, int m_pairs,
+                                   const FusedStore &fs, int n_pairs, int m_pairs, int tile_limit,
                                    cudaStream_t stream) {
     static int sms[64] = {};
     int dev = 0;
@@ -1112,10 +1114,11 @@ cudaError_t launch_pair_persistent(const CUtensorMap &ma, const CUtensorMap &mb,
         if (dev < 64)
             sms[dev] = n_sms;
     }
-    const int64_t tiles = (int64_t)g.L * m_pairs * n_pairs;
+    const int64_t tiles = std::min<int64_t>((int64_t)g.L * m_pairs * n_pairs, tile_limit);
     const int pairs = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, n_sms / 2));
     return launch_pdl(k2_project_pair_persistent<kBmn, kFused>, dim3((unsigned)(2 * pairs)),
-                      dim3(kThreads), PersistCfg::kSmem, stream, 2, ma, mb, g, fs, n_pairs, m_pairs);
+                      dim3(kThreads), PersistCfg::kSmem, stream, 2, ma, mb, g, fs, n_pairs, m_pairs,
+                      tile_limit);
 }
 
 }  // namespace
@@ -1144,6 +1147,35 @@ ProjectPlan plan_kv_project(int32_t L, int64_t T, int32_t D, int32_t N, int num_
     p.kb_per_split = (kb_total + splits - 1) / splits;
     p.splits = (kb_total + p.kb_per_split - 1) / p.kb_per_split;   // no empty split
     p.workspace = p.splits > 1 ? (size_t)p.splits * per_split : 0;
+    p.tail_splits = 1;
+    p.tail_kb_per_split = kb_total;
+    if (p.pair && p.splits == 1) {
+        // Persistent pairs take tiles round-robin, so a last wave of rem <
+        // P tiles costs a whole tile time.  Its tiles (rounded up to whole
+        // 256-row blocks, all in the last layer) can instead run split over
+        // the idle pairs: (full waves) + 1 / s tile times plus a fixed cost
+        // (fill, partials, reduce-and-store: about 20 K blocks' time).
+        const int64_t n_pairs = N / 256, m_pairs = (T + 255) / 256;
+        const int64_t P = std::max(1, num_sms / 2);
+        const int64_t rem = tiles / 2 % P;               // `tiles` counts CTAs here
+        const int64_t tail = (rem + n_pairs - 1) / n_pairs * n_pairs;
+        if (tiles / 2 > P && rem > 0 && tail <= m_pairs * n_pairs && tail < P) {
+            int s = (int)std::min<int64_t>(P / tail, kb_total / 8);
+            const int64_t row0 = (m_pairs - tail / n_pairs) * 256;
+            const size_t per_tail_split = (size_t)(T - row0) * (size_t)N * sizeof(float);
+            while (s > 1 && (size_t)s * per_tail_split > workspace_bytes)
+                --s;
+            const int64_t waves = (tiles / 2 + P - 1) / P;
+            const int64_t full_waves = (tiles / 2 - tail + P - 1) / P;
+            if (s >= 2 && (double)full_waves + 1.0 / s + 20.0 / kb_total < (double)waves) {
+                p.tail_tiles = tail;
+                p.tail_row0 = row0;
+                p.tail_kb_per_split = (kb_total + s - 1) / s;
+                p.tail_splits = (kb_total + p.tail_kb_per_split - 1) / p.tail_kb_per_split;
+                p.workspace = (size_t)p.tail_splits * per_tail_split;
+            }
+        }
+    }
     return p;
 }
 
@@ -1182,9 +1214,12 @@ template <bool kFused>
 cudaError_t launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &g,
                         const FusedStore &fs, bool w_nk, const ProjectPlan &plan, int64_t T,
                         int32_t N, cudaStream_t stream) {
-    if (plan.pair && plan.splits == 1)         // persistent pairs, epilogue under the next mainloop
-        return w_nk ? launch_pair_persistent<false, kFused>(ma, mb, g, fs, N / 256, (int)((T + 255) / 256), stream)
-                    : launch_pair_persistent<true, kFused>(ma, mb, g, fs, N / 256, (int)((T + 255) / 256), stream);
+    if (plan.pair && plan.splits == 1) {       // persistent pairs, epilogue under the next mainloop
+        const int n_pairs = N / 256, m_pairs = (int)((T + 255) / 256);
+        const int limit = (int)((int64_t)g.L * m_pairs * n_pairs - plan.tail_tiles);
+        return w_nk ? launch_pair_persistent<false, kFused>(ma, mb, g, fs, n_pairs, m_pairs, limit, stream)
+                    : launch_pair_persistent<true, kFused>(ma, mb, g, fs, n_pairs, m_pairs, limit, stream);
+    }
     if (plan.pair)
         return w_nk ? launch_pair<false, kFused, false>(ma, mb, g, fs, N / 256, (int)((T + 255) / 256), stream)
                     : launch_pair<true, kFused, false>(ma, mb, g, fs, N / 256, (int)((T + 255) / 256), stream);
@@ -1204,6 +1239,44 @@ cudaError_t launch_reduce(const float *ws, uint16_t *out, int64_t count, int spl
                       count, splits);
 }
 
+// The tail of a persistent plan: rows tail_row0 .. T-1 of the last layer as
+// a one-layer split-K problem of CTA pairs writing FP32 partials to ws
+// ([tail_splits, T - tail_row0, N]); the caller then reduces them.
+cudaError_t launch_tail_partials(const uint16_t *normed, const uint16_t *W, bool w_nk, int32_t L,
+                                 int64_t T, int32_t D, int32_t N, const ProjectPlan &plan,
+                                 float *ws, cudaStream_t stream, const char **why) {
+    const int64_t rows = T - plan.tail_row0;
+    const uint16_t *a = normed + ((int64_t)(L - 1) * T + plan.tail_row0) * D;
+    const uint16_t *b = W + (int64_t)(L - 1) * D * N;
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, a, (uint64_t)D, (uint64_t)rows, 1, BK, BM)) {
+        *why = "tensor map of the tail rows could not be encoded";
+        return cudaErrorInvalidValue;
+    }
+    const bool ok_b = w_nk ? make_map(&mb, b, (uint64_t)D, (uint64_t)N, 1, BK, 128)
+                           : make_map(&mb, b, (uint64_t)N, (uint64_t)D, 1, 64, BK);
+    if (!ok_b) {
+        *why = "tensor map of the last layer's weights could not be encoded";
+        return cudaErrorInvalidValue;
+    }
+    GemmArgs g{};
+    g.T = (int32_t)rows;
+    g.N = N;
+    g.L = 1;
+    g.kb_total = D / BK;
+    g.kb_per_split = plan.tail_kb_per_split;
+    g.splits = plan.tail_splits;
+    g.out = nullptr;
+    g.partial = ws;
+    g.row_scale = nullptr;
+    g.col_gain = nullptr;
+    FusedStore none{};
+    *why = "tail projection launch";
+    const int m_pairs = (int)((rows + 255) / 256);
+    return w_nk ? launch_pair<false, false, false>(ma, mb, g, none, N / 256, m_pairs, stream)
+                : launch_pair<true, false, false>(ma, mb, g, none, N / 256, m_pairs, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_kv_project(const uint16_t *normed, const uint16_t *W, bool w_nk, uint16_t *out,
@@ -1216,7 +1289,18 @@ cudaError_t launch_kv_project(const uint16_t *normed, const uint16_t *W, bool w_
         return cudaErrorInvalidValue;
     FusedStore none{};
     cudaError_t e = launch_gemm<false>(ma, mb, g, none, w_nk, plan, T, N, stream);
-    if (e != cudaSuccess || plan.splits == 1)
+    if (e != cudaSuccess)
+        return e;
+    if (plan.tail_tiles > 0) {
+        // the last layer's tail rows: split partials, then their reduction
+        e = launch_tail_partials(normed, W, w_nk, L, T, D, N, plan, ws, stream, why);
+        if (e != cudaSuccess)
+            return e;
+        const int64_t rows = T - plan.tail_row0;
+        return launch_reduce(ws, out + ((int64_t)(L - 1) * T + plan.tail_row0) * N, rows * N,
+                             plan.tail_splits, stream);
+    }
+    if (plan.splits == 1)
         return e;
     return launch_reduce(ws, out, (int64_t)L * T * N, plan.splits, stream);
 }
@@ -1239,8 +1323,34 @@ cudaError_t launch_kv_project_store(const uint16_t *normed, const uint16_t *W, b
         *why = "reduce-and-store launch";
         return launch_reduce_store(fs, ws, plan.splits, L, (int32_t)T, stream);
     }
-    if (plan.pair)                                 // the epilogue stores
-        return launch_gemm<true>(ma, mb, g, fs, w_nk, plan, T, N, stream);
+    if (plan.pair) {                               // the epilogue stores
+        e = launch_gemm<true>(ma, mb, g, fs, w_nk, plan, T, N, stream);
+        if (e != cudaSuccess || plan.tail_tiles == 0)
+            return e;
+        // the last layer's tail rows: split partials, then reduce-and-store
+        // them as a one-layer problem
+        e = launch_tail_partials(normed, W, w_nk, L, T, D, N, plan, ws, stream, why);
+        if (e != cudaSuccess)
+            return e;
+        const int64_t row0 = plan.tail_row0, rows = T - row0;
+        const int32_t last = L - 1;
+        FusedStore ts = fs;
+        const int64_t kept = std::min<int64_t>(std::max<int64_t>(fs.rows[last] - row0, 0), rows);
+        ts.slots[0] = kept > 0 ? fs.slots[last] + row0 : nullptr;
+        ts.caches[0] = fs.caches[last];
+        ts.rows[0] = (int32_t)kept;
+        for (int i = 1; i < kMaxFusedLayers; ++i) {
+            ts.slots[i] = nullptr;
+            ts.caches[i] = nullptr;
+            ts.rows[i] = 0;
+        }
+        if (fs.positions != nullptr)
+            ts.positions = fs.positions + row0;
+        if (fs.kv_out != nullptr)
+            ts.kv_out = fs.kv_out + ((int64_t)last * T + row0) * N;
+        *why = "tail reduce-and-store launch";
+        return launch_reduce_store(ts, ws, plan.tail_splits, 1, (int32_t)rows, stream);
+    }
     // single CTAs without a split: the projection lands in kv_out, then the
     // store kernel reads it (8 layers per launch)
     if (fs.kv_out == nullptr) {

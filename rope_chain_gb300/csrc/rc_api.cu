@@ -289,7 +289,7 @@ rc_status rc_kv_project(const uint16_t *normed, const uint16_t *W, int32_t w_lay
         return fail(RC_ERR_CUDA, "rc_kv_project: no current CUDA device");
     const rc::ProjectPlan plan =
         rc::plan_kv_project(L, T, D, N, sms, workspace ? workspace_bytes : 0);
-    if (plan.splits > 1 && overlap(workspace, plan.workspace, out, obytes))
+    if (plan.workspace > 0 && overlap(workspace, plan.workspace, out, obytes))
         return fail(RC_ERR_INVALID_ARG, "rc_kv_project: workspace overlaps out");
     const char *why = "launch";
     const cudaError_t e = rc::launch_kv_project(normed, W, w_layout == RC_W_NK, out, L, T, D, N,
@@ -485,6 +485,23 @@ rc_status rc_kv_project_store_rows(const uint16_t *normed, const uint16_t *W, in
                                  workspace_bytes, stream);
 }
 
+namespace {
+
+// The whole-chain calls run the forming projection, which takes every tile
+// itself: their plans have no tail launch and no tail workspace (tail plans
+// never split K, so their only workspace is the tail's).
+rc::ProjectPlan whole_chain_plan(int32_t L, int64_t T, int32_t D, int32_t N, int sms,
+                                 size_t workspace_bytes) {
+    rc::ProjectPlan p = rc::plan_kv_project(L, T, D, N, sms, workspace_bytes);
+    if (p.tail_tiles > 0) {
+        p.tail_tiles = 0;
+        p.workspace = 0;
+    }
+    return p;
+}
+
+}  // namespace
+
 size_t rc_context_kv_workspace_size(int32_t L, int64_t T, int32_t D, int32_t H)
 {
     if (!supported_heads(H) || D != rc::kHidden || L < 1 || L > rc::kMaxFusedLayers)
@@ -495,7 +512,7 @@ size_t rc_context_kv_workspace_size(int32_t L, int64_t T, int32_t D, int32_t H)
     const int sms = num_sms_current();
     if (sms <= 0)
         return 0;
-    const rc::ProjectPlan plan = rc::plan_kv_project(L, T, D, N, sms, SIZE_MAX);
+    const rc::ProjectPlan plan = whole_chain_plan(L, T, D, N, sms, SIZE_MAX);
     return context_kv_fixed_bytes(plan.pair, L, T, D) + plan.workspace;
 }
 
@@ -541,7 +558,7 @@ rc_status rc_context_kv(const uint16_t *x, int64_t T, int32_t D, const uint16_t 
                     fixed, workspace_bytes);
     char *wsb = static_cast<char *>(workspace);
     float *partials = reinterpret_cast<float *>(wsb + fixed);
-    const rc::ProjectPlan plan = rc::plan_kv_project(L, T, D, N, sms, workspace_bytes - fixed);
+    const rc::ProjectPlan plan = whole_chain_plan(L, T, D, N, sms, workspace_bytes - fixed);
     const char *why = "launch";
     cudaError_t e;
     if (plan.pair) {
@@ -624,7 +641,7 @@ rc_status rc_context_kv_from_rows(const uint16_t *z, const float *r2, int64_t T,
     const int sms = num_sms_current();
     if (sms <= 0)
         return fail(RC_ERR_CUDA, "%s: no current CUDA device", fn);
-    const rc::ProjectPlan plan = rc::plan_kv_project(L, T, D, N, sms, workspace ? workspace_bytes : 0);
+    const rc::ProjectPlan plan = whole_chain_plan(L, T, D, N, sms, workspace ? workspace_bytes : 0);
     if (!plan.pair)
         return fail(RC_ERR_UNSUPPORTED,
                     "%s: needs T > 128 and H >= 2 (CTA-pair tiles); use rc_context_kv", fn);

@@ -260,7 +260,15 @@ struct ProjectPlan {
     int bn;                // 128 or 256
     int splits;            // >= 1
     int kb_per_split;      // 64-wide K blocks per split
-    size_t workspace;      // bytes of FP32 partials when splits > 1
+    // Persistent pair plans whose last wave would leave most pairs idle:
+    // the last tail_tiles tiles (rows tail_row0 .. T-1 of the last layer)
+    // run as their own split-K launch (tail_splits splits of
+    // tail_kb_per_split K blocks) after the persistent kernel's full waves.
+    int64_t tail_tiles;    // 0: no tail launch
+    int64_t tail_row0;
+    int tail_splits;
+    int tail_kb_per_split;
+    size_t workspace;      // bytes of FP32 partials (split-K or the tail's)
 };
 
 // Choose tile width and split count for the device's SM count.

@@ -83,6 +83,8 @@ def check(case, normed, W, *, workspace, rows=None, layout=rc.RC_W_KN, slots=Non
     (200, 1, 2, True, False),      # CTA pairs, 16 splits of 8 K blocks, ragged rows
     (200, 2, 16, False, False),    # CTA pairs, epilogue store, no RoPE
     (1000, 10, 4, False, True),    # persistent pairs: 80 tiles over at most 76 pairs (both accumulators)
+    (1000, 10, 4, True, True),     # persistent pairs over 76 tiles, then the last layer's last two
+                                   # row blocks (rows 512-999) split 16 ways and reduced and stored
     (129, 1, 32, True, True),      # H = 32, ragged rows
     (64, 2, 8, True, True),        # single CTAs, split-K, reduce-and-store
     (100, 2, 1, False, True),      # N = 128: single CTAs without split, kv_out then store
@@ -130,6 +132,37 @@ def test_fused_matches_unfused_chain(layout):
     for a, b in zip(caches, got["caches"]):
         assert np.array_equal(a, b)
     assert err == got["err"]
+
+
+def test_tail_split_projection():
+    # 80 tiles of 256 x 256 over 76 CTA pairs: the persistent kernel takes
+    # 76, and the last layer's final row block (rows 2304-2499, ragged) runs
+    # as a split-K launch of its own when a workspace is given
+    T, L, H = 2500, 2, 8
+    N = 128 * H
+    case = workloads.random_case(4242, T=T, L=L, H=H, max_position=512,
+                                 num_blocks=(T + 15) // 16 + 4, block_size=16)
+    assert rc.workspace_size(L, T, 8192, N) > 0, "no tail split planned on this device"
+    normed = oracle.context_norms(case["x"], case["hidden_w"], case["pre_w"], L, case["eps"])
+    nd, wd = parity.dev_bf16(normed, DEV), parity.dev_bf16(case["W"], DEV)
+    ws = rc.new_workspace(L, T, 8192, N, DEV)
+    tailed = parity.host_bits(rc.kv_project(nd, wd, workspace=ws))
+    plain = parity.host_bits(rc.kv_project(nd, wd))
+    sample = np.unique(np.r_[0, 2303, 2304, 2305, T - 1, np.linspace(0, T - 1, 120).astype(int),
+                             np.arange(2304, T, 9)])
+    ref64, ab = oracle.kv_project(normed, case["W"], rows=sample)
+    parity.assert_projection_close(tailed[:, sample], ref64, ab, "projection with the tail split")
+    parity.assert_projection_close(plain[:, sample], ref64, ab, "projection without it")
+    # rows outside the tail come from the same persistent kernel either way
+    assert np.array_equal(tailed[0], plain[0]) and np.array_equal(tailed[1, :2304], plain[1, :2304])
+    caches, kv, err = run_fused(case, nd, wd, workspace=True, kv_out=True)
+    assert np.array_equal(kv, tailed), "the fused call's projection differs from rc_kv_project's"
+    ref_caches = parity.make_caches(case, L, parity.SENTINEL)
+    ref_err = oracle.kv_store_from_projection(kv, H, case["positions"], case["slots"],
+                                              case["cos_sin"], ref_caches, case["eps"], T)
+    for g, r in zip(caches, ref_caches):
+        assert np.array_equal(g, r)
+    assert err == ref_err
 
 
 @pytest.mark.parametrize("index", [1, 2, 3, 4, 5])

@@ -207,6 +207,9 @@ def test_store_per_layer_rows(T, L, H, rows):
     (512, 3, 8, True, [1, 512, 400]),        # CTA pairs, split-K, reduce-and-store
     (100, 2, 1, False, [100, 3]),            # single CTAs: kv_out, then the store kernel
     (257, 10, 2, True, [257, 0, 5, 256, 100, 1, 2, 3, 250, 257]),
+    # persistent pairs with a tail split (rows 512-999 of the last layer):
+    # the last layer stores its first 700 rows, so the tail stores 188
+    (1000, 10, 4, True, [1000, 999, 0, 500, 1000, 3, 1000, 256, 1000, 700]),
 ])
 def test_project_store_per_layer_rows(T, L, H, workspace, rows):
     case = _store_case(77 + T + L, T, L, H, rows)
