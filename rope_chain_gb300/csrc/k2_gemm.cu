@@ -119,6 +119,19 @@ k2_project(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = words[0];
+    if (warp == 0 && lane == 0) {
+        // the first stages' weights into L2 while the previous kernel
+        // finishes (a hint: the loads below still wait for it)
+        for (int i = 0; i < min(nkb, S); ++i) {
+            const int kc = (kb0 + i) * BK;
+            if (kBmn) {
+                for (int c = 0; c < BN / 64; ++c)
+                    tma_prefetch_3d(&tmB, n0 + 64 * c, kc, l);
+            } else {
+                tma_prefetch_3d(&tmB, kc, n0, l);
+            }
+        }
+    }
     pdl_wait();                                   // the previous kernel's writes are visible
     const bool skip = faulted();
 
@@ -539,6 +552,19 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = words[0];
     const bool skip = words[2] != 0u;
+    if (warp == 0 && lane == 0) {
+        // the first stages' weights into L2 while the previous kernel
+        // finishes (a hint: the loads below still wait for it)
+        for (int i = 0; i < min(nkb, S); ++i) {
+            const int kc = (kb0 + i) * BK;
+            if (kBmn) {
+                tma_prefetch_3d(&tmB, nb, kc, l);
+                tma_prefetch_3d(&tmB, nb + 64, kc, l);
+            } else {
+                tma_prefetch_3d(&tmB, kc, nb, l);
+            }
+        }
+    }
     pdl_wait();                                   // the previous kernel's writes are visible
 
     int issued = 0;
@@ -914,6 +940,20 @@ k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
     tc_fence_after();
     const uint32_t tmem = words[0];
     const bool skip = words[2] != 0u;
+    if (warp == 0 && lane == 0 && pair_id < num_tiles) {
+        // the first tile's first stages of weights into L2 while the
+        // previous kernel finishes (a hint: the loads below still wait)
+        const int np = pair_id % n_pairs, l = pair_id / n_pairs / m_pairs;
+        const int nb = np * 256 + 128 * (int)rank;
+        for (int i = 0; i < min(nkb, S); ++i) {
+            if (kBmn) {
+                tma_prefetch_3d(&tmB, nb, i * BK, l);
+                tma_prefetch_3d(&tmB, nb + 64, i * BK, l);
+            } else {
+                tma_prefetch_3d(&tmB, i * BK, nb, l);
+            }
+        }
+    }
     pdl_wait();                                   // the previous kernel's writes are visible
 
     int issued = 0;
