@@ -36,10 +36,10 @@ L2_FLUSH_BYTES = 512 << 20          # > 129 MB L2: written between timed steps
 # summed over the kernels the timed call launches); keyed by (workload, path,
 # kernel).  An entry is removed whenever one of its kernels changes.
 NCU_TRAFFIC = {
-    # rc_kv_project_store at workload 2: k2_project_pair (75.67 MB read,
-    # 0.88 MB written) + k3_reduce_store (18.99 MB read); ncu with its default
+    # rc_kv_project_store at workload 2: k2_project_pair (75.69 MB read,
+    # 0.83 MB written) + k3_reduce_store (18.99 MB read); ncu with its default
     # cache flush before each launch.
-    (2, "store", "project_store"): 95_530_176,
+    (2, "store", "project_store"): 95_506_752,
 }
 
 
