@@ -18,7 +18,11 @@
  * Conventions for every call:
  *   - Tensor pointers are DEVICE pointers owned by the caller; the library
  *     never frees or retains them.  Pointer ARRAYS (slots, caches) are HOST
- *     arrays of device pointers, read during the call only.
+ *     arrays of device pointers, read during the call only.  A pointer
+ *     to an INPUT may also be the device address of page-locked host memory
+ *     (rc_device_address): the kernels then read it over the host link
+ *     (NVLink-C2C on GB300) with no staging copy.  The host memory must
+ *     stay allocated and unchanged until the stream has passed the call.
  *   - bf16 values travel as uint16_t bit patterns.
  *   - Work is enqueued on `stream`; calls do not synchronise and do not
  *     allocate device memory, so they can be issued inside CUDA graph
@@ -418,6 +422,15 @@ rc_status rc_qkv_front(const uint16_t *hidden, int32_t M, int32_t D, const uint1
                        const uint16_t *cos_sin, int64_t max_position, const int64_t *slots,
                        uint16_t *cache, int32_t num_blocks, int32_t block_size, float eps,
                        uint16_t *out, uint16_t *raw_out, int32_t *err, cudaStream_t stream);
+
+/* rc_device_address -- the address at which the current device reads p:
+   p itself for device or managed memory; for page-locked host memory
+   mapped into the device's address space (cudaHostAlloc, or
+   cudaHostRegister with mapping), its device address (the same value under
+   unified addressing).  RC_ERR_INVALID_ARG when the device cannot address p
+   through the CUDA runtime (pageable host memory, NULL); dev untouched then.
+   Host-only; no page counterpart. */
+rc_status rc_device_address(const void *p, const void **dev);
 
 /* Sticky fault bits raised on the device when a bounded wait gives up: bits
    0-3 by the projection kernels, bits 8-11 by the QKV front (per kernel:

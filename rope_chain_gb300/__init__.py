@@ -48,6 +48,7 @@ SIGNATURES = {
                      _c.POINTER(_vp), _vp, _c.c_int64, _c.POINTER(_vp), _c.c_int32, _c.c_int32,
                      _c.c_int32, _c.c_int32, _c.c_float, _c.c_int64, _vp, _vp], _c.c_int),
     "rc_read_device_faults": ([_c.POINTER(_c.c_uint32), _c.c_int32], _c.c_int),
+    "rc_device_address": ([_vp, _c.POINTER(_vp)], _c.c_int),
     "rc_kv_project_no_alloc": ([_vp, _vp, _c.c_int32, _vp, _c.c_int32, _c.c_int64, _c.c_int32,
                                 _c.c_int32, _vp], _c.c_int),
     "rc_context_kv": ([_vp, _c.c_int64, _c.c_int32, _vp, _vp, _c.c_int32, _c.c_float, _vp,
@@ -129,21 +130,50 @@ def _bf16(t: torch.Tensor, name: str) -> None:
         raise ValueError(f"{name} must be contiguous")
 
 
+def device_address(t: torch.Tensor) -> int:
+    """The address at which the current GPU reads t's data: t's own for a
+    CUDA tensor; for a pinned (page-locked) CPU tensor its mapped device
+    address (rc_device_address), so that a kernel reads it in place over the
+    host link."""
+    if t.is_cuda:
+        return t.data_ptr()
+    if t.device.type == "cpu" and t.is_pinned():
+        d = _vp(0)
+        _check(lib().rc_device_address(t.data_ptr(), ctypes.byref(d)))
+        return int(d.value)
+    raise TypeError("expected a CUDA tensor or a pinned CPU tensor")
+
+
+def _in_bf16(t: torch.Tensor, name: str) -> int:
+    """A bf16 input the kernels may read in place (CUDA or pinned host
+    memory); returns its device address."""
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be a bfloat16 tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return device_address(t)
+
+
+def _out_device(x: torch.Tensor) -> torch.device:
+    return x.device if x.is_cuda else torch.device("cuda", torch.cuda.current_device())
+
+
 # ------------------------------------------------------------------- calls
 
 def context_norms(x: torch.Tensor, hidden_w: Optional[torch.Tensor],
                   pre_w: Optional[torch.Tensor], L: int, eps: float,
                   out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """bf16 [L, T, 8192] = stack_l(pre_norm_l(bf16(hidden_norm(x))))."""
-    _bf16(x, "x")
+    """bf16 [L, T, 8192] = stack_l(pre_norm_l(bf16(hidden_norm(x)))).  x may
+    be a pinned CPU tensor (read in place over the host link)."""
+    xa = _in_bf16(x, "x")
     T, D = x.shape
     if out is None:
-        out = torch.empty((L, T, D), dtype=torch.bfloat16, device=x.device)
+        out = torch.empty((L, T, D), dtype=torch.bfloat16, device=_out_device(x))
     _bf16(out, "out")
     for w, n in ((hidden_w, "hidden_w"), (pre_w, "pre_w")):
         if w is not None:
             _bf16(w, n)
-    _check(lib().rc_context_norms(x.data_ptr(), T, D, _ptr(hidden_w), _ptr(pre_w), L, eps,
+    _check(lib().rc_context_norms(xa, T, D, _ptr(hidden_w), _ptr(pre_w), L, eps,
                                   out.data_ptr(), _stream(stream)))
     return out
 
@@ -170,11 +200,12 @@ def context_norms_ex(x: torch.Tensor, L: int, *, hidden_w: Optional[torch.Tensor
                      out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """context_norms with every norm option (rc_context_norms_ex): weights
     bf16 or float32 ([8192] hidden, [L, 8192] layers), each norm's eps and
-    gain center, and whether each weight scales the norm's input."""
-    _bf16(x, "x")
+    gain center, and whether each weight scales the norm's input.  x may be a
+    pinned CPU tensor."""
+    xa = _in_bf16(x, "x")
     T, D = x.shape
     if out is None:
-        out = torch.empty((L, T, D), dtype=torch.bfloat16, device=x.device)
+        out = torch.empty((L, T, D), dtype=torch.bfloat16, device=_out_device(x))
     _bf16(out, "out")
     if hidden_w is not None and tuple(hidden_w.shape) != (D,):
         raise ValueError("hidden_w must be [8192]")
@@ -182,7 +213,7 @@ def context_norms_ex(x: torch.Tensor, L: int, *, hidden_w: Optional[torch.Tensor
         raise ValueError("pre_w must be [L, 8192]")
     h = _norm_params(hidden_w, hidden_input_scale, hidden_center, hidden_eps, "hidden_w")
     p = _norm_params(pre_w, pre_input_scale, pre_center, pre_eps, "pre_w")
-    _check(lib().rc_context_norms_ex(x.data_ptr(), T, D, ctypes.byref(h), ctypes.byref(p), L,
+    _check(lib().rc_context_norms_ex(xa, T, D, ctypes.byref(h), ctypes.byref(p), L,
                                      out.data_ptr(), _stream(stream)))
     return out
 
@@ -392,7 +423,7 @@ def context_kv(x: torch.Tensor, hidden_w, pre_w, W: torch.Tensor, H: int, positi
                stream=None) -> None:
     """The whole chain in one call (rc_context_kv): norms fused into the
     projection, store fused after it.  ``workspace``: context_kv_workspace()."""
-    _bf16(x, "x")
+    xa = _in_bf16(x, "x")                          # CUDA or pinned host memory
     _bf16(W, "W")
     T, D = x.shape
     L = len(caches)
@@ -404,7 +435,7 @@ def context_kv(x: torch.Tensor, hidden_w, pre_w, W: torch.Tensor, H: int, positi
     if not (workspace.is_cuda and workspace.is_contiguous()):
         raise ValueError("workspace must be a contiguous CUDA tensor")
     slot_arr, cache_arr, nb, bs, rows = _store_operands(H, slots, caches, positions, cos_sin, rows)
-    _check(lib().rc_context_kv(x.data_ptr(), T, D, _ptr(hidden_w), _ptr(pre_w), L, eps,
+    _check(lib().rc_context_kv(xa, T, D, _ptr(hidden_w), _ptr(pre_w), L, eps,
                                W.data_ptr(), w_layout, H, _ptr(positions), slot_arr, _ptr(cos_sin),
                                0 if cos_sin is None else cos_sin.shape[0], cache_arr, nb, bs, rows,
                                _ptr(err), _ptr(kv_out), workspace.data_ptr(),
@@ -413,16 +444,17 @@ def context_kv(x: torch.Tensor, hidden_w, pre_w, W: torch.Tensor, H: int, positi
 
 def context_rows(x: torch.Tensor, hidden_w, eps: float, z: Optional[torch.Tensor] = None,
                  r2: Optional[torch.Tensor] = None, stream=None):
-    """The row pass of context_kv: (z bf16 [T, 8192], r2 float32 [T])."""
-    _bf16(x, "x")
+    """The row pass of context_kv: (z bf16 [T, 8192], r2 float32 [T]); x may
+    be a pinned CPU tensor."""
+    xa = _in_bf16(x, "x")
     T, D = x.shape
     if z is None:
-        z = torch.empty((T, D), dtype=torch.bfloat16, device=x.device)
+        z = torch.empty((T, D), dtype=torch.bfloat16, device=_out_device(x))
     if r2 is None:
-        r2 = torch.empty((T,), dtype=torch.float32, device=x.device)
+        r2 = torch.empty((T,), dtype=torch.float32, device=_out_device(x))
     if hidden_w is not None:
         _bf16(hidden_w, "hidden_w")
-    _check(lib().rc_context_rows(x.data_ptr(), T, D, _ptr(hidden_w), eps, z.data_ptr(),
+    _check(lib().rc_context_rows(xa, T, D, _ptr(hidden_w), eps, z.data_ptr(),
                                  r2.data_ptr(), _stream(stream)))
     return z, r2
 

@@ -653,6 +653,35 @@ rc_status rc_context_kv_from_rows(const uint16_t *z, const float *r2, int64_t T,
     return ok();
 }
 
+rc_status rc_device_address(const void *p, const void **dev)
+{
+    if (!p || !dev)
+        return fail(RC_ERR_INVALID_ARG, "rc_device_address: p and dev must not be NULL");
+    cudaPointerAttributes a{};
+    cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();                       // not sticky: clear it
+        return fail(RC_ERR_INVALID_ARG, "rc_device_address: %p: %s", p, cudaGetErrorString(e));
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+        *dev = p;
+        return ok();
+    }
+    if (a.type != cudaMemoryTypeHost)
+        return fail(RC_ERR_INVALID_ARG,
+                    "rc_device_address: %p is not device memory or page-locked host memory", p);
+    void *d = nullptr;
+    e = cudaHostGetDevicePointer(&d, const_cast<void *>(p), 0);
+    if (e != cudaSuccess) {
+        cudaGetLastError();                       // not sticky: clear it
+        return fail(RC_ERR_INVALID_ARG,
+                    "rc_device_address: page-locked memory at %p is not mapped for the device (%s)",
+                    p, cudaGetErrorString(e));
+    }
+    *dev = d;
+    return ok();
+}
+
 rc_status rc_read_device_faults(uint32_t *flags, int32_t clear)
 {
     if (!flags)
