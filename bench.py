@@ -52,7 +52,8 @@ def load_peaks():
 
 
 def algorithmic_counts(w, splits: int):
-    """Per-step algorithmic bytes / flops of each kernel ('Rooflines')."""
+    """Per-step algorithmic bytes / flops of each kernel: the norms read x once
+    and write L rows (plus the gains), the projection does 2 L T D N FLOP."""
     T, D, L, H, N = w.T, w.D, w.L, w.H, w.N
     k1 = 2 * T * D * (1 + L) + 2 * D * ((1 if w.hidden_weighted else 0) + (L if w.pre_weighted else 0))
     k2_flops = 2 * L * T * D * N

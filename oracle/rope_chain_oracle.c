@@ -17,7 +17,7 @@
  * without -ffast-math, so each C operator below is exactly one such
  * operation; fmaf() is the one fused multiply-add the pages write.
  *
- * Readings where the pages are silent (each is also listed in the design doc):
+ * Readings where the pages are silent:
  *   R1  The order of the 8192-wide sum of squares ("row_norm.py" is not on
  *       the pages): thread t < 256 holds columns 2048k + 8t + i (k < 4,
  *       i < 8) as the norms kernel maps them ([ctx] _ContextNormsKernel);
