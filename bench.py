@@ -17,6 +17,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -156,6 +157,18 @@ def oracle_chain_rows(case, w, R: int, threads: int = 0) -> float:
     return time.perf_counter() - t0
 
 
+def host_cpu() -> str:
+    """The host CPU's model name (lscpu), else the machine type."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return f"{line.split(':', 1)[1].strip()} ({platform.machine()})"
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
+
+
 def cpu_sample_rows(w) -> int:
     return min(w.T, 256)
 
@@ -188,7 +201,7 @@ def run_reference(args, w):
     value = R * args.steps / total
     rec = base_record(args, w, world)
     rec.update({"impl": "reference", "value": value, "ms_per_step": 1e3 * total / args.steps,
-                "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "cpu": host_cpu(), "kind": "oracle",
                                  "sample": f"first {R} rows of the workload per step, whole chain"},
                 "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}})
@@ -489,7 +502,7 @@ def run_ours(args, w):
         "ms_per_step": total_ms / args.steps,
         "roofline": roof,
         "kernels": kern,
-        "cpu_baseline": {"value": R / cpu_s, "unit": "rows/s", "cores": oracle.max_threads(),
+        "cpu_baseline": {"value": R / cpu_s, "unit": "rows/s", "cores": oracle.max_threads(), "cpu": host_cpu(),
                          "kind": "oracle", "sample": f"first {R} rows of the workload, whole chain, once",
                          "one_core": {"value": R1 / cpu1_s, "unit": "rows/s", "cores": 1,
                                       "sample": f"first {R1} rows, whole chain, once"}},
@@ -557,7 +570,7 @@ def run_front(args):
         value = M * args.steps / total
         rec = front_record(args, case, world, M)
         rec.update({"impl": "reference", "value": value, "ms_per_step": 1e3 * total / args.steps,
-                    "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.max_threads(),
+                    "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.max_threads(), "cpu": host_cpu(),
                                      "kind": "oracle", "sample": f"all {M} tokens per step"},
                     "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                             "d2h_bytes_per_step": 0}})
@@ -669,7 +682,7 @@ def run_front(args):
                      "traffic": NCU_TRAFFIC.get(("front", M, "k4_qkv_front")),
                      "peak_source": f"hbm_gbs of {peak_src}"},
         "kernels": {"qkv_front": {"us": t_us, "GB/s": nbytes / t_us / 1e3, "bytes": nbytes}},
-        "cpu_baseline": {"value": M / cpu_s, "unit": "tokens/s", "cores": oracle.max_threads(),
+        "cpu_baseline": {"value": M / cpu_s, "unit": "tokens/s", "cores": oracle.max_threads(), "cpu": host_cpu(),
                          "kind": "oracle", "sample": f"all {M} tokens, once"},
         "e2e": {"value": world * M * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": M * D * 2, "d2h_bytes_per_step": M * N * 2,
