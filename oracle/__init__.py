@@ -58,7 +58,10 @@ class _Norm(ctypes.Structure):
 def lib():
     global _lib
     if _lib is None:
-        L = ctypes.CDLL(build())
+        # RCO_ORACLE_LIB: tests of the pins load a copy of the oracle with
+        # one mistake planted (tests/test_oracle_mutants.py) through it
+        override = os.environ.get("RCO_ORACLE_LIB")
+        L = ctypes.CDLL(override if override else build())
         sig = {
             "rco_f32": ([_c.c_uint16], _c.c_float),
             "rco_bf16_rn": ([_c.c_float], _c.c_uint16),

@@ -1,0 +1,103 @@
+"""The oracle's pins catch plausible mistakes.  Each case plants one mistake
+in a copy of rope_chain_oracle.c (an exact text substitution, so the case
+fails loudly if the source no longer holds the line), builds it with the
+oracle's own flags, and runs the pin tests against it: at least one must
+fail (or the run must crash, for a mistake that writes out of bounds).
+The unmodified copy, built the same way, must pass them all."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+PINS = ["tests/test_oracle_bf16.py", "tests/test_oracle_norms.py",
+        "tests/test_oracle_project_store.py", "tests/test_oracle_variants.py",
+        "tests/test_oracle_qkv_front.py"]
+
+MUTANTS = [
+    ("hidden norm output not rounded to bf16",
+     "            z[c] = rco_f32(rco_bf16_rn(y));\n",
+     "            z[c] = y;\n"),
+    ("8192-wide sum: warp sums added right to left",
+     "    float s = butterfly32(&lane[0]);\n    for (int w = 1; w < 8; ++w) {\n",
+     "    float s = butterfly32(&lane[224]);\n    for (int w = 6; w >= 0; --w) {\n"),
+    ("8192-wide sum: in-thread order (i, k) instead of (k, i)",
+     "        for (int k = 0; k < 4; ++k)\n            for (int i = 0; i < 8; ++i) {\n",
+     "        for (int i = 0; i < 8; ++i)\n            for (int k = 0; k < 4; ++k) {\n"),
+    ("K-norm mean over 128 instead of 64",
+     "    const float inv_hd = 1.0f / 64.0f;   /* exact: 2^-6 */\n",
+     "    const float inv_hd = 1.0f / 128.0f;\n"),
+    ("64-wide sum: even and odd squares added pairwise first",
+     "        ev[j] = k[2 * j] * k[2 * j];\n        od[j] = k[2 * j + 1] * k[2 * j + 1];\n",
+     "        ev[j] = k[2 * j] * k[2 * j] + k[2 * j + 1] * k[2 * j + 1];\n        od[j] = 0.0f;\n"),
+    ("RoPE: wrong sign on the first output",
+     "    *xo = fmaf(x, c, -ys);\n",
+     "    *xo = fmaf(x, c, ys);\n"),
+    ("store: cos and sin columns swapped",
+     "                        float c = rco_f32(cos_sin[pos * RCO_HEAD + j]);\n"
+     "                        float sn = rco_f32(cos_sin[pos * RCO_HEAD + RCO_HEAD / 2 + j]);\n",
+     "                        float c = rco_f32(cos_sin[pos * RCO_HEAD + RCO_HEAD / 2 + j]);\n"
+     "                        float sn = rco_f32(cos_sin[pos * RCO_HEAD + j]);\n"),
+    ("store: V half of the cache written from K",
+     "memcpy(dst + RCO_HEAD, vh,", "memcpy(dst + RCO_HEAD, kh,"),
+    ("store: block and page of a slot swapped",
+     "            int64_t blk = s / block_size, page = s % block_size;\n",
+     "            int64_t page = s / block_size, blk = s % block_size;\n"),
+    ("inverse RMS without eps",
+     "    float v = fmaf(sumsq, inv_width, eps);\n",
+     "    float v = sumsq * inv_width;\n"),
+    ("bf16 rounding: ties away from zero instead of to even",
+     "    u += 0x7FFFu + ((u >> 16) & 1u);\n",
+     "    u += 0x8000u;\n"),
+    ("layer norms: gains not applied",
+     "                float y = z[c] * r2;\n                if (g)\n                    y = y * rco_f32(g[c]);\n",
+     "                float y = z[c] * r2;\n"),
+    ("norm options: gain center not added",
+     "    if (n->center != 0.0f)\n        g = g + n->center;\n",
+     "    (void)n->center;\n"),
+    ("norm options: input-scale weight applied after the sum of squares",
+     "        u[c] = pre_scale ? norm_gain(n, offset, c) * v[c] : v[c];\n",
+     "        u[c] = v[c];\n"),
+    ("norm options: FP32 weights read as bf16",
+     "    if (n->fp32)\n        g = ((const float *)n->weight)[offset + c];\n",
+     "    if (n->fp32)\n        g = rco_f32(rco_bf16_rn(((const float *)n->weight)[offset + c]));\n"),
+    ("QKV front: cached K taken from the raw projection",
+     "                memcpy(dst, o + q_size + h * RCO_HEAD,",
+     "                memcpy(dst, rr + q_size + h * RCO_HEAD,"),
+    ("QKV front: cached K taken from the Q heads",
+     "                memcpy(dst, o + q_size + h * RCO_HEAD,",
+     "                memcpy(dst, o + h * RCO_HEAD,"),
+]
+
+
+def _run_pins(tmp_path, old, new):
+    src = open(oracle._SRC).read()
+    if old is not None:
+        assert src.count(old) == 1, "the line to mutate is no longer in the oracle"
+        src = src.replace(old, new)
+    c_file = tmp_path / "mutant.c"
+    c_file.write_text(src)
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", *oracle.CFLAGS, "-o", str(so), str(c_file), "-lm"], check=True)
+    env = dict(os.environ, RCO_ORACLE_LIB=str(so))
+    return subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "not gpu",
+                           "-p", "no:cacheprovider", *PINS],
+                          cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+
+
+def test_unmodified_copy_passes_the_pins(tmp_path):
+    r = _run_pins(tmp_path, None, None)
+    assert r.returncode == 0, r.stdout[-2000:]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(tmp_path, name, old, new):
+    r = _run_pins(tmp_path, old, new)
+    # 1: a pin failed; a negative code: the planted mistake crashed the run
+    # (an address mistake can write outside the cache).  Collection or
+    # usage errors (2-5) do not count as caught.
+    assert r.returncode == 1 or r.returncode < 0, \
+        f"no pin failed with the mistake '{name}' planted (exit {r.returncode}):\n{r.stdout[-1500:]}"

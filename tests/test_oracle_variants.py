@@ -105,6 +105,27 @@ def test_input_scale_single_nonzero(orc):
         assert np.all((out[0, 0, others] & 0x7FFF) == 0)
 
 
+def test_input_scale_weight_shapes_the_row(orc):
+    # two non-zero inputs 1 and 1 at columns 5 and 900, gains 1 and 2 there,
+    # eps = 0: an input-scale weight makes u = (1, 2), so the norm's output
+    # is (1, 2) * sqrt(8192 / 5) = (40.48, 80.95) -> bf16 (40.5, 81.0); a
+    # weight that were dropped would leave (64, 64).  Seen through either
+    # norm (the other weightless; a weightless layer norm of a row shaped
+    # (1, 2) gives the same (1, 2) * sqrt(8192 / 5) again).
+    x = np.zeros((1, D), dtype=np.uint16)
+    x[0, [5, 900]] = bf16_bits([1.0, 1.0])
+    g = np.full(D, bf16_bits([1.0])[0], dtype=np.uint16)
+    g[900] = bf16_bits([2.0])[0]
+    want = np.array([1.0, 2.0]) * math.sqrt(8192.0 / 5.0)
+    assert all(far_from_bf16_boundary(v) for v in want)
+    hidden = norms(orc, x, 1, hidden_w=g, hidden_input_scale=True)
+    layer = norms(orc, x, 1, pre_w=g[None, :], pre_input_scale=True)
+    for out in (hidden, layer):
+        assert np.array_equal(out[0, 0, [5, 900]], bf16_bits(want))
+        others = np.delete(np.arange(D), [5, 900])
+        assert np.all((out[0, 0, others] & 0x7FFF) == 0)
+
+
 def test_pre_input_scale_layers_equal_weightless(orc):
     # gamma_l == 2^l scales u by 2^l and r by 2^-l: with eps = 0 every
     # layer's output equals the weightless norm's, bit for bit (exact)
