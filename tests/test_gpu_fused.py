@@ -134,7 +134,8 @@ def test_fused_matches_unfused_chain(layout):
     assert err == got["err"]
 
 
-def test_tail_split_projection():
+@pytest.mark.parametrize("layout", [rc.RC_W_KN, rc.RC_W_NK])
+def test_tail_split_projection(layout):
     # 80 tiles of 256 x 256 over 76 CTA pairs: the persistent kernel takes
     # 76, and the last layer's final row block (rows 2304-2499, ragged) runs
     # as a split-K launch of its own when a workspace is given
@@ -144,10 +145,11 @@ def test_tail_split_projection():
                                  num_blocks=(T + 15) // 16 + 4, block_size=16)
     assert rc.workspace_size(L, T, 8192, N) > 0, "no tail split planned on this device"
     normed = oracle.context_norms(case["x"], case["hidden_w"], case["pre_w"], L, case["eps"])
-    nd, wd = parity.dev_bf16(normed, DEV), parity.dev_bf16(case["W"], DEV)
+    Wl = case["W"] if layout == rc.RC_W_KN else np.ascontiguousarray(case["W"].transpose(0, 2, 1))
+    nd, wd = parity.dev_bf16(normed, DEV), parity.dev_bf16(Wl, DEV)
     ws = rc.new_workspace(L, T, 8192, N, DEV)
-    tailed = parity.host_bits(rc.kv_project(nd, wd, workspace=ws))
-    plain = parity.host_bits(rc.kv_project(nd, wd))
+    tailed = parity.host_bits(rc.kv_project(nd, wd, w_layout=layout, workspace=ws))
+    plain = parity.host_bits(rc.kv_project(nd, wd, w_layout=layout))
     sample = np.unique(np.r_[0, 2303, 2304, 2305, T - 1, np.linspace(0, T - 1, 120).astype(int),
                              np.arange(2304, T, 9)])
     ref64, ab = oracle.kv_project(normed, case["W"], rows=sample)
@@ -155,7 +157,7 @@ def test_tail_split_projection():
     parity.assert_projection_close(plain[:, sample], ref64, ab, "projection without it")
     # rows outside the tail come from the same persistent kernel either way
     assert np.array_equal(tailed[0], plain[0]) and np.array_equal(tailed[1, :2304], plain[1, :2304])
-    caches, kv, err = run_fused(case, nd, wd, workspace=True, kv_out=True)
+    caches, kv, err = run_fused(case, nd, wd, workspace=True, kv_out=True, layout=layout)
     assert np.array_equal(kv, tailed), "the fused call's projection differs from rc_kv_project's"
     ref_caches = parity.make_caches(case, L, parity.SENTINEL)
     ref_err = oracle.kv_store_from_projection(kv, H, case["positions"], case["slots"],
@@ -163,6 +165,29 @@ def test_tail_split_projection():
     for g, r in zip(caches, ref_caches):
         assert np.array_equal(g, r)
     assert err == ref_err
+
+
+@pytest.mark.parametrize("last_rows", [2000, 2304, 2400])
+def test_tail_split_with_layer_row_counts(last_rows):
+    # the last layer stores its first last_rows rows: none of the tail's rows
+    # (2304-2499) when last_rows <= 2304, some of them otherwise
+    T, L, H = 2500, 2, 8
+    case = workloads.random_case(4343, T=T, L=L, H=H, max_position=512,
+                                 num_blocks=(T + 15) // 16 + 4, block_size=16)
+    case = dict(case, slots=[case["slots"][0], np.ascontiguousarray(case["slots"][1][:last_rows])])
+    normed = oracle.context_norms(case["x"], case["hidden_w"], case["pre_w"], L, case["eps"])
+    nd, wd = parity.dev_bf16(normed, DEV), parity.dev_bf16(case["W"], DEV)
+    caches, kv, err = run_fused(case, nd, wd, workspace=True, kv_out=True)
+    ref_caches = parity.make_caches(case, L, parity.SENTINEL)
+    ref_err = oracle.kv_store_from_projection(kv, H, case["positions"], case["slots"],
+                                              case["cos_sin"], ref_caches, case["eps"],
+                                              np.array([T, last_rows]))
+    for g, r in zip(caches, ref_caches):
+        assert np.array_equal(g, r)
+    assert err == ref_err
+    sample = np.array([0, 2303, 2304, 2400, T - 1])
+    ref64, ab = oracle.kv_project(normed, case["W"], rows=sample)
+    parity.assert_projection_close(kv[:, sample], ref64, ab)
 
 
 @pytest.mark.parametrize("index", [1, 2, 3, 4, 5])
