@@ -611,21 +611,23 @@ def run_front(args):
     cache = torch.zeros(case["cache_shape"], dtype=torch.bfloat16, device=dev)
     out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     nh, nkv, eps = case["num_heads"], case["num_kv_heads"], case["eps"]
-    call = lambda: rc.qkv_front(hidden, W, nh, nkv, positions, cs, slots, cache, eps, out=out, err=err)
-    for i in range(args.warmup):
-        flush.fill_(i & 0xFF)
-        call()
+    # Consecutive steps use two draft layers' weights in turn, as a decode
+    # step's layers do: each W (151 MB) exceeds L2 and the other was read
+    # since, so every step reads its W from HBM, and no flush is needed.
+    Ws = [W, bf(workloads.front_case(4000 + M, M)["W"])]
+    call = lambda i: rc.qkv_front(hidden, Ws[i % 2], nh, nkv, positions, cs, slots, cache, eps,
+                                  out=out, err=err)
+    for i in range(max(args.warmup, 2)):
+        call(i)
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True, external=True),
             torch.cuda.Event(enable_timing=True, external=True)) for _ in range(args.steps)]
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)
             evs[i][0].record()
-            call()
+            call(i)
             evs[i][1].record()
     g.replay()
     torch.cuda.synchronize()
@@ -647,18 +649,17 @@ def run_front(args):
     # end to end: hidden rows in from pinned memory, the output rows back
     h_h = torch.from_numpy(case["hidden"].view(np.int16)).view(torch.bfloat16).pin_memory()
     o_h = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
-    def e2e_step(ev=None):
+    def e2e_step(i, ev=None):
         if ev:
             ev[0].record()
         hidden.copy_(h_h, non_blocking=True)
-        call()
+        call(i)
         o_h.copy_(out, non_blocking=True)
         if ev:
             ev[1].record()
 
-    for i in range(args.warmup):
-        flush.fill_(i & 0xFF)
-        e2e_step()
+    for i in range(max(args.warmup, 2)):
+        e2e_step(i)
     torch.cuda.synchronize()
     # as one captured graph, like the timed device steps
     e2e_evs = [(torch.cuda.Event(enable_timing=True, external=True),
@@ -666,8 +667,7 @@ def run_front(args):
     ge = torch.cuda.CUDAGraph()
     with torch.cuda.graph(ge):
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)
-            e2e_step(e2e_evs[i])
+            e2e_step(i, e2e_evs[i])
     ge.replay()
     torch.cuda.synchronize()
     if world > 1:
@@ -684,7 +684,8 @@ def run_front(args):
     oracle.build()
     cpu_s = oracle_front_seconds(case, M)
     rec = front_record(args, case, world, M)
-    rec["config"]["l2"] = "flushed (512 MiB write) before every timed step; W (151 MB) exceeds L2"
+    rec["config"]["l2"] = ("no flush: inputs larger than L2 (steps alternate two layers' weights, "
+                           "2 x 151 MB against 129 MB of L2, so each step reads its W from HBM)")
     rec["config"]["timing"] = "cuda graph"
     rec.update({
         "value": world * M * args.steps / (total_ms / 1e3),
