@@ -42,6 +42,10 @@ NCU_TRAFFIC = {
     # 0.83 MB written) + k3_reduce_store (18.99 MB read); ncu with its default
     # cache flush before each launch.
     (2, "store", "project_store"): 95_506_752,
+    # workload 3: k2_project_pair_persistent (339.69 MB read, 23.36 MB
+    # written) + the tail's k2_project_pair (46.16 + 1.09 MB) +
+    # k3_reduce_store (14.73 MB read); ncu's default cache flush as above.
+    (3, "store", "project_store"): 425_024_768,
 }
 
 
