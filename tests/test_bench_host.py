@@ -1,0 +1,79 @@
+"""bench.py's host-side arithmetic on CPU: the algorithmic byte and FLOP
+counts behind the roofline figures, the clock summary behind the
+throttle check, and the L2 flush sizes.  The counts are checked against
+sums taken element by element over the operands, not against the formulas
+themselves."""
+import numpy as np
+
+import bench
+import workloads
+
+L2_BYTES = 129 * 10**6        # GB300's L2
+
+
+def test_norm_and_projection_counts_by_operand():
+    for w in workloads.WORKLOADS.values():
+        c = bench.algorithmic_counts(w, splits=1)
+        # norms: x read once, L rows written, and each gain vector read once
+        operands = [(w.T, w.D)] + [(w.T, w.D)] * w.L
+        if w.hidden_weighted:
+            operands.append((w.D,))
+        if w.pre_weighted:
+            operands += [(w.D,)] * w.L
+        assert c["k1_bytes"] == sum(2 * int(np.prod(s)) for s in operands)
+        # projection: one multiply and one add per (layer, row, k, column)
+        assert c["k2_flops"] == 2 * w.L * w.T * w.D * w.N
+        assert c["k2_bytes"] == 2 * (w.L * w.T * w.D + w.L * w.D * w.N + w.L * w.T * w.N)
+    w2 = workloads.WORKLOADS[2]
+    assert bench.algorithmic_counts(w2, 3)["k1_bytes"] == 33_619_968
+    assert bench.algorithmic_counts(w2, 3)["k2_flops"] == 25_769_803_776
+
+
+def test_store_bytes_counts_live_rows():
+    w = workloads.WORKLOADS[2]
+    cap = w.num_blocks * w.block_size
+    rng = np.random.default_rng(5)
+    slots = [rng.integers(-3, cap + 3, size=40).astype(np.int64) for _ in range(2)]
+    for rope in (False, True):
+        expect = 0
+        for s in slots:
+            for v in s:
+                expect += 8                           # the slot itself
+                if 0 <= v < cap:
+                    expect += w.H * 64 * 2 * 2        # K and V read
+                    expect += w.H * 128 * 2           # the cache row written
+                    if rope:
+                        expect += 8 + 64 * 2          # position and table row
+        assert bench.store_bytes(w, slots, rope) == expect
+
+
+def test_front_bytes_by_operand():
+    M, nh, nkv, D = 3, 4, 2, 256
+    case = workloads.front_case(11, M, D=D, num_heads=nh, num_kv_heads=nkv)
+    N = case["W"].shape[0]
+    live = M
+    expect = (case["W"].nbytes + case["hidden"].nbytes + M * N * 2 + case["positions"].nbytes
+              + case["slots"].nbytes + M * case["cos_sin"].shape[1] * 2 + live * nkv * 128 * 2)
+    assert bench.front_bytes(M, D, N, nkv, live) == expect
+
+
+def test_clock_summary():
+    lines = [
+        "0, 2070, 2070, 900.1, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n",
+        "0, 1950, 2070, 1390.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n",
+        "0, 1980, 2070, 1380.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n",
+        "garbage line\n",
+    ]
+    c = bench.summarise_clocks(lines)
+    assert c == {"sm_mhz": 1980.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    hot = lines[:1] + ["0, 1500, 2070, 1200.0, 0x48, Active, Active, Not Active, Not Active\n"]
+    assert bench.summarise_clocks(hot)["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
+    assert bench.summarise_clocks(["\n"]) is None
+
+
+def test_flush_buffers_exceed_l2():
+    assert bench.L2_FLUSH_BYTES > L2_BYTES and bench.L2_CLEAN_BYTES > L2_BYTES
+    f = bench.L2Flush("cpu")
+    f(7)
+    assert f.w.numel() == bench.L2_FLUSH_BYTES and int(f.w[0]) == 7
+    assert f.r.numel() * f.r.element_size() == bench.L2_CLEAN_BYTES
