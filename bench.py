@@ -68,6 +68,61 @@ class L2Flush:
         torch.sum(self.r, dim=0, keepdim=True, dtype=torch.int32, out=self.s)
 
 
+def row_chunks(T: int, n: int):
+    """n nearly equal row ranges covering rows 0..T-1; n = 0 picks 8 ranges
+    from 16384 rows and one range below that (measured on GB300: with 8
+    ranges the end-to-end step took 4.54 ms instead of 5.14 at 32768 rows and
+    2.66 ms instead of 2.74 at 16384, while at 512 and 4096 rows the ranges'
+    smaller projections cost more than the overlap saved)."""
+    if n <= 0:
+        n = 8 if T >= 16384 else 1
+    n = max(1, min(n, T))
+    edges = [T * i // n for i in range(n + 1)]
+    return [(edges[i], edges[i + 1]) for i in range(n)]
+
+
+class OverlappedChain:
+    """rc_context_norms + rc_kv_project_store over row ranges, so that the
+    norms of range c + 1 (which may read x in place from pinned host memory
+    over the host link) run while range c is projected and stored on a
+    second stream.  Rows are independent, so every row's K and V reach the
+    caches as the single pair of calls would store them; only the
+    projection's split plan follows the range's size, so its FP32 summation
+    order (and with it the last bit of a K/V value) may differ.  Each range
+    gets its own slice of one [L, T, D] norms buffer; the ranges' projections
+    run in order on the second stream and share one split-K workspace."""
+
+    def __init__(self, L: int, T: int, D: int, N: int, chunks, dev):
+        import torch
+        import rope_chain_gb300 as rc
+        self.rc, self.L, self.chunks = rc, L, chunks
+        flat = torch.empty(L * T * D, dtype=torch.bfloat16, device=dev)
+        self.normed = [flat[L * r0 * D:L * r1 * D].view(L, r1 - r0, D) for r0, r1 in chunks]
+        ws = max(rc.workspace_size(L, r1 - r0, D, N) for r0, r1 in chunks)
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=dev) if ws else None
+        self.proj = torch.cuda.Stream(device=dev)
+        self.done = [torch.cuda.Event() for _ in chunks]
+
+    def __call__(self, x, hidden_w, pre_w, W, H, positions, slots, cos_sin, caches, eps, err,
+                 inputs_ready=None):
+        """One pass on the current stream; inputs_ready (a stream) is waited
+        for before the first projection (positions and slots copied there)."""
+        import torch
+        main = torch.cuda.current_stream()
+        self.proj.wait_stream(main)
+        if inputs_ready is not None:
+            self.proj.wait_stream(inputs_ready)
+        for (r0, r1), nc, ev in zip(self.chunks, self.normed, self.done):
+            self.rc.context_norms(x[r0:r1], hidden_w, pre_w, self.L, eps, out=nc)
+            ev.record(main)
+            self.proj.wait_event(ev)
+            with torch.cuda.stream(self.proj):
+                self.rc.kv_project_store(nc, W, H, positions[r0:r1],
+                                         [None if s_ is None else s_[r0:r1] for s_ in slots],
+                                         cos_sin, caches, eps, err=err, workspace=self.ws)
+        main.wait_stream(self.proj)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -441,6 +496,10 @@ def run_ours(args, w):
     h2d = x_h.numel() * 2 + meta_h.numel() * 8
 
     side = torch.cuda.Stream(device=dev)
+    # On the default path the rows go through in ranges (OverlappedChain):
+    # the host read of x for range c + 1 overlaps the projection of range c.
+    chunks = row_chunks(w.T, args.e2e_chunks) if args.path == "store" else [(0, w.T)]
+    overlapped = OverlappedChain(w.L, w.T, w.D, w.N, chunks, dev) if len(chunks) > 1 else None
 
     def e2e_step(ev0, ev1):
         # the metadata copy runs on a side stream while the norms read x;
@@ -450,7 +509,11 @@ def run_ours(args, w):
         side.wait_stream(main)
         with torch.cuda.stream(side):
             meta_d.copy_(meta_h, non_blocking=True)
-        chain(xs=x_h, pos=pos_e, sl=slots_e, before_store=lambda: main.wait_stream(side))
+        if overlapped is not None:
+            overlapped(x_h, hw, pw, W, w.H, pos_e, slots_e, cs, caches, w.eps, err,
+                       inputs_ready=side)
+        else:
+            chain(xs=x_h, pos=pos_e, sl=slots_e, before_store=lambda: main.wait_stream(side))
         err_h.copy_(err, non_blocking=True)
         ev1.record()
 
@@ -554,7 +617,11 @@ def run_ours(args, w):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4, "timing": timing,
                 "inputs": "x read in place from pinned host memory by the norms kernel "
                           "(NVLink-C2C); positions and slot maps in one pinned buffer, one "
-                          "copy per step" + ("" if whole else " alongside the norms")},
+                          "copy per step" + ("" if whole else " alongside the norms"),
+                "row_ranges": len(chunks),
+                "overlap": (f"{len(chunks)} row ranges: the norms of range c + 1 read x "
+                            "while range c is projected and stored on a second stream")
+                           if overlapped is not None else "none"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     })
@@ -744,6 +811,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--e2e-chunks", type=int, default=0, metavar="N",
+                    help="row ranges of the end-to-end steps on the default path "
+                         "(0: 8 from 16384 rows, else 1)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="store", choices=["store", "whole", "variants", "front"],
                     help="store: norms + fused projection/store; whole: rc_context_kv; variants: "

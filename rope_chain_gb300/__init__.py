@@ -138,9 +138,12 @@ def device_address(t: torch.Tensor) -> int:
     if t.is_cuda:
         return t.data_ptr()
     if t.device.type == "cpu" and t.is_pinned():
+        # the mapping of the storage's start, plus t's offset into it (t may
+        # be a slice of a pinned buffer)
+        base = t.untyped_storage().data_ptr()
         d = _vp(0)
-        _check(lib().rc_device_address(t.data_ptr(), ctypes.byref(d)))
-        return int(d.value)
+        _check(lib().rc_device_address(base, ctypes.byref(d)))
+        return int(d.value) + (t.data_ptr() - base)
     raise TypeError("expected a CUDA tensor or a pinned CPU tensor")
 
 
