@@ -64,6 +64,28 @@ MUTANTS = [
     ("norm options: FP32 weights read as bf16",
      "    if (n->fp32)\n        g = ((const float *)n->weight)[offset + c];\n",
      "    if (n->fp32)\n        g = rco_f32(rco_bf16_rn(((const float *)n->weight)[offset + c]));\n"),
+    ("projection: every layer uses layer 0's W",
+     "                const uint16_t *w = W + (int64_t)l * D * N;\n",
+     "                const uint16_t *w = W;\n"),
+    ("projection: W [L, N, D] read as [L, D, N]",
+     "                        double p = (double)rco_f32(a[k]) * (double)rco_f32(wn[k]);\n",
+     "                        double p = (double)rco_f32(a[k]) * (double)rco_f32(w[(int64_t)k * N + n]);\n"),
+    ("store: RoPE at the row index instead of the row's position",
+     "                pos = positions[t];\n",
+     "                pos = t;\n"),
+    ("store: a slot past the cache skipped without being counted",
+     "            if (s >= capacity) {\n                skipped += 1;\n",
+     "            if (s >= capacity) {\n"),
+    ("store: K heads addressed with V's row stride",
+     "                const uint16_t *kh = k + l * k_layer_stride + t * k_row_stride + (int64_t)h * RCO_HEAD;\n",
+     "                const uint16_t *kh = k + l * k_layer_stride + t * v_row_stride + (int64_t)h * RCO_HEAD;\n"),
+    ("QKV front: Q heads passed through without the QK-norm",
+     "        for (int32_t h = 0; h < num_heads + num_kv_heads; ++h) {\n",
+     "        memcpy(o, rr, (size_t)q_size * sizeof(uint16_t));\n"
+     "        for (int32_t h = num_heads; h < num_heads + num_kv_heads; ++h) {\n"),
+    ("QKV front: a bad position still inserted",
+     "        const int insert = s >= 0 && !bad_slot && !bad_pos;\n",
+     "        const int insert = s >= 0 && !bad_slot;\n"),
     ("QKV front: cached K taken from the raw projection",
      "                memcpy(dst, o + q_size + h * RCO_HEAD,",
      "                memcpy(dst, rr + q_size + h * RCO_HEAD,"),

@@ -179,6 +179,60 @@ def test_rope_identity_quarter_turn_and_norm(orc):
     assert np.array_equal(roped[0][..., HD:], plain[0][..., HD:])
 
 
+def test_rope_follows_each_rows_position(orc):
+    # the rotation of row t comes from table row positions[t], not from t:
+    # positions [1, 2, 0] give row 0 the quarter turn and row 2 the identity;
+    # and permuting the rows with their positions and slots stores the same
+    # cache bits
+    rng = np.random.default_rng(14)
+    H, L, T = 2, 1, 3
+    kv = rnd_bf16(rng, (L, T, 2 * H * HD))
+    slots = [np.arange(T, dtype=np.int64)]
+    plain = _caches(L, 1, H, 4)
+    _store(orc, kv, H, None, slots, None, plain)
+    ang = rng.uniform(0, 2 * np.pi, 32)
+    tab = np.zeros((3, HD), dtype=np.uint16)
+    tab[0] = _table(1, np.ones(32), np.zeros(32))[0]
+    tab[1] = _table(1, np.zeros(32), np.ones(32))[0]
+    tab[2] = _table(1, np.cos(ang), np.sin(ang))[0]
+    positions = np.array([1, 2, 0], dtype=np.int64)
+    roped = _caches(L, 1, H, 4)
+    _store(orc, kv, H, positions, slots, tab, roped)
+    n = to_f64(plain[0][0, :, :, :HD])
+    r = to_f64(roped[0][0, :, :, :HD])
+    assert np.array_equal(r[:, 0, 0::2], -n[:, 0, 1::2]) and np.array_equal(r[:, 0, 1::2], n[:, 0, 0::2])
+    assert np.array_equal(r[:, 2], n[:, 2])
+    perm = np.array([2, 0, 1])
+    again = _caches(L, 1, H, 4)
+    _store(orc, np.ascontiguousarray(kv[:, perm]), H, positions[perm], [slots[0][perm]], tab, again)
+    assert np.array_equal(again[0], roped[0])
+
+
+def test_store_separate_k_and_v_strides(orc):
+    # K from a packed [L, T, 64H] buffer and V from the middle third of a
+    # [L, T, 192H] buffer (different row and layer strides) store the same
+    # cache bits as the [K | V] rows of the projection
+    rng = np.random.default_rng(15)
+    H, L, T, P = 2, 2, 5, 4
+    kv = rnd_bf16(rng, (L, T, 2 * H * HD))
+    slots = [rng.permutation(8)[:T].astype(np.int64) for _ in range(L)]
+    positions = rng.integers(0, P, T).astype(np.int64)
+    inv = 10000.0 ** (-np.arange(32) / 32.0)
+    tab = np.concatenate([_table(1, np.cos(p * inv), np.sin(p * inv)) for p in range(P)])
+    ref = _caches(L, 2, H, 4)
+    assert _store(orc, kv, H, positions, slots, tab, ref) == 0
+    k = np.ascontiguousarray(kv[..., :H * HD]).reshape(-1)
+    wide = np.zeros((L, T, 3 * H * HD), dtype=np.uint16)
+    wide[..., H * HD:2 * H * HD] = kv[..., H * HD:]
+    v = wide.reshape(-1)[H * HD:]
+    got = _caches(L, 2, H, 4)
+    err = orc.kv_store(k, v, T * H * HD, H * HD, T * 3 * H * HD, 3 * H * HD, positions, slots,
+                       tab, got, H, 1e-6, T)
+    assert err == 0
+    for g, r in zip(got, ref):
+        assert np.array_equal(g, r)
+
+
 def test_rope_reads_cos_then_sin_per_pair(orc):
     # pair j gets cos from column j and sin from column 32 + j: a table whose
     # pair j rotates by a quarter turn only for even j tells them apart
