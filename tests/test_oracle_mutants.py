@@ -86,6 +86,27 @@ MUTANTS = [
     ("QKV front: a bad position still inserted",
      "        const int insert = s >= 0 && !bad_slot && !bad_pos;\n",
      "        const int insert = s >= 0 && !bad_slot;\n"),
+    ("layer norms: every layer takes layer 0's gains",
+     "            const uint16_t *g = pre_w ? pre_w + (int64_t)l * RCO_D : NULL;\n",
+     "            const uint16_t *g = pre_w ? pre_w : NULL;\n"),
+    ("hidden norm: gain applied before the inverse RMS is rounded in",
+     "            float y = v[c] * r;\n            if (hidden_w)\n                y = y * rco_f32(hidden_w[c]);\n",
+     "            float y = v[c];\n            if (hidden_w)\n                y = y * rco_f32(hidden_w[c]);\n            y = y * r;\n"),
+    ("inverse RMS: eps added after the square root",
+     "    float v = fmaf(sumsq, inv_width, eps);\n    float root = sqrtf(v);\n",
+     "    float v = sumsq * inv_width;\n    float root = sqrtf(v) + eps;\n"),
+    ("RoPE: rounded products instead of the fused multiply-adds",
+     "    *xo = fmaf(x, c, -ys);\n",
+     "    *xo = x * c - ys;\n"),
+    ("float64 to bf16: rounded through binary32 first",
+     "    if (isnan(d))\n        return (uint16_t)0x7FFFu;\n    uint16_t sign",
+     "    if (isnan(d))\n        return (uint16_t)0x7FFFu;\n    if (d == d)\n        return rco_bf16_rn((float)d);\n    uint16_t sign"),
+    ("store: a negative slot counted as an error",
+     "            if (s < 0)\n                continue;\n            if (s >= capacity) {",
+     "            if (s < 0) {\n                skipped += 1;\n                continue;\n            }\n            if (s >= capacity) {"),
+    ("QKV front: the gate columns dropped",
+     "(size_t)(kv_size + q_size) * sizeof(uint16_t));",
+     "(size_t)(kv_size) * sizeof(uint16_t));"),
     ("QKV front: cached K taken from the raw projection",
      "                memcpy(dst, o + q_size + h * RCO_HEAD,",
      "                memcpy(dst, rr + q_size + h * RCO_HEAD,"),

@@ -210,3 +210,46 @@ def test_rms_of_output_is_one(orc):
     of = (out.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     ms = np.mean(of ** 2, axis=-1)
     assert np.all(np.abs(ms - 1.0) < 2.0 ** -7)
+
+
+def test_hidden_gain_multiplies_after_the_inverse_rms(orc):
+    # z_c = bf16((x_c * r) * g_c): the row is scaled by its inverse RMS, then
+    # by the gain.  (x_c * g_c) * r rounds differently now and then; among
+    # two-sparse rows (one rounding in their sum of squares, so r is
+    # unambiguous) find some where the two orders give different outputs and
+    # check the oracle follows the first.
+    eps = np.float32(1e-6)
+    rng = np.random.default_rng(21)
+    n = 1 << 20
+    f = lambda bits: (bits.astype(np.uint32) << 16).view(np.float32)
+    x = f(rng_bf16(rng, (n, 2), 0.0, 1.0))
+    g = f(rng_bf16(rng, (n, 2), 1.0, 0.1))
+    keep = np.all(np.abs(x) >= 0.25, axis=1)
+    x, g = x[keep], g[keep]
+    S = x[:, 0] * x[:, 0] + x[:, 1] * x[:, 1]
+    # fma(S, 2^-13, eps): exact in float64 for these S, then one rounding
+    v = (S.astype(np.float64) * 2.0 ** -13 + np.float64(eps)).astype(np.float32)
+    r = np.float32(1.0) / np.sqrt(v)
+    rn = lambda a: bf16_bits(a.astype(np.float64)).reshape(a.shape)   # bf16 of float32, RNE
+    first = rn((x * r[:, None]) * g)
+    other = rn((x * g) * r[:, None])
+    hits = np.flatnonzero(np.any(first != other, axis=1))
+    a, b = 100, 5000
+    checked = 0
+    for i in hits:
+        expect = []
+        for z_bits in (first[i], other[i]):
+            z = f(z_bits.astype(np.uint16))
+            r2 = orc.inv_rms(z[0] * z[0] + z[1] * z[1], 2.0 ** -13, eps)
+            expect.append(rn(z * np.float32(r2)))
+        if np.array_equal(expect[0], expect[1]):
+            continue                     # the layer norm hides the difference
+        assert orc.inv_rms(S[i], 2.0 ** -13, eps) == r[i]
+        row = np.zeros((1, D), dtype=np.uint16)
+        row[0, a], row[0, b] = bits_of(x[i])
+        hid = np.full(D, 0x3F80, dtype=np.uint16)
+        hid[a], hid[b] = bits_of(g[i])
+        out = orc.context_norms(row, hid, None, 1, float(eps))
+        assert out[0, 0, a] == expect[0][0] and out[0, 0, b] == expect[0][1]
+        checked += 1
+    assert checked >= 2

@@ -259,6 +259,28 @@ def test_rope_scalar_closed_forms(orc):
     assert orc.rope(0.75, -2.5, -1.0, 0.0) == (np.float32(-0.75), np.float32(2.5))
 
 
+def test_rope_uses_fused_multiply_adds(orc):
+    # x' = fma(x, c, -(y s)) and y' = fma(y, c, x s): x c enters unrounded.
+    # For random pairs where rounding x c (or y c) first changes the float32
+    # result, the oracle gives the fused one, computed here exactly.
+    from fractions import Fraction
+    rng = np.random.default_rng(22)
+    n = 4096
+    x, y, c, s = (rng.uniform(0.5, 2.0, n).astype(np.float32) for _ in range(4))
+    f64 = lambda a: a.astype(np.float64)
+    ys, xs = (f64(y) * f64(s)).astype(np.float32), (f64(x) * f64(s)).astype(np.float32)
+    ex, ey = f64(x) * f64(c) - f64(ys), f64(y) * f64(c) + f64(xs)    # exact (checked below)
+    fused_x, fused_y = ex.astype(np.float32), ey.astype(np.float32)
+    split_x, split_y = (x * c) - ys, (y * c) + xs
+    hits = np.flatnonzero((fused_x != split_x) | (fused_y != split_y))
+    assert len(hits) >= 20
+    for i in hits[:20]:
+        fr = lambda v: Fraction(float(v))
+        assert fr(x[i]) * fr(c[i]) - fr(ys[i]) == Fraction(float(ex[i]))
+        assert fr(y[i]) * fr(c[i]) + fr(xs[i]) == Fraction(float(ey[i]))
+        assert orc.rope(x[i], y[i], c[i], s[i]) == (fused_x[i], fused_y[i])
+
+
 def test_out_of_range_rows_are_counted_not_written(orc):
     rng = np.random.default_rng(5)
     H, L, T, nb, bs = 2, 2, 5, 2, 4
