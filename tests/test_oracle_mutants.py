@@ -107,6 +107,21 @@ MUTANTS = [
     ("QKV front: the gate columns dropped",
      "(size_t)(kv_size + q_size) * sizeof(uint16_t));",
      "(size_t)(kv_size) * sizeof(uint16_t));"),
+    ("norm options: the layer norms read the hidden norm's options",
+     "            norm_row(z, pre, (int64_t)l * RCO_D, y);\n",
+     "            norm_row(z, hidden, 0, y);\n"),
+    ("norm options: the layer norm reads the unrounded hidden output",
+     "        for (int c = 0; c < RCO_D; ++c)\n            z[c] = rco_f32(rco_bf16_rn(y[c]));\n",
+     "        for (int c = 0; c < RCO_D; ++c)\n            z[c] = y[c];\n"),
+    ("bf16 rounding: subnormal results flushed to zero",
+     "    u += 0x7FFFu + ((u >> 16) & 1u);\n",
+     "    if ((u & 0x7F800000u) == 0u)\n        u &= 0x80000000u;\n    u += 0x7FFFu + ((u >> 16) & 1u);\n"),
+    ("QKV front: only the K heads rotated",
+     "                if (rotate) {\n",
+     "                if (rotate && h >= num_heads) {\n"),
+    ("QKV front: a bad row counted once per problem",
+     "        if ((bad_pos || bad_slot) && err)\n            *err += 1;\n",
+     "        if (err)\n            *err += bad_pos + bad_slot;\n"),
     ("QKV front: cached K taken from the raw projection",
      "                memcpy(dst, o + q_size + h * RCO_HEAD,",
      "                memcpy(dst, rr + q_size + h * RCO_HEAD,"),

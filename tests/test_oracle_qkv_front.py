@@ -75,14 +75,15 @@ def test_no_table_is_norm_only(orc):
 
 def test_cache_insert_and_skips(orc):
     rng = np.random.default_rng(3)
-    M, nh, nkv, nb, bs = 6, 2, 4, 3, 4
+    M, nh, nkv, nb, bs = 7, 2, 4, 3, 4
     raw = bf16_bits(rng.standard_normal((M, 64 * (2 * nh + 2 * nkv))))
-    pos = np.array([0, 1, 2, 3, 99, 5], dtype=np.int64)      # row 4: position past the table
-    slots = np.array([7, -1, 0, 12, 3, 11], dtype=np.int64)  # row 3: slot past the cache (12)
+    # row 3: slot past the cache (12); row 4: position past the table; row 6: both
+    pos = np.array([0, 1, 2, 3, 99, 5, 100], dtype=np.int64)
+    slots = np.array([7, -1, 0, 12, 3, 11, 13], dtype=np.int64)
     cs = table(8)
     cache = np.full((nb, nkv, bs, 128), SENT, dtype=np.uint16)
     out, err = orc.qkv_front_post(raw, nh, nkv, pos, cs, slots, cache, 1e-5)
-    assert err == 2                                # rows 3 and 4
+    assert err == 3                                # one per bad row: 3, 4 and 6
     q, kv = 64 * nh, 64 * nkv
     written = {}
     for m in (0, 2, 5):                            # valid slots
