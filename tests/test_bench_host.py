@@ -77,3 +77,16 @@ def test_flush_buffers_exceed_l2():
     f(7)
     assert f.w.numel() == bench.L2_FLUSH_BYTES and int(f.w[0]) == 7
     assert f.r.numel() * f.r.element_size() == bench.L2_CLEAN_BYTES
+
+
+def test_row_chunks_cover_rows_once():
+    for T in (1, 5, 64, 512, 600, 4096, 16384, 32768):
+        for n in (0, 1, 2, 3, 8):
+            ch = bench.row_chunks(T, n)
+            assert ch[0][0] == 0 and ch[-1][1] == T
+            assert all(a < b for a, b in ch)
+            assert all(ch[i][1] == ch[i + 1][0] for i in range(len(ch) - 1))
+            assert max(b - a for a, b in ch) - min(b - a for a, b in ch) <= 1
+            if n > 0:
+                assert len(ch) == min(n, T)
+    assert len(bench.row_chunks(4096, 0)) == 1 and len(bench.row_chunks(16384, 0)) == 8
