@@ -427,9 +427,12 @@ rc_status rc_qkv_front(const uint16_t *hidden, int32_t M, int32_t D, const uint1
    p itself for device or managed memory; for page-locked host memory
    mapped into the device's address space (cudaHostAlloc, or
    cudaHostRegister with mapping), its device address (the same value under
-   unified addressing).  RC_ERR_INVALID_ARG when the device cannot address p
-   through the CUDA runtime (pageable host memory, NULL); dev untouched then.
-   Host-only; no page counterpart. */
+   unified addressing).  Pass the start of the page-locked allocation; the
+   device address of a byte inside it is the result plus that byte's offset
+   (the Python binding maps slices of pinned tensors this way).
+   RC_ERR_INVALID_ARG when the device cannot address p through the CUDA
+   runtime (pageable host memory, NULL); dev untouched then.  Host-only; no
+   page counterpart. */
 rc_status rc_device_address(const void *p, const void **dev);
 
 /* Sticky fault bits raised on the device when a bounded wait gives up: bits
