@@ -122,6 +122,15 @@ MUTANTS = [
     ("QKV front: a bad row counted once per problem",
      "        if ((bad_pos || bad_slot) && err)\n            *err += 1;\n",
      "        if (err)\n            *err += bad_pos + bad_slot;\n"),
+    ("projection: the magnitude bound sums signed products",
+     "                        if (ab)\n                            ab[n] = ab[n] + fabs(p);\n",
+     "                        if (ab)\n                            ab[n] = ab[n] + p;\n"),
+    ("projection: the selected rows ignored",
+     "            int64_t t = rows ? rows[i] : i;\n",
+     "            int64_t t = i;\n"),
+    ("bf16 rounding: NaN to 0x7FC0 instead of the box's canonical NaN",
+     "    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0u)\n        return (uint16_t)0x7FFFu;\n",
+     "    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0u)\n        return (uint16_t)0x7FC0u;\n"),
     ("QKV front: cached K taken from the raw projection",
      "                memcpy(dst, o + q_size + h * RCO_HEAD,",
      "                memcpy(dst, rr + q_size + h * RCO_HEAD,"),
