@@ -131,6 +131,17 @@ MUTANTS = [
     ("bf16 rounding: NaN to 0x7FC0 instead of the box's canonical NaN",
      "    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0u)\n        return (uint16_t)0x7FFFu;\n",
      "    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0u)\n        return (uint16_t)0x7FC0u;\n"),
+    ("layer norms: the sum of squares taken over x instead of the hidden output",
+     "            float r2 = rco_inv_rms(rco_row_sumsq(z), inv_d, eps);\n",
+     "            float r2 = rco_inv_rms(rco_row_sumsq(v), inv_d, eps);\n"),
+    ("projection: every layer reads layer 0's normed rows",
+     "            const uint16_t *a = normed + ((int64_t)l * T + t) * D;\n",
+     "            const uint16_t *a = normed + t * D;\n"),
+    ("store: NeoX pairs (j, j + 32) instead of GPT-J pairs (2j, 2j + 1)",
+     "                    float y0 = kf[2 * j] * r;\n"
+     "                    float y1 = kf[2 * j + 1] * r;\n",
+     "                    float y0 = kf[j] * r;\n"
+     "                    float y1 = kf[j + RCO_HEAD / 2] * r;\n"),
     ("QKV front: cached K taken from the raw projection",
      "                memcpy(dst, o + q_size + h * RCO_HEAD,",
      "                memcpy(dst, rr + q_size + h * RCO_HEAD,"),
