@@ -142,6 +142,15 @@ MUTANTS = [
      "                    float y1 = kf[2 * j + 1] * r;\n",
      "                    float y0 = kf[j] * r;\n"
      "                    float y1 = kf[j + RCO_HEAD / 2] * r;\n"),
+    ("norm options: a gain centre of 0 still added (-0.0 weights become +0.0)",
+     "    if (n->center != 0.0f)\n        g = g + n->center;\n",
+     "    g = g + n->center;\n"),
+    ("float64 to bf16: subnormals rounded at binary32's spacing",
+     "    if (qe < -133)\n        qe = -133;                   /* subnormal spacing 2^-133 */\n",
+     "    if (qe < -149)\n        qe = -149;\n"),
+    ("QKV front: a negative slot counted as an error",
+     "        const int bad_slot = s >= capacity;\n",
+     "        const int bad_slot = s >= capacity || (slots && s < 0);\n"),
     ("QKV front: cached K taken from the raw projection",
      "                memcpy(dst, o + q_size + h * RCO_HEAD,",
      "                memcpy(dst, rr + q_size + h * RCO_HEAD,"),
