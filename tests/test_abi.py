@@ -199,3 +199,16 @@ def test_qkv_front_rejections(lib):
     assert call(out=A(w + 64)) == rc.RC_ERR_INVALID_ARG                    # out overlaps W
     assert "overlaps" in last(lib)
     assert call(M=0) == rc.RC_OK
+
+
+def test_device_address_rejections(lib):
+    # NULL arguments are refused before any CUDA call; without a GPU (or for
+    # pageable memory) the runtime cannot address a host buffer: an error
+    # status, dev left untouched
+    d = ctypes.c_void_p(0x1234)
+    assert lib.rc_device_address(None, ctypes.byref(d)) == rc.RC_ERR_INVALID_ARG
+    assert "must not be NULL" in last(lib) and d.value == 0x1234
+    buf = ctypes.create_string_buffer(64)
+    assert lib.rc_device_address(ctypes.addressof(buf), None) == rc.RC_ERR_INVALID_ARG
+    assert lib.rc_device_address(ctypes.addressof(buf), ctypes.byref(d)) == rc.RC_ERR_INVALID_ARG
+    assert "rc_device_address" in last(lib) and d.value == 0x1234
