@@ -1,8 +1,8 @@
 """Benchmark of the context K/V chain (norms -> projection -> store).
 
 One step = one pass of the whole chain over one batch of context rows of a
-workload (default: workload 2, T=512 rows, L=3 layers, H=8 KV heads, RoPE),
-inputs resident in HBM.  Prints one JSON line (rank 0).
+workload (default: workload 5, the largest: T=32768 rows, L=8 layers, H=8 KV
+heads, RoPE), inputs resident in HBM.  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I]
   python bench.py --impl reference ...   # the CPU oracle as the reference arm
@@ -33,20 +33,40 @@ L2_FLUSH_BYTES = 512 << 20          # > 129 MB L2: written between timed steps
 L2_CLEAN_BYTES = 256 << 20          # > 129 MB L2: then read, so the written lines leave it
 
 
-# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
-# capture of this bench command (dram__bytes_read.sum + dram__bytes_write.sum,
-# summed over the kernels the timed call launches); keyed by (workload, path,
-# kernel).  An entry is removed whenever one of its kernels changes.
-NCU_TRAFFIC = {
-    # rc_kv_project_store at workload 2: k2_project_pair (75.69 MB read,
-    # 0.83 MB written) + k3_reduce_store (18.99 MB read); ncu with its default
-    # cache flush before each launch.
-    (2, "store", "project_store"): 95_506_752,
-    # workload 3: k2_project_pair_persistent (339.69 MB read, 23.36 MB
-    # written) + the tail's k2_project_pair (46.16 + 1.09 MB) +
-    # k3_reduce_store (14.73 MB read); ncu's default cache flush as above.
-    (3, "store", "project_store"): 425_024_768,
-}
+# DRAM bytes (read + write) per call, from ncu captures of this bench
+# command (dram__bytes_read.sum + dram__bytes_write.sum, summed over the
+# kernels the call launches), keyed by (workload, path, call).  Each entry
+# carries the digest of the kernel sources it was measured on
+# (source_digest(): the CUDA sources under rope_chain_gb300/csrc); when the
+# sources change the figure no longer describes the kernels and the bench
+# reports traffic as null.
+NCU_TRAFFIC = {}
+
+
+def source_digest() -> str:
+    """Short digest of every CUDA source and header the library is built
+    from (rope_chain_gb300/csrc), in name order."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "rope_chain_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(key):
+    """(bytes, note) of NCU_TRAFFIC[key] when it was measured on the current
+    sources, else (None, why)."""
+    entry = NCU_TRAFFIC.get(key)
+    if entry is None:
+        return None, "no ncu capture of this call at this workload"
+    nbytes, digest, how = entry
+    if digest != source_digest():
+        return None, "the ncu capture predates the current kernel sources"
+    return nbytes, how
 
 
 class L2Flush:
@@ -150,6 +170,19 @@ def store_bytes(w, slots, rope: bool) -> int:
     for s in slots:
         live = int(((s >= 0) & (s < cap)).sum())
         total += 8 * len(s) + live * (512 * w.H + (8 + 128 if rope else 0))
+    return total
+
+
+def project_store_bytes(w, slots, rope: bool) -> int:
+    """Algorithmic bytes of the fused projection + store call: the normed
+    rows and W read once, and per (row, layer) the slot, plus for a row
+    whose slot is in range its cache row written (256 H B) and with RoPE its
+    position and table row; the projection itself never leaves the chip."""
+    total = 2 * (w.L * w.T * w.D + w.L * w.D * w.N)
+    cap = w.num_blocks * w.block_size
+    for s in slots:
+        live = int(((s >= 0) & (s < cap)).sum())
+        total += 8 * len(s) + live * (256 * w.H + (8 + 128 if rope else 0))
     return total
 
 
@@ -579,15 +612,20 @@ def run_ours(args, w):
     first = "row_pass" if fused_norms else "norms"
     dominant = "project_store" if kern["project_store"]["us"] >= kern[first]["us"] else first
     d = kern[dominant]
-    traffic = NCU_TRAFFIC.get((args.workload, args.path, dominant))
+    traffic, traffic_note = ncu_traffic((args.workload, args.path, dominant))
+    for name, entry in (("norms", kern["unfused"]["norms"]), ("store", kern["unfused"]["store"])):
+        entry["traffic"], entry["traffic_note"] = ncu_traffic((args.workload, "unfused", name))
     if d["bound"] == "tensor":
         roof = {"kernel": dominant, "bound": "tensor", "achieved": d["TFLOP/s"], "peak": tc,
                 "unit": "TFLOP/s", "frac": d["frac"], "traffic": traffic,
-                "peak_source": f"bf16_tflops (burst) of {peak_src}"}
+                "traffic_note": traffic_note,
+                "algorithmic_bytes": project_store_bytes(w, case["slots"], w.rope),
+                "peak_source": f"bf16_tflops (burst) of {peak_src}",
+                "frac_of_sustained": d["TFLOP/s"] / peaks.get("bf16_tflops_sustained", tc)}
     else:
         roof = {"kernel": dominant, "bound": "hbm", "achieved": d["GB/s"], "peak": hbm,
                 "unit": "GB/s", "frac": d["frac"], "traffic": traffic,
-                "peak_source": f"hbm_gbs of {peak_src}"}
+                "traffic_note": traffic_note, "peak_source": f"hbm_gbs of {peak_src}"}
     import oracle
     oracle.build()
     R = cpu_sample_rows(w)
@@ -618,6 +656,8 @@ def run_ours(args, w):
                 "inputs": "x read in place from pinned host memory by the norms kernel "
                           "(NVLink-C2C); positions and slot maps in one pinned buffer, one "
                           "copy per step" + ("" if whole else " alongside the norms"),
+                "outputs": "the K/V result stays in the device caches (the operation's "
+                           "output); only the 4-byte skip count is copied back per step",
                 "row_ranges": len(chunks),
                 "overlap": (f"{len(chunks)} row ranges: the norms of range c + 1 read x "
                             "while range c is projected and stored on a second stream")
@@ -791,7 +831,7 @@ def run_front(args):
         "roofline": {"kernel": "k4_qkv_front", "bound": "hbm", "achieved": nbytes / t_us / 1e3,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": nbytes / t_us / 1e3 / peaks["hbm_gbs"],
-                     "traffic": NCU_TRAFFIC.get(("front", M, "k4_qkv_front")),
+                     "traffic": ncu_traffic(("front", M, "k4_qkv_front"))[0],
                      "peak_source": f"hbm_gbs of {peak_src}"},
         "kernels": {"qkv_front": {"us": t_us, "GB/s": nbytes / t_us / 1e3, "bytes": nbytes}},
         "cpu_baseline": {"value": M / cpu_s, "unit": "tokens/s", "cores": oracle.max_threads(), "cpu": host_cpu(),
@@ -810,7 +850,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--workload", type=int, default=5, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--e2e-chunks", type=int, default=0, metavar="N",
                     help="row ranges of the end-to-end steps on the default path "
                          "(0: 8 from 16384 rows, else 1)")

@@ -172,6 +172,12 @@ rc_status rc_kv_project(const uint16_t *normed, const uint16_t *W,
    attribute query; returns 0 for invalid sizes. */
 size_t rc_kv_project_workspace_size(int32_t L, int64_t T, int32_t D, int32_t N);
 
+/* The same figure for a GPU with num_sms streaming multiprocessors, with no
+   device involved (plan allocations ahead of time, or for another GPU).
+   Host-only; returns 0 for invalid sizes or num_sms < 1. */
+size_t rc_kv_project_workspace_size_sms(int32_t L, int64_t T, int32_t D, int32_t N,
+                                        int32_t num_sms);
+
 /*
  * rc_kv_store -- step 4.  [ctx] ContextKvStore / _ContextKvStoreKernel,
  * _sum_squares_64, _rope; [rt] ContextKV.store.
@@ -364,8 +370,11 @@ rc_status rc_context_kv_from_rows(const uint16_t *z, const float *r2, int64_t T,
  * owns every device allocation, serving paths that must not touch the
  * allocator once running).  This call takes the same operands as
  * rc_kv_project minus the workspace and allocates nothing: its split-K
- * scratch is a 24 MiB array inside the library, held on every GPU that loads
- * the library until the process exits.
+ * scratch is an array of RC_NO_ALLOC_SCRATCH_BYTES (24 MiB) inside the
+ * library, held on every GPU that loads the library until the process
+ * exits.  Arguments are checked as rc_kv_project checks them (sizes, layout,
+ * NULL and 16-byte alignment, out overlapping normed or W); out, normed or
+ * W overlapping the array itself is refused too.
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
  *     stream capture.
@@ -375,8 +384,10 @@ rc_status rc_context_kv_from_rows(const uint16_t *z, const float *r2, int64_t T,
  *     calls whose work overlaps on the GPU (e.g. on different streams) race
  *     on it, so order them on one stream.  Nothing in it needs clearing:
  *     each call writes every partial it reads.
- * Results equal rc_kv_project's with a full-size workspace.
+ * Results are bit-identical to rc_kv_project's given a workspace of
+ * rc_kv_project_workspace_size() bytes (the same plan, the same kernels).
  */
+#define RC_NO_ALLOC_SCRATCH_BYTES ((size_t)24 << 20)
 rc_status rc_kv_project_no_alloc(const uint16_t *normed, const uint16_t *W,
                                  int32_t w_layout, uint16_t *out, int32_t L,
                                  int64_t T, int32_t D, int32_t N,

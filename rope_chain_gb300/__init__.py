@@ -44,6 +44,8 @@ SIGNATURES = {
     "rc_kv_project": ([_vp, _vp, _c.c_int32, _vp, _c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32,
                        _vp, _c.c_size_t, _vp], _c.c_int),
     "rc_kv_project_workspace_size": ([_c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32], _c.c_size_t),
+    "rc_kv_project_workspace_size_sms": ([_c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32, _c.c_int32],
+                                         _c.c_size_t),
     "rc_kv_store": ([_vp, _vp, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _vp,
                      _c.POINTER(_vp), _vp, _c.c_int64, _c.POINTER(_vp), _c.c_int32, _c.c_int32,
                      _c.c_int32, _c.c_int32, _c.c_float, _c.c_int64, _vp, _vp], _c.c_int),
@@ -257,19 +259,49 @@ def new_workspace(L: int, T: int, D: int, N: int, device) -> Optional[torch.Tens
     return torch.empty(n, dtype=torch.uint8, device=device) if n else None
 
 
+def _project_shapes(normed: torch.Tensor, W: torch.Tensor, w_layout: int):
+    """(L, T, D, N) of a projection; W must be [L, D, N] (RC_W_KN) or
+    [L, N, D] (RC_W_NK) for normed [L, T, D]."""
+    _bf16(normed, "normed")
+    _bf16(W, "W")
+    if normed.dim() != 3 or W.dim() != 3:
+        raise ValueError("normed and W must be 3-dimensional")
+    L, T, D = normed.shape
+    if w_layout == RC_W_KN:
+        N = W.shape[2]
+        want = (L, D, N)
+    elif w_layout == RC_W_NK:
+        N = W.shape[1]
+        want = (L, N, D)
+    else:
+        raise ValueError(f"unknown weight layout {w_layout}")
+    if tuple(W.shape) != want:
+        raise ValueError(f"W has shape {tuple(W.shape)}; normed {tuple(normed.shape)} needs {want}")
+    return L, T, D, N
+
+
+def _project_out_shape(out: torch.Tensor, L: int, T: int, N: int) -> None:
+    if tuple(out.shape) != (L, T, N):
+        raise ValueError(f"out has shape {tuple(out.shape)}; the projection writes {(L, T, N)}")
+
+
+def workspace_size_for(L: int, T: int, D: int, N: int, num_sms: int) -> int:
+    """Split-K workspace bytes of a projection on a GPU with num_sms SMs
+    (host-only: no device is needed)."""
+    return int(lib().rc_kv_project_workspace_size_sms(L, T, D, N, num_sms))
+
+
 def kv_project(normed: torch.Tensor, W: torch.Tensor, out: Optional[torch.Tensor] = None,
                w_layout: int = RC_W_KN, workspace: Optional[torch.Tensor] = None,
                stream=None) -> torch.Tensor:
     """bf16 [L, T, N] = normed [L, T, D] x W, W [L, D, N] (RC_W_KN) or
     [L, N, D] (RC_W_NK).  ``workspace`` (any dtype, contiguous; see
     new_workspace() and workspace_size()) enables split-K for small T."""
-    _bf16(normed, "normed")
-    _bf16(W, "W")
-    L, T, D = normed.shape
-    N = W.shape[2] if w_layout == RC_W_KN else W.shape[1]
+    L, T, D, N = _project_shapes(normed, W, w_layout)
     if out is None:
         out = torch.empty((L, T, N), dtype=torch.bfloat16, device=normed.device)
     _bf16(out, "out")
+    _project_out_shape(out, L, T, N)
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         if not (workspace.is_cuda and workspace.is_contiguous()):
@@ -286,11 +318,9 @@ def kv_project_no_alloc(normed: torch.Tensor, W: torch.Tensor, out: torch.Tensor
     scratch lives inside the library (24 MiB per GPU), ``out`` must be given,
     and calls that overlap on the GPU must not be issued (they share the
     scratch)."""
-    _bf16(normed, "normed")
-    _bf16(W, "W")
+    L, T, D, N = _project_shapes(normed, W, w_layout)
     _bf16(out, "out")
-    L, T, D = normed.shape
-    N = W.shape[2] if w_layout == RC_W_KN else W.shape[1]
+    _project_out_shape(out, L, T, N)
     _check(lib().rc_kv_project_no_alloc(normed.data_ptr(), W.data_ptr(), w_layout,
                                         out.data_ptr(), L, T, D, N, _stream(stream)))
     return out

@@ -165,6 +165,28 @@ rc_status kv_store_impl(const char *fn, const uint16_t *k, const uint16_t *v,
 
 namespace rc {
 void set_last_error(const char *msg) { snprintf(g_err, sizeof g_err, "%s", msg); }
+
+rc_status check_project_call(const char *fn, const uint16_t *normed, const uint16_t *W,
+                             int32_t w_layout, const uint16_t *out, int32_t L, int64_t T,
+                             int32_t D, int32_t N)
+{
+    const rc_status s = check_project_sizes(L, T, D, N);
+    if (s != RC_OK)
+        return s;
+    if (w_layout != RC_W_KN && w_layout != RC_W_NK)
+        return fail(RC_ERR_INVALID_ARG, "%s: unknown weight layout %d", fn, w_layout);
+    if (!normed || !W || !out)
+        return fail(RC_ERR_INVALID_ARG, "%s: normed, W and out must not be NULL", fn);
+    if (!aligned(normed, 16) || !aligned(W, 16) || !aligned(out, 16))
+        return fail(RC_ERR_INVALID_ARG, "%s: operands must be 16-byte aligned", fn);
+    if (T == 0)
+        return RC_OK;
+    const size_t obytes = (size_t)L * T * N * 2;
+    if (overlap(out, obytes, normed, (size_t)L * T * D * 2) ||
+        overlap(out, obytes, W, (size_t)L * D * N * 2))
+        return fail(RC_ERR_INVALID_ARG, "%s: out overlaps an input", fn);
+    return RC_OK;
+}
 }  // namespace rc
 
 extern "C" {
@@ -264,26 +286,26 @@ size_t rc_kv_project_workspace_size(int32_t L, int64_t T, int32_t D, int32_t N)
     return rc::plan_kv_project(L, T, D, N, sms, SIZE_MAX).workspace;
 }
 
+size_t rc_kv_project_workspace_size_sms(int32_t L, int64_t T, int32_t D, int32_t N,
+                                        int32_t num_sms)
+{
+    if (check_project_sizes(L, T, D, N) != RC_OK || T == 0 || num_sms < 1)
+        return 0;
+    return rc::plan_kv_project(L, T, D, N, num_sms, SIZE_MAX).workspace;
+}
+
 rc_status rc_kv_project(const uint16_t *normed, const uint16_t *W, int32_t w_layout, uint16_t *out,
                         int32_t L, int64_t T, int32_t D, int32_t N, void *workspace,
                         size_t workspace_bytes, cudaStream_t stream)
 {
-    const rc_status s = check_project_sizes(L, T, D, N);
+    const rc_status s = rc::check_project_call("rc_kv_project", normed, W, w_layout, out, L, T, D, N);
     if (s != RC_OK)
         return s;
-    if (w_layout != RC_W_KN && w_layout != RC_W_NK)
-        return fail(RC_ERR_INVALID_ARG, "rc_kv_project: unknown weight layout %d", w_layout);
-    if (!normed || !W || !out)
-        return fail(RC_ERR_INVALID_ARG, "rc_kv_project: normed, W and out must not be NULL");
-    if (!aligned(normed, 16) || !aligned(W, 16) || !aligned(out, 16) ||
-        (workspace && !aligned(workspace, 16)))
+    if (workspace && !aligned(workspace, 16))
         return fail(RC_ERR_INVALID_ARG, "rc_kv_project: operands must be 16-byte aligned");
     if (T == 0)
         return ok();
     const size_t obytes = (size_t)L * T * N * 2;
-    if (overlap(out, obytes, normed, (size_t)L * T * D * 2) ||
-        overlap(out, obytes, W, (size_t)L * D * N * 2))
-        return fail(RC_ERR_INVALID_ARG, "rc_kv_project: out overlaps an input");
     const int sms = num_sms_current();
     if (sms <= 0)
         return fail(RC_ERR_CUDA, "rc_kv_project: no current CUDA device");

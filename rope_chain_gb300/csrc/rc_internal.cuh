@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
+#include "rope_chain.h"
+
 namespace rc {
 
 constexpr int kHidden = 8192;        // row width of the context norms
@@ -283,6 +285,13 @@ cudaError_t launch_kv_project(const uint16_t *normed, const uint16_t *W, bool w_
 
 // Sets the message rc_last_error() returns on this host thread.
 void set_last_error(const char *msg);
+
+// The argument checks of rc_kv_project (sizes, weight layout, NULL and
+// 16-byte alignment of normed, W and out, out overlapping an input); on a
+// refusal the message names `fn` and the status is returned.
+rc_status check_project_call(const char *fn, const uint16_t *normed, const uint16_t *W,
+                             int32_t w_layout, const uint16_t *out, int32_t L, int64_t T,
+                             int32_t D, int32_t N);
 
 // Projection + store: the pair kernel's epilogue stores when it does not
 // split; split plans go through launch_reduce_store; single-CTA plans that do

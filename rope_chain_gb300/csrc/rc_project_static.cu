@@ -26,8 +26,9 @@
 namespace {
 
 // 24 MiB: on a 152-SM GB300 a split-K plan never needs more than
-// (SMs) x 128 x 256 FP32 partials = 19.9 MB.
-constexpr size_t kScratchBytes = 24u << 20;
+// (SMs) x 128 x 256 FP32 partials = 19.9 MB, and a persistent plan's tail
+// split stays below that too (a host-only test sweeps the planner).
+constexpr size_t kScratchBytes = RC_NO_ALLOC_SCRATCH_BYTES;
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_project_scratch[kScratchBytes];
@@ -72,7 +73,10 @@ rc_status reject(rc_status s, const char *msg) {
     return s;
 }
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
 
 }  // namespace
 
@@ -82,16 +86,12 @@ rc_status rc_kv_project_no_alloc(const uint16_t *normed, const uint16_t *W, int3
                                  uint16_t *out, int32_t L, int64_t T, int32_t D, int32_t N,
                                  cudaStream_t stream)
 {
-    if (L < 1 || L > 4096 || T < 0 || T > 65535LL * 128)
-        return reject(RC_ERR_INVALID_ARG, "rc_kv_project_no_alloc: L or T out of range");
-    if (D < 64 || D % 64 != 0 || N < 128 || N % 128 != 0)
-        return reject(RC_ERR_UNSUPPORTED,
-                      "rc_kv_project_no_alloc: D must be a multiple of 64, N of 128");
-    if (w_layout != RC_W_KN && w_layout != RC_W_NK)
-        return reject(RC_ERR_INVALID_ARG, "rc_kv_project_no_alloc: unknown weight layout");
-    if (!normed || !W || !out || !aligned16(normed) || !aligned16(W) || !aligned16(out))
-        return reject(RC_ERR_INVALID_ARG,
-                      "rc_kv_project_no_alloc: normed, W and out must be 16-byte aligned device pointers");
+    // the checks rc_kv_project makes: sizes, layout, NULL, alignment, and
+    // out overlapping normed or W
+    const rc_status st = rc::check_project_call("rc_kv_project_no_alloc", normed, W, w_layout, out,
+                                                L, T, D, N);
+    if (st != RC_OK)
+        return st;
     char msg[256];
     if (T == 0) {
         rc::set_last_error("");
@@ -104,6 +104,12 @@ rc_status rc_kv_project_no_alloc(const uint16_t *normed, const uint16_t *W, int3
                  cudaGetErrorString(e));
         return reject(RC_ERR_CUDA, msg);
     }
+    // No operand may lie inside the library's own scratch.
+    if (overlaps(out, (size_t)L * T * N * 2, slot->scratch, kScratchBytes) ||
+        overlaps(normed, (size_t)L * T * D * 2, slot->scratch, kScratchBytes) ||
+        overlaps(W, (size_t)L * D * N * 2, slot->scratch, kScratchBytes))
+        return reject(RC_ERR_INVALID_ARG,
+                      "rc_kv_project_no_alloc: an operand overlaps the library's static scratch");
     // The same plan rc_kv_project makes with an unlimited workspace; a plan
     // whose partials do not fit the static array is refused, not shrunk.
     const rc::ProjectPlan plan = rc::plan_kv_project(L, T, D, N, slot->num_sms, SIZE_MAX);

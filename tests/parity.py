@@ -12,6 +12,8 @@ Rules (written once here, used by every GPU test and by smoke()):
 """
 from __future__ import annotations
 
+import json
+import os
 from typing import Optional
 
 import numpy as np
@@ -52,6 +54,48 @@ def assert_projection_close(gpu_bits: np.ndarray, ref64: np.ndarray, abs64: np.n
             f"{what}: {int(bad.sum())} of {bad.size} outside 2 ulp; first at {tuple(i)}: "
             f"gpu={g[tuple(i)]!r} ref={ref64[tuple(i)]!r} tol={tol[tuple(i)]!r}")
     return float(np.max(err / tol)) if err.size else 0.0
+
+
+# Bins of an error measured in bf16 ulps at the comparison's scale: exact,
+# within rounding (<= 1/2), one rounding step (<= 1), up to the rule's bound
+# (<= 2), and beyond it (a failure).
+ULP_BINS = ((0.0, "0"), (0.5, "(0,0.5]"), (1.0, "(0.5,1]"), (1.5, "(1,1.5]"), (2.0, "(1.5,2]"),
+            (np.inf, ">2"))
+
+
+def ulp_stats(err: np.ndarray, scale: np.ndarray) -> dict:
+    """Max error and a histogram of |error| in units of ulp_bf16(scale)."""
+    u = err / ulp_bf16(np.where(scale > 0, scale, 2.0 ** -133))
+    u = u.reshape(-1)
+    hist, lo = {}, -1.0
+    for hi, name in ULP_BINS:
+        hist[name] = int(np.count_nonzero((u > lo) & (u <= hi))) if hi > 0 else int(np.count_nonzero(u == 0))
+        lo = hi
+    return {"n": int(u.size), "max_ulp": float(u.max()) if u.size else 0.0,
+            "over_1_ulp": int(np.count_nonzero(u > 1.0)), "hist": hist}
+
+
+def projection_ulp_stats(gpu_bits: np.ndarray, ref64: np.ndarray, abs64: np.ndarray) -> dict:
+    """The projection's error in ulps at the 2-ulp rule's scale
+    max(|ref|, 2^-12 sum|a*w|), and separately in ulps of |ref| itself over
+    the outputs away from cancellation (|ref| >= 2^-12 sum|a*w|)."""
+    g = (gpu_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    err = np.abs(g - ref64)
+    floor = 2.0 ** -12 * abs64
+    st = ulp_stats(err, np.maximum(np.abs(ref64), floor))
+    away = np.abs(ref64) >= floor
+    st["relative_away_from_cancellation"] = ulp_stats(err[away], np.abs(ref64[away]))
+    return st
+
+
+def report(name: str, stats: dict) -> None:
+    """Appends one JSON line {name, stats} to the file named by the
+    RC_PARITY_REPORT environment variable (nothing when it is unset)."""
+    path = os.environ.get("RC_PARITY_REPORT")
+    if not path:
+        return
+    with open(path, "a") as f:
+        f.write(json.dumps({"name": name, **stats}) + "\n")
 
 
 def make_caches(case, L: int, fill: int) -> list:

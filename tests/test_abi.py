@@ -212,3 +212,55 @@ def test_device_address_rejections(lib):
     assert lib.rc_device_address(ctypes.addressof(buf), None) == rc.RC_ERR_INVALID_ARG
     assert lib.rc_device_address(ctypes.addressof(buf), ctypes.byref(d)) == rc.RC_ERR_INVALID_ARG
     assert "rc_device_address" in last(lib) and d.value == 0x1234
+
+
+def test_no_alloc_rejections(lib):
+    """rc_kv_project_no_alloc refuses on the host, before any CUDA call,
+    what rc_kv_project refuses: sizes, layout, NULL, misalignment, and out
+    overlapping normed or W."""
+    a, w, o = 0x100000, 0x4000000, 0x8000000
+    call = lambda *args: lib.rc_kv_project_no_alloc(*args)
+    assert call(A(a), A(w), 0, A(o), 1, 8, 8192, 100, None) == rc.RC_ERR_UNSUPPORTED
+    assert call(A(a), A(w), 0, A(o), 1, 8, 8100, 1024, None) == rc.RC_ERR_UNSUPPORTED
+    assert call(A(a), A(w), 7, A(o), 1, 8, 8192, 1024, None) == rc.RC_ERR_INVALID_ARG
+    assert "layout" in last(lib) and "rc_kv_project_no_alloc" in last(lib)
+    assert call(A(a), A(w), 0, A(o), 0, 8, 8192, 1024, None) == rc.RC_ERR_INVALID_ARG
+    assert call(A(a), A(w), 0, A(o), 1, -1, 8192, 1024, None) == rc.RC_ERR_INVALID_ARG
+    assert call(A(a), A(w), 0, A(o + 2), 1, 8, 8192, 1024, None) == rc.RC_ERR_INVALID_ARG
+    assert "aligned" in last(lib)
+    assert call(None, A(w), 0, A(o), 1, 8, 8192, 1024, None) == rc.RC_ERR_INVALID_ARG
+    assert call(A(a), None, 0, A(o), 1, 8, 8192, 1024, None) == rc.RC_ERR_INVALID_ARG
+    # out overlapping normed ([1, 8, 8192] bf16 = 128 KiB from a) or W
+    assert call(A(a), A(w), 0, A(a + 4096), 1, 8, 8192, 1024, None) == rc.RC_ERR_INVALID_ARG
+    assert "overlaps" in last(lib)
+    assert call(A(a), A(w), 0, A(w + 4096), 1, 8, 8192, 1024, None) == rc.RC_ERR_INVALID_ARG
+    # T == 0 succeeds without touching a device
+    assert call(A(a), A(w), 0, A(o), 1, 0, 8192, 1024, None) == rc.RC_OK
+    assert last(lib) == ""
+
+
+NO_ALLOC_SCRATCH = 24 << 20     # RC_NO_ALLOC_SCRATCH_BYTES
+
+
+def test_no_alloc_scratch_covers_every_plan_on_a_gb300():
+    """Every projection plan a 152-SM GB300 makes for the workload shapes
+    (and a sweep of T around them) fits the no-alloc call's static scratch,
+    so none of them is refused."""
+    from rope_chain_gb300 import _build
+    _build.build()
+    assert "RC_NO_ALLOC_SCRATCH_BYTES ((size_t)24 << 20)" in open(HEADER).read()
+    shapes = [(1, 8192, 1024), (3, 8192, 1024), (4, 8192, 1024), (5, 8192, 2048),
+              (8, 8192, 1024), (1, 8192, 128), (2, 1024, 128), (9, 8192, 1024), (1, 8192, 4096)]
+    Ts = sorted({1, 2, 63, 64, 65, 100, 127, 128, 129, 255, 256, 257, 300, 384, 511, 512, 513,
+                 1000, 1024, 2047, 2048, 3000, 4096, 6000, 8192, 10000, 16384, 20000, 32768,
+                 65536, 131072})
+    worst = 0
+    for L, D, N in shapes:
+        for T in Ts:
+            nbytes = rc.workspace_size_for(L, T, D, N, 152)
+            worst = max(worst, nbytes)
+            assert nbytes <= NO_ALLOC_SCRATCH, (L, T, D, N, nbytes)
+    assert worst > 16 << 20        # the sweep reaches plans near the bound
+    # the planner needs no device: 0 for invalid sizes or SM counts
+    assert rc.workspace_size_for(1, 64, 8192, 100, 152) == 0
+    assert rc.workspace_size_for(1, 64, 8192, 1024, 0) == 0

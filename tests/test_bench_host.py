@@ -47,6 +47,23 @@ def test_store_bytes_counts_live_rows():
         assert bench.store_bytes(w, slots, rope) == expect
 
 
+def test_project_store_bytes_by_operand():
+    w = workloads.WORKLOADS[2]
+    cap = w.num_blocks * w.block_size
+    rng = np.random.default_rng(9)
+    slots = [rng.integers(-3, cap + 3, size=w.T).astype(np.int64) for _ in range(w.L)]
+    for rope in (False, True):
+        expect = w.L * w.T * w.D * 2 + w.L * w.D * w.N * 2     # normed rows and W, once
+        for s in slots:
+            for v in s:
+                expect += 8
+                if 0 <= v < cap:
+                    expect += w.H * 128 * 2                     # the cache row written
+                    if rope:
+                        expect += 8 + 64 * 2
+        assert bench.project_store_bytes(w, slots, rope) == expect
+
+
 def test_front_bytes_by_operand():
     M, nh, nkv, D = 3, 4, 2, 256
     case = workloads.front_case(11, M, D=D, num_heads=nh, num_kv_heads=nkv)

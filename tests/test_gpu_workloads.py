@@ -59,6 +59,7 @@ def _check_end_to_end(case, got, ref, rows):
     bs = case["cache_shape"][2]
     cap = case["cache_shape"][0] * bs
     worst_k = 0.0
+    k_err, k_pair, k_tol, v_bits, v_ref, v_abs = [], [], [], [], [], []
     for l in range(L):
         for i, t in enumerate(rows):
             s = int(case["slots"][l][t])
@@ -82,10 +83,23 @@ def _check_end_to_end(case, got, ref, rows):
             err = np.abs(gk - rk)
             assert np.all(err <= tol), (l, t, float(np.max(err / tol)))
             worst_k = max(worst_k, float(np.max(err / tol)))
+            k_err.append(err.reshape(-1))
+            k_pair.append(pair.reshape(-1))
+            k_tol.append(scale.reshape(-1))
             gv = g[:, 64:].reshape(-1)
             parity.assert_projection_close(gv, ref["kv64"][l, i, 64 * H:], ref["kvabs"][l, i, 64 * H:],
                                            what="end-to-end V")
-    return worst_k
+            v_bits.append(gv)
+            v_ref.append(ref["kv64"][l, i, 64 * H:])
+            v_abs.append(ref["kvabs"][l, i, 64 * H:])
+    if k_err:
+        e = np.concatenate(k_err)
+        k = parity.ulp_stats(e, np.concatenate(k_pair))
+        k["at_rule_scale"] = parity.ulp_stats(e, np.concatenate(k_tol))
+        v = parity.projection_ulp_stats(np.concatenate(v_bits), np.concatenate(v_ref),
+                                        np.concatenate(v_abs))
+        return worst_k, k, v
+    return worst_k, None, None
 
 
 @pytest.mark.parametrize("index", [1, 2, 3, 4, 5])
@@ -102,7 +116,13 @@ def test_workload_parity(index):
     for l, (g, r) in enumerate(zip(got["caches"], ref["caches"])):
         assert np.array_equal(g, r), f"store, layer {l}"
     assert got["err"] == ref["err"] == 0
-    _check_end_to_end(case, got, ref, rows)
+    _, k_stats, v_stats = _check_end_to_end(case, got, ref, rows)
+    # the error itself, not only pass/fail: max ulps and a histogram per
+    # workload for the projection and the end-to-end K and V
+    parity.report(f"workload {index} projection",
+                  parity.projection_ulp_stats(kv_rows, ref["kv64"], ref["kvabs"]))
+    parity.report(f"workload {index} end-to-end K (ulps of the pair magnitude)", k_stats)
+    parity.report(f"workload {index} end-to-end V", v_stats)
 
 
 def test_workload_parity_nk_layout_and_no_workspace():
