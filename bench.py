@@ -35,12 +35,19 @@ L2_CLEAN_BYTES = 256 << 20          # > 129 MB L2: then read, so the written lin
 
 # DRAM bytes (read + write) per call, from ncu captures of this bench
 # command (dram__bytes_read.sum + dram__bytes_write.sum, summed over the
-# kernels the call launches), keyed by (workload, path, call).  Each entry
-# carries the digest of the kernel sources it was measured on
-# (source_digest(): the CUDA sources under rope_chain_gb300/csrc); when the
-# sources change the figure no longer describes the kernels and the bench
-# reports traffic as null.
-NCU_TRAFFIC = {}
+# kernels the call launches), keyed by (workload, path, call): (bytes,
+# digest of the kernel sources, how).  The digest (source_digest()) covers
+# every CUDA source and header under rope_chain_gb300/csrc; when the sources
+# change the figure no longer describes the kernels and the bench reports
+# traffic as null.
+NCU_TRAFFIC = {
+    # rc_kv_project_store at workload 5: one k2_project_pair_persistent
+    # launch (dynamic tile order), 5,027,994,112 B read + 528,940,800 B
+    # written; profiles/k2_pair_persistent_workload5.md
+    (5, "store", "project_store"): (5_556_934_912, "cd64a1b96674a022",
+                                    "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, "
+                                    "one launch at full size (one pass)"),
+}
 
 
 def source_digest() -> str:
@@ -230,6 +237,7 @@ def summarise_clocks(lines):
     if not rows:
         return None
     sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+    watts = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
     reasons = set()
     names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
     for r in rows:
@@ -238,6 +246,7 @@ def summarise_clocks(lines):
                 reasons.add(n)
     return {"sm_mhz": statistics.median(sm) if sm else None,
             "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+            "power_w": statistics.median(watts) if watts else None,
             "reasons": sorted(reasons), "samples": len(rows)}
 
 
@@ -287,6 +296,14 @@ def host_cpu() -> str:
     return platform.machine()
 
 
+def make_case(args, w):
+    """The workload's inputs; with --rows, the first rows of the full draw."""
+    import workloads
+    if getattr(args, "full_T", None):
+        return workloads.make_inputs(workloads.WORKLOADS[args.workload], T=w.T)
+    return workloads.make_inputs(w)
+
+
 def cpu_sample_rows(w) -> int:
     return min(w.T, 256)
 
@@ -309,7 +326,7 @@ def run_reference(args, w):
     import oracle
     import workloads
     oracle.build()
-    case = workloads.make_inputs(w)
+    case = make_case(args, w)
     R = cpu_sample_rows(w)
     cores = oracle.max_threads()
     for _ in range(args.warmup):
@@ -346,7 +363,7 @@ def run_ours(args, w):
         torch.distributed.barrier()
     rc.lib()
 
-    case = workloads.make_inputs(w)
+    case = make_case(args, w)
     bf = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
     x, hw, pw, W, cs = bf(case["x"]), bf(case["hidden_w"]), bf(case["pre_w"]), bf(case["W"]), bf(case["cos_sin"])
     positions = torch.from_numpy(case["positions"]).to(dev)
@@ -361,15 +378,13 @@ def run_ours(args, w):
     z = torch.empty((w.T, w.D), dtype=torch.bfloat16, device=dev)
     r2 = torch.empty((w.T,), dtype=torch.float32, device=dev)
     flush = L2Flush(dev)
-    pair = w.T > 128 and w.N % 256 == 0                  # CTA-pair plans
     use_ws = ws_bytes > 0
-    # With CTA pairs the library splits K when the tiles need fewer CTAs
-    # than the GPU has SMs, and otherwise (persistent pairs) uses the
-    # workspace for a split-K launch of the last layer's final row blocks.
+    # how the library runs this projection with that workspace
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    pair_ctas = 2 * w.L * ((w.T + 255) // 256) * (w.N // 256)
-    tail = use_ws and pair and pair_ctas >= sms
-    split = use_ws and not tail
+    plan = rc.project_plan(w.L, w.T, w.D, w.N, sms, ws_bytes)
+    pair = plan["kernel"] != "single CTAs"
+    tail = plan["tail_splits"] > 0
+    split = plan["splits"] > 1
     # norms (or row pass) + GEMM + (reduce-and-store when K is split; the
     # pair epilogue stores otherwise, plus the tail's split GEMM and
     # reduce-and-store; single CTAs without split: store kernel).  The
@@ -603,8 +618,9 @@ def run_ours(args, w):
     kern = {
         "row_pass" if fused_norms else "norms": hbm_entry(rows_bytes if fused_norms else counts["k1_bytes"],
                                                           us(k1_ms)),
-        "project_store": dict(tc_entry(us(ps_ms)), split_k_workspace_bytes=ws_bytes,
-                              tail_split=bool(tail and not fused_norms), norms_fused=fused_norms),
+        "project_store": dict(tc_entry(us(ps_ms)), workspace_bytes=ws_bytes,
+                              plan=plan, tail_split=bool(tail and not fused_norms),
+                              norms_fused=fused_norms),
         "unfused": {"norms": hbm_entry(counts["k1_bytes"], us(u_ms[0])),
                     "project": tc_entry(us(u_ms[1])),
                     "store": hbm_entry(k3_bytes, us(u_ms[2]))},
@@ -854,6 +870,9 @@ def main():
     ap.add_argument("--e2e-chunks", type=int, default=0, metavar="N",
                     help="row ranges of the end-to-end steps on the default path "
                          "(0: 8 from 16384 rows, else 1)")
+    ap.add_argument("--rows", type=int, default=0, metavar="R",
+                    help="run only the first R rows of the workload (a smaller case of its "
+                         "shape, for profiler captures; 0: all rows)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="store", choices=["store", "whole", "variants", "front"],
                     help="store: norms + fused projection/store; whole: rc_context_kv; variants: "
@@ -867,8 +886,13 @@ def main():
     if args.path == "front":
         run_front(args)
         return
+    import dataclasses
     import workloads
     w = workloads.WORKLOADS[args.workload]
+    if 0 < args.rows < w.T:
+        # the first R rows of the same draw (workloads.make_inputs(w, T=R))
+        w = dataclasses.replace(w, T=args.rows, label=f"{w.label}; first {args.rows} rows")
+        args.full_T = workloads.WORKLOADS[args.workload].T
     if args.impl == "reference":
         run_reference(args, w)
     else:

@@ -178,6 +178,34 @@ size_t rc_kv_project_workspace_size(int32_t L, int64_t T, int32_t D, int32_t N);
 size_t rc_kv_project_workspace_size_sms(int32_t L, int64_t T, int32_t D, int32_t N,
                                         int32_t num_sms);
 
+/* How rc_kv_project (and rc_kv_project_store) run these sizes on a GPU with
+   num_sms SMs given workspace_bytes of workspace.  Host-only.
+     kernel          0: single CTAs (128-row tiles), 1: CTA pairs, one tile
+                     each (256 x 256), 2: persistent CTA pairs walking the tiles
+     splits          K splits of the main launch (1: none; > 1: FP32 partials
+                     in the workspace, then a reduction launch)
+     tail_splits     persistent plans: 0 without a tail launch; else the K
+                     splits of the last layer's final row blocks, run as a
+                     launch of their own (plus their reduction)
+     tail_row0       the first of those rows (T without a tail launch)
+     dynamic_tiles   persistent plans: 1 when the pairs take tiles in order
+                     from a counter in the workspace (so pairs that share rows
+                     of `normed` stay in step), 0 for a fixed tile sequence
+     workspace_bytes the part of the workspace used
+   RC_ERR_INVALID_ARG / RC_ERR_UNSUPPORTED for sizes rc_kv_project refuses
+   or num_sms < 1; *plan untouched then. */
+typedef struct {
+    int32_t kernel;
+    int32_t splits;
+    int32_t tail_splits;
+    int32_t dynamic_tiles;
+    int64_t tail_row0;
+    size_t workspace_bytes;
+} rc_project_plan;
+
+rc_status rc_kv_project_plan(int32_t L, int64_t T, int32_t D, int32_t N, int32_t num_sms,
+                             size_t workspace_bytes, rc_project_plan *plan);
+
 /*
  * rc_kv_store -- step 4.  [ctx] ContextKvStore / _ContextKvStoreKernel,
  * _sum_squares_64, _rope; [rt] ContextKV.store.

@@ -86,6 +86,18 @@ class NormParams(ctypes.Structure):
                 ("gain_center", _c.c_float), ("eps", _c.c_float)]
 
 
+class ProjectPlan(ctypes.Structure):
+    """rc_project_plan: how a projection runs (kernel 0 single CTAs, 1 CTA
+    pairs, 2 persistent CTA pairs; K splits; tail splits; dynamic tiles;
+    workspace bytes used)."""
+    _fields_ = [("kernel", _c.c_int32), ("splits", _c.c_int32), ("tail_splits", _c.c_int32),
+                ("dynamic_tiles", _c.c_int32), ("tail_row0", _c.c_int64),
+                ("workspace_bytes", _c.c_size_t)]
+
+
+SIGNATURES["rc_kv_project_plan"] = ([_c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32, _c.c_int32,
+                                     _c.c_size_t, _c.POINTER(ProjectPlan)], _c.c_int)
+
 RC_NORM_NONE, RC_NORM_BF16, RC_NORM_F32 = 0, 1, 2
 SIGNATURES["rc_qkv_front"] = ([_vp, _c.c_int32, _c.c_int32, _vp, _c.c_int32, _c.c_int32, _vp, _vp,
                                _c.c_int64, _vp, _vp, _c.c_int32, _c.c_int32, _c.c_float, _vp, _vp,
@@ -283,6 +295,17 @@ def _project_shapes(normed: torch.Tensor, W: torch.Tensor, w_layout: int):
 def _project_out_shape(out: torch.Tensor, L: int, T: int, N: int) -> None:
     if tuple(out.shape) != (L, T, N):
         raise ValueError(f"out has shape {tuple(out.shape)}; the projection writes {(L, T, N)}")
+
+
+def project_plan(L: int, T: int, D: int, N: int, num_sms: int, workspace_bytes: int) -> dict:
+    """How a projection of these sizes runs on a GPU with num_sms SMs given
+    workspace_bytes of workspace (host-only)."""
+    p = ProjectPlan()
+    _check(lib().rc_kv_project_plan(L, T, D, N, num_sms, workspace_bytes, ctypes.byref(p)))
+    return {"kernel": ("single CTAs", "CTA pairs", "persistent CTA pairs")[p.kernel],
+            "splits": p.splits, "tail_splits": p.tail_splits,
+            "dynamic_tiles": bool(p.dynamic_tiles), "tail_row0": int(p.tail_row0),
+            "workspace_bytes": int(p.workspace_bytes)}
 
 
 def workspace_size_for(L: int, T: int, D: int, N: int, num_sms: int) -> int:

@@ -348,10 +348,41 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
 // and odd squares separately, then even + odd), so the stored key is the
 // same bits the unfused store would write.
 
-// The tile's store for one row (all 32 lanes call it: TMEM loads are
-// warp-collective).  tbase: this warp's TMEM lanes, column 0 of the tile.
+// One head of the warp's 32 rows (w: this lane's row, 32 packed bf16 pairs)
+// leaves for memory through the warp's staging rows in shared memory (32
+// rows 144 bytes apart: conflict-free both ways), so that each store
+// instruction writes four whole 128-byte rows instead of 32 scattered 16-byte
+// pieces.  dst: this lane's destination row (64 bf16), or NULL; every lane
+// takes part.
+__device__ __forceinline__ void store_head_rows(uint32_t stage, int lane, const uint32_t (&w)[32],
+                                                uint16_t *dst) {
+    const uint32_t own = stage + (uint32_t)lane * 144u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        st_shared_v4(own + 16u * j, make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]));
+    __syncwarp();
+    const int piece = lane & 7;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = (lane >> 3) + 4 * i;
+        uint16_t *d = reinterpret_cast<uint16_t *>(
+            __shfl_sync(0xFFFFFFFFu, reinterpret_cast<uintptr_t>(dst), r));
+        const uint4 v = ld_shared_v4(stage + (uint32_t)r * 144u + 16u * piece);
+        if (d != nullptr)
+            reinterpret_cast<uint4 *>(d)[piece] = v;
+    }
+    __syncwarp();                                      // reads done before the next head's writes
+}
+
+// The tile's store for one row (all 32 lanes call it: TMEM loads and the
+// staged stores are warp-collective).  tbase: this warp's TMEM lanes, column
+// 0 of the tile; stage: the warp's staging rows (32 x 144 bytes).
+// kPreload: the table row is read once per tile (in registers), else once
+// per key head (for kernels that cannot spare the registers).
+template <bool kPreload>
 __device__ __forceinline__ void fused_store_tile(const FusedStore &fs, const GemmArgs &g,
-                                                 uint32_t tbase, int l, int row, int n0) {
+                                                 uint32_t tbase, int l, int row, int n0,
+                                                 uint32_t stage, int lane) {
     const bool live = row < g.T;
     const bool rope = fs.cos_sin != nullptr;
     const int H = fs.H;
@@ -371,12 +402,25 @@ __device__ __forceinline__ void fused_store_tile(const FusedStore &fs, const Gem
             }
         }
     }
-    uint16_t *dst_row = nullptr;
+    uint16_t *dst_row = nullptr;                       // this row's cache row, head 0
     if (store) {
         const uint32_t bs = (uint32_t)fs.block_size;
         const uint32_t blk = (uint32_t)slot / bs;
         const uint32_t page = (uint32_t)slot - blk * bs;
         dst_row = fs.caches[l] + (((int64_t)blk * H) * bs + page) * (2 * kHeadDim);
+    }
+    // the row's cos | sin table row, fetched once for the tile's key heads
+    uint4 cq[4], sq[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        cq[q] = sq[q] = make_uint4(0, 0, 0, 0);
+    const uint4 *cs = rope && store ? reinterpret_cast<const uint4 *>(fs.cos_sin + pos * kHeadDim) : nullptr;
+    if (kPreload && cs != nullptr && (n0 >> 6) < H) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            cq[q] = __ldg(cs + q);                     // cos of pairs 8q .. 8q+7
+            sq[q] = __ldg(cs + 4 + q);                 // sin of the same pairs
+        }
     }
 #pragma unroll 1
     for (int hh = 0; hh < 4; ++hh) {
@@ -387,19 +431,14 @@ __device__ __forceinline__ void fused_store_tile(const FusedStore &fs, const Gem
 #pragma unroll
         for (int j = 0; j < 32; ++j)
             kp[j] = pack_acc(r[2 * j], r[2 * j + 1]);
-        if (live && fs.kv_out != nullptr) {
-            uint4 *o = reinterpret_cast<uint4 *>(fs.kv_out + ((int64_t)l * g.T + row) * N + n0 + 64 * hh);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                o[j] = make_uint4(kp[4 * j], kp[4 * j + 1], kp[4 * j + 2], kp[4 * j + 3]);
-        }
-        if (!store)
-            continue;
+        if (fs.kv_out != nullptr)
+            store_head_rows(stage, lane, kp,
+                            live ? fs.kv_out + ((int64_t)l * g.T + row) * N + n0 + 64 * hh : nullptr);
         const int gidx = (n0 >> 6) + hh;               // head index within [K heads | V heads]
-        const bool is_k = gidx < H;
+        const bool is_k = gidx < H;                    // the same for the whole warp
         const int h = is_k ? gidx : gidx - H;
-        uint4 *dst = reinterpret_cast<uint4 *>(dst_row + (int64_t)h * fs.block_size * (2 * kHeadDim) +
-                                               (is_k ? 0 : kHeadDim));
+        uint16_t *dst = store ? dst_row + (int64_t)h * fs.block_size * (2 * kHeadDim) + (is_k ? 0 : kHeadDim)
+                              : nullptr;
         if (is_k) {
             float ev[32], od[32];
 #pragma unroll
@@ -409,39 +448,32 @@ __device__ __forceinline__ void fused_store_tile(const FusedStore &fs, const Gem
                 od[j] = __fmul_rn(k1, k1);
             }
             const float rr = inv_rms(__fadd_rn(fold32(ev), fold32(od)), 0x1p-6f, fs.eps);
-            const uint4 *cs = rope ? reinterpret_cast<const uint4 *>(fs.cos_sin + pos * kHeadDim) : nullptr;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {              // 8 pairs at a time
-                uint4 cq = make_uint4(0, 0, 0, 0), sq = cq;
-                if (rope) {
-                    cq = __ldg(cs + q);                // cos of pairs 8q .. 8q+7
-                    sq = __ldg(cs + 4 + q);            // sin of the same pairs
+                if (!kPreload && cs != nullptr) {
+                    cq[q] = __ldg(cs + q);
+                    sq[q] = __ldg(cs + 4 + q);
                 }
-                const uint32_t cw[4] = {cq.x, cq.y, cq.z, cq.w}, sw[4] = {sq.x, sq.y, sq.z, sq.w};
-                uint32_t out[8];
+                const uint32_t cw[4] = {cq[q].x, cq[q].y, cq[q].z, cq[q].w};
+                const uint32_t sw[4] = {sq[q].x, sq[q].y, sq[q].z, sq[q].w};
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
                     const int j = 8 * q + t;
-                    float n0 = round_bf16(__fmul_rn(bf16_lo(kp[j]), rr));
-                    float n1 = round_bf16(__fmul_rn(bf16_hi(kp[j]), rr));
+                    float n0v = round_bf16(__fmul_rn(bf16_lo(kp[j]), rr));
+                    float n1v = round_bf16(__fmul_rn(bf16_hi(kp[j]), rr));
                     if (rope) {
                         const float c = (t & 1) ? bf16_hi(cw[t >> 1]) : bf16_lo(cw[t >> 1]);
                         const float sn = (t & 1) ? bf16_hi(sw[t >> 1]) : bf16_lo(sw[t >> 1]);
-                        const float x = __fmaf_rn(n0, c, -__fmul_rn(n1, sn));
-                        const float y = __fmaf_rn(n1, c, __fmul_rn(n0, sn));
-                        n0 = x;
-                        n1 = y;
+                        const float x = __fmaf_rn(n0v, c, -__fmul_rn(n1v, sn));
+                        const float y = __fmaf_rn(n1v, c, __fmul_rn(n0v, sn));
+                        n0v = x;
+                        n1v = y;
                     }
-                    out[t] = pack_bf16x2(n0, n1);
+                    kp[j] = pack_bf16x2(n0v, n1v);
                 }
-                dst[2 * q] = make_uint4(out[0], out[1], out[2], out[3]);
-                dst[2 * q + 1] = make_uint4(out[4], out[5], out[6], out[7]);
             }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                dst[j] = make_uint4(kp[4 * j], kp[4 * j + 1], kp[4 * j + 2], kp[4 * j + 3]);
         }
+        store_head_rows(stage, lane, kp, dst);         // K' (or V, a bit copy of the projection)
     }
 }
 
@@ -706,7 +738,8 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             raise_fault(kFaultAccum);
         if (ok && kFused && g.splits == 1) {
             tc_fence_after();
-            fused_store_tile(fs, g, tmem + ((uint32_t)(32 * q) << 16), l, m0 + 32 * q + lane, n0);
+            fused_store_tile<!kTransform>(fs, g, tmem + ((uint32_t)(32 * q) << 16), l, m0 + 32 * q + lane, n0,
+                             sA + (uint32_t)q * kStageRowsBytes, lane);
         } else if (ok) {
             // Each thread holds one row's 32 accumulators per TMEM load; they
             // pass through this warp's staging rows in shared memory (the
@@ -813,9 +846,11 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 struct PersistCfg {
     static constexpr int kStages = PairCfg::kStages;
     static constexpr uint32_t kStageBytes = PairCfg::kStageBytes;
-    static constexpr uint32_t kStagingBytes = 4u * 32u * 80u;   // bf16 rows of 4 epilogue warps
+    // staging rows of the 4 epilogue warps: 32 rows of 144 bytes each (the
+    // fused store's 128-byte head rows; the bf16 rows use 80 bytes of each)
+    static constexpr uint32_t kStagingBytes = 4u * kStageRowsBytes;
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kStagingBytes + 512;
-    static_assert((2 * kStages + 5) * 8 + 4 * 4 <= 512, "barriers and words fit the tail");
+    static_assert((2 * kStages + 5 + 2 * 4) * 8 + 8 * 4 <= 512, "barriers and words fit the tail");
 };
 
 // Arrive on a barrier of any CTA of the cluster, releasing at cluster scope.
@@ -823,7 +858,17 @@ __device__ __forceinline__ void mbar_arrive_release_cluster(uint32_t bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Bounded wait on a barrier that other CTAs of the cluster arrive on.
+// Dynamic tile order of the persistent kernel.  Each pair's first tile is
+// pair_id; after it, the leader's loader of a pair takes the next output
+// tile from a counter in global memory when it starts loading it, so tiles
+// that share A rows (consecutive indices) start within a fraction of a tile
+// time of each other on whichever pairs are free, and their A reads meet in
+// L2.  With a fixed assignment over many rounds, the pairs that share A
+// drift apart until they read it from DRAM again (2.5 times the A bytes
+// measured at 54 rounds).  The call zeroes the counter before the launch.
+constexpr int kMaxDynTiles = 1 << 30;
+
+// Bounded wait on a barrier that other CTAs of the cluster arrive on.// Bounded wait on a barrier that other CTAs of the cluster arrive on.
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
     const unsigned long long t0 = globaltimer();
     for (uint32_t it = 0;; ++it) {
@@ -872,12 +917,18 @@ __device__ __forceinline__ void write_bf16_rows(const GemmArgs &g, uint32_t tbas
     }
 }
 
+// Slots of the ring through which the leader's loader hands out dynamically
+// taken tiles (to the peer's loader, the MMA thread and both CTAs' epilogue
+// warps), and the readers that release each slot.
+constexpr int kTileSlots = 4;
+constexpr int kTileReaders = 1 + 4 + 1 + 4;   // leader MMA + epilogue, peer loader + epilogue
+
 template <bool kBmn, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
 k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, const GemmArgs g,
                            const __grid_constant__ FusedStore fs, int n_pairs, int m_pairs,
-                           int tile_limit)
+                           int tile_limit, unsigned int *tile_ctr)
 {
     using C = PersistCfg;
     constexpr int S = C::kStages;
@@ -889,14 +940,17 @@ k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
     const uint32_t sStage = sA + S * C::kStageBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * C::kStageBytes + C::kStagingBytes);
     // full[s], empty[s], afull[2] (accumulator b complete), aempty[2]
-    // (leader: both CTAs' epilogues are done with accumulator b), done
+    // (leader: both CTAs' epilogues are done with accumulator b), done,
+    // tfull[4] (tile slot written), tempty[4] (leader: slot read by all)
     const uint32_t bar0 = smem_u32(bars);
     const uint32_t empty0 = bar0 + 8u * S, afull0 = bar0 + 16u * S, aempty0 = afull0 + 16u;
     const uint32_t done = aempty0 + 16u;
+    const uint32_t tfull0 = done + 8u, tempty0 = tfull0 + 8u * kTileSlots;
     // words[0]: TMEM base; [1]: stages the leader's MMA thread consumed;
     // [2]: skip flag (written by the leader into both CTAs); [3]: stages the
-    // peer's loader issued (written by the peer into the leader)
-    volatile uint32_t *words = reinterpret_cast<volatile uint32_t *>(bars + 2 * S + 5);
+    // peer's loader issued (written by the peer into the leader); [4..7]:
+    // the tile slots (written by the leader's loader into both CTAs)
+    volatile uint32_t *words = reinterpret_cast<volatile uint32_t *>(bars + 2 * S + 5 + 2 * kTileSlots);
     const uint32_t words_addr = smem_u32((const void *)words);
 
     const int warp = __shfl_sync(0xFFFFFFFFu, (int)(threadIdx.x >> 5), 0);
@@ -907,6 +961,7 @@ k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
     // the first tile_limit tiles (the rest, if any, are another launch's)
     const int num_tiles = min(g.L * m_pairs * n_pairs, tile_limit);
     const int nkb = g.kb_total;
+    const bool dyn = tile_ctr != nullptr;
     pdl_trigger();
 
     if (threadIdx.x == 0) {
@@ -919,6 +974,10 @@ k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
             mbar_init(aempty0 + 8u * b, 8);        // 4 epilogue warps in each CTA of the pair
         }
         mbar_init(done, 1);
+        for (int i = 0; i < kTileSlots; ++i) {
+            mbar_init(tfull0 + 8u * i, 1);         // the leader's loader
+            mbar_init(tempty0 + 8u * i, kTileReaders);
+        }
         words[1] = 0u;
         words[3] = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -956,12 +1015,64 @@ k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
     }
     pdl_wait();                                   // the previous kernel's writes are visible
 
+    // Tile j of this pair: with a fixed order pair_id + j * num_pairs; with
+    // dynamic tiles the first one is pair_id and for j >= 1 the leader's
+    // loader takes a ticket (publish = true) and every other role reads the
+    // tile from slot (j - 1) % 4 and releases the slot.  -1: no more tiles,
+    // or a wait that gave up (fault raised).
+    const uint32_t tiles_addr = words_addr + 16u;
+    const uint32_t lead_tempty0 = map_to_rank(tempty0, 0);
+    auto tile_of = [&](int j, bool publish, bool warp_wide) -> int {
+        if (!dyn || j == 0) {
+            // the fixed sequence; with dynamic tiles the first round as well,
+            // so that the pairs do not all take their first ticket at once
+            const int t = pair_id + j * num_pairs;
+            return t < num_tiles ? t : -1;
+        }
+        const int slot = (j - 1) % kTileSlots;       // ring use j - 1 (round 0 needs none)
+        const uint32_t ph = (uint32_t)((j - 1) / kTileSlots) & 1u;
+        if (publish) {
+            if (!mbar_wait_cluster(tempty0 + 8u * slot, ph ^ 1u)) {
+                raise_fault(kFaultLoad);
+                return -1;
+            }
+            // tickets count the tiles after round 0
+            const unsigned int ticket = atomicAdd(tile_ctr, 1u);
+            const int t = ticket < (unsigned int)(num_tiles - num_pairs) ? (int)ticket + num_pairs : -1;
+            words[4 + slot] = (uint32_t)t;
+            st_cluster_u32(map_to_rank(tiles_addr + 4u * slot, 1), (uint32_t)t);
+            mbar_arrive_local(tfull0 + 8u * slot);
+            mbar_arrive_release_cluster(map_to_rank(tfull0 + 8u * slot, 1));
+            return t;
+        }
+        // one thread waits, reads the slot and releases it (a warp gets the
+        // index from its lane 0)
+        int t = -1;
+        if (!warp_wide || lane == 0) {
+            if (mbar_wait_cluster(tfull0 + 8u * slot, ph)) {
+                t = (int)words[4 + slot];
+                if (leader)
+                    mbar_arrive_local(tempty0 + 8u * slot);
+                else
+                    mbar_arrive_release_cluster(lead_tempty0 + 8u * slot);
+            } else {
+                raise_fault(kFaultAccum);
+            }
+        }
+        if (warp_wide)
+            t = __shfl_sync(0xFFFFFFFFu, t, 0);
+        return t;
+    };
+
     int issued = 0;
     if (warp == 0) {
         if (lane == 0 && !skip) {
             int it = 0;
             bool ok = true;
-            for (int t = pair_id; t < num_tiles && ok; t += num_pairs) {
+            for (int j = 0; ok; ++j) {
+                const int t = tile_of(j, leader, false);
+                if (t < 0)
+                    break;
                 const int np = t % n_pairs, rest = t / n_pairs;
                 const int mp = rest % m_pairs, l = rest / m_pairs;
                 const int m0 = mp * 256 + 128 * (int)rank;
@@ -994,9 +1105,12 @@ k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
             int consumed = 0;
             if (!skip) {
                 constexpr uint32_t idesc = make_idesc(256, 256, kBmn);
-                int it = 0, j = 0;
+                int it = 0;
                 bool ok = true;
-                for (int t = pair_id; t < num_tiles && ok; t += num_pairs, ++j) {
+                for (int j = 0; ok; ++j) {
+                    const int t = tile_of(j, false, false);
+                    if (t < 0)
+                        break;
                     const int b = j & 1;
                     // both epilogues are done reading accumulator b (tile j - 2)
                     if (!mbar_wait_cluster(aempty0 + 8u * b, ((uint32_t)(j >> 1) & 1u) ^ 1u)) {
@@ -1035,9 +1149,11 @@ k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
         __syncwarp();
     } else {
         const int q = warp & 3;
-        const uint32_t stage = sStage + (uint32_t)q * (32u * 80u);
-        int j = 0;
-        for (int t = pair_id; t < num_tiles && !skip; t += num_pairs, ++j) {
+        const uint32_t stage = sStage + (uint32_t)q * kStageRowsBytes;
+        for (int j = 0; !skip; ++j) {
+            const int t = tile_of(j, false, true);
+            if (t < 0)
+                break;
             const int b = j & 1;
             bool ok = mbar_wait(afull0 + 8u * b, (uint32_t)(j >> 1) & 1u);
             ok = __all_sync(0xFFFFFFFFu, ok);
@@ -1052,7 +1168,7 @@ k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
             const int m0 = mp * 256 + 128 * (int)rank, n0 = np * 256;
             const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + 256u * (uint32_t)b;
             if (kFused)
-                fused_store_tile(fs, g, tbase, l, m0 + 32 * q + lane, n0);
+                fused_store_tile<true>(fs, g, tbase, l, m0 + 32 * q + lane, n0, stage, lane);
             else
                 write_bf16_rows(g, tbase, stage, m0 + 32 * q, l, n0, lane);
             tc_fence_before();
@@ -1136,7 +1252,7 @@ cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const Gemm
 template <bool kBmn, bool kFused>
 cudaError_t launch_pair_persistent(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &g,
                                    const FusedStore &fs, int n_pairs, int m_pairs, int tile_limit,
-                                   cudaStream_t stream) {
+                                   unsigned int *tile_ctr, cudaStream_t stream) {
     static int sms[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1158,7 +1274,7 @@ cudaError_t launch_pair_persistent(const CUtensorMap &ma, const CUtensorMap &mb,
     const int pairs = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, n_sms / 2));
     return launch_pdl(k2_project_pair_persistent<kBmn, kFused>, dim3((unsigned)(2 * pairs)),
                       dim3(kThreads), PersistCfg::kSmem, stream, 2, ma, mb, g, fs, n_pairs, m_pairs,
-                      tile_limit);
+                      tile_limit, tile_ctr);
 }
 
 }  // namespace
@@ -1193,6 +1309,7 @@ ProjectPlan plan_kv_project(int32_t L, int64_t T, int32_t D, int32_t N, int num_
     p.workspace = p.splits > 1 ? (size_t)p.splits * per_split : 0;
     p.tail_splits = 1;
     p.tail_kb_per_split = kb_total;
+    p.tile_ctr_offset = -1;
     if (p.pair && p.splits == 1) {
         // Persistent pairs take tiles round-robin, so a last wave of rem <
         // P tiles costs a whole tile time.  Its tiles (rounded up to whole
@@ -1218,6 +1335,19 @@ ProjectPlan plan_kv_project(int32_t L, int64_t T, int32_t D, int32_t N, int num_
                 p.tail_splits = (kb_total + p.tail_kb_per_split - 1) / p.tail_kb_per_split;
                 p.workspace = (size_t)p.tail_splits * per_tail_split;
             }
+        }
+        // Eight rounds of tiles or more: pairs take tiles from a counter in
+        // the workspace (after the tail's partials), when it has room.  With
+        // fewer rounds the pairs do not drift apart far enough to lose their
+        // shared A reads in L2 (workload 3, 3 rounds: 11 % more DRAM bytes
+        // than the operands; workload 5, 54 rounds: 2.5 times), and the fixed
+        // order keeps the launch overlapping the previous kernel's end.
+        const int64_t persistent_tiles = tiles / 2 - p.tail_tiles;
+        const size_t off = (p.workspace + 255) / 256 * 256;
+        if (persistent_tiles >= 8 * P && persistent_tiles < kMaxDynTiles &&
+            off + 256 <= workspace_bytes) {
+            p.tile_ctr_offset = (int64_t)off;
+            p.workspace = off + 256;
         }
     }
     return p;
@@ -1261,8 +1391,16 @@ cudaError_t launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const Gemm
     if (plan.pair && plan.splits == 1) {       // persistent pairs, epilogue under the next mainloop
         const int n_pairs = N / 256, m_pairs = (int)((T + 255) / 256);
         const int limit = (int)((int64_t)g.L * m_pairs * n_pairs - plan.tail_tiles);
-        return w_nk ? launch_pair_persistent<false, kFused>(ma, mb, g, fs, n_pairs, m_pairs, limit, stream)
-                    : launch_pair_persistent<true, kFused>(ma, mb, g, fs, n_pairs, m_pairs, limit, stream);
+        unsigned int *ctr = nullptr;
+        if (plan.tile_ctr_offset >= 0 && g.partial != nullptr) {
+            ctr = reinterpret_cast<unsigned int *>(reinterpret_cast<char *>(g.partial) +
+                                                   plan.tile_ctr_offset);
+            const cudaError_t e = cudaMemsetAsync(ctr, 0, sizeof(unsigned int), stream);
+            if (e != cudaSuccess)
+                return e;
+        }
+        return w_nk ? launch_pair_persistent<false, kFused>(ma, mb, g, fs, n_pairs, m_pairs, limit, ctr, stream)
+                    : launch_pair_persistent<true, kFused>(ma, mb, g, fs, n_pairs, m_pairs, limit, ctr, stream);
     }
     if (plan.pair)
         return w_nk ? launch_pair<false, kFused, false>(ma, mb, g, fs, N / 256, (int)((T + 255) / 256), stream)

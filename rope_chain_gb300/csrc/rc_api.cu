@@ -294,6 +294,24 @@ size_t rc_kv_project_workspace_size_sms(int32_t L, int64_t T, int32_t D, int32_t
     return rc::plan_kv_project(L, T, D, N, num_sms, SIZE_MAX).workspace;
 }
 
+rc_status rc_kv_project_plan(int32_t L, int64_t T, int32_t D, int32_t N, int32_t num_sms,
+                             size_t workspace_bytes, rc_project_plan *plan)
+{
+    const rc_status s = check_project_sizes(L, T, D, N);
+    if (s != RC_OK)
+        return s;
+    if (num_sms < 1 || plan == nullptr)
+        return fail(RC_ERR_INVALID_ARG, "rc_kv_project_plan: need num_sms >= 1 and a plan to fill");
+    const rc::ProjectPlan p = rc::plan_kv_project(L, T, D, N, num_sms, workspace_bytes);
+    plan->kernel = !p.pair ? 0 : (p.splits == 1 ? 2 : 1);
+    plan->splits = p.splits;
+    plan->tail_splits = p.tail_tiles > 0 ? p.tail_splits : 0;
+    plan->dynamic_tiles = p.tile_ctr_offset >= 0 ? 1 : 0;
+    plan->tail_row0 = p.tail_tiles > 0 ? p.tail_row0 : T;
+    plan->workspace_bytes = p.workspace;
+    return ok();
+}
+
 rc_status rc_kv_project(const uint16_t *normed, const uint16_t *W, int32_t w_layout, uint16_t *out,
                         int32_t L, int64_t T, int32_t D, int32_t N, void *workspace,
                         size_t workspace_bytes, cudaStream_t stream)

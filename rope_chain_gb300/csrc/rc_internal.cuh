@@ -270,7 +270,12 @@ struct ProjectPlan {
     int64_t tail_row0;
     int tail_splits;
     int tail_kb_per_split;
-    size_t workspace;      // bytes of FP32 partials (split-K or the tail's)
+    // Persistent pair plans of eight rounds of tiles or more: byte offset in
+    // the workspace of the 4-byte counter (zeroed by the call) from which
+    // the pairs take tiles in order (dynamic tile order); -1: each pair takes
+    // a fixed sequence.
+    int64_t tile_ctr_offset;
+    size_t workspace;      // bytes used: FP32 partials (split-K or the tail's), then the counter
 };
 
 // Choose tile width and split count for the device's SM count.

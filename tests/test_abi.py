@@ -264,3 +264,32 @@ def test_no_alloc_scratch_covers_every_plan_on_a_gb300():
     # the planner needs no device: 0 for invalid sizes or SM counts
     assert rc.workspace_size_for(1, 64, 8192, 100, 152) == 0
     assert rc.workspace_size_for(1, 64, 8192, 1024, 0) == 0
+
+
+def test_project_plan_describes_the_workloads():
+    """rc_kv_project_plan, host-only: on a 152-SM GB300 the workloads run
+    split-K single CTAs (1), split-K CTA pairs (2), persistent pairs with a
+    tail launch (3) and persistent pairs taking tiles from a counter (4, 5);
+    without a workspace nothing splits and the tile order is fixed."""
+    from rope_chain_gb300 import _build
+    _build.build()
+    import workloads
+    want = {1: ("single CTAs", 16, 0, False), 2: ("CTA pairs", 3, 0, False),
+            3: ("persistent CTA pairs", 1, 2, False), 4: ("persistent CTA pairs", 1, 0, True),
+            5: ("persistent CTA pairs", 1, 0, True)}
+    for i, w in workloads.WORKLOADS.items():
+        ws = rc.workspace_size_for(w.L, w.T, w.D, w.N, 152)
+        p = rc.project_plan(w.L, w.T, w.D, w.N, 152, ws)
+        assert (p["kernel"], p["splits"], p["tail_splits"], p["dynamic_tiles"]) == want[i], (i, p)
+        assert p["workspace_bytes"] == ws
+        assert p["tail_row0"] == (w.T if p["tail_splits"] == 0 else 2304)
+        bare = rc.project_plan(w.L, w.T, w.D, w.N, 152, 0)
+        assert bare["splits"] == 1 and bare["tail_splits"] == 0 and not bare["dynamic_tiles"]
+        assert bare["workspace_bytes"] == 0
+        # a workspace one byte short of the counter keeps the fixed order
+        if p["dynamic_tiles"]:
+            assert not rc.project_plan(w.L, w.T, w.D, w.N, 152, ws - 1)["dynamic_tiles"]
+    with pytest.raises(rc.RopeChainError):
+        rc.project_plan(1, 64, 8192, 100, 152, 0)
+    with pytest.raises(rc.RopeChainError):
+        rc.project_plan(1, 64, 8192, 1024, 0, 0)

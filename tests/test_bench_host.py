@@ -82,7 +82,8 @@ def test_clock_summary():
         "garbage line\n",
     ]
     c = bench.summarise_clocks(lines)
-    assert c == {"sm_mhz": 1980.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    assert c == {"sm_mhz": 1980.0, "sm_max_mhz": 2070.0, "power_w": 1380.0, "reasons": ["sw_power_cap"],
+                 "samples": 3}
     hot = lines[:1] + ["0, 1500, 2070, 1200.0, 0x48, Active, Active, Not Active, Not Active\n"]
     assert bench.summarise_clocks(hot)["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
     assert bench.summarise_clocks(["\n"]) is None

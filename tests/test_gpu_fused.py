@@ -197,3 +197,70 @@ def test_fused_workloads(index):
     normed = oracle.context_norms(case["x"], case["hidden_w"], case["pre_w"], w.L, w.eps)
     check(case, normed, case["W"], workspace=True)
 
+
+
+@pytest.mark.parametrize("L,T,D,H,layout,tail", [(4, 8192, 1024, 16, rc.RC_W_KN, False),
+                                                 (4, 8192, 1024, 16, rc.RC_W_NK, False),
+                                                 (8, 8192, 4096, 8, rc.RC_W_KN, True)])
+def test_dynamic_tile_order_repeats_and_graph_replays(L, T, D, H, layout, tail):
+    # persistent pairs over eight rounds of tiles or more (1024 tiles of 256 x
+    # 256): given a workspace the pairs take tiles from a counter in it (the
+    # last shape also splits its final row blocks into a tail launch).  Each
+    # tile's arithmetic is the fixed-order kernel's, so every call (back to
+    # back on one workspace, with other inputs in between, and as CUDA-graph
+    # replays) must match the fixed order outside the tail bit for bit.
+    N = 128 * H
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    nbytes = rc.workspace_size(L, T, D, N)
+    plan = rc.project_plan(L, T, D, N, sms, nbytes)
+    assert plan["kernel"] == "persistent CTA pairs" and plan["dynamic_tiles"], plan
+    assert (plan["tail_splits"] > 0) == tail, plan
+    assert not rc.project_plan(L, T, D, N, sms, 0)["dynamic_tiles"]
+    rng = np.random.default_rng(4242 + D)
+    ins, raw = [], []
+    for _ in range(2):
+        a = workloads.normal_bf16(rng, (L, T, D), 0.0, 1.0)
+        W = workloads.normal_bf16(rng, (L, D, N), 0.0, 0.02)
+        Wl = W if layout == rc.RC_W_KN else np.ascontiguousarray(W.transpose(0, 2, 1))
+        ins.append((parity.dev_bf16(a, DEV), parity.dev_bf16(Wl, DEV)))
+        raw.append((a, W))
+    fixed = [parity.host_bits(rc.kv_project(a_d, w_d, w_layout=layout)) for a_d, w_d in ins]
+    # the tail's rows (the last layer's final row blocks) use another split
+    # and so another summation order: those are checked against float64
+    rows_fixed = plan["tail_row0"]
+    tail_rows = np.arange(rows_fixed, T)
+
+    def check(got, i, what):
+        if not tail:
+            assert np.array_equal(got, fixed[i]), what
+            return
+        assert np.array_equal(got[:L - 1], fixed[i][:L - 1]), what
+        assert np.array_equal(got[L - 1, :rows_fixed], fixed[i][L - 1, :rows_fixed]), what
+        sample = tail_rows[:: max(1, len(tail_rows) // 16)]
+        ref64, ab = oracle.kv_project(raw[i][0][L - 1:], raw[i][1][L - 1:], rows=sample)
+        parity.assert_projection_close(got[L - 1:, sample], ref64, ab, what + " (tail rows)")
+
+    ws = torch.full((nbytes,), 0xA5, dtype=torch.uint8, device=DEV)    # any initial contents
+    for i in (0, 1, 0, 0, 1):
+        check(parity.host_bits(rc.kv_project(ins[i][0], ins[i][1], w_layout=layout, workspace=ws)),
+              i, f"call on input {i}")
+    # as CUDA-graph replays
+    outs = [torch.empty((L, T, N), dtype=torch.bfloat16, device=DEV) for _ in range(2)]
+    s = torch.cuda.Stream(DEV)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(2):
+            rc.kv_project(ins[i][0], ins[i][1], out=outs[i], w_layout=layout, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(2):
+            rc.kv_project(ins[i][0], ins[i][1], out=outs[i], w_layout=layout, workspace=ws)
+    for _ in range(3):
+        for o in outs:
+            o.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        for i in range(2):
+            check(parity.host_bits(outs[i]), i, f"graph replay, input {i}")
+    assert rc.read_device_faults(clear=True) == 0
