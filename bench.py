@@ -97,38 +97,46 @@ class L2Flush:
 
 def row_chunks(T: int, n: int):
     """n nearly equal row ranges covering rows 0..T-1; n = 0 picks 8 ranges
-    from 16384 rows and one range below that (measured on GB300: with 8
-    ranges the end-to-end step took 4.54 ms instead of 5.14 at 32768 rows and
-    2.66 ms instead of 2.74 at 16384, while at 512 and 4096 rows the ranges'
-    smaller projections cost more than the overlap saved)."""
+    from 16384 rows, 4 from 2048 rows and one range below that (at 512 rows
+    the ranges' smaller projections cost more than the overlap saves)."""
     if n <= 0:
-        n = 8 if T >= 16384 else 1
+        n = 8 if T >= 16384 else (4 if T >= 2048 else 1)
     n = max(1, min(n, T))
     edges = [T * i // n for i in range(n + 1)]
     return [(edges[i], edges[i + 1]) for i in range(n)]
 
 
 class OverlappedChain:
-    """rc_context_norms + rc_kv_project_store over row ranges, so that the
-    norms of range c + 1 (which may read x in place from pinned host memory
-    over the host link) run while range c is projected and stored on a
-    second stream.  Rows are independent, so every row's K and V reach the
-    caches as the single pair of calls would store them; only the
-    projection's split plan follows the range's size, so its FP32 summation
-    order (and with it the last bit of a K/V value) may differ.  Each range
-    gets its own slice of one [L, T, D] norms buffer; the ranges' projections
-    run in order on the second stream and share one split-K workspace."""
+    """rc_context_norms + rc_kv_project_store over row ranges of x held in
+    pinned host memory, overlapping the host-to-device transfer of x with
+    the chain.  Rows are independent, so every row's K and V reach the caches
+    as the single pair of calls would store them; only the projection's plan
+    follows the range's size, so its FP32 summation order (and with it the
+    last bit of a K/V value) may differ.  Each range gets its own slice of one
+    [L, T, D] norms buffer, and the ranges' projections share one workspace.
 
-    def __init__(self, L: int, T: int, D: int, N: int, chunks, dev):
+    mode "copy": the copy engines move range c + 1 of x into one of two
+    device buffers (one cudaMemcpyAsync per range on a copy stream) while
+    the current stream runs the norms and the projection + store of range c,
+    so the transfer takes no SM time.  mode "inplace": the norms kernel of
+    range c + 1 reads its rows of x in place over the host link while range
+    c is projected and stored on a second stream."""
+
+    def __init__(self, L: int, T: int, D: int, N: int, chunks, dev, mode: str = "copy"):
         import torch
         import rope_chain_gb300 as rc
-        self.rc, self.L, self.chunks = rc, L, chunks
+        assert mode in ("copy", "inplace")
+        self.rc, self.L, self.chunks, self.mode = rc, L, chunks, mode
         flat = torch.empty(L * T * D, dtype=torch.bfloat16, device=dev)
         self.normed = [flat[L * r0 * D:L * r1 * D].view(L, r1 - r0, D) for r0, r1 in chunks]
         ws = max(rc.workspace_size(L, r1 - r0, D, N) for r0, r1 in chunks)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=dev) if ws else None
-        self.proj = torch.cuda.Stream(device=dev)
+        self.side = torch.cuda.Stream(device=dev)
         self.done = [torch.cuda.Event() for _ in chunks]
+        if mode == "copy":
+            rows = max(r1 - r0 for r0, r1 in chunks)
+            self.xbuf = [torch.empty((rows, D), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+            self.copied = [torch.cuda.Event() for _ in chunks]
 
     def __call__(self, x, hidden_w, pre_w, W, H, positions, slots, cos_sin, caches, eps, err,
                  inputs_ready=None):
@@ -136,18 +144,40 @@ class OverlappedChain:
         for before the first projection (positions and slots copied there)."""
         import torch
         main = torch.cuda.current_stream()
-        self.proj.wait_stream(main)
+        sl = lambda r0, r1: [None if s_ is None else s_[r0:r1] for s_ in slots]
+        if self.mode == "copy":
+            # copy stream: range c into buffer c % 2 once the norms of range
+            # c - 2 (the buffer's last reader) are done.  Each copy is queued
+            # just before its range's chain, so the event it waits for has
+            # already been recorded in this pass (a wait on an event not yet
+            # recorded would not wait).
+            self.side.wait_stream(main)
+            if inputs_ready is not None:
+                main.wait_stream(inputs_ready)
+            for c, ((r0, r1), nc) in enumerate(zip(self.chunks, self.normed)):
+                with torch.cuda.stream(self.side):
+                    if c >= 2:
+                        self.side.wait_event(self.done[c - 2])
+                    self.xbuf[c % 2][:r1 - r0].copy_(x[r0:r1], non_blocking=True)
+                    self.copied[c].record(self.side)
+                main.wait_event(self.copied[c])
+                self.rc.context_norms(self.xbuf[c % 2][:r1 - r0], hidden_w, pre_w, self.L, eps, out=nc)
+                self.done[c].record(main)
+                self.rc.kv_project_store(nc, W, H, positions[r0:r1], sl(r0, r1), cos_sin, caches,
+                                         eps, err=err, workspace=self.ws)
+            main.wait_stream(self.side)
+            return
+        self.side.wait_stream(main)
         if inputs_ready is not None:
-            self.proj.wait_stream(inputs_ready)
+            self.side.wait_stream(inputs_ready)
         for (r0, r1), nc, ev in zip(self.chunks, self.normed, self.done):
             self.rc.context_norms(x[r0:r1], hidden_w, pre_w, self.L, eps, out=nc)
             ev.record(main)
-            self.proj.wait_event(ev)
-            with torch.cuda.stream(self.proj):
-                self.rc.kv_project_store(nc, W, H, positions[r0:r1],
-                                         [None if s_ is None else s_[r0:r1] for s_ in slots],
-                                         cos_sin, caches, eps, err=err, workspace=self.ws)
-        main.wait_stream(self.proj)
+            self.side.wait_event(ev)
+            with torch.cuda.stream(self.side):
+                self.rc.kv_project_store(nc, W, H, positions[r0:r1], sl(r0, r1), cos_sin, caches,
+                                         eps, err=err, workspace=self.ws)
+        main.wait_stream(self.side)
 
 
 def load_peaks():
@@ -545,9 +575,13 @@ def run_ours(args, w):
 
     side = torch.cuda.Stream(device=dev)
     # On the default path the rows go through in ranges (OverlappedChain):
-    # the host read of x for range c + 1 overlaps the projection of range c.
+    # the transfer of x for range c + 1 overlaps the chain of range c, by the
+    # copy engines into device buffers ("copy") or by the norms kernel
+    # reading host memory in place ("inplace").  One range: the norms read x
+    # in place (the read overlaps the norms' own work).
     chunks = row_chunks(w.T, args.e2e_chunks) if args.path == "store" else [(0, w.T)]
-    overlapped = OverlappedChain(w.L, w.T, w.D, w.N, chunks, dev) if len(chunks) > 1 else None
+    e2e_mode = ("copy" if args.e2e_mode == "auto" else args.e2e_mode) if len(chunks) > 1 else "inplace"
+    overlapped = OverlappedChain(w.L, w.T, w.D, w.N, chunks, dev, e2e_mode) if len(chunks) > 1 else None
 
     def e2e_step(ev0, ev1):
         # the metadata copy runs on a side stream while the norms read x;
@@ -669,15 +703,21 @@ def run_ours(args, w):
                                       "sample": f"first {R1} rows, whole chain, once"}},
         "e2e": {"value": world * w.T * args.steps / (e2e_ms / 1e3), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4, "timing": timing,
-                "inputs": "x read in place from pinned host memory by the norms kernel "
-                          "(NVLink-C2C); positions and slot maps in one pinned buffer, one "
-                          "copy per step" + ("" if whole else " alongside the norms"),
+                "inputs": ("x copied from pinned host memory by the copy engines, one "
+                           "cudaMemcpyAsync per row range into two device buffers"
+                           if e2e_mode == "copy" else
+                           "x read in place from pinned host memory by the norms kernel "
+                           "(NVLink-C2C)") +
+                          "; positions and slot maps in one pinned buffer, one copy per step" +
+                          ("" if whole else " alongside the norms"),
                 "outputs": "the K/V result stays in the device caches (the operation's "
                            "output); only the 4-byte skip count is copied back per step",
                 "row_ranges": len(chunks),
-                "overlap": (f"{len(chunks)} row ranges: the norms of range c + 1 read x "
-                            "while range c is projected and stored on a second stream")
-                           if overlapped is not None else "none"},
+                "overlap": ("none" if overlapped is None else
+                            f"{len(chunks)} row ranges: the copy of range c + 1 runs while "
+                            "range c goes through the chain" if e2e_mode == "copy" else
+                            f"{len(chunks)} row ranges: the norms of range c + 1 read x "
+                            "while range c is projected and stored on a second stream")},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     })
@@ -869,7 +909,10 @@ def main():
     ap.add_argument("--workload", type=int, default=5, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--e2e-chunks", type=int, default=0, metavar="N",
                     help="row ranges of the end-to-end steps on the default path "
-                         "(0: 8 from 16384 rows, else 1)")
+                         "(0: 8 from 16384 rows, 4 from 2048, else 1)")
+    ap.add_argument("--e2e-mode", default="auto", choices=["auto", "copy", "inplace"],
+                    help="how x reaches the GPU in the end-to-end row ranges: copy engines "
+                         "(copy; the default) or the norms reading host memory (inplace)")
     ap.add_argument("--rows", type=int, default=0, metavar="R",
                     help="run only the first R rows of the workload (a smaller case of its "
                          "shape, for profiler captures; 0: all rows)")

@@ -159,8 +159,15 @@ rc_status rc_context_norms_ex(const uint16_t *x, int64_t T, int32_t D,
  *              (deterministic for a given workspace size).  With many
  *              tiles whose last round would leave most SMs idle, the last
  *              layer's final row blocks are split the same way in a launch
- *              of their own.  The bytes that give the full split are
- *              rc_kv_project_workspace_size().
+ *              of their own.  From eight rounds of tiles the persistent
+ *              kernel's CTA pairs take their tiles in order from a 4-byte
+ *              counter in the workspace (zeroed by the call), so the pairs
+ *              that read the same rows of `normed` stay in step and share
+ *              them in L2 (with a fixed tile order they drift apart and read
+ *              them from DRAM again).  The tile order does not change the
+ *              results.  The bytes that give all of this are
+ *              rc_kv_project_workspace_size(); calls sharing one workspace
+ *              must not overlap on the GPU.
  */
 rc_status rc_kv_project(const uint16_t *normed, const uint16_t *W,
                         int32_t w_layout, uint16_t *out, int32_t L, int64_t T,

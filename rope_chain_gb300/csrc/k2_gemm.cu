@@ -923,8 +923,11 @@ __device__ __forceinline__ void write_bf16_rows(const GemmArgs &g, uint32_t tbas
 constexpr int kTileSlots = 4;
 constexpr int kTileReaders = 1 + 4 + 1 + 4;   // leader MMA + epilogue, peer loader + epilogue
 
+// Register bound of two CTAs per SM (168): one CTA per SM runs (shared
+// memory), and the registers it leaves free hold two 8-warp norms CTAs that
+// another stream may run beside it (the end-to-end row ranges).
 template <bool kBmn, bool kFused>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, const GemmArgs g,
                            const __grid_constant__ FusedStore fs, int n_pairs, int m_pairs,

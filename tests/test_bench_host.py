@@ -107,4 +107,5 @@ def test_row_chunks_cover_rows_once():
             assert max(b - a for a, b in ch) - min(b - a for a, b in ch) <= 1
             if n > 0:
                 assert len(ch) == min(n, T)
-    assert len(bench.row_chunks(4096, 0)) == 1 and len(bench.row_chunks(16384, 0)) == 8
+    assert len(bench.row_chunks(512, 0)) == 1 and len(bench.row_chunks(4096, 0)) == 4
+    assert len(bench.row_chunks(16384, 0)) == 8

@@ -95,12 +95,15 @@ def test_slice_of_pinned_buffer():
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-@pytest.mark.parametrize("T,L,H,n", [(600, 3, 8, 3), (512, 3, 8, 2), (1000, 2, 16, 4)])
-def test_overlapped_ranges_from_host_x(T, L, H, n):
-    # bench.py's end-to-end pass: the norms of row range c + 1 read x from
-    # pinned host memory while range c is projected and stored on a second
-    # stream.  Its caches equal those of the same calls made one after
-    # another from device memory, and those match the oracle.
+@pytest.mark.parametrize("T,L,H,n,mode", [(600, 3, 8, 3, "inplace"), (512, 3, 8, 2, "inplace"),
+                                          (1000, 2, 16, 4, "inplace"), (600, 3, 8, 3, "copy"),
+                                          (1000, 2, 16, 5, "copy"), (513, 3, 8, 2, "copy")])
+def test_overlapped_ranges_from_host_x(T, L, H, n, mode):
+    # bench.py's end-to-end pass: row range c + 1 of x crosses from pinned
+    # host memory (copied by the copy engines into one of two device
+    # buffers, or read in place by the norms kernel) while range c goes
+    # through the chain.  Its caches equal those of the same calls made one
+    # after another from device memory, and those match the oracle.
     import oracle
     import bench
     oracle.build()
@@ -117,7 +120,7 @@ def test_overlapped_ranges_from_host_x(T, L, H, n):
 
     caches_a = [parity.dev_bf16(c, DEV) for c in parity.make_caches(case, L, parity.SENTINEL)]
     err_a = torch.zeros(1, dtype=torch.int32, device=DEV)
-    run = bench.OverlappedChain(L, T, 8192, N, chunks, DEV)
+    run = bench.OverlappedChain(L, T, 8192, N, chunks, DEV, mode)
     for _ in range(2):                     # a second pass rewrites the same bits
         run(x_h, hw, pw, W, H, pos, slots, cs, caches_a, case["eps"], err_a)
     torch.cuda.synchronize()
