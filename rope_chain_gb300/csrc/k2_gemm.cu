@@ -686,17 +686,26 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 const int row = m0 + r0 + 16 * j;
                 rs[j] = row < g.T ? __ldg(g.row_scale + row) : 0.0f;
             }
-            const uint16_t *gain = g.col_gain ? g.col_gain + (int64_t)l * (g.kb_total * BK) : nullptr;
+            const uint16_t *gain =
+                g.col_gain ? g.col_gain + (int64_t)l * (g.kb_total * BK) + 8 * c : nullptr;
+            // the gains of the group's next stage are fetched while the
+            // current one is formed, so no stage waits for them
+            uint4 g_next = make_uint4(0, 0, 0, 0);
+            if (gain && grp < nkb)
+                g_next = __ldg(reinterpret_cast<const uint4 *>(gain + (kb0 + grp) * BK));
             for (int i = grp; i < nkb; i += kFormGroups) {
                 const int s = i % S;
                 const uint32_t ph = (uint32_t)(i / S) & 1u;
+                float gm[8];
+                if (gain) {
+                    unpack8f(g_next, gm);
+                    if (i + kFormGroups < nkb)
+                        g_next = __ldg(reinterpret_cast<const uint4 *>(gain + (kb0 + i + kFormGroups) * BK));
+                }
                 if (!mbar_wait(aload0 + 8u * s, ph)) {
                     raise_fault(kFaultLoad);
                     break;
                 }
-                float gm[8];
-                if (gain)
-                    unpack8f(__ldg(reinterpret_cast<const uint4 *>(gain + (kb0 + i) * BK + 8 * c)), gm);
                 // all 8 rows' chunks in flight, then formed, then written back
                 const uint32_t st = sA + s * kABytes;
                 uint32_t addr[8];
@@ -849,8 +858,9 @@ struct PersistCfg {
     // staging rows of the 4 epilogue warps: 32 rows of 144 bytes each (the
     // fused store's 128-byte head rows; the bf16 rows use 80 bytes of each)
     static constexpr uint32_t kStagingBytes = 4u * kStageRowsBytes;
-    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kStagingBytes + 512;
-    static_assert((2 * kStages + 5 + 2 * 4) * 8 + 8 * 4 <= 512, "barriers and words fit the tail");
+    static constexpr uint32_t kTailBytes = 1024;   // barriers and words
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kStagingBytes + kTailBytes;
+    static_assert((5 * kStages + 13) * 8 + 8 * 4 <= kTailBytes, "barriers and words fit the tail");
 };
 
 // Arrive on a barrier of any CTA of the cluster, releasing at cluster scope.
@@ -921,13 +931,28 @@ __device__ __forceinline__ void write_bf16_rows(const GemmArgs &g, uint32_t tbas
 // taken tiles (to the peer's loader, the MMA thread and both CTAs' epilogue
 // warps), and the readers that release each slot.
 constexpr int kTileSlots = 4;
-constexpr int kTileReaders = 1 + 4 + 1 + 4;   // leader MMA + epilogue, peer loader + epilogue
+// leader MMA + epilogue, peer loader + epilogue; with forming warps also the
+// peer's forwarding thread and both CTAs' 8 forming warps
+__host__ __device__ constexpr int tile_readers(bool form) { return 1 + 4 + 1 + 4 + (form ? 1 + 16 : 0); }
 
-// Register bound of two CTAs per SM (168): one CTA per SM runs (shared
-// memory), and the registers it leaves free hold two 8-warp norms CTAs that
-// another stream may run beside it (the end-to-end row ranges).
-template <bool kBmn, bool kFused>
-__global__ void __launch_bounds__(kThreads, 2)
+// Threads of the persistent kernel: loader warp, MMA warp, 4 epilogue warps,
+// and with the forming flag kPersistFormGroups groups of 4 forming warps.
+constexpr int kPersistFormGroups = 2;                      // groups taking stages in turn
+constexpr int kFormWarpsPerGroup = 8 / kPersistFormGroups;  // 8 forming warps in all
+constexpr int kFormRows = 32 / kFormWarpsPerGroup;          // rows of a stage per thread
+__host__ __device__ constexpr int persist_threads(bool form) { return kThreads + (form ? 256 : 0); }
+
+// kForm: A is formed in shared memory from the hidden-norm rows z (TMA
+// loads of z [T, D] into the A stage, then bf16((z * row_scale) * col_gain_l)
+// written in place by the forming warps, as the norms kernel's layer step
+// computes it), for the whole chain; kForm implies the fused store.
+//
+// Register bound without forming: two CTAs per SM (168).  One CTA per SM
+// runs (shared memory), and the registers it leaves free hold two 8-warp
+// norms CTAs that another stream may run beside it (the end-to-end row
+// ranges).
+template <bool kBmn, bool kFused, bool kForm>
+__global__ void __launch_bounds__(persist_threads(kForm), kForm ? 1 : 2)
 k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, const GemmArgs g,
                            const __grid_constant__ FusedStore fs, int n_pairs, int m_pairs,
@@ -942,18 +967,22 @@ k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
     const uint32_t sB = sA + S * kABytes;
     const uint32_t sStage = sA + S * C::kStageBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * C::kStageBytes + C::kStagingBytes);
-    // full[s], empty[s], afull[2] (accumulator b complete), aempty[2]
-    // (leader: both CTAs' epilogues are done with accumulator b), done,
-    // tfull[4] (tile slot written), tempty[4] (leader: slot read by all)
+    // full[s] (leader: B, and A unless kForm), empty[s], afull[2]
+    // (accumulator b complete), aempty[2] (leader: both CTAs' epilogues are
+    // done with accumulator b), done, tfull[4] (tile slot written), tempty[4]
+    // (leader: slot read by all); with kForm aload[s] (this CTA's z rows
+    // landed), ready[s] (this CTA's A formed), peer[s] (leader: the peer's A
+    // formed, forwarded by the peer's warp 1)
     const uint32_t bar0 = smem_u32(bars);
     const uint32_t empty0 = bar0 + 8u * S, afull0 = bar0 + 16u * S, aempty0 = afull0 + 16u;
     const uint32_t done = aempty0 + 16u;
     const uint32_t tfull0 = done + 8u, tempty0 = tfull0 + 8u * kTileSlots;
+    const uint32_t aload0 = tempty0 + 8u * kTileSlots, ready0 = aload0 + 8u * S, peer0 = ready0 + 8u * S;
     // words[0]: TMEM base; [1]: stages the leader's MMA thread consumed;
     // [2]: skip flag (written by the leader into both CTAs); [3]: stages the
     // peer's loader issued (written by the peer into the leader); [4..7]:
     // the tile slots (written by the leader's loader into both CTAs)
-    volatile uint32_t *words = reinterpret_cast<volatile uint32_t *>(bars + 2 * S + 5 + 2 * kTileSlots);
+    volatile uint32_t *words = reinterpret_cast<volatile uint32_t *>(bars + 5 * S + 13);
     const uint32_t words_addr = smem_u32((const void *)words);
 
     const int warp = __shfl_sync(0xFFFFFFFFu, (int)(threadIdx.x >> 5), 0);
@@ -979,7 +1008,14 @@ k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
         mbar_init(done, 1);
         for (int i = 0; i < kTileSlots; ++i) {
             mbar_init(tfull0 + 8u * i, 1);         // the leader's loader
-            mbar_init(tempty0 + 8u * i, kTileReaders);
+            mbar_init(tempty0 + 8u * i, tile_readers(kForm));
+        }
+        if (kForm) {
+            for (int s = 0; s < S; ++s) {
+                mbar_init(aload0 + 8u * s, 1);     // this CTA's loader (expect_tx)
+                mbar_init(ready0 + 8u * s, kFormWarpsPerGroup);   // the forming warps of the stage's group
+                mbar_init(peer0 + 8u * s, 1);      // forwarded by the peer's warp 1
+            }
         }
         words[1] = 0u;
         words[3] = 0u;
@@ -1090,9 +1126,15 @@ k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
                     }
                     const uint32_t full = map_to_rank(bar0 + 8u * s, 0);
                     if (leader)
-                        mbar_expect_tx(bar0 + 8u * s, PairCfg::kPairTx);
+                        mbar_expect_tx(bar0 + 8u * s, kForm ? 2u * PairCfg::kBHalf : PairCfg::kPairTx);
                     const int kc = kb * BK;
-                    tma_load_3d_pair(sA + s * kABytes, &tmA, kc, m0, l, full);
+                    if (kForm) {
+                        // this CTA's z rows into its own A stage (z is [T, D]: one "layer")
+                        mbar_expect_tx(aload0 + 8u * s, kABytes);
+                        tma_load_3d(sA + s * kABytes, &tmA, kc, m0, 0, aload0 + 8u * s);
+                    } else {
+                        tma_load_3d_pair(sA + s * kABytes, &tmA, kc, m0, l, full);
+                    }
                     if (kBmn) {
                         tma_load_3d_pair(sB + s * PairCfg::kBHalf, &tmB, nb, kc, l, full);
                         tma_load_3d_pair(sB + s * PairCfg::kBHalf + 8192u, &tmB, nb + 64, kc, l, full);
@@ -1103,6 +1145,28 @@ k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
                 }
             }
         }
+    } else if (kForm && warp == 1 && !leader) {
+        // the peer's idle MMA thread forwards "A formed" to the leader, so
+        // the forming warps never pay for a cluster-scope release
+        if (lane == 0 && !skip) {
+            const uint32_t peer_lead = map_to_rank(peer0, 0);
+            int it = 0;
+            bool ok = true;
+            for (int j = 0; ok; ++j) {
+                if (tile_of(j, false, false) < 0)
+                    break;
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const int s = it % S;
+                    if (!mbar_wait(ready0 + 8u * s, (uint32_t)(it / S) & 1u)) {
+                        raise_fault(kFaultMma);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_cluster(peer_lead + 8u * s);
+                }
+            }
+        }
+        __syncwarp();
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             int consumed = 0;
@@ -1125,7 +1189,9 @@ k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
                     for (int kb = 0; kb < nkb; ++kb, ++it) {
                         const int s = it % S;
                         const uint32_t ph = (uint32_t)(it / S) & 1u;
-                        if (!mbar_wait(bar0 + 8u * s, ph)) {
+                        if (!mbar_wait(bar0 + 8u * s, ph) ||
+                            (kForm && (!mbar_wait(ready0 + 8u * s, ph) ||
+                                       !mbar_wait(peer0 + 8u * s, ph)))) {
                             raise_fault(kFaultMma);
                             ok = false;
                             break;
@@ -1150,6 +1216,87 @@ k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
             mma_commit_pair(done);
         }
         __syncwarp();
+    } else if (kForm && warp >= 6) {
+        // Forming warps: group grp (warps 6 + 4 grp ...) forms the stages it
+        // with it % kPersistFormGroups == grp (the ring's stage count is a
+        // multiple of the groups, so a stage always serves one group); thread
+        // t of a group takes logical chunk c = t % 8 (8 columns) of rows
+        // t / 8 + 16 j of this CTA's 128 rows.
+        const int grp = (warp - 6) / kFormWarpsPerGroup;
+        const int t8 = ((int)threadIdx.x - kThreads) % (32 * kFormWarpsPerGroup);
+        const int c = t8 & 7, r0 = t8 >> 3;
+        constexpr int kRowStep = 4 * kFormWarpsPerGroup;   // rows between one thread's rows
+        int it = 0;
+        bool ok = true;
+        for (int j = 0; ok && !skip; ++j) {
+            const int t = tile_of(j, false, true);
+            if (t < 0)
+                break;
+            const int mp = t / n_pairs % m_pairs, l = t / n_pairs / m_pairs;
+            const int m0 = mp * 256 + 128 * (int)rank;
+            float rs[kFormRows];
+#pragma unroll
+            for (int jj = 0; jj < kFormRows; ++jj) {
+                const int row = m0 + r0 + kRowStep * jj;
+                rs[jj] = row < g.T ? __ldg(g.row_scale + row) : 0.0f;
+            }
+            const uint16_t *gain = g.col_gain ? g.col_gain + (int64_t)l * (nkb * BK) + 8 * c : nullptr;
+            // the gains of this group's next stage of the tile are fetched
+            // while the current one is formed, so no stage waits for them
+            const int kb_first = ((grp - it) % kPersistFormGroups + kPersistFormGroups) % kPersistFormGroups;
+            uint4 g_next = make_uint4(0, 0, 0, 0);
+            if (gain && kb_first < nkb)
+                g_next = __ldg(reinterpret_cast<const uint4 *>(gain + kb_first * BK));
+            for (int kb = 0; kb < nkb; ++kb, ++it) {
+                if (it % kPersistFormGroups != grp)
+                    continue;
+                const int s = it % S;
+                float gm[8];
+                if (gain) {
+                    unpack8f(g_next, gm);
+                    if (kb + kPersistFormGroups < nkb)
+                        g_next = __ldg(reinterpret_cast<const uint4 *>(gain + (kb + kPersistFormGroups) * BK));
+                }
+                if (!mbar_wait(aload0 + 8u * s, (uint32_t)(it / S) & 1u)) {
+                    raise_fault(kFaultLoad);
+                    ok = false;
+                    break;
+                }
+                // all rows' chunks in flight, then formed, then written back
+                const uint32_t st = sA + s * kABytes;
+                uint32_t addr[kFormRows];
+                uint4 v[kFormRows];
+#pragma unroll
+                for (int jj = 0; jj < kFormRows; ++jj) {
+                    const int r = r0 + kRowStep * jj;
+                    addr[jj] = st + r * 128 + ((c ^ (r & 7)) << 4);
+                    v[jj] = ld_shared_v4(addr[jj]);
+                }
+#pragma unroll
+                for (int jj = 0; jj < kFormRows; ++jj) {
+                    float f[8];
+                    unpack8f(v[jj], f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        f[e] = __fmul_rn(f[e], rs[jj]);
+                    if (gain) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            f[e] = __fmul_rn(f[e], gm[e]);
+                    }
+                    v[jj] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                       pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                }
+#pragma unroll
+                for (int jj = 0; jj < kFormRows; ++jj)
+                    st_shared_v4(addr[jj], v[jj]);
+                // generic-proxy writes, then visible to the tensor core
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_local(ready0 + 8u * s);
+            }
+        }
     } else {
         const int q = warp & 3;
         const uint32_t stage = sStage + (uint32_t)q * kStageRowsBytes;
@@ -1171,7 +1318,7 @@ k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
             const int m0 = mp * 256 + 128 * (int)rank, n0 = np * 256;
             const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + 256u * (uint32_t)b;
             if (kFused)
-                fused_store_tile<true>(fs, g, tbase, l, m0 + 32 * q + lane, n0, stage, lane);
+                fused_store_tile<!kForm>(fs, g, tbase, l, m0 + 32 * q + lane, n0, stage, lane);
             else
                 write_bf16_rows(g, tbase, stage, m0 + 32 * q, l, n0, lane);
             tc_fence_before();
@@ -1196,6 +1343,12 @@ k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
                 break;
             }
     }
+    if (kForm && warp == 0 && lane == 0)              // this CTA's own z loads
+        for (int i = max(0, issued - S); i < issued; ++i)
+            if (!mbar_wait_own(aload0 + 8u * (i % S), (uint32_t)(i / S) & 1u)) {
+                raise_fault(kFaultDrain);
+                break;
+            }
     if (leader && warp == 1 && lane == 0 && !mbar_wait_own(done, 0u))
         raise_fault(kFaultDrain);
     __syncwarp();
@@ -1252,7 +1405,7 @@ cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const Gemm
 }
 
 // One CTA pair per two SMs (fewer when there are fewer tiles).
-template <bool kBmn, bool kFused>
+template <bool kBmn, bool kFused, bool kForm = false>
 cudaError_t launch_pair_persistent(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &g,
                                    const FusedStore &fs, int n_pairs, int m_pairs, int tile_limit,
                                    unsigned int *tile_ctr, cudaStream_t stream) {
@@ -1263,7 +1416,7 @@ cudaError_t launch_pair_persistent(const CUtensorMap &ma, const CUtensorMap &mb,
         return e;
     int n_sms = dev < 64 ? sms[dev] : 0;
     if (n_sms == 0) {
-        e = cudaFuncSetAttribute(k2_project_pair_persistent<kBmn, kFused>,
+        e = cudaFuncSetAttribute(k2_project_pair_persistent<kBmn, kFused, kForm>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PersistCfg::kSmem);
         if (e != cudaSuccess)
             return e;
@@ -1275,15 +1428,15 @@ cudaError_t launch_pair_persistent(const CUtensorMap &ma, const CUtensorMap &mb,
     }
     const int64_t tiles = std::min<int64_t>((int64_t)g.L * m_pairs * n_pairs, tile_limit);
     const int pairs = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, n_sms / 2));
-    return launch_pdl(k2_project_pair_persistent<kBmn, kFused>, dim3((unsigned)(2 * pairs)),
-                      dim3(kThreads), PersistCfg::kSmem, stream, 2, ma, mb, g, fs, n_pairs, m_pairs,
-                      tile_limit, tile_ctr);
+    return launch_pdl(k2_project_pair_persistent<kBmn, kFused, kForm>, dim3((unsigned)(2 * pairs)),
+                      dim3(persist_threads(kForm)), PersistCfg::kSmem, stream, 2, ma, mb, g, fs,
+                      n_pairs, m_pairs, tile_limit, tile_ctr);
 }
 
 }  // namespace
 
 ProjectPlan plan_kv_project(int32_t L, int64_t T, int32_t D, int32_t N, int num_sms,
-                            size_t workspace_bytes)
+                            size_t workspace_bytes, bool allow_tail)
 {
     ProjectPlan p{};
     // 256-wide N tiles where there are rows to fill them; with one 128-row
@@ -1323,7 +1476,7 @@ ProjectPlan plan_kv_project(int32_t L, int64_t T, int32_t D, int32_t N, int num_
         const int64_t P = std::max(1, num_sms / 2);
         const int64_t rem = tiles / 2 % P;               // `tiles` counts CTAs here
         const int64_t tail = (rem + n_pairs - 1) / n_pairs * n_pairs;
-        if (tiles / 2 > P && rem > 0 && tail <= m_pairs * n_pairs && tail < P) {
+        if (allow_tail && tiles / 2 > P && rem > 0 && tail <= m_pairs * n_pairs && tail < P) {
             int s = (int)std::min<int64_t>(P / tail, kb_total / 8);
             const int64_t row0 = (m_pairs - tail / n_pairs) * 256;
             const size_t per_tail_split = (size_t)(T - row0) * (size_t)N * sizeof(float);
@@ -1596,7 +1749,22 @@ cudaError_t launch_kv_from_rows(const uint16_t *z, const float *r2, int64_t T,
     g.col_gain = pre_w;
     const int n_pairs = N / 256, m_pairs = (int)((T + 255) / 256);
     *why = "fused projection launch";
-    if (plan.splits == 1)
+    if (plan.splits == 1 && plan.tile_ctr_offset >= 0 && ws != nullptr) {
+        // eight rounds of tiles or more: persistent pairs forming A in shared
+        // memory (2 groups of 4 forming warps), every tile in this launch, the
+        // tiles taken from the workspace's counter
+        unsigned int *ctr =
+            reinterpret_cast<unsigned int *>(reinterpret_cast<char *>(ws) + plan.tile_ctr_offset);
+        const cudaError_t e = cudaMemsetAsync(ctr, 0, sizeof(unsigned int), stream);
+        if (e != cudaSuccess)
+            return e;
+        const int limit = L * m_pairs * n_pairs;
+        return w_nk ? launch_pair_persistent<false, true, true>(ma, mb, g, fs, n_pairs, m_pairs, limit,
+                                                                ctr, stream)
+                    : launch_pair_persistent<true, true, true>(ma, mb, g, fs, n_pairs, m_pairs, limit,
+                                                               ctr, stream);
+    }
+    if (plan.splits == 1)      // one CTA pair per tile, 3 groups of 4 forming warps
         return w_nk ? launch_pair<false, true, true>(ma, mb, g, fs, n_pairs, m_pairs, stream)
                     : launch_pair<true, true, true>(ma, mb, g, fs, n_pairs, m_pairs, stream);
     cudaError_t e = w_nk ? launch_pair<false, false, true>(ma, mb, g, fs, n_pairs, m_pairs, stream)

@@ -528,16 +528,11 @@ rc_status rc_kv_project_store_rows(const uint16_t *normed, const uint16_t *W, in
 namespace {
 
 // The whole-chain calls run the forming projection, which takes every tile
-// itself: their plans have no tail launch and no tail workspace (tail plans
-// never split K, so their only workspace is the tail's).
+// itself: their plans have no tail launch (the workspace holds split-K
+// partials, or the persistent kernel's tile counter).
 rc::ProjectPlan whole_chain_plan(int32_t L, int64_t T, int32_t D, int32_t N, int sms,
                                  size_t workspace_bytes) {
-    rc::ProjectPlan p = rc::plan_kv_project(L, T, D, N, sms, workspace_bytes);
-    if (p.tail_tiles > 0) {
-        p.tail_tiles = 0;
-        p.workspace = 0;
-    }
-    return p;
+    return rc::plan_kv_project(L, T, D, N, sms, workspace_bytes, false);
 }
 
 }  // namespace

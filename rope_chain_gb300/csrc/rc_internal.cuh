@@ -278,9 +278,11 @@ struct ProjectPlan {
     size_t workspace;      // bytes used: FP32 partials (split-K or the tail's), then the counter
 };
 
-// Choose tile width and split count for the device's SM count.
+// Choose tile width and split count for the device's SM count.  Without
+// allow_tail no tail launch is planned (the forming projection of the whole
+// chain takes every tile itself).
 ProjectPlan plan_kv_project(int32_t L, int64_t T, int32_t D, int32_t N, int num_sms,
-                            size_t workspace_bytes);
+                            size_t workspace_bytes, bool allow_tail = true);
 
 // Projection; `ws` holds the FP32 partials when plan.splits > 1.
 cudaError_t launch_kv_project(const uint16_t *normed, const uint16_t *W, bool w_nk,
