@@ -42,11 +42,21 @@ L2_CLEAN_BYTES = 256 << 20          # > 129 MB L2: then read, so the written lin
 # traffic as null.
 NCU_TRAFFIC = {
     # rc_kv_project_store at workload 5: one k2_project_pair_persistent
-    # launch (dynamic tile order), 5,027,994,112 B read + 528,940,800 B
-    # written; profiles/k2_pair_persistent_workload5.md
-    (5, "store", "project_store"): (5_556_934_912, "cd64a1b96674a022",
+    # launch (dynamic tile order): 4,670,522,624 B read + 528,221,952 B
+    # written (profiles/k2_pair_persistent_workload5.md)
+    (5, "store", "project_store"): (5_198_744_576, "04d1adf9e50504c3",
                                     "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, "
                                     "one launch at full size (one pass)"),
+    # rc_context_norms at workload 5: one k1_context_norms2 launch,
+    # 537,220,608 B read + 4,245,021,184 B written
+    (5, "unfused", "norms"): (4_782_241_792, "04d1adf9e50504c3",
+                              "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, "
+                              "one launch at full size (one pass)"),
+    # rc_kv_store at workload 5: one k3_kv_store_heads launch (8 layers),
+    # 574,449,664 B read + 484,061,184 B written
+    (5, "unfused", "store"): (1_058_510_848, "04d1adf9e50504c3",
+                              "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, "
+                              "one launch at full size (one pass)"),
 }
 
 
