@@ -931,16 +931,20 @@ __device__ __forceinline__ void write_bf16_rows(const GemmArgs &g, uint32_t tbas
 // taken tiles (to the peer's loader, the MMA thread and both CTAs' epilogue
 // warps), and the readers that release each slot.
 constexpr int kTileSlots = 4;
+constexpr int kPersistFormGroups = 2;                       // groups taking stages in turn
+constexpr int kFormWarpsPerGroup = 4;
+constexpr int kFormRows = 32 / kFormWarpsPerGroup;          // rows of a stage per thread
 // leader MMA + epilogue, peer loader + epilogue; with forming warps also the
-// peer's forwarding thread and both CTAs' 8 forming warps
-__host__ __device__ constexpr int tile_readers(bool form) { return 1 + 4 + 1 + 4 + (form ? 1 + 16 : 0); }
+// peer's forwarding thread and both CTAs' forming warps
+__host__ __device__ constexpr int tile_readers(bool form) {
+    return 1 + 4 + 1 + 4 + (form ? 1 + 2 * kFormWarpsPerGroup * kPersistFormGroups : 0);
+}
 
 // Threads of the persistent kernel: loader warp, MMA warp, 4 epilogue warps,
 // and with the forming flag kPersistFormGroups groups of 4 forming warps.
-constexpr int kPersistFormGroups = 2;                      // groups taking stages in turn
-constexpr int kFormWarpsPerGroup = 8 / kPersistFormGroups;  // 8 forming warps in all
-constexpr int kFormRows = 32 / kFormWarpsPerGroup;          // rows of a stage per thread
-__host__ __device__ constexpr int persist_threads(bool form) { return kThreads + (form ? 256 : 0); }
+__host__ __device__ constexpr int persist_threads(bool form) {
+    return kThreads + (form ? 32 * kFormWarpsPerGroup * kPersistFormGroups : 0);
+}
 
 // kForm: A is formed in shared memory from the hidden-norm rows z (TMA
 // loads of z [T, D] into the A stage, then bf16((z * row_scale) * col_gain_l)
