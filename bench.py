@@ -42,21 +42,28 @@ L2_CLEAN_BYTES = 256 << 20          # > 129 MB L2: then read, so the written lin
 # traffic as null.
 NCU_TRAFFIC = {
     # rc_kv_project_store at workload 5: one k2_project_pair_persistent
-    # launch (dynamic tile order): 4,670,522,624 B read + 528,221,952 B
+    # launch (dynamic tile order): 4,653,444,608 B read + 527,944,192 B
     # written (profiles/k2_pair_persistent_workload5.md)
-    (5, "store", "project_store"): (5_198_744_576, "04d1adf9e50504c3",
+    (5, "store", "project_store"): (5_181_388_800, "1ff9a7592f57c63a",
                                     "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, "
                                     "one launch at full size (one pass)"),
     # rc_context_norms at workload 5: one k1_context_norms2 launch,
-    # 537,220,608 B read + 4,245,021,184 B written
-    (5, "unfused", "norms"): (4_782_241_792, "04d1adf9e50504c3",
+    # 537,231,104 B read + 4,244,999,168 B written
+    (5, "unfused", "norms"): (4_782_230_272, "1ff9a7592f57c63a",
                               "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, "
                               "one launch at full size (one pass)"),
     # rc_kv_store at workload 5: one k3_kv_store_heads launch (8 layers),
-    # 574,449,664 B read + 484,061,184 B written
-    (5, "unfused", "store"): (1_058_510_848, "04d1adf9e50504c3",
+    # 574,431,232 B read + 483,943,424 B written
+    (5, "unfused", "store"): (1_058_374_656, "1ff9a7592f57c63a",
                               "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, "
                               "one launch at full size (one pass)"),
+    # rc_kv_project_store at workload 2: k2_project_pair (52,103,936 B read,
+    # 18,594,304 B written) then k3_reduce_store (82,176 B read, 1,606,400 B
+    # written), captured in sequence without ncu's cache flush between them
+    # (the split-K partials are read back from L2, as in the step)
+    (2, "store", "project_store"): (72_386_816, "1ff9a7592f57c63a",
+                                    "ncu --cache-control none --metrics dram__bytes_read.sum,"
+                                    "dram__bytes_write.sum, the call's two launches in sequence"),
 }
 
 
