@@ -36,48 +36,55 @@ L2_CLEAN_BYTES = 256 << 20          # > 129 MB L2: then read, so the written lin
 # DRAM bytes (read + write) per call, from ncu captures of this bench
 # command (dram__bytes_read.sum + dram__bytes_write.sum, summed over the
 # kernels the call launches), keyed by (workload, path, call): (bytes,
-# digest of the kernel sources, how).  The digest (source_digest()) covers
-# every CUDA source and header under rope_chain_gb300/csrc; when the sources
-# change the figure no longer describes the kernels and the bench reports
-# traffic as null.
+# digest of the sources the call's kernels are built from, how).  The digest
+# (source_digest(CALL_SOURCES[call])) covers the call's kernel file, the
+# shared headers and the host launch path; when one of them changes the
+# figure no longer describes the kernels and the bench reports traffic as
+# null.
+_SHARED_SOURCES = ("rc_internal.cuh", "rc_api.cu")
+CALL_SOURCES = {
+    "project_store": ("k2_gemm.cu", "k3_store.cu", "rc_tcgen05.cuh") + _SHARED_SOURCES,
+    "norms": ("k1_norms.cu",) + _SHARED_SOURCES,
+    "store": ("k3_store.cu",) + _SHARED_SOURCES,
+    "k4_qkv_front": ("k4_qkv_front.cu", "rc_tcgen05.cuh") + _SHARED_SOURCES,
+}
 NCU_TRAFFIC = {
     # rc_kv_project_store at workload 5: one k2_project_pair_persistent
     # launch (dynamic tile order): 4,653,444,608 B read + 527,944,192 B
     # written (profiles/k2_pair_persistent_workload5.md)
-    (5, "store", "project_store"): (5_181_388_800, "1ff9a7592f57c63a",
+    (5, "store", "project_store"): (5_181_388_800, "45b107848a2e1ce4",
                                     "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, "
                                     "one launch at full size (one pass)"),
     # rc_context_norms at workload 5: one k1_context_norms2 launch,
     # 537,231,104 B read + 4,244,999,168 B written
-    (5, "unfused", "norms"): (4_782_230_272, "1ff9a7592f57c63a",
+    (5, "unfused", "norms"): (4_782_230_272, "7ec7758f9e9a9b66",
                               "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, "
                               "one launch at full size (one pass)"),
     # rc_kv_store at workload 5: one k3_kv_store_heads launch (8 layers),
     # 574,431,232 B read + 483,943,424 B written
-    (5, "unfused", "store"): (1_058_374_656, "1ff9a7592f57c63a",
+    (5, "unfused", "store"): (1_058_374_656, "3c9ac4b62e8522e0",
                               "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, "
                               "one launch at full size (one pass)"),
     # rc_kv_project_store at workload 2: k2_project_pair (52,103,936 B read,
     # 18,594,304 B written) then k3_reduce_store (82,176 B read, 1,606,400 B
     # written), captured in sequence without ncu's cache flush between them
     # (the split-K partials are read back from L2, as in the step)
-    (2, "store", "project_store"): (72_386_816, "1ff9a7592f57c63a",
+    (2, "store", "project_store"): (72_386_816, "45b107848a2e1ce4",
                                     "ncu --cache-control none --metrics dram__bytes_read.sum,"
                                     "dram__bytes_write.sum, the call's two launches in sequence"),
 }
 
 
-def source_digest() -> str:
-    """Short digest of every CUDA source and header the library is built
-    from (rope_chain_gb300/csrc), in name order."""
+def source_digest(names) -> str:
+    """Short digest of the named sources under rope_chain_gb300/csrc, in
+    name order."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "rope_chain_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            h.update(name.encode())
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+    for name in sorted(names):
+        h.update(name.encode())
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -88,7 +95,7 @@ def ncu_traffic(key):
     if entry is None:
         return None, "no ncu capture of this call at this workload"
     nbytes, digest, how = entry
-    if digest != source_digest():
+    if digest != source_digest(CALL_SOURCES[key[2]]):
         return None, "the ncu capture predates the current kernel sources"
     return nbytes, how
 

@@ -418,7 +418,8 @@ rc_status rc_context_kv_from_rows(const uint16_t *z, const float *r2, int64_t T,
  *   - All calls share the array and it keeps the last call's contents; two
  *     calls whose work overlaps on the GPU (e.g. on different streams) race
  *     on it, so order them on one stream.  Nothing in it needs clearing:
- *     each call writes every partial it reads.
+ *     each call writes every partial it reads and zeroes the tile counter
+ *     it uses (an asynchronous memset on `stream`, which allocates nothing).
  * Results are bit-identical to rc_kv_project's given a workspace of
  * rc_kv_project_workspace_size() bytes (the same plan, the same kernels).
  */

@@ -120,8 +120,10 @@ rc_status rc_kv_project_no_alloc(const uint16_t *normed, const uint16_t *W, int3
                  plan.workspace, kScratchBytes);
         return reject(RC_ERR_UNSUPPORTED, msg);
     }
-    // Nothing in the scratch has to start at zero: every FP32 partial the
-    // reduction reads is written earlier in the same call.
+    // Nothing in the scratch has to start at zero when the call begins:
+    // every FP32 partial the reduction reads is written earlier in the same
+    // call, and the persistent kernel's tile counter (plans of eight rounds
+    // of tiles or more) is zeroed by the call before its launch.
     const char *why = "launch";
     e = rc::launch_kv_project(normed, W, w_layout == RC_W_NK, out, L, T, D, N, plan,
                               static_cast<float *>(slot->scratch), stream, &why);

@@ -109,3 +109,26 @@ def test_row_chunks_cover_rows_once():
                 assert len(ch) == min(n, T)
     assert len(bench.row_chunks(512, 0)) == 1 and len(bench.row_chunks(4096, 0)) == 4
     assert len(bench.row_chunks(16384, 0)) == 8
+
+
+def test_traffic_figures_expire_with_their_sources(tmp_path, monkeypatch):
+    """A stored ncu traffic figure is reported only while the sources of its
+    call's kernels are those it was measured on: a change to the projection
+    kernel's file voids the projection's figures, not the norms'."""
+    import os
+    import shutil
+    src = os.path.join(bench.ROOT, "rope_chain_gb300", "csrc")
+    dst = tmp_path / "rope_chain_gb300" / "csrc"
+    shutil.copytree(src, dst)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    keys = list(bench.NCU_TRAFFIC)
+    assert keys and all(bench.ncu_traffic(k)[0] is not None for k in keys)
+    with open(dst / "k2_gemm.cu", "a") as f:
+        f.write("\n// changed\n")
+    for k in keys:
+        nbytes, note = bench.ncu_traffic(k)
+        if "k2_gemm.cu" in bench.CALL_SOURCES[k[2]]:
+            assert nbytes is None and "predates" in note
+        else:
+            assert nbytes == bench.NCU_TRAFFIC[k][0]
+    assert bench.ncu_traffic((9, "store", "project_store"))[0] is None

@@ -1,7 +1,9 @@
 """rc_kv_project_no_alloc, the projection for callers that cannot allocate
 device memory (its split-K scratch is a static array inside the library).
 
-Called through the C ABI on two calls in a row, for shapes that split K:
+Called through the C ABI on two calls in a row, for shapes that use its
+scratch (split-K partials, a tail launch's partials, or the counter from
+which the persistent kernel's CTA pairs take tiles):
 each output must be bit-identical to rc_kv_project given a full workspace
 (the same plan and kernels), and within the projection tolerance the other
 tests use of the oracle's float64 product.  Also: the Python wrapper, an
@@ -43,7 +45,8 @@ def _call(a_d, w_d, layout, out, L, T, D, N):
                                             (3, 128, 8192, 8, rc.RC_W_KN),
                                             (1, 64, 8192, 8, rc.RC_W_KN),
                                             (2, 100, 1024, 1, rc.RC_W_NK),
-                                            (4, 4096, 8192, 8, rc.RC_W_KN)])
+                                            (4, 4096, 8192, 8, rc.RC_W_KN),
+                                            (4, 8192, 1024, 16, rc.RC_W_KN)])
 def test_no_alloc_matches_workspace_path_twice(L, T, D, H, layout):
     N = 128 * H
     rng = np.random.default_rng(L * 1000 + T)
@@ -52,7 +55,7 @@ def test_no_alloc_matches_workspace_path_twice(L, T, D, H, layout):
     Wl = W if layout == rc.RC_W_KN else np.ascontiguousarray(W.transpose(0, 2, 1))
     a_d, w_d = parity.dev_bf16(a, DEV), parity.dev_bf16(Wl, DEV)
     nbytes = rc.workspace_size(L, T, D, N)
-    assert nbytes > 0, "this shape should use split-K scratch"
+    assert nbytes > 0, "this shape should use scratch (split-K partials or the tile counter)"
     ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
     ref = rc.kv_project(a_d, w_d, w_layout=layout, workspace=ws)
     torch.cuda.synchronize()
