@@ -498,6 +498,34 @@ __device__ __forceinline__ void unpack8f(const uint4 &q, float *f) {
     f[6] = bf16_lo(q.w); f[7] = bf16_hi(q.w);
 }
 
+// (a, b) <- (a * x, b * y), each product rounded to nearest once (the
+// packed FP32 multiply of the sm_100 family: one instruction, the bits of
+// two __fmul_rn; no flush to zero).
+__device__ __forceinline__ void mul2_rn(float &a, float &b, float x, float y) {
+    unsigned long long p, q, r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(p) : "f"(a), "f"(b));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(q) : "f"(x), "f"(y));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(p), "l"(q));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+
+// One 8-value chunk of a layer's normed row from the hidden-norm output z:
+// bf16((z * rs) * gm[e]) per value (gm == nullptr: bf16(z * rs)), the
+// operations and roundings of the norms kernel's layer step.
+__device__ __forceinline__ uint4 form_chunk(const uint4 &v, float rs, const float *gm) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float lo = bf16_lo(w[k]), hi = bf16_hi(w[k]);
+        mul2_rn(lo, hi, rs, rs);
+        if (gm != nullptr)
+            mul2_rn(lo, hi, gm[2 * k], gm[2 * k + 1]);
+        o[k] = pack_bf16x2(lo, hi);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // kTransform: the A tile is formed in shared memory from the hidden-norm
 // output z (TMA-loaded): A = bf16((z * row_scale) * col_gain_l), the same
 // operations and roundings as the norms kernel's layer step, so the operand
@@ -717,20 +745,8 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     v[j] = ld_shared_v4(addr[j]);
                 }
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    float f[8];
-                    unpack8f(v[j], f);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        f[e] = __fmul_rn(f[e], rs[j]);
-                    if (gain) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            f[e] = __fmul_rn(f[e], gm[e]);
-                    }
-                    v[j] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                                      pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
-                }
+                for (int j = 0; j < 8; ++j)
+                    v[j] = form_chunk(v[j], rs[j], gain ? gm : nullptr);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     st_shared_v4(addr[j], v[j]);
@@ -1277,20 +1293,8 @@ k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
                     v[jj] = ld_shared_v4(addr[jj]);
                 }
 #pragma unroll
-                for (int jj = 0; jj < kFormRows; ++jj) {
-                    float f[8];
-                    unpack8f(v[jj], f);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        f[e] = __fmul_rn(f[e], rs[jj]);
-                    if (gain) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            f[e] = __fmul_rn(f[e], gm[e]);
-                    }
-                    v[jj] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                                       pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
-                }
+                for (int jj = 0; jj < kFormRows; ++jj)
+                    v[jj] = form_chunk(v[jj], rs[jj], gain ? gm : nullptr);
 #pragma unroll
                 for (int jj = 0; jj < kFormRows; ++jj)
                     st_shared_v4(addr[jj], v[jj]);
