@@ -440,14 +440,11 @@ __device__ __forceinline__ void fused_store_tile(const FusedStore &fs, const Gem
         uint16_t *dst = store ? dst_row + (int64_t)h * fs.block_size * (2 * kHeadDim) + (is_k ? 0 : kHeadDim)
                               : nullptr;
         if (is_k) {
-            float ev[32], od[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float k0 = bf16_lo(kp[j]), k1 = bf16_hi(kp[j]);
-                ev[j] = __fmul_rn(k0, k0);
-                od[j] = __fmul_rn(k1, k1);
-            }
-            const float rr = inv_rms(__fadd_rn(fold32(ev), fold32(od)), 0x1p-6f, fs.eps);
+            // the K-norm's even and odd square sums in the store kernel's
+            // fold order, then the bf16 key and its rotation per pair
+            float even, odd;
+            fold32_squares2(kp, even, odd);
+            const float rr = inv_rms(__fadd_rn(even, odd), 0x1p-6f, fs.eps);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {              // 8 pairs at a time
                 if (!kPreload && cs != nullptr) {
@@ -459,17 +456,10 @@ __device__ __forceinline__ void fused_store_tile(const FusedStore &fs, const Gem
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
                     const int j = 8 * q + t;
-                    float n0v = round_bf16(__fmul_rn(bf16_lo(kp[j]), rr));
-                    float n1v = round_bf16(__fmul_rn(bf16_hi(kp[j]), rr));
-                    if (rope) {
-                        const float c = (t & 1) ? bf16_hi(cw[t >> 1]) : bf16_lo(cw[t >> 1]);
-                        const float sn = (t & 1) ? bf16_hi(sw[t >> 1]) : bf16_lo(sw[t >> 1]);
-                        const float x = __fmaf_rn(n0v, c, -__fmul_rn(n1v, sn));
-                        const float y = __fmaf_rn(n1v, c, __fmul_rn(n0v, sn));
-                        n0v = x;
-                        n1v = y;
-                    }
-                    kp[j] = pack_bf16x2(n0v, n1v);
+                    const float c = (t & 1) ? bf16_hi(cw[t >> 1]) : bf16_lo(cw[t >> 1]);
+                    const float sn = (t & 1) ? bf16_hi(sw[t >> 1]) : bf16_lo(sw[t >> 1]);
+                    kp[j] = rope ? norm_rope_pair<true>(kp[j], rr, c, sn)
+                                 : norm_rope_pair<false>(kp[j], rr, c, sn);
                 }
             }
         }
@@ -496,17 +486,6 @@ __device__ __forceinline__ void unpack8f(const uint4 &q, float *f) {
     f[2] = bf16_lo(q.y); f[3] = bf16_hi(q.y);
     f[4] = bf16_lo(q.z); f[5] = bf16_hi(q.z);
     f[6] = bf16_lo(q.w); f[7] = bf16_hi(q.w);
-}
-
-// (a, b) <- (a * x, b * y), each product rounded to nearest once (the
-// packed FP32 multiply of the sm_100 family: one instruction, the bits of
-// two __fmul_rn; no flush to zero).
-__device__ __forceinline__ void mul2_rn(float &a, float &b, float x, float y) {
-    unsigned long long p, q, r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(p) : "f"(a), "f"(b));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(q) : "f"(x), "f"(y));
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(p), "l"(q));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
 }
 
 // One 8-value chunk of a layer's normed row from the hidden-norm output z:

@@ -87,24 +87,83 @@ __device__ __forceinline__ float fold32(const float (&q)[32]) {
     return __fadd_rn(a[0], a[1]);
 }
 
-// fold32 of the squares of the low (hi = false) or high halves of 32 packed
-// bf16 pairs, its first level taken as the squares are formed.
-template <bool kHi>
-__device__ __forceinline__ float fold32_squares(const uint32_t (&w)[32]) {
-    float a[16];
+// ------------------------------------------------ packed FP32 pairs
+//
+// The sm_100 family's .f32x2 arithmetic: one instruction works on two FP32
+// values, each lane rounded to nearest once and nothing flushed to zero, so
+// a lane's result has the bits of the scalar __fadd_rn / __fmul_rn /
+// __fmaf_rn.
+
+__device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
+    unsigned long long p;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(p) : "f"(a), "f"(b));
+    return p;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long p, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(p));
+}
+
+// (a, b) <- (a + x, b + y)
+__device__ __forceinline__ void add2_rn(float &a, float &b, float x, float y) {
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_pack(a, b)), "l"(f2_pack(x, y)));
+    f2_unpack(r, a, b);
+}
+// (a, b) <- (a * x, b * y)
+__device__ __forceinline__ void mul2_rn(float &a, float &b, float x, float y) {
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_pack(a, b)), "l"(f2_pack(x, y)));
+    f2_unpack(r, a, b);
+}
+// (a, b) <- (fma(a, x, u), fma(b, y, v))
+__device__ __forceinline__ void fma2_rn(float &a, float &b, float x, float y, float u, float v) {
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(r) : "l"(f2_pack(a, b)), "l"(f2_pack(x, y)), "l"(f2_pack(u, v)));
+    f2_unpack(r, a, b);
+}
+
+// The even and the odd square sums of a key head (w[j]: pair j = elements
+// (2j, 2j+1) as packed bf16), each folded as fold32 folds: (j, j+16), then
+// partners +8, +4, +2, +1.  The two trees run side by side in packed pairs.
+__device__ __forceinline__ void fold32_squares2(const uint32_t (&w)[32], float &even, float &odd) {
+    float e[16], o[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-        const float x = kHi ? bf16_hi(w[j]) : bf16_lo(w[j]);
-        const float y = kHi ? bf16_hi(w[j + 16]) : bf16_lo(w[j + 16]);
-        a[j] = __fadd_rn(__fmul_rn(x, x), __fmul_rn(y, y));
+        float x0 = bf16_lo(w[j]), x1 = bf16_hi(w[j]);
+        float y0 = bf16_lo(w[j + 16]), y1 = bf16_hi(w[j + 16]);
+        mul2_rn(x0, x1, x0, x1);
+        mul2_rn(y0, y1, y0, y1);
+        add2_rn(x0, x1, y0, y1);
+        e[j] = x0;
+        o[j] = x1;
     }
 #pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) {
+    for (int s = 8; s >= 1; s >>= 1) {
 #pragma unroll
-        for (int j = 0; j < o; ++j)
-            a[j] = __fadd_rn(a[j], a[j + o]);
+        for (int j = 0; j < s; ++j)
+            add2_rn(e[j], o[j], e[j + s], o[j + s]);
     }
-    return a[0];
+    even = e[0];
+    odd = o[0];
+}
+
+// One key pair kw = (k0, k1) after the head's inverse RMS r: the bf16 key
+// (bf16(k0 * r), bf16(k1 * r)) and with kRope the GPT-J rotation
+// (fma(n0, c, -(n1 * s)), fma(n1, c, n0 * s)), packed to bf16.
+template <bool kRope>
+__device__ __forceinline__ uint32_t norm_rope_pair(uint32_t kw, float r, float c, float s) {
+    float n0 = bf16_lo(kw), n1 = bf16_hi(kw);
+    mul2_rn(n0, n1, r, r);
+    const uint32_t n = pack_bf16x2(n0, n1);
+    if (!kRope)
+        return n;
+    n0 = bf16_lo(n);
+    n1 = bf16_hi(n);
+    float p1 = n1, p0 = n0;                       // (n1 * s, n0 * s)
+    mul2_rn(p1, p0, s, s);
+    fma2_rn(n0, n1, c, c, -p1, p0);
+    return pack_bf16x2(n0, n1);
 }
 
 // One whole key head in one thread: w[j] holds pair j = elements (2j, 2j+1)
@@ -116,8 +175,8 @@ __device__ __forceinline__ float fold32_squares(const uint32_t (&w)[32]) {
 template <bool kRope>
 __device__ __forceinline__ void knorm_rope_head(uint32_t (&w)[32], const uint4 *cs, int swz,
                                                 float eps) {
-    const float even = fold32_squares<false>(w);
-    const float odd = fold32_squares<true>(w);
+    float even, odd;
+    fold32_squares2(w, even, odd);
     const float r = inv_rms(__fadd_rn(even, odd), 0x1p-6f, eps);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {                 // 8 pairs per table chunk
@@ -130,17 +189,9 @@ __device__ __forceinline__ void knorm_rope_head(uint32_t (&w)[32], const uint4 *
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
             const int j = 8 * q + t;
-            float n0 = round_bf16(__fmul_rn(bf16_lo(w[j]), r));
-            float n1 = round_bf16(__fmul_rn(bf16_hi(w[j]), r));
-            if (kRope) {
-                const float c = (t & 1) ? bf16_hi(cw[t >> 1]) : bf16_lo(cw[t >> 1]);
-                const float s = (t & 1) ? bf16_hi(sw[t >> 1]) : bf16_lo(sw[t >> 1]);
-                const float x = __fmaf_rn(n0, c, -__fmul_rn(n1, s));
-                const float y = __fmaf_rn(n1, c, __fmul_rn(n0, s));
-                n0 = x;
-                n1 = y;
-            }
-            w[j] = pack_bf16x2(n0, n1);
+            const float c = (t & 1) ? bf16_hi(cw[t >> 1]) : bf16_lo(cw[t >> 1]);
+            const float s = (t & 1) ? bf16_hi(sw[t >> 1]) : bf16_lo(sw[t >> 1]);
+            w[j] = norm_rope_pair<kRope>(w[j], r, c, s);
         }
     }
 }
