@@ -713,22 +713,20 @@ k2_project_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     raise_fault(kFaultLoad);
                     break;
                 }
-                // all 8 rows' chunks in flight, then formed, then written back
-                const uint32_t st = sA + s * kABytes;
-                uint32_t addr[8];
+                // all 8 rows' chunks in flight, then formed, then written
+                // back; rows r0 + 16 j share r % 8, so their swizzled chunks
+                // sit 2048 bytes apart from one base
+                const uint32_t base = sA + s * kABytes + r0 * 128 + ((c ^ (r0 & 7)) << 4);
                 uint4 v[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int r = r0 + 16 * j;
-                    addr[j] = st + r * 128 + ((c ^ (r & 7)) << 4);
-                    v[j] = ld_shared_v4(addr[j]);
-                }
+                for (int j = 0; j < 8; ++j)
+                    v[j] = ld_shared_v4(base + 2048u * j);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     v[j] = form_chunk(v[j], rs[j], gain ? gm : nullptr);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    st_shared_v4(addr[j], v[j]);
+                    st_shared_v4(base + 2048u * j, v[j]);
                 // generic-proxy writes, then visible to the tensor core
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
@@ -1261,22 +1259,21 @@ k2_project_pair_persistent(const __grid_constant__ CUtensorMap tmA,
                     ok = false;
                     break;
                 }
-                // all rows' chunks in flight, then formed, then written back
-                const uint32_t st = sA + s * kABytes;
-                uint32_t addr[kFormRows];
+                // all rows' chunks in flight, then formed, then written back;
+                // rows r0 + kRowStep jj share r % 8 (kRowStep is a multiple of
+                // 8), so their swizzled chunks sit kRowStep * 128 bytes apart
+                static_assert(kRowStep % 8 == 0, "one swizzle phase for a thread's rows");
+                const uint32_t base = sA + s * kABytes + r0 * 128 + ((c ^ (r0 & 7)) << 4);
                 uint4 v[kFormRows];
 #pragma unroll
-                for (int jj = 0; jj < kFormRows; ++jj) {
-                    const int r = r0 + kRowStep * jj;
-                    addr[jj] = st + r * 128 + ((c ^ (r & 7)) << 4);
-                    v[jj] = ld_shared_v4(addr[jj]);
-                }
+                for (int jj = 0; jj < kFormRows; ++jj)
+                    v[jj] = ld_shared_v4(base + 128u * kRowStep * jj);
 #pragma unroll
                 for (int jj = 0; jj < kFormRows; ++jj)
                     v[jj] = form_chunk(v[jj], rs[jj], gain ? gm : nullptr);
 #pragma unroll
                 for (int jj = 0; jj < kFormRows; ++jj)
-                    st_shared_v4(addr[jj], v[jj]);
+                    st_shared_v4(base + 128u * kRowStep * jj, v[jj]);
                 // generic-proxy writes, then visible to the tensor core
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
