@@ -50,26 +50,26 @@ CALL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # rc_kv_project_store at workload 5: one k2_project_pair_persistent
-    # launch (dynamic tile order): 4,653,444,608 B read + 527,944,192 B
+    # launch (dynamic tile order): 4,774,993,664 B read + 528,049,152 B
     # written (profiles/k2_pair_persistent_workload5.md)
-    (5, "store", "project_store"): (5_181_388_800, "45b107848a2e1ce4",
+    (5, "store", "project_store"): (5_303_042_816, "36ceca48e1f66057",
                                     "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, "
                                     "one launch at full size (one pass)"),
     # rc_context_norms at workload 5: one k1_context_norms2 launch,
-    # 537,231,104 B read + 4,244,999,168 B written
-    (5, "unfused", "norms"): (4_782_230_272, "7ec7758f9e9a9b66",
+    # 537,246,976 B read + 4,245,162,240 B written
+    (5, "unfused", "norms"): (4_782_409_216, "b22eb1f75ec280f1",
                               "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, "
                               "one launch at full size (one pass)"),
     # rc_kv_store at workload 5: one k3_kv_store_heads launch (8 layers),
-    # 574,431,232 B read + 483,943,424 B written
-    (5, "unfused", "store"): (1_058_374_656, "3c9ac4b62e8522e0",
+    # 574,434,304 B read + 483,296,000 B written
+    (5, "unfused", "store"): (1_057_730_304, "af574945006ccd2a",
                               "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, "
                               "one launch at full size (one pass)"),
-    # rc_kv_project_store at workload 2: k2_project_pair (52,103,936 B read,
-    # 18,594,304 B written) then k3_reduce_store (82,176 B read, 1,606,400 B
+    # rc_kv_project_store at workload 2: k2_project_pair (52,292,352 B read,
+    # 19,631,360 B written) then k3_reduce_store (81,408 B read, 1,568,768 B
     # written), captured in sequence without ncu's cache flush between them
     # (the split-K partials are read back from L2, as in the step)
-    (2, "store", "project_store"): (72_386_816, "45b107848a2e1ce4",
+    (2, "store", "project_store"): (73_573_888, "36ceca48e1f66057",
                                     "ncu --cache-control none --metrics dram__bytes_read.sum,"
                                     "dram__bytes_write.sum, the call's two launches in sequence"),
 }
