@@ -429,6 +429,9 @@ def run_ours(args, w):
     ws_bytes = rc.workspace_size(w.L, w.T, w.D, w.N)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     cws = rc.context_kv_workspace(w.L, w.T, w.H, dev)   # the whole-chain call's workspace
+    chunked = args.path == "store" and args.chunks != 1
+    if chunked:                                      # the chunked chain's normed rows and counters
+        kws = rc.context_kv_chunked_workspace(w.L, w.T, w.H, dev, chunks=args.chunks)
     z = torch.empty((w.T, w.D), dtype=torch.bfloat16, device=dev)
     r2 = torch.empty((w.T,), dtype=torch.float32, device=dev)
     flush = L2Flush(dev)
@@ -446,6 +449,11 @@ def run_ours(args, w):
     launches_per_step = 2 + (1 if split else (0 if pair else (w.L + 7) // 8))
     if tail and args.path != "whole":
         launches_per_step += 2
+    # the chunked chain: per row chunk the norms and one persistent
+    # projection + store (a memset of the chunks' tile counters first)
+    n_chunks = rc.context_kv_chunks(w.L, w.T, w.H, sms, args.chunks) if chunked else 1
+    if n_chunks > 1:
+        launches_per_step = 2 * n_chunks
 
     whole = args.path == "whole"
     variants = args.path == "variants"
@@ -483,6 +491,10 @@ def run_ours(args, w):
             ready()
             rc.kv_project_store(normed, W, w.H, pos, sl, cs, caches, w.eps, rows=layer_rows,
                                 err=err, workspace=ws if use_ws else None)
+        elif chunked:
+            ready()
+            rc.context_kv_chunked(xs, hw, pw, W, w.H, pos, sl, cs, caches, w.eps, kws, err=err,
+                                  chunks=args.chunks)
         else:
             rc.context_norms(xs, hw, pw, w.L, w.eps, out=normed)
             ready()
@@ -492,7 +504,9 @@ def run_ours(args, w):
             ev[2].record()
 
     def chain_split(ev):
-        """The same work as chain(), an event between its kernels (breakdown)."""
+        """The work of chain() over all rows in one chunk, an event between
+        its two calls (breakdown; the projection + store call is the one the
+        roofline times)."""
         ev[0].record()
         if whole and pair:
             rc.context_rows(x, hw, w.eps, z=z, r2=r2)
@@ -503,12 +517,12 @@ def run_ours(args, w):
             norms_variant()
             ev[1].record()
             rc.kv_project_store(normed, W, w.H, positions, slots, cs, caches, w.eps, rows=layer_rows,
-                                err=err, kv_out=kv, workspace=ws if use_ws else None)
+                                err=err, workspace=ws if use_ws else None)
         else:
             rc.context_norms(x, hw, pw, w.L, w.eps, out=normed)
             ev[1].record()
             rc.kv_project_store(normed, W, w.H, positions, slots, cs, caches, w.eps, err=err,
-                                kv_out=kv, workspace=ws if use_ws else None)
+                                workspace=ws if use_ws else None)
         ev[2].record()
 
     def chain_unfused(ev):
@@ -683,6 +697,9 @@ def run_ours(args, w):
                     "project": tc_entry(us(u_ms[1])),
                     "store": hbm_entry(k3_bytes, us(u_ms[2]))},
     }
+    if n_chunks > 1:
+        kern["note"] = ("norms and project_store: the step's two kernels over all rows, one "
+                        "after the other between events (the chunked step overlaps them)")
     first = "row_pass" if fused_norms else "norms"
     dominant = "project_store" if kern["project_store"]["us"] >= kern[first]["us"] else first
     d = kern[dominant]
@@ -715,7 +732,12 @@ def run_ours(args, w):
                              "rc_context_norms_ex (FP32 gains, hidden gain on the input, layer "
                              "gain centre 1, separate eps) + rc_kv_project_store_rows (per-layer "
                              "slot lengths)" if variants else
+                             f"rc_context_kv_chunked ({n_chunks} row chunks: the norms of chunk "
+                             "c + 1 run beside the projection + store of chunk c)" if n_chunks > 1 else
+                             "rc_context_kv_chunked (one chunk: rc_context_norms, then "
+                             "rc_kv_project_store with the store fused)" if chunked else
                              "rc_context_norms + rc_kv_project_store (projection with the store fused)")
+    rec["config"]["row_chunks"] = n_chunks
     rec.update({
         "value": world * w.T * args.steps / (total_ms / 1e3),
         "ms_per_step": total_ms / args.steps,
@@ -733,7 +755,7 @@ def run_ours(args, w):
                            "x read in place from pinned host memory by the norms kernel "
                            "(NVLink-C2C)") +
                           "; positions and slot maps in one pinned buffer, one copy per step" +
-                          ("" if whole else " alongside the norms"),
+                          ("" if whole or chunked else " alongside the norms"),
                 "outputs": "the K/V result stays in the device caches (the operation's "
                            "output); only the 4-byte skip count is copied back per step",
                 "row_ranges": len(chunks),
@@ -940,6 +962,11 @@ def main():
     ap.add_argument("--rows", type=int, default=0, metavar="R",
                     help="run only the first R rows of the workload (a smaller case of its "
                          "shape, for profiler captures; 0: all rows)")
+    ap.add_argument("--chunks", type=int, default=0, metavar="N",
+                    help="row chunks of the store path's step (rc_context_kv_chunked: each "
+                         "chunk's norms beside the previous chunk's projection); 0: the "
+                         "library's choice; 1: the two calls rc_context_norms and "
+                         "rc_kv_project_store")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="store", choices=["store", "whole", "variants", "front"],
                     help="store: norms + fused projection/store; whole: rc_context_kv; variants: "

@@ -372,6 +372,59 @@ rc_status rc_context_kv(const uint16_t *x, int64_t T, int32_t D,
 size_t rc_context_kv_workspace_size(int32_t L, int64_t T, int32_t D, int32_t H);
 
 /*
+ * rc_context_kv_chunked -- steps 1 to 4 ([rt] ContextKV.store /
+ * MuseSparkDSparkModel.precompute_and_store_context_kv) as
+ * rc_context_norms followed by rc_kv_project_store, by row chunks: the
+ * norms of chunk c + 1 run on the GPU beside the projection + store of
+ * chunk c (each SM holds one persistent projection CTA and one norms CTA),
+ * so that the norms' HBM traffic overlaps the tensor-bound projection.  The
+ * caches receive exactly the bits of rc_context_norms + rc_kv_project_store
+ * (the normed rows, each projection sum and each stored bit are the same;
+ * only the order in which rows are stored differs, so two rows sharing a
+ * slot may leave either row's values, as in rc_kv_project_store).
+ *
+ *   x, T, D, hidden_w, pre_w, L, eps   as rc_context_norms (D = 8192,
+ *                                      L <= 64)
+ *   W, w_layout, H                     as rc_kv_project (N = 128*H)
+ *   positions ... err                  as rc_kv_project_store (no kv_out)
+ *   chunks      row chunks wanted (<= 0: chosen for the sizes); fewer are
+ *               used where a chunk's projection would not run as
+ *               persistent CTA pairs without workspace (rc_context_kv_chunks
+ *               says how many)
+ *   workspace   device scratch, 256-byte aligned, required, not
+ *               overlapping x or W: the normed rows [L, T, D] (chunk by
+ *               chunk), then a 256-byte tile counter per chunk (or, with one
+ *               chunk, the projection's workspace);
+ *               rc_context_kv_chunked_workspace_size() gives the bytes
+ * The call ends with the last chunk's projection, which starts after every
+ * earlier kernel of the call has completed; a later kernel or copy in the
+ * stream sees all of the call's writes.  Errors as rc_kv_project_store; in
+ * addition RC_ERR_UNSUPPORTED where one chunk's projection would need
+ * kv_out (T <= 128 or H = 1 without split-K room in the workspace).
+ */
+rc_status rc_context_kv_chunked(const uint16_t *x, int64_t T, int32_t D,
+                                const uint16_t *hidden_w, const uint16_t *pre_w,
+                                int32_t L, float eps, const uint16_t *W,
+                                int32_t w_layout, int32_t H, const int64_t *positions,
+                                const int64_t *const *slots, const uint16_t *cos_sin,
+                                int64_t max_position, uint16_t *const *caches,
+                                int32_t num_blocks, int32_t block_size, int64_t rows,
+                                int32_t *err, int32_t chunks, void *workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes of rc_context_kv_chunked for these sizes and chunk request
+   on the current device (0 for unsupported sizes). */
+size_t rc_context_kv_chunked_workspace_size(int32_t L, int64_t T, int32_t D, int32_t H,
+                                            int32_t chunks);
+
+/* Host only: the number of row chunks rc_context_kv_chunked uses for these
+   sizes and chunk request on a GPU of num_sms SMs (0 for unsupported
+   sizes).  row0, when not NULL, receives the chunks' first rows and T
+   (count + 1 entries; room for 17). */
+int32_t rc_context_kv_chunks(int32_t L, int64_t T, int32_t D, int32_t H, int32_t chunks,
+                             int32_t num_sms, int64_t *row0);
+
+/*
  * rc_context_kv in two calls.  rc_context_rows is the row pass: per row t,
  *   z[t]  = bf16(hidden_norm(x[t]))          bf16 [T, 8192], 16-byte aligned
  *   r2[t] = 1/sqrt(fma(sum z[t]^2, 1/D, eps)) FP32 [T] (the layer norms'

@@ -104,6 +104,14 @@ SIGNATURES["rc_qkv_front"] = ([_vp, _c.c_int32, _c.c_int32, _vp, _c.c_int32, _c.
                                _vp, _vp], _c.c_int)
 SIGNATURES["rc_context_norms_ex"] = ([_vp, _c.c_int64, _c.c_int32, _c.POINTER(NormParams),
                                       _c.POINTER(NormParams), _c.c_int32, _vp, _vp], _c.c_int)
+SIGNATURES["rc_context_kv_chunked"] = ([_vp, _c.c_int64, _c.c_int32, _vp, _vp, _c.c_int32, _c.c_float,
+                                        _vp, _c.c_int32, _c.c_int32, _vp, _c.POINTER(_vp), _vp,
+                                        _c.c_int64, _c.POINTER(_vp), _c.c_int32, _c.c_int32,
+                                        _c.c_int64, _vp, _c.c_int32, _vp, _c.c_size_t, _vp], _c.c_int)
+SIGNATURES["rc_context_kv_chunked_workspace_size"] = ([_c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32,
+                                                       _c.c_int32], _c.c_size_t)
+SIGNATURES["rc_context_kv_chunks"] = ([_c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32, _c.c_int32,
+                                       _c.c_int32, _c.POINTER(_c.c_int64)], _c.c_int32)
 
 
 def lib():
@@ -496,6 +504,55 @@ def context_kv(x: torch.Tensor, hidden_w, pre_w, W: torch.Tensor, H: int, positi
                                0 if cos_sin is None else cos_sin.shape[0], cache_arr, nb, bs, rows,
                                _ptr(err), _ptr(kv_out), workspace.data_ptr(),
                                workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def context_kv_chunks(L: int, T: int, H: int, num_sms: int, chunks: int = 0, D: int = 8192) -> int:
+    """Row chunks rc_context_kv_chunked uses for these sizes (host only)."""
+    return int(lib().rc_context_kv_chunks(L, T, D, H, chunks, num_sms, None))
+
+
+def context_kv_chunk_rows(L: int, T: int, H: int, num_sms: int, chunks: int = 0,
+                          D: int = 8192) -> list:
+    """The first row of each chunk rc_context_kv_chunked uses, then T (host
+    only; [] for unsupported sizes)."""
+    row0 = (_c.c_int64 * 17)()
+    n = int(lib().rc_context_kv_chunks(L, T, D, H, chunks, num_sms, row0))
+    return [int(row0[i]) for i in range(n + 1)] if n else []
+
+
+def context_kv_chunked_workspace(L: int, T: int, H: int, device, chunks: int = 0,
+                                 D: int = 8192) -> torch.Tensor:
+    """A workspace for context_kv_chunked (rc_context_kv_chunked_workspace_size bytes)."""
+    n = int(lib().rc_context_kv_chunked_workspace_size(L, T, D, H, chunks))
+    if n == 0:
+        raise RopeChainError(RC_ERR_UNSUPPORTED, "no workspace size for these sizes")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def context_kv_chunked(x: torch.Tensor, hidden_w, pre_w, W: torch.Tensor, H: int, positions, slots,
+                       cos_sin, caches, eps: float, workspace: torch.Tensor,
+                       rows: Optional[int] = None, err=None, chunks: int = 0,
+                       w_layout: int = RC_W_KN, stream=None) -> None:
+    """Norms, projection and store by row chunks (rc_context_kv_chunked): a
+    chunk's norms run beside the previous chunk's projection.
+    ``workspace``: context_kv_chunked_workspace() with the same ``chunks``."""
+    xa = _in_bf16(x, "x")                          # CUDA or pinned host memory
+    _bf16(W, "W")
+    T, D = x.shape
+    L = len(caches)
+    for w_, n in ((hidden_w, "hidden_w"), (pre_w, "pre_w")):
+        if w_ is not None:
+            _bf16(w_, n)
+    if not (workspace.is_cuda and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    slot_arr, cache_arr, nb, bs, rows = _store_operands(H, slots, caches, positions, cos_sin, rows)
+    _check(lib().rc_context_kv_chunked(xa, T, D, _ptr(hidden_w), _ptr(pre_w), L, eps,
+                                       W.data_ptr(), w_layout, H, _ptr(positions), slot_arr,
+                                       _ptr(cos_sin), 0 if cos_sin is None else cos_sin.shape[0],
+                                       cache_arr, nb, bs, rows, _ptr(err), chunks,
+                                       workspace.data_ptr(),
+                                       workspace.numel() * workspace.element_size(),
+                                       _stream(stream)))
 
 
 def context_rows(x: torch.Tensor, hidden_w, eps: float, z: Optional[torch.Tensor] = None,

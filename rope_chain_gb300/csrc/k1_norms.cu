@@ -64,17 +64,29 @@ __device__ __forceinline__ uint4 pack8(const float *y) {
     return w;
 }
 
+// `early`: the kernel was launched while the kernel before it in the stream
+// still runs, and touches nothing that kernel reads or writes, so it does not
+// wait for it at the start.  It still completes after it: its last CTA waits
+// for that kernel before exiting, so a kernel that waits for this one (the
+// projection of these rows) has also waited for the one before.
+__device__ __forceinline__ void early_join(int early) {
+    if (early && blockIdx.x == gridDim.x - 1 && threadIdx.x == 0)
+        pdl_wait();
+}
+
 template <bool kHiddenW, bool kPreW>
 __global__ void __launch_bounds__(kThreads, 4)
 k1_context_norms(const uint16_t *__restrict__ x, int64_t T,
                  const uint16_t *__restrict__ hidden_w, const uint16_t *__restrict__ pre_w,
-                 int32_t L, float hidden_eps, float pre_eps, uint16_t *__restrict__ out)
+                 int32_t L, float hidden_eps, float pre_eps, uint16_t *__restrict__ out,
+                 int early)
 {
     __shared__ float sums[2][kThreads / 32];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t row = blockIdx.x;
     pdl_trigger();
-    pdl_wait();
+    if (!early)
+        pdl_wait();
 
     // The row (read once: streaming) and the hidden gains (shared by all
     // rows: cached) load together.
@@ -140,6 +152,7 @@ k1_context_norms(const uint16_t *__restrict__ x, int64_t T,
             o[k * kFragStride + tid] = pack8(f);
         }
     }
+    early_join(early);
 }
 
 // The same norms with two rows per CTA: each thread holds its 32 columns of
@@ -150,14 +163,16 @@ template <bool kHiddenW, bool kPreW>
 __global__ void __launch_bounds__(kThreads, 2)
 k1_context_norms2(const uint16_t *__restrict__ x, int64_t T,
                   const uint16_t *__restrict__ hidden_w, const uint16_t *__restrict__ pre_w,
-                  int32_t L, float hidden_eps, float pre_eps, uint16_t *__restrict__ out)
+                  int32_t L, float hidden_eps, float pre_eps, uint16_t *__restrict__ out,
+                  int early)
 {
     __shared__ float sums[2][2][kThreads / 32];    // [norm][row of the pair][warp]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t row0 = 2 * (int64_t)blockIdx.x;
     const bool two = row0 + 1 < T;
     pdl_trigger();
-    pdl_wait();
+    if (!early)
+        pdl_wait();
 
     const uint4 *xa = reinterpret_cast<const uint4 *>(x) + row0 * (kHidden / 8);
     const uint4 *xb = xa + kHidden / 8;
@@ -268,6 +283,7 @@ k1_context_norms2(const uint16_t *__restrict__ x, int64_t T,
                 ob[k * kFragStride + tid] = pack8(fb);
         }
     }
+    early_join(early);
 }
 
 // The row half of the norms for the fused chain: z = bf16(hidden_norm(x))
@@ -732,35 +748,36 @@ cudaError_t launch_context_norms_ex(const uint16_t *x, int64_t T, const NormDesc
 
 cudaError_t launch_context_norms(const uint16_t *x, int64_t T, const uint16_t *hidden_w,
                                  const uint16_t *pre_w, int32_t L, float hidden_eps, float pre_eps,
-                                 uint16_t *out, cudaStream_t stream)
+                                 uint16_t *out, cudaStream_t stream, bool early)
 {
+    const int ea = early ? 1 : 0;
     const dim3 block(kThreads);
     if (T >= kTwoRowsFrom) {                       // two rows per CTA
         const dim3 grid2((unsigned)((T + 1) / 2));
         if (hidden_w && pre_w)
             return launch_pdl(k1_context_norms2<true, true>, grid2, block, 0, stream, 1, x, T,
-                              hidden_w, pre_w, L, hidden_eps, pre_eps, out);
+                              hidden_w, pre_w, L, hidden_eps, pre_eps, out, ea);
         if (hidden_w)
             return launch_pdl(k1_context_norms2<true, false>, grid2, block, 0, stream, 1, x, T,
-                              hidden_w, pre_w, L, hidden_eps, pre_eps, out);
+                              hidden_w, pre_w, L, hidden_eps, pre_eps, out, ea);
         if (pre_w)
             return launch_pdl(k1_context_norms2<false, true>, grid2, block, 0, stream, 1, x, T,
-                              hidden_w, pre_w, L, hidden_eps, pre_eps, out);
+                              hidden_w, pre_w, L, hidden_eps, pre_eps, out, ea);
         return launch_pdl(k1_context_norms2<false, false>, grid2, block, 0, stream, 1, x, T,
-                          hidden_w, pre_w, L, hidden_eps, pre_eps, out);
+                          hidden_w, pre_w, L, hidden_eps, pre_eps, out, ea);
     }
     const dim3 grid((unsigned)T);
     if (hidden_w && pre_w)
         return launch_pdl(k1_context_norms<true, true>, grid, block, 0, stream, 1, x, T, hidden_w,
-                          pre_w, L, hidden_eps, pre_eps, out);
+                          pre_w, L, hidden_eps, pre_eps, out, ea);
     if (hidden_w)
         return launch_pdl(k1_context_norms<true, false>, grid, block, 0, stream, 1, x, T, hidden_w,
-                          pre_w, L, hidden_eps, pre_eps, out);
+                          pre_w, L, hidden_eps, pre_eps, out, ea);
     if (pre_w)
         return launch_pdl(k1_context_norms<false, true>, grid, block, 0, stream, 1, x, T, hidden_w,
-                          pre_w, L, hidden_eps, pre_eps, out);
+                          pre_w, L, hidden_eps, pre_eps, out, ea);
     return launch_pdl(k1_context_norms<false, false>, grid, block, 0, stream, 1, x, T, hidden_w,
-                      pre_w, L, hidden_eps, pre_eps, out);
+                      pre_w, L, hidden_eps, pre_eps, out, ea);
 }
 
 cudaError_t launch_row_prep(const uint16_t *x, int64_t T, const uint16_t *hidden_w, float eps,

@@ -1535,9 +1535,11 @@ cudaError_t launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const Gemm
         if (plan.tile_ctr_offset >= 0 && g.partial != nullptr) {
             ctr = reinterpret_cast<unsigned int *>(reinterpret_cast<char *>(g.partial) +
                                                    plan.tile_ctr_offset);
-            const cudaError_t e = cudaMemsetAsync(ctr, 0, sizeof(unsigned int), stream);
-            if (e != cudaSuccess)
-                return e;
+            if (!plan.ctr_zeroed) {
+                const cudaError_t e = cudaMemsetAsync(ctr, 0, sizeof(unsigned int), stream);
+                if (e != cudaSuccess)
+                    return e;
+            }
         }
         return w_nk ? launch_pair_persistent<false, kFused>(ma, mb, g, fs, n_pairs, m_pairs, limit, ctr, stream)
                     : launch_pair_persistent<true, kFused>(ma, mb, g, fs, n_pairs, m_pairs, limit, ctr, stream);

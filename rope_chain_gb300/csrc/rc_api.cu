@@ -5,6 +5,7 @@
 #include "rc_internal.cuh"
 
 #include <algorithm>
+#include <numeric>
 #include <cstdarg>
 #include <cstdio>
 
@@ -685,6 +686,235 @@ rc_status rc_context_kv_from_rows(const uint16_t *z, const float *r2, int64_t T,
                                                   static_cast<float *>(workspace), fs, stream, &why);
     if (e != cudaSuccess)
         return cuda_fail(e, why);
+    return ok();
+}
+
+}  // extern "C"
+
+namespace {
+
+constexpr int32_t kMaxChunks = 16;
+constexpr size_t kChunkCounterBytes = 256;     // one chunk's tile counter
+// The automatic count: at most 4 chunks of 12 rounds of tiles or more each.
+// Each chunk adds a partly idle last round and a start, which the overlap of
+// the norms pays for only on long chunks (measured on one GB300: workload 5,
+// 54 rounds, 4 chunks 2.8 % faster than one; workload 4, 34 rounds, 2
+// chunks 1.7 % faster, 4 chunks 2 % slower).
+constexpr int32_t kAutoChunks = 4;
+constexpr int64_t kAutoChunkRounds = 12;
+
+// The first chunk's norms run alone (nothing to overlap them with), so the
+// first chunk is about 1 / kFirstChunkDiv of the others' size (measured at
+// workload 5: a half 1.9-3 % faster than equal chunks; a third, a quarter
+// or a sixth no better than a half).
+constexpr int64_t kFirstChunkDiv = 2;
+// Chunk sizes snapped to whole rounds of tiles (measured: workload 5 1.4 %,
+// workload 4 1.8 % faster than unsnapped halves).
+constexpr bool kSnapRounds = true;
+
+// Row chunks of rc_context_kv_chunked: chunk c holds rows [row0[c],
+// row0[c + 1]), each boundary a multiple of 256.  More than one chunk only
+// where every chunk's projection runs as persistent CTA pairs that need no
+// workspace but their tile counter (no split-K partials, no tail launch);
+// with the automatic count (requested <= 0) only where every chunk after the
+// first also has eight rounds of tiles or more (dynamic tile order).
+struct RowChunks {
+    int32_t count;
+    int64_t row0[kMaxChunks + 1];
+};
+
+RowChunks plan_row_chunks(int32_t L, int64_t T, int32_t D, int32_t N, int sms, int32_t requested)
+{
+    int32_t most = std::min(requested, kMaxChunks);
+    if (requested <= 0) {
+        const int64_t pairs = std::max(1, sms / 2);
+        const int64_t tiles = (int64_t)L * ((T + 255) / 256) * (N / 256);
+        most = (int32_t)std::min<int64_t>(kAutoChunks, tiles / (kAutoChunkRounds * pairs));
+    }
+    auto fits = [&](int64_t rows, bool need_dyn) {
+        const rc::ProjectPlan p = rc::plan_kv_project(L, rows, D, N, sms, kChunkCounterBytes);
+        return p.pair && p.splits == 1 && p.tail_tiles == 0 && (!need_dyn || p.tile_ctr_offset >= 0);
+    };
+    // A chunk of b 256-row blocks has L * b * (N / 256) tiles; with b a
+    // multiple of q its last round is full (no pair idle while the chunk
+    // ends).  A chunk size snaps to the nearest multiple of q within a
+    // quarter of it.
+    const int64_t pairs = std::max(1, sms / 2);
+    const int64_t per_block = (int64_t)L * (N / 256);
+    const int64_t q = pairs / std::gcd(pairs, per_block);
+    const int64_t blocks = (T + 255) / 256;
+    auto snap = [&](int64_t b) {
+        const int64_t m = std::max<int64_t>(q, (b + q / 2) / q * q);
+        return kSnapRounds && 4 * (m > b ? m - b : b - m) <= b ? m : b;
+    };
+    RowChunks out{};
+    for (int32_t n = most; n >= 2; --n) {
+        // n - 1 chunks of `per` blocks after a first chunk of per / div blocks
+        const int64_t per = (blocks * kFirstChunkDiv + (n - 1) * kFirstChunkDiv) /
+                            ((n - 1) * kFirstChunkDiv + 1);
+        int32_t count = 0;
+        int64_t b0 = 0;
+        out.row0[0] = 0;
+        while (b0 < blocks && count < kMaxChunks) {
+            int64_t b = snap(count == 0 ? std::max<int64_t>(1, per / kFirstChunkDiv) : per);
+            if (count == n - 1 || b0 + b >= blocks)
+                b = blocks - b0;                     // the last chunk takes the rest
+            b0 += b;
+            out.row0[++count] = std::min(T, b0 * 256);
+        }
+        bool ok = count >= 2 && b0 >= blocks;
+        for (int32_t c = 0; ok && c < count; ++c)
+            ok = fits(out.row0[c + 1] - out.row0[c], requested <= 0 && c > 0);
+        if (ok) {
+            out.count = count;
+            return out;
+        }
+    }
+    out.count = 1;
+    out.row0[0] = 0;
+    out.row0[1] = T;
+    return out;
+}
+
+rc_status chunked_sizes(const char *fn, int32_t L, int64_t T, int32_t D, int32_t H) {
+    if (D != rc::kHidden)
+        return fail(RC_ERR_UNSUPPORTED, "%s: D=%d, the row norm takes D=8192", fn, D);
+    if (!supported_heads(H))
+        return fail(RC_ERR_UNSUPPORTED, "%s: H=%d is not a power of two <= 32", fn, H);
+    if (L < 1 || L > rc::kMaxFusedLayers)
+        return fail(RC_ERR_UNSUPPORTED, "%s: L=%d outside [1, %d]", fn, L, rc::kMaxFusedLayers);
+    return check_project_sizes(L, T, D, 2 * H * rc::kHeadDim);
+}
+
+// Workspace of rc_context_kv_chunked: the normed rows, then one tile counter
+// per chunk (several chunks) or the projection's workspace (one chunk).
+size_t chunked_workspace(int32_t L, int64_t T, int32_t D, int32_t N, int sms, const RowChunks &rcn) {
+    const size_t normed = round256((size_t)L * T * D * 2);
+    if (rcn.count > 1)
+        return normed + kChunkCounterBytes * rcn.count;
+    return normed + rc::plan_kv_project(L, T, D, N, sms, SIZE_MAX).workspace;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t rc_context_kv_chunks(int32_t L, int64_t T, int32_t D, int32_t H, int32_t chunks,
+                             int32_t num_sms, int64_t *row0)
+{
+    if (chunked_sizes("rc_context_kv_chunks", L, T, D, H) != RC_OK || T == 0 || num_sms < 2)
+        return 0;
+    const RowChunks rcn = plan_row_chunks(L, T, D, 2 * H * rc::kHeadDim, num_sms, chunks);
+    if (row0)
+        for (int32_t c = 0; c <= rcn.count; ++c)
+            row0[c] = rcn.row0[c];
+    return rcn.count;
+}
+
+size_t rc_context_kv_chunked_workspace_size(int32_t L, int64_t T, int32_t D, int32_t H,
+                                            int32_t chunks)
+{
+    if (chunked_sizes("rc_context_kv_chunked_workspace_size", L, T, D, H) != RC_OK || T == 0)
+        return 0;
+    const int sms = num_sms_current();
+    if (sms <= 0)
+        return 0;
+    const int32_t N = 2 * H * rc::kHeadDim;
+    return chunked_workspace(L, T, D, N, sms, plan_row_chunks(L, T, D, N, sms, chunks));
+}
+
+rc_status rc_context_kv_chunked(const uint16_t *x, int64_t T, int32_t D, const uint16_t *hidden_w,
+                                const uint16_t *pre_w, int32_t L, float eps, const uint16_t *W,
+                                int32_t w_layout, int32_t H, const int64_t *positions,
+                                const int64_t *const *slots, const uint16_t *cos_sin,
+                                int64_t max_position, uint16_t *const *caches, int32_t num_blocks,
+                                int32_t block_size, int64_t rows, int32_t *err, int32_t chunks,
+                                void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    const char *fn = "rc_context_kv_chunked";
+    rc_status st = chunked_sizes(fn, L, T, D, H);
+    if (st != RC_OK)
+        return st;
+    const int32_t N = 2 * H * rc::kHeadDim;
+    if (w_layout != RC_W_KN && w_layout != RC_W_NK)
+        return fail(RC_ERR_INVALID_ARG, "%s: unknown weight layout %d", fn, w_layout);
+    if (!x || !W || !workspace)
+        return fail(RC_ERR_INVALID_ARG, "%s: x, W and workspace must not be NULL", fn);
+    if (!aligned(x, 16) || !aligned(W, 16) || !aligned(workspace, 256) ||
+        (hidden_w && !aligned(hidden_w, 16)) || (pre_w && !aligned(pre_w, 16)))
+        return fail(RC_ERR_INVALID_ARG,
+                    "%s: x, W and weights must be 16-byte aligned, workspace 256-byte aligned", fn);
+    rc::FusedStore fs;
+    st = fused_store_args(fn, L, T, H, positions, slots, cos_sin, max_position, caches, num_blocks,
+                          block_size, eps, rows, err, nullptr, &fs);
+    if (st != RC_OK)
+        return st;
+    if (T == 0)
+        return ok();
+    const int sms = num_sms_current();
+    if (sms <= 0)
+        return fail(RC_ERR_CUDA, "%s: no current CUDA device", fn);
+    const RowChunks rcn = plan_row_chunks(L, T, D, N, sms, chunks);
+    const size_t nbytes = round256((size_t)L * T * D * 2);
+    const size_t need = rcn.count > 1 ? nbytes + kChunkCounterBytes * rcn.count : nbytes;
+    if (workspace_bytes < need)
+        return fail(RC_ERR_INVALID_ARG, "%s: the workspace needs at least %zu bytes (%zu given)", fn,
+                    need, workspace_bytes);
+    if (overlap(workspace, workspace_bytes, x, (size_t)T * D * 2) ||
+        overlap(workspace, workspace_bytes, W, (size_t)L * D * N * 2))
+        return fail(RC_ERR_INVALID_ARG, "%s: the workspace overlaps x or W", fn);
+    char *wsb = static_cast<char *>(workspace);
+    uint16_t *normed = reinterpret_cast<uint16_t *>(wsb);
+    const bool nk = w_layout == RC_W_NK;
+    const char *why = "launch";
+    cudaError_t e;
+    if (rcn.count == 1) {
+        const rc::ProjectPlan plan = rc::plan_kv_project(L, T, D, N, sms, workspace_bytes - nbytes);
+        if (plan.splits == 1 && !plan.pair)
+            return fail(RC_ERR_UNSUPPORTED,
+                        "%s: at these sizes the store reads the projection from kv_out; use "
+                        "rc_context_norms and rc_kv_project_store", fn);
+        e = rc::launch_context_norms(x, T, hidden_w, pre_w, L, eps, eps, normed, stream);
+        if (e == cudaSuccess)
+            e = rc::launch_kv_project_store(normed, W, nk, L, T, D, N, plan,
+                                            reinterpret_cast<float *>(wsb + nbytes), fs, stream, &why);
+        if (e != cudaSuccess)
+            return cuda_fail(e, why);
+        return ok();
+    }
+    // Chunk c's norms run beside chunk c - 1's projection: launched right
+    // behind it (PDL), they take the registers its persistent CTAs leave on
+    // each SM.  Rows of different chunks share no buffer, so only the
+    // projection of a chunk waits for that chunk's norms; the counters of
+    // all chunks are zeroed first, so no memset separates the kernels.
+    char *ctrs = wsb + nbytes;
+    e = cudaMemsetAsync(ctrs, 0, kChunkCounterBytes * rcn.count, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "tile counter memset");
+    for (int32_t c = 0; c < rcn.count; ++c) {
+        const int64_t r0 = rcn.row0[c];
+        const int64_t tc = rcn.row0[c + 1] - r0;
+        uint16_t *normed_c = normed + (size_t)L * r0 * D;     // [L, tc, D]
+        e = rc::launch_context_norms(x + r0 * D, tc, hidden_w, pre_w, L, eps, eps, normed_c, stream,
+                                     c > 0);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "norms launch");
+        rc::FusedStore fc = fs;
+        if (fs.positions)
+            fc.positions = fs.positions + r0;
+        for (int32_t l = 0; l < L; ++l) {
+            if (fs.slots[l])
+                fc.slots[l] = fs.slots[l] + r0;
+            fc.rows[l] = (int32_t)std::min<int64_t>(std::max<int64_t>(fs.rows[l] - r0, 0), tc);
+        }
+        rc::ProjectPlan plan = rc::plan_kv_project(L, tc, D, N, sms, kChunkCounterBytes);
+        plan.ctr_zeroed = true;
+        e = rc::launch_kv_project_store(normed_c, W, nk, L, tc, D, N, plan,
+                                        reinterpret_cast<float *>(ctrs + kChunkCounterBytes * c), fc,
+                                        stream, &why);
+        if (e != cudaSuccess)
+            return cuda_fail(e, why);
+    }
     return ok();
 }
 

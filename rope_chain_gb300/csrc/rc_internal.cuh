@@ -239,11 +239,14 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
 
 // ------------------------------------------------------------- launches
 
-// Norms: grid of T CTAs x 256 threads; returns the launch error.  bf16
-// output-scale weights (or none), gain center 0.
+// Norms: grid of T CTAs x 256 threads (T / 2 with two rows per CTA);
+// returns the launch error.  bf16 output-scale weights (or none), gain
+// center 0.  `early`: the kernel does not wait for the kernel before it in
+// the stream (the caller guarantees that kernel neither reads out nor writes
+// x or the weights), and its last CTA waits for it before exiting.
 cudaError_t launch_context_norms(const uint16_t *x, int64_t T, const uint16_t *hidden_w,
                                  const uint16_t *pre_w, int32_t L, float hidden_eps, float pre_eps,
-                                 uint16_t *out, cudaStream_t stream);
+                                 uint16_t *out, cudaStream_t stream, bool early = false);
 
 // One norm of the variant kernel: weight NULL (weightless), bf16 or FP32
 // ([8192] hidden, [L, 8192] layers), whether it scales the input, its gain
@@ -327,6 +330,9 @@ struct ProjectPlan {
     // a fixed sequence.
     int64_t tile_ctr_offset;
     size_t workspace;      // bytes used: FP32 partials (split-K or the tail's), then the counter
+    // The caller zeroed the tile counter earlier in the stream (no memset
+    // between the kernel before and the projection).
+    bool ctr_zeroed;
 };
 
 // Choose tile width and split count for the device's SM count.  Without

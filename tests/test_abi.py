@@ -293,3 +293,45 @@ def test_project_plan_describes_the_workloads():
         rc.project_plan(1, 64, 8192, 100, 152, 0)
     with pytest.raises(rc.RopeChainError):
         rc.project_plan(1, 64, 8192, 1024, 0, 0)
+
+
+def test_chunked_chain_row_chunks():
+    """rc_context_kv_chunks, host-only: the automatic choice gives each chunk
+    after the first 12 rounds of tiles or more on 152 SMs (76 CTA pairs), at
+    most 4 chunks, the first chunk about half the others (its norms run
+    alone), and chunk sizes snapped to whole rounds of tiles (workload 5:
+    8, 16, 16 and 13.9 rounds; workload 4: 2 chunks; workloads 1-3 one).
+    Every boundary is a multiple of 256 rows, an explicit request is met
+    down to chunks of one 256-row block, and every chunk's plan is persistent
+    CTA pairs without workspace."""
+    from rope_chain_gb300 import _build
+    _build.build()
+    import workloads
+    want = {1: [0, 64], 2: [0, 512], 3: [0, 4096], 4: [0, 4864, 16384],
+            5: [0, 4864, 14592, 24320, 32768]}
+    for i, w in workloads.WORKLOADS.items():
+        assert rc.context_kv_chunk_rows(w.L, w.T, w.H, 152) == want[i], i
+        assert rc.context_kv_chunks(w.L, w.T, w.H, 152, 0) == len(want[i]) - 1
+        assert rc.context_kv_chunks(w.L, w.T, w.H, 152, 1) == 1
+        b = want[i]
+        for c in range(1, len(b) - 1):          # the automatic chunks after the first
+            rows = b[c + 1] - b[c]
+            p = rc.project_plan(w.L, rows, w.D, w.N, 152, 256)
+            assert p["dynamic_tiles"], (i, c)
+    w5 = workloads.WORKLOADS[5]
+    for n in (2, 3, 6, 8, 16):
+        b = rc.context_kv_chunk_rows(w5.L, w5.T, w5.H, 152, n)
+        assert 2 <= len(b) - 1 <= n and b[0] == 0 and b[-1] == w5.T
+        assert all(r % 256 == 0 for r in b[:-1]) and all(x < y for x, y in zip(b, b[1:]))
+        for x, y in zip(b, b[1:]):
+            p = rc.project_plan(w5.L, y - x, w5.D, w5.N, 152, 256)
+            assert p["kernel"] == "persistent CTA pairs" and p["splits"] == 1 and p["tail_splits"] == 0
+            assert p["workspace_bytes"] <= 256
+    assert rc.context_kv_chunks(3, 512, 8, 152, 4) == 2          # 256-row chunks at most
+    assert rc.context_kv_chunks(2, 300, 1, 152, 4) == 1          # N = 128: no CTA pairs
+    assert rc.context_kv_chunks(2, 256, 8, 152, 4) == 1          # one tile row: nothing to split
+    assert rc.context_kv_chunks(2, 0, 8, 152, 4) == 0            # empty
+    assert rc.context_kv_chunk_rows(2, 1024, 8, 152, 100) == [0, 256, 512, 768, 1024]
+    assert rc.context_kv_chunks(2, 1024, 6, 152, 2) == 0         # H not a power of two
+    assert rc.context_kv_chunks(2, 1024, 8, 1, 2) == 0           # no SMs to plan for
+    assert rc.context_kv_chunks(65, 1024, 8, 152, 2) == 0        # more layers than a call stores

@@ -121,6 +121,10 @@ def test_traffic_figures_expire_with_their_sources(tmp_path, monkeypatch):
     dst = tmp_path / "rope_chain_gb300" / "csrc"
     shutil.copytree(src, dst)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    # the stored figures as if taken on the sources of this tree
+    fresh = {k: (v[0], bench.source_digest(bench.CALL_SOURCES[k[2]]), v[2])
+             for k, v in bench.NCU_TRAFFIC.items()}
+    monkeypatch.setattr(bench, "NCU_TRAFFIC", fresh)
     keys = list(bench.NCU_TRAFFIC)
     assert keys and all(bench.ncu_traffic(k)[0] is not None for k in keys)
     with open(dst / "k2_gemm.cu", "a") as f:
