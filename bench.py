@@ -49,27 +49,28 @@ CALL_SOURCES = {
     "k4_qkv_front": ("k4_qkv_front.cu", "rc_tcgen05.cuh") + _SHARED_SOURCES,
 }
 NCU_TRAFFIC = {
-    # rc_kv_project_store at workload 5: one k2_project_pair_persistent
-    # launch (dynamic tile order): 4,774,993,664 B read + 528,049,152 B
-    # written (profiles/k2_pair_persistent_workload5.md)
-    (5, "store", "project_store"): (5_303_042_816, "36ceca48e1f66057",
+    # rc_kv_project_store at workload 5 over all rows (the breakdown's call,
+    # the one the roofline times): one k2_project_pair_persistent launch
+    # (dynamic tile order), 5,151,410,688 B read + 528,989,184 B written
+    # (profiles/k2_pair_persistent_workload5.md)
+    (5, "store", "project_store"): (5_680_399_872, "805b059bd2b249bd",
                                     "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, "
                                     "one launch at full size (one pass)"),
     # rc_context_norms at workload 5: one k1_context_norms2 launch,
-    # 537,246,976 B read + 4,245,162,240 B written
-    (5, "unfused", "norms"): (4_782_409_216, "b22eb1f75ec280f1",
+    # 537,242,112 B read + 4,232,972,032 B written
+    (5, "unfused", "norms"): (4_770_214_144, "c001eb57c7a754da",
                               "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, "
                               "one launch at full size (one pass)"),
     # rc_kv_store at workload 5: one k3_kv_store_heads launch (8 layers),
-    # 574,434,304 B read + 483,296,000 B written
-    (5, "unfused", "store"): (1_057_730_304, "af574945006ccd2a",
+    # 574,430,976 B read + 482,549,760 B written
+    (5, "unfused", "store"): (1_056_980_736, "5f93bb8ca1dd192b",
                               "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, "
                               "one launch at full size (one pass)"),
-    # rc_kv_project_store at workload 2: k2_project_pair (52,292,352 B read,
-    # 19,631,360 B written) then k3_reduce_store (81,408 B read, 1,568,768 B
+    # rc_kv_project_store at workload 2: k2_project_pair (52,663,040 B read,
+    # 18,846,208 B written) then k3_reduce_store (82,944 B read, 1,635,072 B
     # written), captured in sequence without ncu's cache flush between them
     # (the split-K partials are read back from L2, as in the step)
-    (2, "store", "project_store"): (73_573_888, "36ceca48e1f66057",
+    (2, "store", "project_store"): (73_227_264, "805b059bd2b249bd",
                                     "ncu --cache-control none --metrics dram__bytes_read.sum,"
                                     "dram__bytes_write.sum, the call's two launches in sequence"),
 }
