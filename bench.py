@@ -618,7 +618,16 @@ def run_ours(args, w):
     # copy engines into device buffers ("copy") or by the norms kernel
     # reading host memory in place ("inplace").  One range: the norms read x
     # in place (the read overlaps the norms' own work).
-    chunks = row_chunks(w.T, args.e2e_chunks) if args.path == "store" else [(0, w.T)]
+    # With the chunked call, x in host memory is chunked by the call itself
+    # (a plan of its own for x read over the host link): one call whose
+    # chunks' norms read their rows of x in place beside the previous
+    # chunk's projection, unless the ranges are asked for.
+    host_chunks = (rc.context_kv_chunks(w.L, w.T, w.H, sms, args.chunks, x_on_host=True)
+                   if chunked else 1)
+    if args.path == "store" and not (host_chunks > 1 and args.e2e_chunks == 0):
+        chunks = row_chunks(w.T, args.e2e_chunks)
+    else:
+        chunks = [(0, w.T)]
     e2e_mode = ("copy" if args.e2e_mode == "auto" else args.e2e_mode) if len(chunks) > 1 else "inplace"
     overlapped = OverlappedChain(w.L, w.T, w.D, w.N, chunks, dev, e2e_mode) if len(chunks) > 1 else None
 
@@ -760,7 +769,11 @@ def run_ours(args, w):
                 "outputs": "the K/V result stays in the device caches (the operation's "
                            "output); only the 4-byte skip count is copied back per step",
                 "row_ranges": len(chunks),
-                "overlap": ("none" if overlapped is None else
+                "row_chunks": host_chunks if overlapped is None else 1,
+                "overlap": (f"{host_chunks} row chunks in one call: the norms of chunk c + 1 read "
+                            "their rows of x over the host link while chunk c is projected and "
+                            "stored" if overlapped is None and host_chunks > 1 else
+                            "none" if overlapped is None else
                             f"{len(chunks)} row ranges: the copy of range c + 1 runs while "
                             "range c goes through the chain" if e2e_mode == "copy" else
                             f"{len(chunks)} row ranges: the norms of range c + 1 read x "

@@ -199,8 +199,9 @@ size_t rc_kv_project_workspace_size_sms(int32_t L, int64_t T, int32_t D, int32_t
                      from a counter in the workspace (so pairs that share rows
                      of `normed` stay in step), 0 for a fixed tile sequence
      workspace_bytes the part of the workspace used
-   RC_ERR_INVALID_ARG / RC_ERR_UNSUPPORTED for sizes rc_kv_project refuses
-   or num_sms < 1; *plan untouched then. */
+   T = 0 launches nothing: the plan reads single CTAs, 1 split, no
+   workspace.  RC_ERR_INVALID_ARG / RC_ERR_UNSUPPORTED for sizes
+   rc_kv_project refuses or num_sms < 1; *plan untouched then. */
 typedef struct {
     int32_t kernel;
     int32_t splits;
@@ -387,15 +388,17 @@ size_t rc_context_kv_workspace_size(int32_t L, int64_t T, int32_t D, int32_t H);
  *                                      L <= 64)
  *   W, w_layout, H                     as rc_kv_project (N = 128*H)
  *   positions ... err                  as rc_kv_project_store (no kv_out)
- *   chunks      row chunks wanted (<= 0: chosen for the sizes); fewer are
- *               used where a chunk's projection would not run as
- *               persistent CTA pairs without workspace (rc_context_kv_chunks
- *               says how many)
+ *   chunks      row chunks wanted (<= 0: chosen for the sizes and for where
+ *               x lives); fewer are used where a chunk's projection would
+ *               not run as persistent CTA pairs without workspace
+ *               (rc_context_kv_chunks says how many); x may be page-locked
+ *               host memory (its device address, rc_device_address), which
+ *               the norms of each chunk read over the host link
  *   workspace   device scratch, 256-byte aligned, required, not
  *               overlapping x or W: the normed rows [L, T, D] (chunk by
  *               chunk), then a 256-byte tile counter per chunk (or, with one
  *               chunk, the projection's workspace);
- *               rc_context_kv_chunked_workspace_size() gives the bytes
+ *               rc_context_kv_chunked_workspace_size() gives enough bytes
  * The call ends with the last chunk's projection, which starts after every
  * earlier kernel of the call has completed; a later kernel or copy in the
  * stream sees all of the call's writes.  Errors as rc_kv_project_store; in
@@ -412,17 +415,20 @@ rc_status rc_context_kv_chunked(const uint16_t *x, int64_t T, int32_t D,
                                 int32_t *err, int32_t chunks, void *workspace,
                                 size_t workspace_bytes, cudaStream_t stream);
 
-/* Workspace bytes of rc_context_kv_chunked for these sizes and chunk request
-   on the current device (0 for unsupported sizes). */
+/* Workspace bytes of rc_context_kv_chunked for these sizes on the current
+   device, enough for any chunk request and for x in device or host memory
+   (0 for unsupported sizes; `chunks` is accepted for symmetry). */
 size_t rc_context_kv_chunked_workspace_size(int32_t L, int64_t T, int32_t D, int32_t H,
                                             int32_t chunks);
 
 /* Host only: the number of row chunks rc_context_kv_chunked uses for these
-   sizes and chunk request on a GPU of num_sms SMs (0 for unsupported
-   sizes).  row0, when not NULL, receives the chunks' first rows and T
+   sizes and chunk request on a GPU of num_sms SMs, with x in device memory
+   (x_on_host = 0) or page-locked host memory read over the host link
+   (x_on_host != 0; the call tells the two apart itself); 0 for unsupported
+   sizes.  row0, when not NULL, receives the chunks' first rows and T
    (count + 1 entries; room for 17). */
 int32_t rc_context_kv_chunks(int32_t L, int64_t T, int32_t D, int32_t H, int32_t chunks,
-                             int32_t num_sms, int64_t *row0);
+                             int32_t x_on_host, int32_t num_sms, int64_t *row0);
 
 /*
  * rc_context_kv in two calls.  rc_context_rows is the row pass: per row t,

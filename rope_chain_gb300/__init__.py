@@ -111,7 +111,7 @@ SIGNATURES["rc_context_kv_chunked"] = ([_vp, _c.c_int64, _c.c_int32, _vp, _vp, _
 SIGNATURES["rc_context_kv_chunked_workspace_size"] = ([_c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32,
                                                        _c.c_int32], _c.c_size_t)
 SIGNATURES["rc_context_kv_chunks"] = ([_c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32, _c.c_int32,
-                                       _c.c_int32, _c.POINTER(_c.c_int64)], _c.c_int32)
+                                       _c.c_int32, _c.c_int32, _c.POINTER(_c.c_int64)], _c.c_int32)
 
 
 def lib():
@@ -506,17 +506,18 @@ def context_kv(x: torch.Tensor, hidden_w, pre_w, W: torch.Tensor, H: int, positi
                                workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
-def context_kv_chunks(L: int, T: int, H: int, num_sms: int, chunks: int = 0, D: int = 8192) -> int:
+def context_kv_chunks(L: int, T: int, H: int, num_sms: int, chunks: int = 0, D: int = 8192,
+                      x_on_host: bool = False) -> int:
     """Row chunks rc_context_kv_chunked uses for these sizes (host only)."""
-    return int(lib().rc_context_kv_chunks(L, T, D, H, chunks, num_sms, None))
+    return int(lib().rc_context_kv_chunks(L, T, D, H, chunks, int(x_on_host), num_sms, None))
 
 
 def context_kv_chunk_rows(L: int, T: int, H: int, num_sms: int, chunks: int = 0,
-                          D: int = 8192) -> list:
+                          D: int = 8192, x_on_host: bool = False) -> list:
     """The first row of each chunk rc_context_kv_chunked uses, then T (host
     only; [] for unsupported sizes)."""
     row0 = (_c.c_int64 * 17)()
-    n = int(lib().rc_context_kv_chunks(L, T, D, H, chunks, num_sms, row0))
+    n = int(lib().rc_context_kv_chunks(L, T, D, H, chunks, int(x_on_host), num_sms, row0))
     return [int(row0[i]) for i in range(n + 1)] if n else []
 
 

@@ -1423,6 +1423,14 @@ ProjectPlan plan_kv_project(int32_t L, int64_t T, int32_t D, int32_t N, int num_
                             size_t workspace_bytes, bool allow_tail)
 {
     ProjectPlan p{};
+    p.tile_ctr_offset = -1;
+    if (T <= 0 || L <= 0 || D < BK || N < 128 || num_sms < 1) {
+        // nothing to launch: single CTAs without splits, no workspace
+        p.bn = 128;
+        p.splits = p.tail_splits = 1;
+        p.kb_per_split = p.tail_kb_per_split = std::max(1, D / BK);
+        return p;
+    }
     // 256-wide N tiles where there are rows to fill them; with one 128-row
     // block (T <= 128) the projection streams W at too few bytes of work per
     // byte to be tensor-bound, so 128-wide tiles put twice the CTAs (SMs) on

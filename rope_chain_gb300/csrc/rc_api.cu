@@ -702,6 +702,14 @@ constexpr size_t kChunkCounterBytes = 256;     // one chunk's tile counter
 // chunks 1.7 % faster, 4 chunks 2 % slower).
 constexpr int32_t kAutoChunks = 4;
 constexpr int64_t kAutoChunkRounds = 12;
+// With x in host memory the norms of a chunk wait for its rows to cross the
+// host link: the count is chosen by the score in plan_row_chunks, in which a
+// 256-row block of the first chunk costs as much as kHostBlockRounds idle
+// rounds of tiles (fitted on GB300 to eight end-to-end steps, workloads 4
+// and 5 at 2-12 chunks: the first chunk's rows cross the link at about
+// 0.06 us a row, an idle round costs about 59 us).  An explicit request
+// gets equal-sized chunks.
+constexpr double kHostBlockRounds = 0.26;
 
 // The first chunk's norms run alone (nothing to overlap them with), so the
 // first chunk is about 1 / kFirstChunkDiv of the others' size (measured at
@@ -723,14 +731,21 @@ struct RowChunks {
     int64_t row0[kMaxChunks + 1];
 };
 
-RowChunks plan_row_chunks(int32_t L, int64_t T, int32_t D, int32_t N, int sms, int32_t requested)
+RowChunks plan_row_chunks(int32_t L, int64_t T, int32_t D, int32_t N, int sms, int32_t requested,
+                          bool x_on_host)
 {
+    const int64_t pairs = std::max(1, sms / 2);
+    const int64_t blocks = (T + 255) / 256;
     int32_t most = std::min(requested, kMaxChunks);
     if (requested <= 0) {
-        const int64_t pairs = std::max(1, sms / 2);
-        const int64_t tiles = (int64_t)L * ((T + 255) / 256) * (N / 256);
+        const int64_t tiles = (int64_t)L * blocks * (N / 256);
         most = (int32_t)std::min<int64_t>(kAutoChunks, tiles / (kAutoChunkRounds * pairs));
     }
+    // x read over the host link: a chunk's norms take about as long as the
+    // projection of an equal chunk, so the first chunk is not made smaller
+    // (nor snapped larger), and chunks need not be long enough for the
+    // dynamic tile order
+    const int64_t div = x_on_host ? 1 : kFirstChunkDiv;
     auto fits = [&](int64_t rows, bool need_dyn) {
         const rc::ProjectPlan p = rc::plan_kv_project(L, rows, D, N, sms, kChunkCounterBytes);
         return p.pair && p.splits == 1 && p.tail_tiles == 0 && (!need_dyn || p.tile_ctr_offset >= 0);
@@ -739,24 +754,69 @@ RowChunks plan_row_chunks(int32_t L, int64_t T, int32_t D, int32_t N, int sms, i
     // multiple of q its last round is full (no pair idle while the chunk
     // ends).  A chunk size snaps to the nearest multiple of q within a
     // quarter of it.
-    const int64_t pairs = std::max(1, sms / 2);
-    const int64_t per_block = (int64_t)L * (N / 256);
-    const int64_t q = pairs / std::gcd(pairs, per_block);
-    const int64_t blocks = (T + 255) / 256;
+    const int64_t q = pairs / std::gcd(pairs, (int64_t)L * (N / 256));
     auto snap = [&](int64_t b) {
         const int64_t m = std::max<int64_t>(q, (b + q / 2) / q * q);
         return kSnapRounds && 4 * (m > b ? m - b : b - m) <= b ? m : b;
     };
     RowChunks out{};
-    for (int32_t n = most; n >= 2; --n) {
-        // n - 1 chunks of `per` blocks after a first chunk of per / div blocks
-        const int64_t per = (blocks * kFirstChunkDiv + (n - 1) * kFirstChunkDiv) /
-                            ((n - 1) * kFirstChunkDiv + 1);
+    if (x_on_host && requested <= 0 && blocks >= 2) {
+        // x over the host link: equal chunks, their count chosen to spend the
+        // least on the first chunk, whose rows cross the link with nothing
+        // to overlap them (kHostBlockRounds rounds of tiles per 256-row
+        // block), plus the partly idle last round of every chunk's
+        // projection
+        // one chunk: every row crosses the link before its projection, which
+        // then runs with split-K partials (no idle round) or as persistent
+        // pairs (the idle part of its last round)
+        const rc::ProjectPlan whole = rc::plan_kv_project(L, T, D, N, sms, SIZE_MAX);
+        const int64_t whole_tiles = (int64_t)L * blocks * (N / 256);
+        double best = kHostBlockRounds * (double)blocks +
+                      (whole.splits > 1 || !whole.pair ? 0.0
+                       : (double)((whole_tiles + pairs - 1) / pairs) - (double)whole_tiles / (double)pairs);
+        for (int32_t n = 2; n <= kMaxChunks && n <= blocks; ++n) {
+            const int64_t even = (blocks + n - 1) / n;
+            RowChunks cand{};
+            int32_t count = 0;
+            int64_t b0 = 0;
+            double score = kHostBlockRounds * (double)even;
+            bool ok = true;
+            while (b0 < blocks && ok) {
+                const int64_t b = std::min(even, blocks - b0);
+                const int64_t tiles = (int64_t)L * b * (N / 256);
+                score += (double)((tiles + pairs - 1) / pairs) - (double)tiles / (double)pairs;
+                ok = fits(std::min(T, (b0 + b) * 256) - b0 * 256, false);
+                b0 += b;
+                cand.row0[++count] = std::min(T, b0 * 256);
+            }
+            if (ok && count >= 2 && score < best - 1e-9) {
+                cand.count = count;
+                out = cand;
+                best = score;
+            }
+        }
+        if (out.count >= 2)
+            return out;
+        out = RowChunks{};
+    }
+    for (int32_t n = blocks >= 2 ? most : 1; n >= 2; --n) {
+        // a first chunk of about per / div blocks, then n - 1 chunks sharing
+        // the rest; the snapped size only where it leaves the last chunk
+        // between half and one and a half of the others
+        const int64_t per = (blocks * div + (n - 1) * div) / ((n - 1) * div + 1);
+        const int64_t first0 = std::max<int64_t>(1, per / div);
+        const int64_t first = std::min(blocks - 1, x_on_host ? first0 : snap(first0));
+        const int64_t rest = blocks - first;
+        const int64_t even = (rest + n - 2) / (n - 1);
+        int64_t mid = snap(even);
+        const int64_t last_snapped = rest - (int64_t)(n - 2) * mid;
+        if (mid != even && !(2 * last_snapped >= mid && 2 * last_snapped <= 3 * mid))
+            mid = even;
         int32_t count = 0;
         int64_t b0 = 0;
         out.row0[0] = 0;
         while (b0 < blocks && count < kMaxChunks) {
-            int64_t b = snap(count == 0 ? std::max<int64_t>(1, per / kFirstChunkDiv) : per);
+            int64_t b = std::max<int64_t>(1, count == 0 ? first : mid);
             if (count == n - 1 || b0 + b >= blocks)
                 b = blocks - b0;                     // the last chunk takes the rest
             b0 += b;
@@ -764,7 +824,7 @@ RowChunks plan_row_chunks(int32_t L, int64_t T, int32_t D, int32_t N, int sms, i
         }
         bool ok = count >= 2 && b0 >= blocks;
         for (int32_t c = 0; ok && c < count; ++c)
-            ok = fits(out.row0[c + 1] - out.row0[c], requested <= 0 && c > 0);
+            ok = fits(out.row0[c + 1] - out.row0[c], requested <= 0 && !x_on_host && c > 0);
         if (ok) {
             out.count = count;
             return out;
@@ -786,13 +846,25 @@ rc_status chunked_sizes(const char *fn, int32_t L, int64_t T, int32_t D, int32_t
     return check_project_sizes(L, T, D, 2 * H * rc::kHeadDim);
 }
 
-// Workspace of rc_context_kv_chunked: the normed rows, then one tile counter
-// per chunk (several chunks) or the projection's workspace (one chunk).
-size_t chunked_workspace(int32_t L, int64_t T, int32_t D, int32_t N, int sms, const RowChunks &rcn) {
+// Workspace of rc_context_kv_chunked: the normed rows, then room for a tile
+// counter per chunk (the most chunks a call makes) or the projection's
+// workspace (one chunk), whichever is larger: the same for x in device or
+// host memory.
+size_t chunked_workspace(int32_t L, int64_t T, int32_t D, int32_t N, int sms) {
     const size_t normed = round256((size_t)L * T * D * 2);
-    if (rcn.count > 1)
-        return normed + kChunkCounterBytes * rcn.count;
-    return normed + rc::plan_kv_project(L, T, D, N, sms, SIZE_MAX).workspace;
+    return normed + std::max(kChunkCounterBytes * kMaxChunks,
+                             rc::plan_kv_project(L, T, D, N, sms, SIZE_MAX).workspace);
+}
+
+// Whether x is page-locked host memory (read by the norms over the host
+// link).
+bool on_host(const void *x) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, x) != cudaSuccess) {
+        cudaGetLastError();                       // not sticky: clear it
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost;
 }
 
 }  // namespace
@@ -800,11 +872,12 @@ size_t chunked_workspace(int32_t L, int64_t T, int32_t D, int32_t N, int sms, co
 extern "C" {
 
 int32_t rc_context_kv_chunks(int32_t L, int64_t T, int32_t D, int32_t H, int32_t chunks,
-                             int32_t num_sms, int64_t *row0)
+                             int32_t x_on_host, int32_t num_sms, int64_t *row0)
 {
     if (chunked_sizes("rc_context_kv_chunks", L, T, D, H) != RC_OK || T == 0 || num_sms < 2)
         return 0;
-    const RowChunks rcn = plan_row_chunks(L, T, D, 2 * H * rc::kHeadDim, num_sms, chunks);
+    const RowChunks rcn =
+        plan_row_chunks(L, T, D, 2 * H * rc::kHeadDim, num_sms, chunks, x_on_host != 0);
     if (row0)
         for (int32_t c = 0; c <= rcn.count; ++c)
             row0[c] = rcn.row0[c];
@@ -819,8 +892,8 @@ size_t rc_context_kv_chunked_workspace_size(int32_t L, int64_t T, int32_t D, int
     const int sms = num_sms_current();
     if (sms <= 0)
         return 0;
-    const int32_t N = 2 * H * rc::kHeadDim;
-    return chunked_workspace(L, T, D, N, sms, plan_row_chunks(L, T, D, N, sms, chunks));
+    (void)chunks;                                 // every chunk plan fits the same workspace
+    return chunked_workspace(L, T, D, 2 * H * rc::kHeadDim, sms);
 }
 
 rc_status rc_context_kv_chunked(const uint16_t *x, int64_t T, int32_t D, const uint16_t *hidden_w,
@@ -854,7 +927,7 @@ rc_status rc_context_kv_chunked(const uint16_t *x, int64_t T, int32_t D, const u
     const int sms = num_sms_current();
     if (sms <= 0)
         return fail(RC_ERR_CUDA, "%s: no current CUDA device", fn);
-    const RowChunks rcn = plan_row_chunks(L, T, D, N, sms, chunks);
+    const RowChunks rcn = plan_row_chunks(L, T, D, N, sms, chunks, on_host(x));
     const size_t nbytes = round256((size_t)L * T * D * 2);
     const size_t need = rcn.count > 1 ? nbytes + kChunkCounterBytes * rcn.count : nbytes;
     if (workspace_bytes < need)

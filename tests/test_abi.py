@@ -289,6 +289,11 @@ def test_project_plan_describes_the_workloads():
         # a workspace one byte short of the counter keeps the fixed order
         if p["dynamic_tiles"]:
             assert not rc.project_plan(w.L, w.T, w.D, w.N, 152, ws - 1)["dynamic_tiles"]
+    # T = 0 launches nothing (the planner must not divide by its zero tiles)
+    empty = rc.project_plan(2, 0, 8192, 1024, 152, 1 << 30)
+    assert empty["kernel"] == "single CTAs" and empty["splits"] == 1
+    assert empty["tail_splits"] == 0 and not empty["dynamic_tiles"] and empty["workspace_bytes"] == 0
+    assert rc.workspace_size_for(2, 0, 8192, 1024, 152) == 0
     with pytest.raises(rc.RopeChainError):
         rc.project_plan(1, 64, 8192, 100, 152, 0)
     with pytest.raises(rc.RopeChainError):
@@ -335,3 +340,13 @@ def test_chunked_chain_row_chunks():
     assert rc.context_kv_chunks(2, 1024, 6, 152, 2) == 0         # H not a power of two
     assert rc.context_kv_chunks(2, 1024, 8, 1, 2) == 0           # no SMs to plan for
     assert rc.context_kv_chunks(65, 1024, 8, 152, 2) == 0        # more layers than a call stores
+    # x in host memory: equal chunks, their count the least exposed first
+    # chunk plus idle tile rounds (workload 5: 7 chunks of 19 blocks, whole
+    # rounds; workload 4: 6; workload 3: 4 of 1024 rows; workload 2 one
+    # chunk, its split-K projection leaving no round idle)
+    host = {1: [0, 64], 2: [0, 512], 3: [0, 1024, 2048, 3072, 4096],
+            4: [0, 2816, 5632, 8448, 11264, 14080, 16384],
+            5: [4864 * i for i in range(7)] + [32768]}
+    for i, w in workloads.WORKLOADS.items():
+        assert rc.context_kv_chunk_rows(w.L, w.T, w.H, 152, x_on_host=True) == host[i], i
+    assert rc.context_kv_chunk_rows(3, 2048, 8, 152, 3, x_on_host=True) == [0, 768, 1536, 2048]

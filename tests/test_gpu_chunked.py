@@ -161,6 +161,23 @@ def test_chunked_repeated_calls_and_graph_replay():
         assert_same(dict(caches=[parity.host_bits(c) for c in caches], err=int(err.item())), ref)
 
 
+@pytest.mark.parametrize("chunks", [0, 3])
+def test_chunked_x_in_host_memory(chunks):
+    # x in page-locked host memory: each chunk's norms read their rows over
+    # the host link, and the chunk plan is the host one; the bits do not
+    # depend on the chunks
+    T, L, H = 2048, 3, 8
+    case = workloads.random_case(1822, T=T, L=L, H=H, max_position=512,
+                                 num_blocks=(T + 15) // 16 + 3, block_size=16)
+    ops = _operands(case, rc.RC_W_KN)
+    ops["x"] = ops["x"].cpu().pin_memory()
+    want = rc.context_kv_chunks(L, T, H, sms(), chunks, x_on_host=True)
+    assert want == (2 if chunks == 0 else 3)
+    got = run_chunked(case, chunks, ops=ops)
+    ref = run_reference(case) if want > 1 else run_reference(case, use_workspace=True)
+    assert_same(got, ref)
+
+
 def test_chunked_one_chunk_uses_the_full_plan():
     # too few tiles per chunk for the automatic choice: one chunk, the
     # projection's full-workspace plan (split-K here), as the default step
@@ -184,8 +201,10 @@ def test_chunked_refusals():
     call = lambda w, **kw: rc.context_kv_chunked(ops["x"], ops["hw"], ops["pw"], ops["W"], H,
                                                  ops["positions"], ops["slots"], ops["cs"], caches,
                                                  case["eps"], w, chunks=2, **kw)
+    need = (L * T * 8192 * 2 + 255) // 256 * 256 + 2 * 256     # normed rows + 2 counters
+    assert ws.numel() >= need
     with pytest.raises(rc.RopeChainError, match="workspace needs"):
-        call(ws[:ws.numel() - 256])              # no room for the second chunk's counter
+        call(ws[:need - 256])                    # no room for the second chunk's counter
     # a workspace holding x
     buf = torch.empty(ws.numel() + T * 8192 * 2, dtype=torch.uint8, device=DEV)
     xv = buf[:T * 8192 * 2].view(torch.bfloat16).view(T, 8192)
