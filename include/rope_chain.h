@@ -397,13 +397,14 @@ size_t rc_context_kv_workspace_size(int32_t L, int64_t T, int32_t D, int32_t H);
  *   workspace   device scratch, 256-byte aligned, required, not
  *               overlapping x or W: the normed rows [L, T, D] (chunk by
  *               chunk), then a 256-byte tile counter per chunk (or, with one
- *               chunk, the projection's workspace);
- *               rc_context_kv_chunked_workspace_size() gives enough bytes
+ *               chunk, the projection's workspace, or where single CTAs
+ *               project without a K split a bf16 copy of the projection
+ *               that the store reads); rc_context_kv_chunked_workspace_size()
+ *               gives enough bytes
  * The call ends with the last chunk's projection, which starts after every
  * earlier kernel of the call has completed; a later kernel or copy in the
- * stream sees all of the call's writes.  Errors as rc_kv_project_store; in
- * addition RC_ERR_UNSUPPORTED where one chunk's projection would need
- * kv_out (T <= 128 or H = 1 without split-K room in the workspace).
+ * stream sees all of the call's writes.  Errors as rc_kv_project_store
+ * (RC_ERR_INVALID_ARG for a workspace too small for the plan).
  */
 rc_status rc_context_kv_chunked(const uint16_t *x, int64_t T, int32_t D,
                                 const uint16_t *hidden_w, const uint16_t *pre_w,

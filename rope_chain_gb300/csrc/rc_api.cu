@@ -852,8 +852,10 @@ rc_status chunked_sizes(const char *fn, int32_t L, int64_t T, int32_t D, int32_t
 // host memory.
 size_t chunked_workspace(int32_t L, int64_t T, int32_t D, int32_t N, int sms) {
     const size_t normed = round256((size_t)L * T * D * 2);
-    return normed + std::max(kChunkCounterBytes * kMaxChunks,
-                             rc::plan_kv_project(L, T, D, N, sms, SIZE_MAX).workspace);
+    const rc::ProjectPlan p = rc::plan_kv_project(L, T, D, N, sms, SIZE_MAX);
+    // single CTAs without a K split store from a bf16 copy of the projection
+    const size_t kv = p.splits == 1 && !p.pair ? round256((size_t)L * T * N * 2) : 0;
+    return normed + std::max({kChunkCounterBytes * kMaxChunks, p.workspace, kv});
 }
 
 // Whether x is page-locked host memory (read by the norms over the host
@@ -942,11 +944,18 @@ rc_status rc_context_kv_chunked(const uint16_t *x, int64_t T, int32_t D, const u
     const char *why = "launch";
     cudaError_t e;
     if (rcn.count == 1) {
-        const rc::ProjectPlan plan = rc::plan_kv_project(L, T, D, N, sms, workspace_bytes - nbytes);
-        if (plan.splits == 1 && !plan.pair)
-            return fail(RC_ERR_UNSUPPORTED,
-                        "%s: at these sizes the store reads the projection from kv_out; use "
-                        "rc_context_norms and rc_kv_project_store", fn);
+        const size_t avail = workspace_bytes - nbytes;
+        const rc::ProjectPlan plan = rc::plan_kv_project(L, T, D, N, sms, avail);
+        if (plan.splits == 1 && !plan.pair) {
+            // single CTAs without a K split: the projection goes through a
+            // bf16 copy in the workspace, which the store kernel then reads
+            const size_t kvb = round256((size_t)L * T * N * 2);
+            if (avail < kvb)
+                return fail(RC_ERR_INVALID_ARG,
+                            "%s: the workspace needs at least %zu bytes (%zu given)", fn,
+                            nbytes + kvb, workspace_bytes);
+            fs.kv_out = reinterpret_cast<uint16_t *>(wsb + nbytes);
+        }
         e = rc::launch_context_norms(x, T, hidden_w, pre_w, L, eps, eps, normed, stream);
         if (e == cudaSuccess)
             e = rc::launch_kv_project_store(normed, W, nk, L, T, D, N, plan,

@@ -59,7 +59,7 @@ def run_chunked(case, chunks, *, layout=rc.RC_W_KN, rows=None, ops=None, calls=1
     return out if calls > 1 else out[0]
 
 
-def run_reference(case, *, layout=rc.RC_W_KN, rows=None, use_workspace=False):
+def run_reference(case, *, layout=rc.RC_W_KN, rows=None, use_workspace=False, kv_out=False):
     """rc_context_norms + rc_kv_project_store, the default step's two calls."""
     L = len(case["slots"])
     H = case["cache_shape"][1]
@@ -69,8 +69,9 @@ def run_reference(case, *, layout=rc.RC_W_KN, rows=None, use_workspace=False):
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     normed = rc.context_norms(ops["x"], ops["hw"], ops["pw"], L, case["eps"])
     ws = rc.new_workspace(L, T, 8192, 128 * H, DEV) if use_workspace else None
+    kv = torch.empty((L, T, 128 * H), dtype=torch.bfloat16, device=DEV) if kv_out else None
     rc.kv_project_store(normed, ops["W"], H, ops["positions"], ops["slots"], ops["cs"], caches,
-                        case["eps"], rows=rows, err=err, workspace=ws, w_layout=layout)
+                        case["eps"], rows=rows, err=err, workspace=ws, w_layout=layout, kv_out=kv)
     torch.cuda.synchronize()
     return dict(caches=[parity.host_bits(c) for c in caches], err=int(err.item()))
 
@@ -175,6 +176,21 @@ def test_chunked_x_in_host_memory(chunks):
     assert want == (2 if chunks == 0 else 3)
     got = run_chunked(case, chunks, ops=ops)
     ref = run_reference(case) if want > 1 else run_reference(case, use_workspace=True)
+    assert_same(got, ref)
+
+
+@pytest.mark.parametrize("T,L,H", [(2560, 8, 1), (100, 5, 32)])
+def test_chunked_single_ctas_without_split(T, L, H):
+    # N = 128 at 2560 rows, or 100 rows of 32 heads: single CTAs and enough
+    # tiles for no K split, so the store reads a bf16 copy of the
+    # projection, which the chunked call keeps in its workspace
+    assert rc.context_kv_chunks(L, T, H, sms(), 0) == 1
+    p = rc.project_plan(L, T, 8192, 128 * H, sms(), rc.workspace_size_for(L, T, 8192, 128 * H, sms()))
+    assert p["kernel"] == "single CTAs" and p["splits"] == 1
+    case = workloads.random_case(1833 + T, T=T, L=L, H=H, max_position=512,
+                                 num_blocks=(T + 15) // 16 + 3, block_size=16)
+    got = run_chunked(case, 0)
+    ref = run_reference(case, use_workspace=True, kv_out=True)
     assert_same(got, ref)
 
 
