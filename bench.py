@@ -430,7 +430,7 @@ def run_ours(args, w):
     ws_bytes = rc.workspace_size(w.L, w.T, w.D, w.N)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     cws = rc.context_kv_workspace(w.L, w.T, w.H, dev)   # the whole-chain call's workspace
-    chunked = args.path == "store" and args.chunks != 1
+    chunked = args.path in ("store", "variants") and args.chunks != 1
     if chunked:                                      # the chunked chain's normed rows and counters
         kws = rc.context_kv_chunked_workspace(w.L, w.T, w.H, dev, chunks=args.chunks)
     z = torch.empty((w.T, w.D), dtype=torch.bfloat16, device=dev)
@@ -452,7 +452,10 @@ def run_ours(args, w):
         launches_per_step += 2
     # the chunked chain: per row chunk the norms and one persistent
     # projection + store (a memset of the chunks' tile counters first)
-    n_chunks = rc.context_kv_chunks(w.L, w.T, w.H, sms, args.chunks) if chunked else 1
+    # (the variants' FP32 gains keep one chunk with x in device memory unless
+    # more are asked for)
+    n_chunks = (rc.context_kv_chunks(w.L, w.T, w.H, sms, args.chunks)
+                if chunked and not (args.path == "variants" and args.chunks <= 0) else 1)
     if n_chunks > 1:
         launches_per_step = 2 * n_chunks
 
@@ -487,6 +490,12 @@ def run_ours(args, w):
         if whole:
             ready()
             rc.context_kv(xs, hw, pw, W, w.H, pos, sl, cs, caches, w.eps, cws, err=err)
+        elif variants and chunked:
+            ready()
+            rc.context_kv_chunked_ex(xs, W, w.H, pos, sl, cs, caches, w.eps, kws, hidden_w=hw32,
+                                     pre_w=pw32, hidden_eps=w.eps, pre_eps=10.0 * w.eps,
+                                     pre_center=1.0, hidden_input_scale=True, rows=layer_rows,
+                                     err=err, chunks=args.chunks)
         elif variants:
             norms_variant(xs)
             ready()
@@ -739,9 +748,11 @@ def run_ours(args, w):
     rec["config"]["timing"] = timing
     rec["config"]["path"] = ("rc_context_kv (row pass; projection forming the normed rows in shared "
                              "memory, store fused)" if whole else
-                             "rc_context_norms_ex (FP32 gains, hidden gain on the input, layer "
-                             "gain centre 1, separate eps) + rc_kv_project_store_rows (per-layer "
-                             "slot lengths)" if variants else
+                             (f"rc_context_kv_chunked_ex ({n_chunks} row chunks; " if n_chunks > 1 else
+                              "rc_context_kv_chunked_ex (one chunk; " if chunked else
+                              "rc_context_norms_ex + rc_kv_project_store_rows (") +
+                             "FP32 gains, hidden gain on the input, layer gain centre 1, separate "
+                             "eps, per-layer slot lengths)" if variants else
                              f"rc_context_kv_chunked ({n_chunks} row chunks: the norms of chunk "
                              "c + 1 run beside the projection + store of chunk c)" if n_chunks > 1 else
                              "rc_context_kv_chunked (one chunk: rc_context_norms, then "

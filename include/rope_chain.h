@@ -416,6 +416,40 @@ rc_status rc_context_kv_chunked(const uint16_t *x, int64_t T, int32_t D,
                                 int32_t *err, int32_t chunks, void *workspace,
                                 size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * rc_context_kv_chunked_ex -- rc_context_kv_chunked with every norm option
+ * of rc_context_norms_ex and a row count per layer: the caches receive
+ * exactly the bits of rc_context_norms_ex + rc_kv_project_store_rows.
+ *
+ *   x, T, D, hidden, pre, L       as rc_context_norms_ex (D = 8192)
+ *   W, w_layout, H                as rc_kv_project (N = 128*H)
+ *   positions ... block_size      as rc_kv_project_store
+ *   eps                           the K-norm's eps (the norms carry their
+ *                                 own in hidden and pre)
+ *   layer_rows                    HOST array of L row counts, each in
+ *                                 [0, T] (layer l stores its first
+ *                                 layer_rows[l] rows), or NULL for T rows
+ *                                 in every layer
+ *   err, chunks, workspace, ...   as rc_context_kv_chunked (the same
+ *                                 workspace size); with x in device memory
+ *                                 and a norm option beyond bf16 output-scale
+ *                                 weights without a centre, chunks <= 0
+ *                                 means one chunk (the option kernel beside
+ *                                 the projection costs more than the overlap
+ *                                 gains), while x in host memory is chunked
+ *                                 as rc_context_kv_chunks says
+ * Errors as rc_context_norms_ex and rc_context_kv_chunked.
+ */
+rc_status rc_context_kv_chunked_ex(const uint16_t *x, int64_t T, int32_t D,
+                                   const rc_norm_params *hidden, const rc_norm_params *pre,
+                                   int32_t L, const uint16_t *W, int32_t w_layout, int32_t H,
+                                   const int64_t *positions, const int64_t *const *slots,
+                                   const uint16_t *cos_sin, int64_t max_position,
+                                   uint16_t *const *caches, int32_t num_blocks, int32_t block_size,
+                                   float eps, const int64_t *layer_rows, int32_t *err,
+                                   int32_t chunks, void *workspace, size_t workspace_bytes,
+                                   cudaStream_t stream);
+
 /* Workspace bytes of rc_context_kv_chunked for these sizes on the current
    device, enough for any chunk request and for x in device or host memory
    (0 for unsupported sizes; `chunks` is accepted for symmetry). */

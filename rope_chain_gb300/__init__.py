@@ -108,6 +108,12 @@ SIGNATURES["rc_context_kv_chunked"] = ([_vp, _c.c_int64, _c.c_int32, _vp, _vp, _
                                         _vp, _c.c_int32, _c.c_int32, _vp, _c.POINTER(_vp), _vp,
                                         _c.c_int64, _c.POINTER(_vp), _c.c_int32, _c.c_int32,
                                         _c.c_int64, _vp, _c.c_int32, _vp, _c.c_size_t, _vp], _c.c_int)
+SIGNATURES["rc_context_kv_chunked_ex"] = ([_vp, _c.c_int64, _c.c_int32, _c.POINTER(NormParams),
+                                           _c.POINTER(NormParams), _c.c_int32, _vp, _c.c_int32,
+                                           _c.c_int32, _vp, _c.POINTER(_vp), _vp, _c.c_int64,
+                                           _c.POINTER(_vp), _c.c_int32, _c.c_int32, _c.c_float,
+                                           _c.POINTER(_c.c_int64), _vp, _c.c_int32, _vp, _c.c_size_t,
+                                           _vp], _c.c_int)
 SIGNATURES["rc_context_kv_chunked_workspace_size"] = ([_c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32,
                                                        _c.c_int32], _c.c_size_t)
 SIGNATURES["rc_context_kv_chunks"] = ([_c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32, _c.c_int32,
@@ -554,6 +560,43 @@ def context_kv_chunked(x: torch.Tensor, hidden_w, pre_w, W: torch.Tensor, H: int
                                        workspace.data_ptr(),
                                        workspace.numel() * workspace.element_size(),
                                        _stream(stream)))
+
+
+def context_kv_chunked_ex(x: torch.Tensor, W: torch.Tensor, H: int, positions, slots, cos_sin,
+                          caches, eps: float, workspace: torch.Tensor, *,
+                          hidden_w: Optional[torch.Tensor] = None,
+                          pre_w: Optional[torch.Tensor] = None, hidden_eps: float, pre_eps: float,
+                          hidden_center: float = 0.0, pre_center: float = 0.0,
+                          hidden_input_scale: bool = False, pre_input_scale: bool = False,
+                          rows=None, err=None, chunks: int = 0, w_layout: int = RC_W_KN,
+                          stream=None) -> None:
+    """context_kv_chunked with every norm option of context_norms_ex and a
+    row count per layer (rc_context_kv_chunked_ex).  ``eps``: the K-norm's;
+    ``rows``: an int, one count per layer, or None for each layer's
+    slot-mapping length."""
+    xa = _in_bf16(x, "x")                          # CUDA or pinned host memory
+    _bf16(W, "W")
+    T, D = x.shape
+    L = len(caches)
+    if hidden_w is not None and tuple(hidden_w.shape) != (D,):
+        raise ValueError("hidden_w must be [8192]")
+    if pre_w is not None and tuple(pre_w.shape) != (L, D):
+        raise ValueError("pre_w must be [L, 8192]")
+    if not (workspace.is_cuda and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    h = _norm_params(hidden_w, hidden_input_scale, hidden_center, hidden_eps, "hidden_w")
+    p = _norm_params(pre_w, pre_input_scale, pre_center, pre_eps, "pre_w")
+    n_rows, per_layer = _layer_rows(slots, rows)
+    _check_slot_lengths(slots, n_rows, per_layer)
+    slot_arr, cache_arr, nb, bs, _ = _store_operands(H, slots, caches, positions, cos_sin, 0)
+    counts = (_c.c_int64 * L)(*(per_layer if per_layer is not None else [n_rows] * L))
+    _check(lib().rc_context_kv_chunked_ex(xa, T, D, ctypes.byref(h), ctypes.byref(p), L,
+                                          W.data_ptr(), w_layout, H, _ptr(positions), slot_arr,
+                                          _ptr(cos_sin), 0 if cos_sin is None else cos_sin.shape[0],
+                                          cache_arr, nb, bs, eps, counts, _ptr(err), chunks,
+                                          workspace.data_ptr(),
+                                          workspace.numel() * workspace.element_size(),
+                                          _stream(stream)))
 
 
 def context_rows(x: torch.Tensor, hidden_w, eps: float, z: Optional[torch.Tensor] = None,

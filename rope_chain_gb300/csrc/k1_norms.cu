@@ -454,14 +454,15 @@ __device__ __forceinline__ void norm_output(const uint4 (&q)[R][kFrags], const N
 template <int R>
 __global__ void __launch_bounds__(kThreads, 4)
 k1_context_norms_ex(const uint16_t *__restrict__ x, int64_t T, const NormDesc hidden,
-                    const NormDesc pre, int32_t L, uint16_t *__restrict__ out)
+                    const NormDesc pre, int32_t L, uint16_t *__restrict__ out, int early)
 {
     __shared__ float sums[2][R][kThreads / 32];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t row0 = (int64_t)blockIdx.x * R;
     int buf = 0;
     pdl_trigger();
-    pdl_wait();
+    if (!early)
+        pdl_wait();
 
     uint4 q[R][kFrags];
 #pragma unroll
@@ -516,6 +517,7 @@ k1_context_norms_ex(const uint16_t *__restrict__ x, int64_t T, const NormDesc hi
                                                    k * kFragStride + tid] = o[j];
         }
     }
+    early_join(early);
 }
 
 // ---- the same kernel with each weight row staged in shared memory
@@ -644,7 +646,7 @@ __device__ __forceinline__ void staged_output(const uint4 (&q)[R][kFrags], const
 template <int R>
 __global__ void __launch_bounds__(kThreads, 2)
 k1_context_norms_exs(const uint16_t *__restrict__ x, int64_t T, const NormDesc hidden,
-                     const NormDesc pre, int32_t L, uint16_t *__restrict__ out)
+                     const NormDesc pre, int32_t L, uint16_t *__restrict__ out, int early)
 {
     extern __shared__ __align__(16) uint8_t gstage[];   // [2][kGainBytes]
     __shared__ float sums[2][R][kThreads / 32];
@@ -652,7 +654,8 @@ k1_context_norms_exs(const uint16_t *__restrict__ x, int64_t T, const NormDesc h
     const int64_t row0 = (int64_t)blockIdx.x * R;
     int buf = 0;
     pdl_trigger();
-    pdl_wait();
+    if (!early)
+        pdl_wait();
     stage_gains(hidden, 0, gstage, tid);
     stage_gains(pre, 0, gstage + kGainBytes, tid);
 
@@ -712,11 +715,12 @@ k1_context_norms_exs(const uint16_t *__restrict__ x, int64_t T, const NormDesc h
         }
     }
     staged_wait<0>();                               // no copy outlives the CTA
+    early_join(early);
 }
 
 template <int R>
 cudaError_t launch_exs(const uint16_t *x, int64_t T, const NormDesc &hidden, const NormDesc &pre,
-                       int32_t L, uint16_t *out, cudaStream_t stream) {
+                       int32_t L, uint16_t *out, cudaStream_t stream, int early) {
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -731,19 +735,20 @@ cudaError_t launch_exs(const uint16_t *x, int64_t T, const NormDesc &hidden, con
             configured[dev] = true;
     }
     return launch_pdl(k1_context_norms_exs<R>, dim3((unsigned)((T + R - 1) / R)), dim3(kThreads),
-                      (size_t)(2 * kGainBytes), stream, 1, x, T, hidden, pre, L, out);
+                      (size_t)(2 * kGainBytes), stream, 1, x, T, hidden, pre, L, out, early);
 }
 
 }  // namespace
 
 cudaError_t launch_context_norms_ex(const uint16_t *x, int64_t T, const NormDesc &hidden,
                                     const NormDesc &pre, int32_t L, uint16_t *out,
-                                    cudaStream_t stream)
+                                    cudaStream_t stream, bool early)
 {
+    const int ea = early ? 1 : 0;
     if (T >= kExTwoRowsFrom)                     // two rows per CTA, weights staged
-        return launch_exs<2>(x, T, hidden, pre, L, out, stream);
+        return launch_exs<2>(x, T, hidden, pre, L, out, stream, ea);
     return launch_pdl(k1_context_norms_ex<1>, dim3((unsigned)T), dim3(kThreads), 0, stream, 1, x, T,
-                      hidden, pre, L, out);
+                      hidden, pre, L, out, ea);
 }
 
 cudaError_t launch_context_norms(const uint16_t *x, int64_t T, const uint16_t *hidden_w,

@@ -164,6 +164,54 @@ rc_status kv_store_impl(const char *fn, const uint16_t *k, const uint16_t *v,
 
 }  // namespace
 
+namespace {
+
+// The two norms' parameters of the option calls, checked and turned into
+// the kernels' descriptors.
+rc_status norm_descs(const char *fn, const rc_norm_params *hidden, const rc_norm_params *pre,
+                     rc::NormDesc d[2])
+{
+    const rc_norm_params *np[2] = {hidden, pre};
+    for (int i = 0; i < 2; ++i) {
+        const rc_norm_params &n = *np[i];
+        const char *which = i ? "pre" : "hidden";
+        if (n.weight_dtype != RC_NORM_NONE && n.weight_dtype != RC_NORM_BF16 &&
+            n.weight_dtype != RC_NORM_F32)
+            return fail(RC_ERR_INVALID_ARG, "%s: %s weight_dtype=%d unknown", fn, which, n.weight_dtype);
+        if ((n.weight_dtype == RC_NORM_NONE) != (n.weight == nullptr))
+            return fail(RC_ERR_INVALID_ARG, "%s: %s weight must be NULL exactly when weight_dtype is "
+                        "RC_NORM_NONE", fn, which);
+        if (n.weight && !aligned(n.weight, 16))
+            return fail(RC_ERR_INVALID_ARG, "%s: %s weight must be 16-byte aligned", fn, which);
+        d[i].w = n.weight;
+        d[i].fp32 = n.weight_dtype == RC_NORM_F32;
+        d[i].input_scale = n.weight != nullptr && n.input_scale != 0;   // weightless: ignored
+        d[i].center = n.gain_center;
+        d[i].eps = n.eps;
+    }
+    return RC_OK;
+}
+
+// Whether a norm runs in the default kernel: no weight, or a bf16
+// output-scale weight without a centre.
+bool plain_norm(const rc::NormDesc &n) {
+    return n.w == nullptr || (!n.fp32 && !n.input_scale && n.center == 0.0f);
+}
+
+// The norms kernel for two descriptors: the default kernel where both norms
+// are plain, the option kernel otherwise.
+cudaError_t launch_norms(const uint16_t *x, int64_t T, const rc::NormDesc d[2], int32_t L,
+                         uint16_t *out, cudaStream_t stream, bool early = false)
+{
+    if (plain_norm(d[0]) && plain_norm(d[1]))
+        return rc::launch_context_norms(x, T, static_cast<const uint16_t *>(d[0].w),
+                                        static_cast<const uint16_t *>(d[1].w), L, d[0].eps,
+                                        d[1].eps, out, stream, early);
+    return rc::launch_context_norms_ex(x, T, d[0], d[1], L, out, stream, early);
+}
+
+}  // namespace
+
 namespace rc {
 void set_last_error(const char *msg) { snprintf(g_err, sizeof g_err, "%s", msg); }
 
@@ -238,40 +286,15 @@ rc_status rc_context_norms_ex(const uint16_t *x, int64_t T, int32_t D,
     if (!aligned(x, 16) || !aligned(out, 16))
         return fail(RC_ERR_INVALID_ARG, "%s: x and out must be 16-byte aligned", fn);
     rc::NormDesc d[2];
-    const rc_norm_params *np[2] = {hidden, pre};
-    for (int i = 0; i < 2; ++i) {
-        const rc_norm_params &n = *np[i];
-        const char *which = i ? "pre" : "hidden";
-        if (n.weight_dtype != RC_NORM_NONE && n.weight_dtype != RC_NORM_BF16 &&
-            n.weight_dtype != RC_NORM_F32)
-            return fail(RC_ERR_INVALID_ARG, "%s: %s weight_dtype=%d unknown", fn, which, n.weight_dtype);
-        if ((n.weight_dtype == RC_NORM_NONE) != (n.weight == nullptr))
-            return fail(RC_ERR_INVALID_ARG, "%s: %s weight must be NULL exactly when weight_dtype is "
-                        "RC_NORM_NONE", fn, which);
-        if (n.weight && !aligned(n.weight, 16))
-            return fail(RC_ERR_INVALID_ARG, "%s: %s weight must be 16-byte aligned", fn, which);
-        d[i].w = n.weight;
-        d[i].fp32 = n.weight_dtype == RC_NORM_F32;
-        d[i].input_scale = n.weight != nullptr && n.input_scale != 0;   // weightless: ignored
-        d[i].center = n.gain_center;
-        d[i].eps = n.eps;
-    }
+    const rc_status st = norm_descs(fn, hidden, pre, d);
+    if (st != RC_OK)
+        return st;
     const size_t xbytes = (size_t)T * D * 2, obytes = (size_t)L * T * D * 2;
     if (T > 0 && overlap(x, xbytes, out, obytes))
         return fail(RC_ERR_INVALID_ARG, "%s: out overlaps x", fn);
     if (T == 0)
         return ok();
-    // bf16 output-scale weights without a center take the default kernel
-    const auto plain = [](const rc::NormDesc &n) {
-        return n.w == nullptr || (!n.fp32 && !n.input_scale && n.center == 0.0f);
-    };
-    cudaError_t e;
-    if (plain(d[0]) && plain(d[1]))
-        e = rc::launch_context_norms(x, T, static_cast<const uint16_t *>(d[0].w),
-                                     static_cast<const uint16_t *>(d[1].w), L, d[0].eps, d[1].eps,
-                                     out, stream);
-    else
-        e = rc::launch_context_norms_ex(x, T, d[0], d[1], L, out, stream);
+    const cudaError_t e = launch_norms(x, T, d, L, out, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "rc_context_norms_ex launch");
     return ok();
@@ -869,6 +892,119 @@ bool on_host(const void *x) {
     return a.type == cudaMemoryTypeHost;
 }
 
+// rc_context_kv_chunked and rc_context_kv_chunked_ex: the norms given by d,
+// then the projection + store with the K-norm's eps, by row chunks; layer l
+// stores its first layer_rows[l] rows (`rows` for every layer when NULL).
+rc_status chunked_impl(const char *fn, const uint16_t *x, int64_t T, int32_t D,
+                       const rc::NormDesc d[2], int32_t L, float eps, const uint16_t *W,
+                       int32_t w_layout, int32_t H, const int64_t *positions,
+                       const int64_t *const *slots, const uint16_t *cos_sin, int64_t max_position,
+                       uint16_t *const *caches, int32_t num_blocks, int32_t block_size,
+                       const int64_t *layer_rows, int64_t rows, int32_t *err, int32_t chunks,
+                       void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    rc_status st = chunked_sizes(fn, L, T, D, H);
+    if (st != RC_OK)
+        return st;
+    const int32_t N = 2 * H * rc::kHeadDim;
+    if (w_layout != RC_W_KN && w_layout != RC_W_NK)
+        return fail(RC_ERR_INVALID_ARG, "%s: unknown weight layout %d", fn, w_layout);
+    if (!x || !W || !workspace)
+        return fail(RC_ERR_INVALID_ARG, "%s: x, W and workspace must not be NULL", fn);
+    if (!aligned(x, 16) || !aligned(W, 16) || !aligned(workspace, 256))
+        return fail(RC_ERR_INVALID_ARG, "%s: x and W must be 16-byte aligned, workspace 256-byte "
+                    "aligned", fn);
+    rc::FusedStore fs;
+    st = fused_store_args(fn, L, T, H, positions, slots, cos_sin, max_position, caches, num_blocks,
+                          block_size, eps, rows, err, nullptr, &fs, layer_rows);
+    if (st != RC_OK)
+        return st;
+    if (T == 0)
+        return ok();
+    const int sms = num_sms_current();
+    if (sms <= 0)
+        return fail(RC_ERR_CUDA, "%s: no current CUDA device", fn);
+    const bool x_on_host = on_host(x);
+    // With x in device memory, norm options beyond the default kernel's keep
+    // one chunk unless more are asked for: below 16384 rows the option
+    // kernel reads each weight row from L2 once per row (the kernel that
+    // stages them takes 64 KB of shared memory and so cannot run beside a
+    // projection CTA), and beside the projection that costs more than the
+    // overlap gains (workload 5 with FP32 gains: 3398-3410 us in 4 chunks,
+    // 3159-3169 us in one).
+    if (chunks <= 0 && !x_on_host && !(plain_norm(d[0]) && plain_norm(d[1])))
+        chunks = 1;
+    const RowChunks rcn = plan_row_chunks(L, T, D, N, sms, chunks, x_on_host);
+    const size_t nbytes = round256((size_t)L * T * D * 2);
+    const size_t need = rcn.count > 1 ? nbytes + kChunkCounterBytes * rcn.count : nbytes;
+    if (workspace_bytes < need)
+        return fail(RC_ERR_INVALID_ARG, "%s: the workspace needs at least %zu bytes (%zu given)", fn,
+                    need, workspace_bytes);
+    if (overlap(workspace, workspace_bytes, x, (size_t)T * D * 2) ||
+        overlap(workspace, workspace_bytes, W, (size_t)L * D * N * 2))
+        return fail(RC_ERR_INVALID_ARG, "%s: the workspace overlaps x or W", fn);
+    char *wsb = static_cast<char *>(workspace);
+    uint16_t *normed = reinterpret_cast<uint16_t *>(wsb);
+    const bool nk = w_layout == RC_W_NK;
+    const char *why = "launch";
+    cudaError_t e;
+    if (rcn.count == 1) {
+        const size_t avail = workspace_bytes - nbytes;
+        const rc::ProjectPlan plan = rc::plan_kv_project(L, T, D, N, sms, avail);
+        if (plan.splits == 1 && !plan.pair) {
+            // single CTAs without a K split: the projection goes through a
+            // bf16 copy in the workspace, which the store kernel then reads
+            const size_t kvb = round256((size_t)L * T * N * 2);
+            if (avail < kvb)
+                return fail(RC_ERR_INVALID_ARG,
+                            "%s: the workspace needs at least %zu bytes (%zu given)", fn,
+                            nbytes + kvb, workspace_bytes);
+            fs.kv_out = reinterpret_cast<uint16_t *>(wsb + nbytes);
+        }
+        e = launch_norms(x, T, d, L, normed, stream);
+        if (e == cudaSuccess)
+            e = rc::launch_kv_project_store(normed, W, nk, L, T, D, N, plan,
+                                            reinterpret_cast<float *>(wsb + nbytes), fs, stream, &why);
+        if (e != cudaSuccess)
+            return cuda_fail(e, why);
+        return ok();
+    }
+    // Chunk c's norms run beside chunk c - 1's projection: launched right
+    // behind it (PDL), they take the registers its persistent CTAs leave on
+    // each SM.  Rows of different chunks share no buffer, so only the
+    // projection of a chunk waits for that chunk's norms; the counters of
+    // all chunks are zeroed first, so no memset separates the kernels.
+    char *ctrs = wsb + nbytes;
+    e = cudaMemsetAsync(ctrs, 0, kChunkCounterBytes * rcn.count, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "tile counter memset");
+    for (int32_t c = 0; c < rcn.count; ++c) {
+        const int64_t r0 = rcn.row0[c];
+        const int64_t tc = rcn.row0[c + 1] - r0;
+        uint16_t *normed_c = normed + (size_t)L * r0 * D;     // [L, tc, D]
+        e = launch_norms(x + r0 * D, tc, d, L, normed_c, stream, c > 0);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "norms launch");
+        rc::FusedStore fc = fs;
+        if (fs.positions)
+            fc.positions = fs.positions + r0;
+        for (int32_t l = 0; l < L; ++l) {
+            if (fs.slots[l])
+                fc.slots[l] = fs.slots[l] + r0;
+            fc.rows[l] = (int32_t)std::min<int64_t>(std::max<int64_t>(fs.rows[l] - r0, 0), tc);
+        }
+        rc::ProjectPlan plan = rc::plan_kv_project(L, tc, D, N, sms, kChunkCounterBytes);
+        plan.ctr_zeroed = true;
+        e = rc::launch_kv_project_store(normed_c, W, nk, L, tc, D, N, plan,
+                                        reinterpret_cast<float *>(ctrs + kChunkCounterBytes * c), fc,
+                                        stream, &why);
+        if (e != cudaSuccess)
+            return cuda_fail(e, why);
+    }
+    return ok();
+}
+
+
 }  // namespace
 
 extern "C" {
@@ -907,97 +1043,35 @@ rc_status rc_context_kv_chunked(const uint16_t *x, int64_t T, int32_t D, const u
                                 void *workspace, size_t workspace_bytes, cudaStream_t stream)
 {
     const char *fn = "rc_context_kv_chunked";
-    rc_status st = chunked_sizes(fn, L, T, D, H);
+    if ((hidden_w && !aligned(hidden_w, 16)) || (pre_w && !aligned(pre_w, 16)))
+        return fail(RC_ERR_INVALID_ARG, "%s: weights must be 16-byte aligned", fn);
+    // bf16 output-scale weights (or none), gain centre 0, one eps
+    const rc::NormDesc d[2] = {{hidden_w, 0, 0, 0.0f, eps}, {pre_w, 0, 0, 0.0f, eps}};
+    return chunked_impl(fn, x, T, D, d, L, eps, W, w_layout, H, positions, slots, cos_sin,
+                        max_position, caches, num_blocks, block_size, nullptr, rows, err, chunks,
+                        workspace, workspace_bytes, stream);
+}
+
+rc_status rc_context_kv_chunked_ex(const uint16_t *x, int64_t T, int32_t D,
+                                   const rc_norm_params *hidden, const rc_norm_params *pre,
+                                   int32_t L, const uint16_t *W, int32_t w_layout, int32_t H,
+                                   const int64_t *positions, const int64_t *const *slots,
+                                   const uint16_t *cos_sin, int64_t max_position,
+                                   uint16_t *const *caches, int32_t num_blocks, int32_t block_size,
+                                   float eps, const int64_t *layer_rows, int32_t *err,
+                                   int32_t chunks, void *workspace, size_t workspace_bytes,
+                                   cudaStream_t stream)
+{
+    const char *fn = "rc_context_kv_chunked_ex";
+    if (!hidden || !pre)
+        return fail(RC_ERR_INVALID_ARG, "%s: hidden and pre must not be NULL", fn);
+    rc::NormDesc d[2];
+    const rc_status st = norm_descs(fn, hidden, pre, d);
     if (st != RC_OK)
         return st;
-    const int32_t N = 2 * H * rc::kHeadDim;
-    if (w_layout != RC_W_KN && w_layout != RC_W_NK)
-        return fail(RC_ERR_INVALID_ARG, "%s: unknown weight layout %d", fn, w_layout);
-    if (!x || !W || !workspace)
-        return fail(RC_ERR_INVALID_ARG, "%s: x, W and workspace must not be NULL", fn);
-    if (!aligned(x, 16) || !aligned(W, 16) || !aligned(workspace, 256) ||
-        (hidden_w && !aligned(hidden_w, 16)) || (pre_w && !aligned(pre_w, 16)))
-        return fail(RC_ERR_INVALID_ARG,
-                    "%s: x, W and weights must be 16-byte aligned, workspace 256-byte aligned", fn);
-    rc::FusedStore fs;
-    st = fused_store_args(fn, L, T, H, positions, slots, cos_sin, max_position, caches, num_blocks,
-                          block_size, eps, rows, err, nullptr, &fs);
-    if (st != RC_OK)
-        return st;
-    if (T == 0)
-        return ok();
-    const int sms = num_sms_current();
-    if (sms <= 0)
-        return fail(RC_ERR_CUDA, "%s: no current CUDA device", fn);
-    const RowChunks rcn = plan_row_chunks(L, T, D, N, sms, chunks, on_host(x));
-    const size_t nbytes = round256((size_t)L * T * D * 2);
-    const size_t need = rcn.count > 1 ? nbytes + kChunkCounterBytes * rcn.count : nbytes;
-    if (workspace_bytes < need)
-        return fail(RC_ERR_INVALID_ARG, "%s: the workspace needs at least %zu bytes (%zu given)", fn,
-                    need, workspace_bytes);
-    if (overlap(workspace, workspace_bytes, x, (size_t)T * D * 2) ||
-        overlap(workspace, workspace_bytes, W, (size_t)L * D * N * 2))
-        return fail(RC_ERR_INVALID_ARG, "%s: the workspace overlaps x or W", fn);
-    char *wsb = static_cast<char *>(workspace);
-    uint16_t *normed = reinterpret_cast<uint16_t *>(wsb);
-    const bool nk = w_layout == RC_W_NK;
-    const char *why = "launch";
-    cudaError_t e;
-    if (rcn.count == 1) {
-        const size_t avail = workspace_bytes - nbytes;
-        const rc::ProjectPlan plan = rc::plan_kv_project(L, T, D, N, sms, avail);
-        if (plan.splits == 1 && !plan.pair) {
-            // single CTAs without a K split: the projection goes through a
-            // bf16 copy in the workspace, which the store kernel then reads
-            const size_t kvb = round256((size_t)L * T * N * 2);
-            if (avail < kvb)
-                return fail(RC_ERR_INVALID_ARG,
-                            "%s: the workspace needs at least %zu bytes (%zu given)", fn,
-                            nbytes + kvb, workspace_bytes);
-            fs.kv_out = reinterpret_cast<uint16_t *>(wsb + nbytes);
-        }
-        e = rc::launch_context_norms(x, T, hidden_w, pre_w, L, eps, eps, normed, stream);
-        if (e == cudaSuccess)
-            e = rc::launch_kv_project_store(normed, W, nk, L, T, D, N, plan,
-                                            reinterpret_cast<float *>(wsb + nbytes), fs, stream, &why);
-        if (e != cudaSuccess)
-            return cuda_fail(e, why);
-        return ok();
-    }
-    // Chunk c's norms run beside chunk c - 1's projection: launched right
-    // behind it (PDL), they take the registers its persistent CTAs leave on
-    // each SM.  Rows of different chunks share no buffer, so only the
-    // projection of a chunk waits for that chunk's norms; the counters of
-    // all chunks are zeroed first, so no memset separates the kernels.
-    char *ctrs = wsb + nbytes;
-    e = cudaMemsetAsync(ctrs, 0, kChunkCounterBytes * rcn.count, stream);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "tile counter memset");
-    for (int32_t c = 0; c < rcn.count; ++c) {
-        const int64_t r0 = rcn.row0[c];
-        const int64_t tc = rcn.row0[c + 1] - r0;
-        uint16_t *normed_c = normed + (size_t)L * r0 * D;     // [L, tc, D]
-        e = rc::launch_context_norms(x + r0 * D, tc, hidden_w, pre_w, L, eps, eps, normed_c, stream,
-                                     c > 0);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "norms launch");
-        rc::FusedStore fc = fs;
-        if (fs.positions)
-            fc.positions = fs.positions + r0;
-        for (int32_t l = 0; l < L; ++l) {
-            if (fs.slots[l])
-                fc.slots[l] = fs.slots[l] + r0;
-            fc.rows[l] = (int32_t)std::min<int64_t>(std::max<int64_t>(fs.rows[l] - r0, 0), tc);
-        }
-        rc::ProjectPlan plan = rc::plan_kv_project(L, tc, D, N, sms, kChunkCounterBytes);
-        plan.ctr_zeroed = true;
-        e = rc::launch_kv_project_store(normed_c, W, nk, L, tc, D, N, plan,
-                                        reinterpret_cast<float *>(ctrs + kChunkCounterBytes * c), fc,
-                                        stream, &why);
-        if (e != cudaSuccess)
-            return cuda_fail(e, why);
-    }
-    return ok();
+    return chunked_impl(fn, x, T, D, d, L, eps, W, w_layout, H, positions, slots, cos_sin,
+                        max_position, caches, num_blocks, block_size, layer_rows, T, err, chunks,
+                        workspace, workspace_bytes, stream);
 }
 
 rc_status rc_device_address(const void *p, const void **dev)

@@ -261,7 +261,7 @@ struct NormDesc {
 
 cudaError_t launch_context_norms_ex(const uint16_t *x, int64_t T, const NormDesc &hidden,
                                     const NormDesc &pre, int32_t L, uint16_t *out,
-                                    cudaStream_t stream);
+                                    cudaStream_t stream, bool early = false);
 
 // Row prep for the fused chain: z = bf16 [T, 8192] hidden-norm output and
 // r2 [T] = the layers' shared inverse RMS of z.

@@ -241,3 +241,84 @@ def test_chunked_workload5_full_size():
     got = run_chunked(case, 0)
     ref = run_reference(case)
     assert_same(got, ref)
+
+
+def _options(case, L, kind):
+    """Norm options of the _ex call: FP32 gains with the hidden weight on the
+    input and a layer gain centre of 1; bf16 gains with centres; none."""
+    f32 = lambda a: None if a is None else torch.from_numpy(
+        (a.astype(np.uint32) << 16).view(np.float32)).to(DEV)
+    eps = case["eps"]
+    if kind == "fp32":
+        return dict(hidden_w=f32(case["hidden_w"]), pre_w=f32(case["pre_w"]), hidden_eps=eps,
+                    pre_eps=10 * eps, hidden_input_scale=True, pre_center=1.0)
+    if kind == "centred":
+        return dict(hidden_w=parity.dev_bf16(case["hidden_w"], DEV),
+                    pre_w=parity.dev_bf16(case["pre_w"], DEV), hidden_eps=2 * eps, pre_eps=eps,
+                    hidden_center=-0.5, pre_center=0.25)
+    return dict(hidden_w=None, pre_w=None, hidden_eps=eps, pre_eps=eps)
+
+
+@pytest.mark.parametrize("T,L,H,chunks,kind,layout,per_layer,host", [
+    (1536, 3, 8, 3, "fp32", rc.RC_W_KN, True, False),
+    (1536, 3, 8, 2, "centred", rc.RC_W_NK, False, False),
+    (2048, 2, 4, 2, "none", rc.RC_W_KN, True, True),
+    (512, 3, 8, 0, "fp32", rc.RC_W_KN, True, False),     # one chunk: the full plan
+])
+def test_chunked_ex_equals_norms_ex_and_rows_store(T, L, H, chunks, kind, layout, per_layer, host):
+    case = workloads.random_case(1900 + T + L, T=T, L=L, H=H, max_position=512,
+                                 num_blocks=(T + 15) // 16 + 3, block_size=16)
+    ops = _operands(case, layout)
+    opts = _options(case, L, kind)
+    rows = [T - l * (T // (2 * L)) for l in range(L)] if per_layer else T
+    n = rc.context_kv_chunks(L, T, H, sms(), chunks, x_on_host=host)
+    assert (n >= 2) == (chunks != 0)
+    # the reference: the option norms, then the projection + store with a
+    # row count per layer (no workspace where chunks run, as they do)
+    caches_r = [parity.dev_bf16(c, DEV) for c in parity.make_caches(case, L, parity.SENTINEL)]
+    err_r = torch.zeros(1, dtype=torch.int32, device=DEV)
+    normed = rc.context_norms_ex(ops["x"], L, **opts)
+    ws_r = None if n >= 2 else rc.new_workspace(L, T, 8192, 128 * H, DEV)
+    rc.kv_project_store(normed, ops["W"], H, ops["positions"], ops["slots"], ops["cs"], caches_r,
+                        case["eps"], rows=rows, err=err_r, workspace=ws_r, w_layout=layout)
+    # the chunked call
+    caches = [parity.dev_bf16(c, DEV) for c in parity.make_caches(case, L, parity.SENTINEL)]
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    x = ops["x"].cpu().pin_memory() if host else ops["x"]
+    ws = rc.context_kv_chunked_workspace(L, T, H, DEV, chunks=chunks)
+    rc.context_kv_chunked_ex(x, ops["W"], H, ops["positions"], ops["slots"], ops["cs"], caches,
+                             case["eps"], ws, rows=rows, err=err, chunks=chunks, w_layout=layout,
+                             **opts)
+    torch.cuda.synchronize()
+    assert_same(dict(caches=[parity.host_bits(c) for c in caches], err=int(err.item())),
+                dict(caches=[parity.host_bits(c) for c in caches_r], err=int(err_r.item())))
+
+
+@pytest.mark.parametrize("host", [False, True])
+def test_chunked_ex_automatic_count_with_options(host):
+    # at a size the plain call splits (2 chunks), FP32 gains keep one chunk
+    # with x in device memory (the option kernel beside the projection costs
+    # more than the overlap) and take the host plan with x in host memory;
+    # the bits are the same either way
+    T, L, H = 16384, 8, 8
+    assert rc.context_kv_chunks(L, T, H, sms(), 0) >= 2
+    assert rc.context_kv_chunks(L, T, H, sms(), 0, x_on_host=True) >= 2
+    case = workloads.random_case(1950, T=T, L=L, H=H, max_position=512,
+                                 num_blocks=(T + 15) // 16 + 3, block_size=16)
+    ops = _operands(case, rc.RC_W_KN)
+    opts = _options(case, L, "fp32")
+    caches_r = [parity.dev_bf16(c, DEV) for c in parity.make_caches(case, L, parity.SENTINEL)]
+    err_r = torch.zeros(1, dtype=torch.int32, device=DEV)
+    normed = rc.context_norms_ex(ops["x"], L, **opts)
+    rc.kv_project_store(normed, ops["W"], H, ops["positions"], ops["slots"], ops["cs"], caches_r,
+                        case["eps"], err=err_r, workspace=rc.new_workspace(L, T, 8192, 128 * H, DEV))
+    del normed
+    caches = [parity.dev_bf16(c, DEV) for c in parity.make_caches(case, L, parity.SENTINEL)]
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    x = ops["x"].cpu().pin_memory() if host else ops["x"]
+    rc.context_kv_chunked_ex(x, ops["W"], H, ops["positions"], ops["slots"], ops["cs"], caches,
+                             case["eps"], rc.context_kv_chunked_workspace(L, T, H, DEV), err=err,
+                             **opts)
+    torch.cuda.synchronize()
+    assert_same(dict(caches=[parity.host_bits(c) for c in caches], err=int(err.item())),
+                dict(caches=[parity.host_bits(c) for c in caches_r], err=int(err_r.item())))
