@@ -1004,7 +1004,6 @@ rc_status chunked_impl(const char *fn, const uint16_t *x, int64_t T, int32_t D,
     return ok();
 }
 
-
 }  // namespace
 
 extern "C" {

@@ -100,6 +100,7 @@ def sms():
     (800, 2, 16, 3, False, True, True),      # no RoPE, 16 heads (256 and 544)
     (1536, 3, 2, 2, True, False, True),      # weightless hidden norm, K and V heads in one tile
     (1000, 2, 8, 2, True, True, False),      # weightless layer norms (256 and 744)
+    (1024, 9, 2, 2, True, True, True),       # 9 layers: past 8 layers per store launch
 ])
 @pytest.mark.parametrize("layout", [rc.RC_W_KN, rc.RC_W_NK])
 def test_chunked_equals_unfused(T, L, H, chunks, rope, hw, pw, layout):
