@@ -51,26 +51,26 @@ CALL_SOURCES = {
 NCU_TRAFFIC = {
     # rc_kv_project_store at workload 5 over all rows (the breakdown's call,
     # the one the roofline times): one k2_project_pair_persistent launch
-    # (dynamic tile order), 4,642,587,392 B read + 528,178,432 B written
+    # (dynamic tile order), 4,861,931,520 B read + 527,136,512 B written
     # (profiles/k2_pair_persistent_workload5.md)
-    (5, "store", "project_store"): (5_170_765_824, "8481dd249f5d6497",
+    (5, "store", "project_store"): (5_389_068_032, "8bb10d3211a5d91f",
                                     "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, "
                                     "one launch at full size (one pass)"),
     # rc_context_norms at workload 5: one k1_context_norms2 launch,
-    # 537,337,088 B read + 4,233,408,256 B written
-    (5, "unfused", "norms"): (4_770_745_344, "456a34c29a6e5b40",
+    # 537,302,016 B read + 4,233,134,336 B written
+    (5, "unfused", "norms"): (4_770_436_352, "2655d675e990d059",
                               "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, "
                               "one launch at full size (one pass)"),
     # rc_kv_store at workload 5: one k3_kv_store_heads launch (8 layers),
-    # 574,433,280 B read + 482,217,472 B written
-    (5, "unfused", "store"): (1_056_650_752, "52ac374324bb746c",
+    # 574,425,600 B read + 482,196,992 B written
+    (5, "unfused", "store"): (1_056_622_592, "b4f44c2c856746c9",
                               "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, "
                               "one launch at full size (one pass)"),
-    # rc_kv_project_store at workload 2: k2_project_pair (51,769,856 B read,
-    # 16,178,688 B written) then k3_reduce_store (81,664 B read, 1,684,480 B
+    # rc_kv_project_store at workload 2: k2_project_pair (52,795,648 B read,
+    # 19,434,752 B written) then k3_reduce_store (82,688 B read, 1,630,976 B
     # written), captured in sequence without ncu's cache flush between them
     # (the split-K partials are read back from L2, as in the step)
-    (2, "store", "project_store"): (69_714_688, "8481dd249f5d6497",
+    (2, "store", "project_store"): (73_944_064, "8bb10d3211a5d91f",
                                     "ncu --cache-control none --metrics dram__bytes_read.sum,"
                                     "dram__bytes_write.sum, the call's two launches in sequence"),
 }
