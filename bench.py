@@ -131,6 +131,20 @@ def row_chunks(T: int, n: int):
     return [(edges[i], edges[i + 1]) for i in range(n)]
 
 
+def e2e_plan(path: str, T: int, host_chunks: int, e2e_chunks: int, e2e_mode: str):
+    """The end-to-end step's row ranges and transfer mode.  Where the
+    chunked call splits x held in host memory itself (host_chunks > 1), the
+    step is that one call reading x in place, unless ranges are asked for;
+    otherwise the store path copies row ranges (from 2048 rows) and the
+    other paths take one range.  One range always reads x in place."""
+    if path == "store" and not (host_chunks > 1 and e2e_chunks == 0):
+        chunks = row_chunks(T, e2e_chunks)
+    else:
+        chunks = [(0, T)]
+    mode = ("copy" if e2e_mode == "auto" else e2e_mode) if len(chunks) > 1 else "inplace"
+    return chunks, mode
+
+
 class OverlappedChain:
     """rc_context_norms + rc_kv_project_store over row ranges of x held in
     pinned host memory, overlapping the host-to-device transfer of x with
@@ -633,11 +647,7 @@ def run_ours(args, w):
     # chunk's projection, unless the ranges are asked for.
     host_chunks = (rc.context_kv_chunks(w.L, w.T, w.H, sms, args.chunks, x_on_host=True)
                    if chunked else 1)
-    if args.path == "store" and not (host_chunks > 1 and args.e2e_chunks == 0):
-        chunks = row_chunks(w.T, args.e2e_chunks)
-    else:
-        chunks = [(0, w.T)]
-    e2e_mode = ("copy" if args.e2e_mode == "auto" else args.e2e_mode) if len(chunks) > 1 else "inplace"
+    chunks, e2e_mode = e2e_plan(args.path, w.T, host_chunks, args.e2e_chunks, args.e2e_mode)
     overlapped = OverlappedChain(w.L, w.T, w.D, w.N, chunks, dev, e2e_mode) if len(chunks) > 1 else None
 
     def e2e_step(ev0, ev1):

@@ -111,6 +111,26 @@ def test_row_chunks_cover_rows_once():
     assert len(bench.row_chunks(16384, 0)) == 8
 
 
+def test_e2e_plan():
+    """The end-to-end step: one in-place call where the chunked call splits x
+    held in host memory itself; copied ranges on the store path otherwise;
+    one in-place range on the other paths."""
+    # workload 5: the chunked call's host plan has 7 chunks -> one call
+    assert bench.e2e_plan("store", 32768, 7, 0, "auto") == ([(0, 32768)], "inplace")
+    # the two calls (no host chunks) -> 8 copied ranges
+    ch, mode = bench.e2e_plan("store", 32768, 1, 0, "auto")
+    assert len(ch) == 8 and mode == "copy"
+    # ranges asked for win over the chunked call's own plan
+    ch, mode = bench.e2e_plan("store", 32768, 7, 4, "inplace")
+    assert len(ch) == 4 and mode == "inplace"
+    # below 2048 rows one range reads x in place
+    assert bench.e2e_plan("store", 512, 1, 0, "auto") == ([(0, 512)], "inplace")
+    # the variants and whole paths: one range (the variants' chunked call
+    # splits x itself)
+    assert bench.e2e_plan("variants", 32768, 7, 0, "auto") == ([(0, 32768)], "inplace")
+    assert bench.e2e_plan("whole", 32768, 1, 0, "copy") == ([(0, 32768)], "inplace")
+
+
 def test_traffic_figures_expire_with_their_sources(tmp_path, monkeypatch):
     """A stored ncu traffic figure is reported only while the sources of its
     call's kernels are those it was measured on: a change to the projection
