@@ -234,12 +234,18 @@ def test_chunked_refusals():
         assert np.array_equal(parity.host_bits(a), b)
 
 
-def test_chunked_workload5_full_size():
+@pytest.mark.parametrize("host", [False, True])
+def test_chunked_workload5_full_size(host):
+    # the default step (x in device memory, 4 chunks) and the end-to-end
+    # step (x in pinned host memory, the host plan's 7 chunks) at full size
     w = workloads.WORKLOADS[5]
     case = workloads.make_inputs(w)
-    chunks = rc.context_kv_chunks(w.L, w.T, w.H, sms(), 0)
+    chunks = rc.context_kv_chunks(w.L, w.T, w.H, sms(), 0, x_on_host=host)
     assert chunks >= 2
-    got = run_chunked(case, 0)
+    ops = _operands(case, rc.RC_W_KN)
+    if host:
+        ops["x"] = ops["x"].cpu().pin_memory()
+    got = run_chunked(case, 0, ops=ops)
     ref = run_reference(case)
     assert_same(got, ref)
 
