@@ -732,9 +732,12 @@ def run_ours(args, w):
     first = "row_pass" if fused_norms else "norms"
     dominant = "project_store" if kern["project_store"]["us"] >= kern[first]["us"] else first
     d = kern[dominant]
-    traffic, traffic_note = ncu_traffic((args.workload, args.path, dominant))
+    # the stored figures are full-size captures: none for a --rows prefix
+    traffic_of = ((lambda key: (None, f"a --rows case (the first {w.T} rows): no capture of "
+                                      "this size")) if getattr(args, "full_T", None) else ncu_traffic)
+    traffic, traffic_note = traffic_of((args.workload, args.path, dominant))
     for name, entry in (("norms", kern["unfused"]["norms"]), ("store", kern["unfused"]["store"])):
-        entry["traffic"], entry["traffic_note"] = ncu_traffic((args.workload, "unfused", name))
+        entry["traffic"], entry["traffic_note"] = traffic_of((args.workload, "unfused", name))
     if d["bound"] == "tensor":
         roof = {"kernel": dominant, "bound": "tensor", "achieved": d["TFLOP/s"], "peak": tc,
                 "unit": "TFLOP/s", "frac": d["frac"], "traffic": traffic,
