@@ -11,6 +11,8 @@ below T, layers without a slot map, no RoPE, weightless norms, both weight
 layouts, a repeated call and a graph replay (each chunk's tile counter is
 zeroed per call), and workload 5 at full size.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -234,11 +236,13 @@ def test_chunked_refusals():
         assert np.array_equal(parity.host_bits(a), b)
 
 
+@pytest.mark.parametrize("index", [4, 5])
 @pytest.mark.parametrize("host", [False, True])
-def test_chunked_workload5_full_size(host):
-    # the default step (x in device memory, 4 chunks) and the end-to-end
-    # step (x in pinned host memory, the host plan's 7 chunks) at full size
-    w = workloads.WORKLOADS[5]
+def test_chunked_workload_full_size(index, host):
+    # the default step (x in device memory: 2 chunks at workload 4, 4 at
+    # workload 5) and the end-to-end step (x in pinned host memory: the host
+    # plan's 6 and 7 chunks) at full size
+    w = workloads.WORKLOADS[index]
     case = workloads.make_inputs(w)
     chunks = rc.context_kv_chunks(w.L, w.T, w.H, sms(), 0, x_on_host=host)
     assert chunks >= 2
@@ -329,3 +333,35 @@ def test_chunked_ex_automatic_count_with_options(host):
     torch.cuda.synchronize()
     assert_same(dict(caches=[parity.host_bits(c) for c in caches], err=int(err.item())),
                 dict(caches=[parity.host_bits(c) for c in caches_r], err=int(err_r.item())))
+
+
+def test_chunked_ex_refusals():
+    T, L, H = 1024, 2, 8
+    case = workloads.random_case(1961, T=T, L=L, H=H, max_position=512,
+                                 num_blocks=(T + 15) // 16 + 3, block_size=16)
+    ops = _operands(case, rc.RC_W_KN)
+    caches = [parity.dev_bf16(c, DEV) for c in parity.make_caches(case, L, parity.SENTINEL)]
+    before = [parity.host_bits(c) for c in caches]
+    ws = rc.context_kv_chunked_workspace(L, T, H, DEV)
+    slot_arr, cache_arr, nb, bs, _ = rc._store_operands(H, ops["slots"], caches, ops["positions"],
+                                                        ops["cs"], T)
+    ok = rc.NormParams(None, rc.RC_NORM_NONE, 0, 0.0, case["eps"])
+    bad_dtype = rc.NormParams(None, 7, 0, 0.0, case["eps"])
+    stray = rc.NormParams(ops["pw"].data_ptr(), rc.RC_NORM_NONE, 0, 0.0, case["eps"])
+    rows = (ctypes.c_int64 * L)(*([T] * L))
+
+    def call(h, p):
+        return rc.lib().rc_context_kv_chunked_ex(
+            ops["x"].data_ptr(), T, 8192, h, p, L, ops["W"].data_ptr(), rc.RC_W_KN, H,
+            ops["positions"].data_ptr(), slot_arr, ops["cs"].data_ptr(), ops["cs"].shape[0],
+            cache_arr, nb, bs, case["eps"], rows, None, 0, ws.data_ptr(), ws.numel(),
+            torch.cuda.current_stream().cuda_stream)
+
+    assert call(None, ctypes.byref(ok)) == rc.RC_ERR_INVALID_ARG
+    assert call(ctypes.byref(bad_dtype), ctypes.byref(ok)) == rc.RC_ERR_INVALID_ARG
+    assert "weight_dtype" in rc.lib().rc_last_error().decode()
+    assert call(ctypes.byref(ok), ctypes.byref(stray)) == rc.RC_ERR_INVALID_ARG
+    assert "NULL exactly" in rc.lib().rc_last_error().decode()
+    torch.cuda.synchronize()
+    for a, b in zip(caches, before):
+        assert np.array_equal(parity.host_bits(a), b)
