@@ -365,3 +365,33 @@ def test_chunked_ex_refusals():
     torch.cuda.synchronize()
     for a, b in zip(caches, before):
         assert np.array_equal(parity.host_bits(a), b)
+
+
+def test_chunked_ex_workload5_variants_host_x():
+    # the variants' end-to-end step at full size: FP32 gains with the hidden
+    # gain on the input, a layer gain centre of 1, separate eps and layer l
+    # storing T - l * T / (2 L) rows, x in pinned host memory (the host
+    # plan's chunks); against the option norms + the per-layer store
+    w = workloads.WORKLOADS[5]
+    case = workloads.make_inputs(w)
+    L, T, H = w.L, w.T, w.H
+    assert rc.context_kv_chunks(L, T, H, sms(), 0, x_on_host=True) >= 2
+    ops = _operands(case, rc.RC_W_KN)
+    opts = _options(case, L, "fp32")
+    rows = [T - l * (T // (2 * L)) for l in range(L)]
+    caches_r = [torch.zeros(case["cache_shape"], dtype=torch.bfloat16, device=DEV) for _ in range(L)]
+    err_r = torch.zeros(1, dtype=torch.int32, device=DEV)
+    normed = rc.context_norms_ex(ops["x"], L, **opts)
+    rc.kv_project_store(normed, ops["W"], H, ops["positions"], ops["slots"], ops["cs"], caches_r,
+                        case["eps"], rows=rows, err=err_r,
+                        workspace=rc.new_workspace(L, T, 8192, 128 * H, DEV))
+    del normed
+    caches = [torch.zeros(case["cache_shape"], dtype=torch.bfloat16, device=DEV) for _ in range(L)]
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    rc.context_kv_chunked_ex(ops["x"].cpu().pin_memory(), ops["W"], H, ops["positions"],
+                             ops["slots"], ops["cs"], caches, case["eps"],
+                             rc.context_kv_chunked_workspace(L, T, H, DEV), rows=rows, err=err,
+                             **opts)
+    torch.cuda.synchronize()
+    assert_same(dict(caches=[parity.host_bits(c) for c in caches], err=int(err.item())),
+                dict(caches=[parity.host_bits(c) for c in caches_r], err=int(err_r.item())))
