@@ -744,7 +744,11 @@ def run_ours(args, w):
                 "traffic_note": traffic_note,
                 "algorithmic_bytes": project_store_bytes(w, case["slots"], w.rope),
                 "peak_source": f"bf16_tflops (burst) of {peak_src}",
-                "frac_of_sustained": d["TFLOP/s"] / peaks.get("bf16_tflops_sustained", tc)}
+                "frac_of_sustained": d["TFLOP/s"] / peaks.get("bf16_tflops_sustained", tc),
+                # the same FLOPs over the whole timed step (norms, and in the
+                # chunked step their overlap with the projection, included)
+                "step_tflops": counts["k2_flops"] / (total_ms / args.steps) / 1e9,
+                "step_frac": counts["k2_flops"] / (total_ms / args.steps) / 1e9 / tc}
     else:
         roof = {"kernel": dominant, "bound": "hbm", "achieved": d["GB/s"], "peak": hbm,
                 "unit": "GB/s", "frac": d["frac"], "traffic": traffic,
