@@ -350,3 +350,23 @@ def test_chunked_chain_row_chunks():
     for i, w in workloads.WORKLOADS.items():
         assert rc.context_kv_chunk_rows(w.L, w.T, w.H, 152, x_on_host=True) == host[i], i
     assert rc.context_kv_chunk_rows(3, 2048, 8, 152, 3, x_on_host=True) == [0, 768, 1536, 2048]
+
+
+def test_chunk_planner_fuzz():
+    """Every size up to 64 blocks of 256 rows (and ragged ones), every chunk
+    request and both x locations, on a few shapes and SM counts: the host
+    planner returns chunks that cover the rows once, start on 256-row
+    boundaries and number at most 16, and never fails on valid sizes."""
+    from rope_chain_gb300 import _build
+    _build.build()
+    sizes = list(range(1, 2048, 37)) + [256 * b for b in range(1, 65)] + [256 * b + 1 for b in range(1, 65)]
+    for L, H in ((1, 2), (3, 8), (8, 8), (5, 16), (2, 1)):
+        for sms in (152, 148, 132):
+            for T in sizes:
+                for req in (0, 1, 2, 3, 5, 8, 16, 17, 100):
+                    for host in (False, True):
+                        b = rc.context_kv_chunk_rows(L, T, H, sms, req, x_on_host=host)
+                        assert b and b[0] == 0 and b[-1] == T, (L, H, sms, T, req, host, b)
+                        assert all(x < y for x, y in zip(b, b[1:])), b
+                        assert all(r % 256 == 0 for r in b[:-1]), b
+                        assert len(b) - 1 <= 16 and (req != 1 or len(b) == 2), b
